@@ -1,0 +1,278 @@
+"""Pins for the fp64 oracle, against facts the pages and the mathematics fix.
+
+None of these re-types the oracle's own loop.  Each check is one of:
+  * a value the pages print or an example they describe (tests/golden/),
+  * a closed form (pure decay when beta = 0; identity when alpha = 1, beta = 0),
+  * the textbook matrix form of the update, built as explicit dk x dk
+    matrices (I - beta k k^T) Diag(alpha) and multiplied with numpy,
+  * the transition product A_t ... A_{j+1} of the "Kimi K3" article
+    (lshu.cn/news/263999), §五, as an explicit matrix product,
+  * reductions to DeltaNet (alpha = 1) and Gated DeltaNet (scalar alpha), §三-§四,
+  * structural invariants (linearity, split-and-resume, snapshots, contraction),
+  * agreement of the two independent formulations: per-token recurrence and the
+    chunked WY rewrite of §六.
+The last test plants plausible mistakes in the oracle (compiled variants) and
+checks that at least one pin catches each.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#", 1)[0].strip()
+        if "=" in line:
+            key, rhs = line.split("=", 1)
+            vals[key.strip()] = np.array([float(x) for x in rhs.split()])
+    return vals
+
+
+def _inputs(rng, n, T, dk, dv, gate="config", beta=None):
+    q = rng.standard_normal((n, T, dk))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((n, T, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((n, T, dv))
+    lo, hi = (0.001, 0.1) if gate == "config" else (1e-5, 1e-3)
+    la = -rng.uniform(lo, hi, (n, T, dk))
+    b = 1 / (1 + np.exp(-rng.standard_normal((n, T)))) if beta is None else np.full((n, T), float(beta))
+    # round to fp32 once, so what the oracle sees (fp32 inputs) is what numpy sees
+    f = lambda x: x.astype(np.float32).astype(np.float64)
+    return f(q), f(k), f(v), f(la), f(b)
+
+
+def _matrix_form(q, k, v, la, beta, S0):
+    """Textbook form, explicit matrices: S_t = (I - b k k^T) Diag(a) S_{t-1} + b k v^T; o_t = S_t^T q_t."""
+    T, dk = q.shape
+    S = S0.copy()
+    outs = []
+    for t in range(T):
+        A = (np.eye(dk) - beta[t] * np.outer(k[t], k[t])) @ np.diag(np.exp(la[t]))
+        S = A @ S + beta[t] * np.outer(k[t], v[t])
+        outs.append(S.T @ q[t])
+    return np.array(outs), S
+
+
+def rel(a, b):
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+# --------------------------------------------------------------------------- pins
+def pin_matrix_form(lib):
+    rng = np.random.default_rng(1)
+    for dk, dv, T in [(4, 3, 7), (8, 8, 20), (16, 5, 33)]:
+        q, k, v, la, b = _inputs(rng, 2, T, dk, dv)
+        S0 = 0.3 * rng.standard_normal((2, dk, dv))
+        out, Sf = oracle.recurrent(q, k, v, la, b, S0, lib=lib)
+        for h in range(2):
+            o_ref, S_ref = _matrix_form(q[h], k[h], v[h], la[h], b[h], S0[h])
+            assert rel(out[h], o_ref) < 1e-13, rel(out[h], o_ref)
+            assert rel(Sf[h], S_ref) < 1e-13
+
+
+def pin_identity(lib):
+    """alpha = 1, beta = 0: the state is unchanged (bit-exact) and o_t = S0^T q_t."""
+    rng = np.random.default_rng(2)
+    q, k, v, _, _ = _inputs(rng, 2, 9, 8, 6)
+    la = np.zeros_like(q)
+    b = np.zeros(q.shape[:2])
+    S0 = rng.standard_normal((2, 8, 6))
+    out, Sf = oracle.recurrent(q, k, v, la, b, S0, lib=lib)
+    assert np.array_equal(Sf, S0)
+    for h in range(2):
+        assert rel(out[h], q[h] @ S0[h]) < 1e-14
+
+
+def pin_pure_decay(lib):
+    """beta = 0: S_T = Diag(exp(sum_t log alpha_t)) S0, and o_t reads the decayed S0."""
+    rng = np.random.default_rng(3)
+    q, k, v, la, _ = _inputs(rng, 1, 40, 8, 5)
+    b = np.zeros(q.shape[:2])
+    S0 = rng.standard_normal((1, 8, 5))
+    out, Sf = oracle.recurrent(q, k, v, la, b, S0, lib=lib)
+    g = np.cumsum(la[0], axis=0)
+    assert rel(Sf[0], np.exp(g[-1])[:, None] * S0[0]) < 1e-13
+    o_ref = np.stack([(np.exp(g[t])[:, None] * S0[0]).T @ q[0, t] for t in range(40)])
+    assert rel(out[0], o_ref) < 1e-13
+
+
+def pin_overwrite_example(lib):
+    """The pages' overwrite example: the later write under the same key wins, exactly."""
+    gd = _golden("overwrite_example.txt")
+    key, v1, v2 = gd["key"], gd["value_1"], gd["value_2"]
+    q = np.stack([key, key])[None]
+    v = np.stack([v1, v2])[None]
+    la = np.zeros_like(q)
+    b = np.ones((1, 2))
+    out, Sf = oracle.recurrent(q, q, v, la, b, None, lib=lib)
+    assert np.array_equal(out[0, 1], gd["read_delta"])
+    assert not np.allclose(out[0, 1], gd["read_additive"])
+    rng = np.random.default_rng(4)
+    vv = rng.standard_normal((2, 16)).astype(np.float32).astype(np.float64)
+    # an exactly unit key with several nonzero channels: the latest value, exactly
+    kk = np.zeros(16)
+    kk[[1, 5, 6, 11]] = [0.5, -0.5, 0.5, 0.5]
+    out, _ = oracle.recurrent(np.stack([kk, kk])[None], np.stack([kk, kk])[None], vv[None],
+                              np.zeros((1, 2, 16)), np.ones((1, 2)), None, lib=lib)
+    assert np.array_equal(out[0, 1], vv[1])
+    # a random key with |k|^2 = n2 != 1: closed form n2 * (v2 + (1 - n2) v1)
+    kk = rng.standard_normal(16)
+    kk = (kk / np.linalg.norm(kk)).astype(np.float32).astype(np.float64)
+    n2 = kk @ kk
+    out, _ = oracle.recurrent(np.stack([kk, kk])[None], np.stack([kk, kk])[None], vv[None],
+                              np.zeros((1, 2, 16)), np.ones((1, 2)), None, lib=lib)
+    assert np.abs(out[0, 1] - n2 * (vv[1] + (1 - n2) * vv[0])).max() < 1e-14
+
+
+def pin_orthonormal_retrieval(lib):
+    """alpha = 1, beta = 1 and orthonormal keys: every stored value is read back by its key."""
+    rng = np.random.default_rng(5)
+    for exact, dk, n_keys in [(True, 8, 8), (False, 16, 12)]:
+        keys = np.eye(dk)[:n_keys] if exact else np.linalg.qr(rng.standard_normal((dk, dk)))[0].T[:n_keys]
+        vals = rng.standard_normal((n_keys, 6))
+        # write all pairs, then read each key with beta = 0 (read-only steps)
+        kin = np.concatenate([keys, keys])[None]
+        vin = np.concatenate([vals, np.zeros_like(vals)])[None]
+        b = np.concatenate([np.ones(n_keys), np.zeros(n_keys)])[None]
+        out, _ = oracle.recurrent(kin, kin, vin, np.zeros_like(kin), b, None, lib=lib)
+        got = out[0, n_keys:]
+        if exact:
+            assert np.array_equal(got, vals)
+        else:
+            assert np.abs(got - vals).max() < 1e-13
+
+
+def pin_transition_product(lib):
+    """Affine in S0 with the transition product of §五: S_T(S0) - S_T(0) = A_T ... A_1 S0."""
+    rng = np.random.default_rng(6)
+    q, k, v, la, b = _inputs(rng, 1, 25, 8, 4)
+    S0 = rng.standard_normal((1, 8, 4))
+    _, S1 = oracle.recurrent(q, k, v, la, b, S0, lib=lib)
+    _, Sz = oracle.recurrent(q, k, v, la, b, None, lib=lib)
+    Phi = np.eye(8)
+    for t in range(25):
+        Phi = (np.eye(8) - b[0, t] * np.outer(k[0, t], k[0, t])) @ np.diag(np.exp(la[0, t])) @ Phi
+    assert rel(S1[0] - Sz[0], Phi @ S0[0]) < 1e-12
+
+
+def pin_reductions(lib):
+    """alpha = 1 gives DeltaNet; a scalar alpha gives Gated DeltaNet, S = a (I - b k k^T) S + b k v^T."""
+    rng = np.random.default_rng(7)
+    q, k, v, la, b = _inputs(rng, 1, 30, 8, 5)
+    S0 = rng.standard_normal((1, 8, 5))
+    # DeltaNet
+    out, Sf = oracle.recurrent(q, k, v, np.zeros_like(la), b, S0, lib=lib)
+    S = S0[0].copy()
+    for t in range(30):
+        S = (np.eye(8) - b[0, t] * np.outer(k[0, t], k[0, t])) @ S + b[0, t] * np.outer(k[0, t], v[0, t])
+        assert rel(out[0, t], S.T @ q[0, t]) < 1e-13
+    # Gated DeltaNet: the gate outside the bracket (the per-head placement)
+    la_s = np.repeat(la[:, :, :1], 8, axis=2)
+    out, Sf = oracle.recurrent(q, k, v, la_s, b, S0, lib=lib)
+    S = S0[0].copy()
+    for t in range(30):
+        a = np.exp(la_s[0, t, 0])
+        S = a * (np.eye(8) - b[0, t] * np.outer(k[0, t], k[0, t])) @ S + b[0, t] * np.outer(k[0, t], v[0, t])
+    assert rel(Sf[0], S) < 1e-13
+
+
+def pin_recurrent_equals_chunked(lib):
+    rng = np.random.default_rng(8)
+    for T in (1, 63, 64, 65, 200):
+        for C in (1, 4, 64):
+            for gate in ("config", "slow"):
+                q, k, v, la, b = _inputs(rng, 2, T, 16, 8, gate=gate)
+                S0 = 0.5 * rng.standard_normal((2, 16, 8))
+                o1, s1 = oracle.recurrent(q, k, v, la, b, S0, lib=lib)
+                o2, s2 = oracle.chunked(q, k, v, la, b, S0, chunk=C, lib=lib)
+                assert rel(o2, o1) < 1e-12, (T, C, gate, rel(o2, o1))
+                assert rel(s2, s1) < 1e-12
+
+
+def pin_linearity(lib):
+    rng = np.random.default_rng(9)
+    q, k, v, la, b = _inputs(rng, 1, 50, 8, 6)
+    v2 = rng.standard_normal(v.shape).astype(np.float32).astype(np.float64)
+    o1, s1 = oracle.recurrent(q, k, v, la, b, None, lib=lib)
+    o2, s2 = oracle.recurrent(q, k, v2, la, b, None, lib=lib)
+    o3, s3 = oracle.recurrent(q, k, v + v2, la, b, None, lib=lib)
+    assert rel(o3, o1 + o2) < 1e-13 and rel(s3, s1 + s2) < 1e-13
+    o4, s4 = oracle.recurrent(q, k, 2 * v, la, b, None, lib=lib)
+    assert np.array_equal(o4, 2 * o1) and np.array_equal(s4, 2 * s1)
+
+
+def pin_split_resume_and_snapshots(lib):
+    rng = np.random.default_rng(10)
+    q, k, v, la, b = _inputs(rng, 2, 96, 8, 6)
+    S0 = rng.standard_normal((2, 8, 6))
+    o, s, snaps = oracle.recurrent(q, k, v, la, b, S0, snap_interval=32, lib=lib)
+    oa, sa = oracle.recurrent(q[:, :40], k[:, :40], v[:, :40], la[:, :40], b[:, :40], S0, lib=lib)
+    ob, sb = oracle.recurrent(q[:, 40:], k[:, 40:], v[:, 40:], la[:, 40:], b[:, 40:], sa, lib=lib)
+    assert np.array_equal(np.concatenate([oa, ob], axis=1), o) and np.array_equal(sb, s)
+    assert snaps.shape == (2, 3, 8, 6)
+    for m in range(1, 4):
+        _, sm = oracle.recurrent(q[:, :32 * m], k[:, :32 * m], v[:, :32 * m], la[:, :32 * m], b[:, :32 * m],
+                                 S0, lib=lib)
+        assert np.array_equal(snaps[:, m - 1], sm)
+    assert np.array_equal(snaps[:, -1], s)
+    _, sc, snc = oracle.chunked(q, k, v, la, b, S0, chunk=16, snap_interval=32, lib=lib)
+    assert rel(snc, snaps) < 1e-12
+
+
+def pin_contraction(lib):
+    """||k|| = 1, beta in [0,1], alpha <= 1: ||S_t||_2 <= ||S_{t-1}||_2 + beta_t ||v_t||."""
+    rng = np.random.default_rng(11)
+    q, k, v, la, b = _inputs(rng, 1, 60, 8, 5)
+    S0 = rng.standard_normal((1, 8, 5))
+    _, _, snaps = oracle.recurrent(q, k, v, la, b, S0, snap_interval=1, lib=lib)
+    prev = np.linalg.norm(S0[0], 2)
+    for t in range(60):
+        cur = np.linalg.norm(snaps[0, t], 2)
+        assert cur <= prev + b[0, t] * np.linalg.norm(v[0, t]) + 1e-12
+        prev = cur
+
+
+PINS = [pin_matrix_form, pin_identity, pin_pure_decay, pin_overwrite_example, pin_orthonormal_retrieval,
+        pin_transition_product, pin_reductions, pin_recurrent_equals_chunked, pin_linearity,
+        pin_split_resume_and_snapshots, pin_contraction]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+def test_state_bytes_independent_of_T(oracle_lib):
+    """The state is dk x dv per head whatever T is; the K3 session state is 217,055,232 bytes."""
+    gd = _golden("state_bytes.txt")
+    rng = np.random.default_rng(12)
+    shapes = set()
+    for T in (1, 7, 130):
+        q, k, v, la, b = _inputs(rng, 1, T, 128, 128)
+        _, Sf = oracle.recurrent(q, k, v, la, b, None, lib=oracle_lib)
+        shapes.add(Sf.shape[1:])
+    assert shapes == {(128, 128)}
+    per_head = shapes.pop()
+    total = int(gd["layers"][0]) * int(gd["heads"][0]) * per_head[0] * per_head[1] * int(gd["bytes_per_element"][0])
+    assert total == int(gd["state_bytes"][0]) == 217_055_232
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+def test_planted_mistakes_are_caught(mutant, tmp_path):
+    """Each planted mistake (no decay; prediction from the undecayed state; sign of the
+    error; query/key swapped in the read; read before the write) fails at least one pin."""
+    lib = oracle.load(oracle.build(str(tmp_path / f"mutant{mutant}.so"), mutant=mutant))
+    caught = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {mutant} passed every pin"
