@@ -1,0 +1,354 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA forward on GB300: prefill tokens/s on the K3-layer-shaped
+workload (B=1, H=96, T=131072, d_k=d_v=128, chunk=64, bf16 q/k/v, fp32 gates and
+state) plus the batched-decode state bandwidth (256 sessions x 96 heads).
+
+One step = one kda_chunk_fwd over the whole workload (one launch of the
+chunked prefill kernel).  Inputs (19 GB) are far larger than L2 (129 MB), so
+no explicit L2 flush is needed between steps.  Timing: W untimed warm-up
+steps, then K steps between CUDA events on the launching stream, bracketed by
+a barrier and a device synchronize, max over ranks.  With --gpus N > 1 each
+rank runs an independent replica of the workload (the path has no exchange
+step): weak scaling, value = total tokens of all ranks / max time.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+repository) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# workload (the K3-layer-shaped long prefill)
+B, T, H, D, CHUNK = 1, 131072, 96, 128, 64
+DEC_SESSIONS, DEC_STEPS = 256, 64
+# algorithmic bytes per token-head of the prefill: q,k,v bf16 (3 x 256) + log_alpha fp32 (512)
+# + beta fp32 (4) + out (512 fp32 / 256 bf16)
+PREFILL_IN_BYTES = 3 * 256 + 512 + 4
+# flops per token-head of the chunked form at C = 64 (triangles counted half):
+# 6 dk dv + C (3 dk + 2 dv)
+PREFILL_FLOP = 6 * D * D + CHUNK * (3 * D + 2 * D)
+# decode: state read + written (2 x 65,536 B) + q,k,v bf16, log_alpha, beta, out fp32 per session-head
+DEC_BYTES = 2 * D * D * 4 + 3 * 256 + 512 + 4 + 512
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def time_oracle_sample(n_heads: int, T_s: int, threads: int, seed: int = 1):
+    """Run the fp64 oracle on n_heads x T_s token-heads of workload-shaped synthetic input."""
+    import torch
+
+    from kda_recurrent_state_gb300 import synth
+    from oracle import oracle
+
+    x = synth.prefill_inputs(1, T_s, n_heads, seed=synth.SEED_BASE + 2 + seed, device="cpu")
+    hm = lambda t: t[0].transpose(0, 1).to(torch.float64).contiguous().numpy()
+    args = (hm(x["q"]), hm(x["k"]), hm(x["v"]), hm(x["log_alpha"]), x["beta"][0].t().to(torch.float64).numpy())
+    t0 = time.perf_counter()
+    oracle.recurrent(*args, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_baseline(sample_heads=48, sample_T=131072):
+    threads = cpu_cores()
+    dt = time_oracle_sample(sample_heads, sample_T, threads)
+    th_per_s = sample_heads * sample_T / dt
+    return {"value": th_per_s / H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 per-token recurrence on {sample_heads} heads x {sample_T} tokens of the B=1,H=96,"
+                      f"T=131072 workload ({sample_heads * sample_T} token-heads, {dt:.1f} s); tokens/s = "
+                      f"token-heads/s / 96 heads"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import binding, synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    out_dtype = torch.float32 if args.out_dtype == "f32" else torch.bfloat16
+    peaks, peak_src = load_peaks()
+
+    x = synth.prefill_inputs(B, T, H, seed=synth.SEED_BASE + 2, device=dev)
+    out = torch.empty(B, T, H, D, dtype=out_dtype, device=dev)
+    fin = torch.empty(B, H, D, D, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(binding.kda_workspace_size(binding.KDA_OP_CHUNK, B, T, H, D, D, args.chunk), 16),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, out, fin, chunk=args.chunk,
+                          workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0, "device status raised during warm-up"
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(args.steps):
+            step()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    per = [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(args.steps)]
+    elapsed = reduce_max(sum(per), world, dev)
+    tokens = B * T * args.steps * world
+    kern_s = sum(per) / args.steps  # one prefill launch per step: event time = kernel duration
+    out_b = 512 if out_dtype == torch.float32 else 256
+    alg_bytes = B * T * H * (PREFILL_IN_BYTES + out_b)
+    achieved = alg_bytes / kern_s / 1e9
+    flops = B * T * H * PREFILL_FLOP
+    line = {
+        "metric": "KDA prefill tokens/s at H=96,T=128K (% tensor roofline); decode state GB/s",
+        "value": tokens / elapsed, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xf16->f32 tensor products, f32 state" if args.chunk == 64 else "f32",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta sigmoid(N(0,1)), log_alpha -U(0.001,0.1))",
+        "config": {"workload": f"KDA prefill B={B} H={H} T={T} dk=dv={D} chunk={args.chunk}, bf16 q/k/v, fp32 "
+                               f"gates/state, {args.out_dtype} out, zero initial state, final state returned",
+                   "l2": "inputs (19 GB) larger than L2 (129 MB); no flush", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic,
+                     "peak_source": f"hbm_gbs of {peak_src}", "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernel_ms": kern_s * 1e3},
+        "tensor": {"achieved_tflops": flops / kern_s / 1e12, "peak_tflops": peaks["bf16_tflops"],
+                   "frac": flops / kern_s / 1e12 / peaks["bf16_tflops"],
+                   "note": "fp16 dense rate = bf16 dense rate; flops = 139,264 per token-head"},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+    }
+
+    # ---- decode: 256 sessions x 96 heads, 64 steps with the state updated in place
+    d = synth.decode_inputs(DEC_SESSIONS, H, seed=synth.SEED_BASE + 3, steps=DEC_STEPS, device=dev)
+    st = d["state"]
+    dout = torch.empty(DEC_SESSIONS, H, D, dtype=torch.float32, device=dev)
+    dec = lambda s: kda.kda_decode_step(d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s], d["beta"][s], st, dout)
+    for s in range(3):
+        dec(s)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(DEC_STEPS):
+        dec(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dt = e0.elapsed_time(e1) / 1e3 / DEC_STEPS
+    dgbs = DEC_SESSIONS * H * DEC_BYTES / dt / 1e9
+    line["decode"] = {"session_steps_per_s": DEC_SESSIONS / dt, "GB_per_s": dgbs, "us_per_step": dt * 1e6,
+                      "roofline": {"bound": "hbm", "achieved": dgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": dgbs / peaks["hbm_gbs"]},
+                      "workload": "256 sessions x 96 heads, fp32 state in place, 64 steps, bf16 q/k/v, fp32 out"}
+    line["gpu_launches"] += DEC_STEPS + 3
+    del d, st, dout
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, x, out, fin, ws, dev, out_dtype)
+        line["gpu_launches"] += args.e2e_steps
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def e2e(args, x, out, fin, ws, dev, out_dtype):
+    """tokens/s including the H2D copy of the step's inputs from pinned host memory and the D2H
+    read of the step's results (outputs and final state)."""
+    import torch
+
+    import kda_recurrent_state_gb300 as kda
+
+    names = ("q", "k", "v", "log_alpha", "beta")
+    host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
+    for n in names:
+        host[n].copy_(x[n])
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hfin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for n in names:
+            x[n].copy_(host[n], non_blocking=True)
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, out, fin, chunk=args.chunk,
+                          workspace=ws)
+        hout.copy_(out, non_blocking=True)
+        hfin.copy_(fin, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dt = e0.elapsed_time(e1) / 1e3 / args.e2e_steps
+    return {"value": B * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": dt * 1e3, "steps": args.e2e_steps}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    threads = cpu_cores()
+    sample_heads, sample_T = 8, 32768
+    for _ in range(args.warmup):
+        time_oracle_sample(1, 1024, threads)
+    dts = [time_oracle_sample(sample_heads, sample_T, threads, seed=i) for i in range(args.steps)]
+    th = sample_heads * sample_T
+    value = th / (sum(dts) / len(dts)) / H
+    sample = (f"fp64 per-token recurrence, {sample_heads} heads x {sample_T} tokens of the B=1,H=96,T=131072 "
+              f"workload per step; tokens/s = token-heads/s / 96 heads")
+    line = {"impl": "reference", "metric": "KDA prefill tokens/s at H=96,T=128K (% tensor roofline); decode state GB/s",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(dts) / len(dts), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same generator as the GPU arm)",
+            "config": {"workload": f"KDA prefill B={B} H={H} T={T} dk=dv={D} (bounded sample, see cpu_baseline)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--chunk", type=int, default=64, choices=[1, 64])
+    ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the prefill kernel from an ncu capture (null if unknown)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * kda.h -- C ABI of libkda, the GB300 (sm_103a) forward pass of Kimi Delta
+ * Attention (KDA).
+ *
+ * What the library computes (cited by page title and section):
+ *   "Kimi K3" article, lshu.cn/news/263999, §四: per head, a d_k x d_v state
+ *       S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *   with a per-key-channel decay alpha_t = exp(log_alpha_t) in (0,1]^{d_k};
+ *   §二.1: the read o_t = S_t^T q_t (after token t's update, no 1/sqrt(d) scale);
+ *   §三: the delta-rule reading of the same update (predict from the decayed
+ *   state, write beta times the error);
+ *   §六: the chunkwise evaluation (recurrent between chunks, WY form inside).
+ *   "Kimi K3 混合线性注意力", hubwiz.com, §3: the state is 128 x 128 per head
+ *   and independent of the sequence length; §5: state snapshots at fixed token
+ *   intervals make a long run restartable and its prefixes reusable.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps a pointer after the call returns.
+ *   - Layouts are row-major and token-major:
+ *       q, k        [.., H, d_k]   (in_dtype: KDA_BF16 or KDA_F32)
+ *       v           [.., H, d_v]   (in_dtype)
+ *       log_alpha   [.., H, d_k]   float32, finite and <= 0
+ *       beta        [.., H]        float32
+ *       state       [.., H, d_k, d_v] float32, row i = key channel i
+ *       out         [.., H, d_v]   (out_dtype)
+ *     where ".." is [B, T] for the batched prefill, [T_total] for packed
+ *     sequences and [B] for decode.
+ *   - Supported sizes: d_k = d_v = 128.  chunk = 64 (tensor-core chunked
+ *     path) or chunk = 1 (token-serial path).  Anything else returns
+ *     KDA_ERR_UNSUPPORTED.
+ *   - Alignment (KDA_ERR_MISALIGNED otherwise): q, k, v, log_alpha, out and
+ *     every state/snapshot pointer of the prefill calls 16 bytes (tensor-map
+ *     loads); the state of kda_decode_step 16 bytes; beta 4 bytes; cu_seqlens
+ *     and snap_offsets 8 bytes; the other decode operands their element size.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  A return of KDA_OK means the work was enqueued.
+ *     Faults found inside a kernel (a bounded wait that ran out, a gate out of
+ *     the supported range) are recorded in a device status word, never by a
+ *     trap; read them with kda_get_device_status().
+ *   - No C++ exception crosses this boundary.  Results are bit-reproducible
+ *     from run to run on the same GPU.
+ *   - Numerics of the chunk = 64 path: tensor-core products take fp16 operands
+ *     with fp32 accumulation; the state and every carry are fp32.  Inputs must
+ *     stay inside the fp16 range after gating (|q|,|k|,|v| well below 6.5e4)
+ *     and each chunk's cumulative log-decay must be >= -20 per key channel
+ *     (otherwise KDA_STATUS_GATE_RANGE is raised in the device status word).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of q/k/v (in_dtype) and of out (out_dtype). */
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+/* Return codes of every entry point. */
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null required pointer, negative size, bad enum */
+    KDA_ERR_UNSUPPORTED = 2, /* d_k, d_v or chunk outside the supported set */
+    KDA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+    KDA_ERR_TIMEOUT = 5,     /* device status: a bounded wait inside a kernel expired */
+    KDA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than kda_workspace_size() */
+    KDA_STATUS_GATE_RANGE = 7 /* device status: a chunk's cumulative log-decay was below -20 */
+} kda_status;
+
+/* Operation selector of kda_workspace_size(). */
+typedef enum { KDA_OP_CHUNK = 0, KDA_OP_VARLEN = 1, KDA_OP_DECODE = 2 } kda_op;
+
+/*
+ * Batched prefill: B independent sequences of T tokens, H heads each.
+ * "Kimi K3" article (lshu.cn/news/263999) §四 recurrence, evaluated chunkwise
+ * as in §六.
+ *   q, k        [B, T, H, dk]  in_dtype
+ *   v           [B, T, H, dv]  in_dtype
+ *   log_alpha   [B, T, H, dk]  float32
+ *   beta        [B, T, H]      float32
+ *   init_state  [B, H, dk, dv] float32, or NULL for a zero initial state
+ *   out         [B, T, H, dv]  out_dtype, o_t = S_t^T q_t
+ *   final_state [B, H, dk, dv] float32, or NULL if not wanted
+ *   workspace   device scratch of at least kda_workspace_size(KDA_OP_CHUNK, ...)
+ *               bytes (may be NULL when that size is 0); contents need no
+ *               initialisation and are not preserved.
+ * B, T or H equal to 0 is valid (nothing to compute; with T = 0 the final
+ * state is the initial state).  init_state may alias final_state.
+ */
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                  const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
+                  int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
+                  void* stream);
+
+/*
+ * Packed variable-length prefill with state snapshots ("Kimi K3 混合线性注意力",
+ * hubwiz.com, §5: restartable checkpoints of the recurrent state).
+ *   q, k, v, log_alpha, beta, out : token-major over T_total packed tokens,
+ *               shapes as in kda_chunk_fwd with [B, T] replaced by [T_total].
+ *   cu_seqlens  device int64 [N+1], cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[N] = T_total; sequence s is tokens
+ *               [cu_seqlens[s], cu_seqlens[s+1]).
+ *   init_states [N, H, dk, dv] float32, or NULL for zero initial states.
+ *   final_states[N, H, dk, dv] float32 (required).
+ *   snapshot_interval  0 for none, else a positive multiple of `chunk`:
+ *               snapshot m (m = 1 .. floor(len_s / interval)) of sequence s is
+ *               the state right after its token m * interval (counted from the
+ *               sequence start) and is stored at
+ *               snapshots[snap_offsets[s] + m - 1][H][dk][dv].  When len_s is a
+ *               multiple of the interval, the last snapshot equals the final
+ *               state bit for bit.
+ *   snap_offsets device int64 [N+1] from kda_snapshot_offsets() (copied to the
+ *               device by the caller); NULL when snapshot_interval = 0.
+ *   snapshots   float32 [snap_offsets[N], H, dk, dv]; NULL when no snapshot.
+ * Chunks are aligned to each sequence's first token; each sequence's result
+ * is bit-identical to running that sequence alone through this function.
+ */
+int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                   const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv, int chunk,
+                   const float* init_states, float* final_states, int64_t snapshot_interval,
+                   const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
+                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * One decode step for B sessions (one new token each), state updated in place:
+ * "Kimi K3" article §四 applied once; the state is read once and written once.
+ *   q, k [B, H, dk] in_dtype;  v [B, H, dv] in_dtype;
+ *   log_alpha [B, H, dk] float32;  beta [B, H] float32;
+ *   state [B, H, dk, dv] float32, read and overwritten;
+ *   out [B, H, dv] out_dtype.
+ */
+int kda_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                    float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
+                    void* stream);
+
+/* Number of snapshots of a sequence: floor(seqlen / interval); 0 if interval <= 0 or seqlen < 0. */
+int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);
+
+/*
+ * Host helper: exclusive prefix sum of kda_snapshot_count over the N sequences
+ * given by HOST cu_seqlens [N+1]; writes HOST offsets [N+1] (offsets[N] = total).
+ * Returns KDA_ERR_INVALID_ARG on null pointers, N < 0, a negative interval or
+ * decreasing cu_seqlens.
+ */
+int kda_snapshot_offsets(const int64_t* cu_seqlens_host, int N, int64_t interval, int64_t* offsets_host);
+
+/*
+ * Bytes of device workspace the call `op` needs for these sizes (T = T_total
+ * and B = N for KDA_OP_VARLEN).  0 means the workspace may be NULL.
+ */
+size_t kda_workspace_size(int op, int B, int64_t T, int H, int dk, int dv, int chunk);
+
+/* Static, human-readable name of a kda_status value. */
+const char* kda_status_string(int status);
+
+/*
+ * Waits for `stream`, then reads and clears the device status word of the
+ * current device: KDA_OK, KDA_ERR_TIMEOUT or KDA_STATUS_GATE_RANGE (the first
+ * fault recorded since the last read).  Returns KDA_ERR_CUDA if the read fails.
+ */
+int kda_get_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H_ */

@@ -1,0 +1,180 @@
+"""Thin Python binding of libkda (include/kda.h), same names as the C ABI.
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, outputs are allocated with torch when the caller passes none, and
+the raw device pointers go to the C entry points on the current CUDA stream.
+Every step of the computation runs inside libkda's kernels.  If the shared
+library is missing the import of this module's functions fails loudly; there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_BF16, KDA_F32 = 0, 1
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_MISALIGNED = 0, 1, 2, 3
+KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_WORKSPACE, KDA_STATUS_GATE_RANGE = 4, 5, 6, 7
+KDA_OP_CHUNK, KDA_OP_VARLEN, KDA_OP_DECODE = 0, 1, 2
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {kda_status_string(code)} (code {code})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkda.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkda.so not found at {LIB_PATH}; build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        L.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I, P, SZ, P]
+        L.kda_varlen_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, P, P, I64, P, P, P, I, I, P, SZ, P]
+        L.kda_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+        L.kda_snapshot_count.argtypes = [I64, I64]
+        L.kda_snapshot_count.restype = I64
+        L.kda_snapshot_offsets.argtypes = [P, I, I64, P]
+        L.kda_workspace_size.argtypes = [I, I, I64, I, I, I, I]
+        L.kda_workspace_size.restype = SZ
+        L.kda_status_string.argtypes = [I]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_get_device_status.argtypes = [P]
+        for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_snapshot_offsets,
+                  L.kda_get_device_status):
+            f.restype = I
+        _lib = L
+    return _lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libkda must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != KDA_OK:
+        raise KdaError(rc, where)
+
+
+def _dtype_of(code: int):
+    return torch.bfloat16 if code == KDA_BF16 else torch.float32
+
+
+def kda_status_string(code: int) -> str:
+    return lib().kda_status_string(int(code)).decode()
+
+
+def kda_snapshot_count(seqlen: int, interval: int) -> int:
+    return int(lib().kda_snapshot_count(int(seqlen), int(interval)))
+
+
+def kda_snapshot_offsets(cu_seqlens_host, interval: int) -> torch.Tensor:
+    """HOST int64 [N+1] snapshot offsets for HOST cu_seqlens (a list or CPU tensor)."""
+    cu = torch.as_tensor(cu_seqlens_host, dtype=torch.int64).cpu().contiguous()
+    N = cu.numel() - 1
+    off = torch.empty(N + 1, dtype=torch.int64)
+    _check(lib().kda_snapshot_offsets(_ptr(cu), N, int(interval), _ptr(off)), "kda_snapshot_offsets")
+    return off
+
+
+def kda_workspace_size(op: int, B: int, T: int, H: int, dk: int = 128, dv: int = 128, chunk: int = 64) -> int:
+    return int(lib().kda_workspace_size(int(op), int(B), int(T), int(H), int(dk), int(dv), int(chunk)))
+
+
+def kda_get_device_status(stream=None) -> int:
+    st = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(None)
+    return int(lib().kda_get_device_status(st))
+
+
+def _workspace(op, B, T, H, dk, dv, chunk, device, workspace):
+    need = kda_workspace_size(op, B, T, H, dk, dv, chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace, (workspace.numel() * workspace.element_size() if workspace is not None else 0)
+
+
+def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, out=None, final_state=None, *, chunk: int = 64,
+                  out_dtype=torch.float32, return_final_state: bool = True, workspace=None):
+    """Batched prefill.  q,k [B,T,H,dk], v [B,T,H,dv] (bf16/fp32), log_alpha [B,T,H,dk] fp32,
+    beta [B,T,H] fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, T, H, dv, dtype=out_dtype, device=q.device)
+    if final_state is None and return_final_state:
+        final_state = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    ws, ws_bytes = _workspace(KDA_OP_CHUNK, B, T, H, dk, dv, chunk, q.device, workspace)
+    rc = lib().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(out),
+                             _ptr(final_state), B, T, H, dk, dv, int(chunk), _dt(q), _dt(out), _ptr(ws), ws_bytes,
+                             _stream(q.device))
+    _check(rc, "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, chunk: int = 64,
+                   snapshot_interval: int = 0, cu_seqlens_host=None, out=None, final_states=None,
+                   snapshots=None, out_dtype=torch.float32, workspace=None):
+    """Packed sequences.  q,k [Ttot,H,dk], v [Ttot,H,dv], log_alpha [Ttot,H,dk], beta [Ttot,H];
+    cu_seqlens int64 [N+1] on the device.  Returns (out, final_states, snapshots or None)."""
+    Ttot, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty(Ttot, H, dv, dtype=out_dtype, device=q.device)
+    if final_states is None:
+        final_states = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    snap_off = None
+    if snapshot_interval:
+        cu_h = cu_seqlens.cpu() if cu_seqlens_host is None else torch.as_tensor(cu_seqlens_host)
+        off_h = kda_snapshot_offsets(cu_h, snapshot_interval)
+        snap_off = off_h.to(q.device)
+        if snapshots is None:
+            snapshots = torch.empty(max(int(off_h[-1]), 1), H, dk, dv, dtype=torch.float32, device=q.device)
+    ws, ws_bytes = _workspace(KDA_OP_VARLEN, N, Ttot, H, dk, dv, chunk, q.device, workspace)
+    rc = lib().kda_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), N, Ttot, H,
+                              dk, dv, int(chunk), _ptr(init_states), _ptr(final_states), int(snapshot_interval),
+                              _ptr(snap_off), _ptr(snapshots) if snapshot_interval else None, _ptr(out), _dt(q),
+                              _dt(out), _ptr(ws), ws_bytes, _stream(q.device))
+    _check(rc, "kda_varlen_fwd")
+    if snapshot_interval and snapshots is not None:
+        snapshots = snapshots[: int(snap_off[-1].item())] if snapshots.shape[0] > 0 else snapshots
+    return out, final_states, (snapshots if snapshot_interval else None)
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=torch.float32):
+    """One token per session: q,k [B,H,dk], v [B,H,dv], log_alpha [B,H,dk], beta [B,H];
+    state [B,H,dk,dv] fp32 is updated in place.  Returns out [B,H,dv]."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=out_dtype, device=q.device)
+    rc = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(state), _ptr(out), B, H,
+                               dk, dv, _dt(q), _dt(out), _stream(q.device))
+    _check(rc, "kda_decode_step")
+    return out

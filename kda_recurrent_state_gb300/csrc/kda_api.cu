@@ -1,0 +1,197 @@
+// kda_api.cu -- the C ABI of libkda: host-side validation, the device status
+// word and dispatch to the kernels.  Declarations and the contract of every
+// entry point are in include/kda.h.
+#include <mutex>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+// Device status word: kernels record the first fault they see (a bounded wait
+// that ran out, a gate out of range) here instead of trapping.
+__device__ int g_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_addr[kMaxDevices];
+std::mutex g_status_mu;
+
+int* status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<int*>(p);
+    }
+    return g_status_addr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool dtype_ok(int d) { return d == KDA_BF16 || d == KDA_F32; }
+
+// Shape/dtype/alignment checks shared by the prefill entry points.
+int check_common(int dk, int dv, int chunk, int in_dtype, int out_dtype) {
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return KDA_ERR_INVALID_ARG;
+    if (dk != kD || dv != kD) return KDA_ERR_UNSUPPORTED;
+    if (chunk != 1 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+int run_prefill(const SeqProblem& p, int chunk, int in_dtype, int out_dtype, void* ws, size_t ws_bytes,
+                cudaStream_t st) {
+    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, in_dtype, out_dtype, st)
+                                 : launch_chunk_prefill(p, in_dtype, out_dtype, ws, ws_bytes, st);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+const char* kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: null pointer, negative size or bad enum";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: only dk = dv = 128 and chunk in {1, 64}";
+        case KDA_ERR_MISALIGNED: return "KDA_ERR_MISALIGNED: pointers must be 16-byte aligned";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel expired";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
+        case KDA_STATUS_GATE_RANGE: return "KDA_STATUS_GATE_RANGE: a chunk's cumulative log-decay is below -20";
+        default: return "unknown kda status";
+    }
+}
+
+int64_t kda_snapshot_count(int64_t seqlen, int64_t interval) {
+    if (interval <= 0 || seqlen < 0) return 0;
+    return seqlen / interval;
+}
+
+int kda_snapshot_offsets(const int64_t* cu_seqlens_host, int N, int64_t interval, int64_t* offsets_host) {
+    if (!cu_seqlens_host || !offsets_host || N < 0 || interval < 0) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host[0] != 0) return KDA_ERR_INVALID_ARG;
+    offsets_host[0] = 0;
+    for (int s = 0; s < N; ++s) {
+        const int64_t len = cu_seqlens_host[s + 1] - cu_seqlens_host[s];
+        if (len < 0) return KDA_ERR_INVALID_ARG;
+        offsets_host[s + 1] = offsets_host[s] + kda_snapshot_count(len, interval);
+    }
+    return KDA_OK;
+}
+
+size_t kda_workspace_size(int op, int B, int64_t T, int H, int dk, int dv, int chunk) {
+    (void)T; (void)dk; (void)dv;
+    if (op == KDA_OP_DECODE || B <= 0 || H <= 0 || chunk != 64) return 0;
+    return chunk_prefill_workspace(B, H);
+}
+
+int kda_get_device_status(void* stream) {
+    int* addr = status_ptr();
+    if (!addr) return KDA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    if (cudaMemcpyAsync(&host, addr, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(addr, 0, sizeof(int), st) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+    return host;
+}
+
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                  const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
+                  int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
+                  void* stream) {
+    if (B < 0 || T < 0 || H < 0) return KDA_ERR_INVALID_ARG;
+    int rc = check_common(dk, dv, chunk, in_dtype, out_dtype);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (B == 0 || H == 0) return KDA_OK;
+    const size_t state_bytes = (size_t)B * H * kD * kD * sizeof(float);
+    if (T == 0) {  // nothing to run: the final state is the initial state
+        if (!final_state) return KDA_OK;
+        if (!aligned16(final_state) || (init_state && !aligned16(init_state))) return KDA_ERR_MISALIGNED;
+        cudaError_t e = init_state ? (init_state == final_state
+                                          ? cudaSuccess
+                                          : cudaMemcpyAsync(final_state, init_state, state_bytes,
+                                                            cudaMemcpyDeviceToDevice, st))
+                                   : cudaMemsetAsync(final_state, 0, state_bytes, st);
+        return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
+    if (!q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, log_alpha, init_state, out, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if (!aligned(beta, 4)) return KDA_ERR_MISALIGNED;
+    const size_t need = kda_workspace_size(KDA_OP_CHUNK, B, T, H, dk, dv, chunk);
+    if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return KDA_ERR_MISALIGNED;
+
+    SeqProblem p{};
+    p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta;
+    p.init = init_state; p.final_state = final_state; p.out = out;
+    p.cu_seqlens = nullptr; p.T_uniform = T; p.T_total = (int64_t)B * T;
+    p.N = B; p.H = H;
+    p.snap_interval = 0; p.snap_offsets = nullptr; p.snapshots = nullptr;
+    p.status = status_ptr();
+    if (!p.status) return KDA_ERR_CUDA;
+    return run_prefill(p, chunk, in_dtype, out_dtype, workspace, ws_bytes, st);
+}
+
+int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                   const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv, int chunk,
+                   const float* init_states, float* final_states, int64_t snapshot_interval,
+                   const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
+                   void* workspace, size_t ws_bytes, void* stream) {
+    if (N < 0 || T_total < 0 || H < 0 || snapshot_interval < 0) return KDA_ERR_INVALID_ARG;
+    int rc = check_common(dk, dv, chunk, in_dtype, out_dtype);
+    if (rc != KDA_OK) return rc;
+    if (N == 0 || H == 0) return KDA_OK;
+    if (!cu_seqlens || !final_states) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    if (snapshot_interval > 0) {
+        if (snapshot_interval % chunk != 0) return KDA_ERR_INVALID_ARG;
+        if (!snap_offsets) return KDA_ERR_INVALID_ARG;
+    }
+    const void* ptrs[] = {q, k, v, log_alpha, init_states, final_states, snapshots, out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if ((beta && !aligned(beta, 4)) || !aligned(cu_seqlens, 8) || (snap_offsets && !aligned(snap_offsets, 8)))
+        return KDA_ERR_MISALIGNED;
+    const size_t need = kda_workspace_size(KDA_OP_VARLEN, N, T_total, H, dk, dv, chunk);
+    if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return KDA_ERR_MISALIGNED;
+
+    SeqProblem p{};
+    p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta;
+    p.init = init_states; p.final_state = final_states; p.out = out;
+    p.cu_seqlens = cu_seqlens; p.T_uniform = 0; p.T_total = T_total;
+    p.N = N; p.H = H;
+    p.snap_interval = snapshot_interval; p.snap_offsets = snap_offsets; p.snapshots = snapshots;
+    p.status = status_ptr();
+    if (!p.status) return KDA_ERR_CUDA;
+    return run_prefill(p, chunk, in_dtype, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int kda_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                    float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
+                    void* stream) {
+    if (B < 0 || H < 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return KDA_ERR_INVALID_ARG;
+    if (dk != kD || dv != kD) return KDA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    const uintptr_t in_al = in_dtype == KDA_BF16 ? 2 : 4, out_al = out_dtype == KDA_BF16 ? 2 : 4;
+    if (!aligned16(state) || !aligned(q, in_al) || !aligned(k, in_al) || !aligned(v, in_al) ||
+        !aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned(out, out_al))
+        return KDA_ERR_MISALIGNED;
+    DecodeProblem p{q, k, v, log_alpha, beta, state, out, B, H};
+    return launch_decode(p, in_dtype, out_dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
+                                                                                               : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point declared in include/kda.h, and its host helpers and
+argument validation behave as documented.  No call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kda_recurrent_state_gb300 import binding, build
+
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"kda_chunk_fwd", "kda_varlen_fwd", "kda_decode_step"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"libkda.so does not export {n}"
+
+
+def test_snapshot_helpers(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    assert b.kda_snapshot_count(65536, 16384) == 4
+    assert b.kda_snapshot_count(16383, 16384) == 0
+    assert b.kda_snapshot_count(100, 0) == 0
+    assert b.kda_snapshot_count(-5, 64) == 0
+    off = b.kda_snapshot_offsets([0, 100, 300, 300, 1000], 64)
+    assert off.tolist() == [0, 1, 4, 4, 14]
+    with pytest.raises(b.KdaError):
+        b.kda_snapshot_offsets([0, 100, 50], 64)  # decreasing cu_seqlens
+
+
+def test_status_strings(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    for code in range(8):
+        assert b.kda_status_string(code).startswith("KDA_")
+    assert "unknown" in b.kda_status_string(99)
+
+
+def _chunk(L, *, q=16, B=1, T=8, H=1, dk=128, dv=128, chunk=64, in_dt=0, out_dt=1, ws=None, ws_bytes=0):
+    P = ctypes.c_void_p
+    ptr = P(q) if q else None
+    return L.kda_chunk_fwd(ptr, ptr, ptr, ptr, ptr, None, ptr, None, B, T, H, dk, dv, chunk, in_dt, out_dt,
+                           P(ws) if ws else None, ws_bytes, None)
+
+
+def test_argument_validation(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    assert _chunk(L, B=-1) == b.KDA_ERR_INVALID_ARG
+    assert _chunk(L, dk=64) == b.KDA_ERR_UNSUPPORTED
+    assert _chunk(L, chunk=32) == b.KDA_ERR_UNSUPPORTED
+    assert _chunk(L, in_dt=7) == b.KDA_ERR_INVALID_ARG
+    assert _chunk(L, q=0) == b.KDA_ERR_INVALID_ARG
+    assert _chunk(L, q=0x1008) == b.KDA_ERR_MISALIGNED
+    assert _chunk(L, B=0) == b.KDA_OK  # nothing to do
+    assert _chunk(L, H=0) == b.KDA_OK
+    need = L.kda_workspace_size(0, 1, 8, 1, 128, 128, 64)
+    if need:
+        assert _chunk(L, ws=0x2000, ws_bytes=need - 1) == b.KDA_ERR_WORKSPACE
+    P = ctypes.c_void_p
+    # varlen: interval must be a multiple of the chunk; final_states is required
+    assert L.kda_varlen_fwd(P(16), P(16), P(16), P(16), P(16), P(16), 2, 100, 1, 128, 128, 64, None, P(16), 100,
+                            P(16), P(16), P(16), 0, 1, None, 0, None) == b.KDA_ERR_INVALID_ARG
+    assert L.kda_varlen_fwd(P(16), P(16), P(16), P(16), P(16), P(16), 2, 100, 1, 128, 128, 64, None, None, 0,
+                            None, None, P(16), 0, 1, None, 0, None) == b.KDA_ERR_INVALID_ARG
+    assert L.kda_decode_step(P(16), P(16), P(16), P(16), P(16), P(16), P(16), 2, 2, 96, 128, 0, 1,
+                             None) == b.KDA_ERR_UNSUPPORTED
+    assert L.kda_decode_step(P(16), P(16), P(16), P(16), P(16), P(0x1004), P(16), 2, 2, 128, 128, 0, 1,
+                             None) == b.KDA_ERR_MISALIGNED
+    assert L.kda_decode_step(P(16), P(16), P(16), P(16), P(0x1002), P(16), P(16), 2, 2, 128, 128, 0, 1,
+                             None) == b.KDA_ERR_MISALIGNED  # beta needs 4 bytes
+
+
+def test_workspace_size(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    assert b.kda_workspace_size(b.KDA_OP_DECODE, 256, 1, 96) == 0
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96) >= 0
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96, chunk=1) == 0
