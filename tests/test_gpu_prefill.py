@@ -11,7 +11,7 @@ from kda_testutil import assert_close, batch_heads, errors, np64
 from oracle import oracle
 
 pytestmark = pytest.mark.gpu
-CHUNKS = [1]
+CHUNKS = [64, 1]
 
 
 def _ref(x, pairs):
@@ -130,7 +130,7 @@ def test_mid_prefill_full_size_sampled(chunk):
     _check(x, out, fin, pairs, "mid")
 
 
-@pytest.mark.parametrize("chunk", [1])
+@pytest.mark.parametrize("chunk", [64])
 def test_long_prefill_full_size_sampled(chunk):
     """B=1, H=96, T=131072 (128K), zero initial state, in the launch configuration the bench times:
     4 sampled heads over the whole sequence, plus a property that holds at any size

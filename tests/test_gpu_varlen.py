@@ -10,7 +10,7 @@ from kda_testutil import assert_close, np64, packed_heads
 from oracle import oracle
 
 pytestmark = pytest.mark.gpu
-CHUNKS = [1]
+CHUNKS = [64, 1]
 
 
 def _run(x, chunk, interval=0, **kw):
@@ -83,7 +83,7 @@ def test_varlen_equals_single_sequence_runs(chunk):
             assert torch.equal(snaps[off[s + 1] - 1], fin[s])
 
 
-@pytest.mark.parametrize("chunk", [1])
+@pytest.mark.parametrize("chunk", [64])
 def test_varlen_full_size_sampled(chunk):
     """16 packed sequences, lengths log-uniform in [1024, 65536], H=64, every other sequence
     resuming from an N(0,0.02) state, snapshots every 16384 tokens: sampled (sequence, head)
