@@ -20,28 +20,39 @@
 // as X = Diag(e^{ref}) S0 (what the products with Ktil_p / Qtil_p need), and the
 // state accumulator holds D = X + Khat_p^T U, so S_C = Diag(e^{g_63 - ref}) D.
 //
+// The triangular inverse on the tensor cores: split A = A_d + A_o into its
+// 16x16 diagonal blocks and the rest.  With Dg = (I + A_d)^-1 (four small
+// inverses, CUDA cores) and N = Dg A_o (strictly block-lower, N^4 = 0):
+//   I + A = (I + A_d)(I + N)   =>   T = (I + N)^-1 Dg = (I - N)(I + N^2) Dg,
+// evaluated as four 64x64x64 products: N = Dg A_o, N2 = N N, M = Dg + N2 Dg,
+// T = M - N M.
+//
 // Data layout on chip (one CTA = one (sequence, head), all of d_v = 128):
 //   TMEM (fp32 accumulators, lanes = the M rows):
 //     D_S [j][c] state (128 cols)   X16 [j][c] fp16 A operand   D_U [j][r] U'/U
-//     U16 [j][r] fp16 A operand     D_O [j][r] output           D_G [r|64+r][i] Gram
-//     D_W [c][r] W^T                V16 [j][i] fp16 A operand (v^T)
+//     U16 [j][r] fp16 A operand (over D_U)   D_O [j][r] output   D_G [r|64+r][i] Gram
+//     D_W [c][r] W^T, and before that the four M = 64 products of the inverse
+//     V16 [2][j][i] fp16 A operand (v^T), by chunk parity
 //   SMEM (fp16, 128-byte swizzled rows of 64 elements):
 //     KT[c][r] = Ktil_p, QT[c][r] = Qtil_p (adjacent: together the M = 128 A
-//     operand of the Gram), KH[c][r] = Khat_p, PP[r][i] = P, TT[i][r] =
-//     T[r][i] beta_i, WT[c][r] = -W^T; a ring of 16-token input slots (TMA).
-//   Every product is one M = 128 tcgen05.mma chain:
-//     Gram  D_G = [KT;QT] (MN-major) x KH (MN-major)        128x64x128
-//     WY    D_W = KT (K-major) x TT (MN-major)               128x64x64
-//           D_U = V16 (TMEM) x TT                            128x64x64
-//     (i)   D_U += X16 x WT (MN-major)                       128x64x128
-//     (iii) D_O = X16 x QT (MN-major) + U16 x PP (K-major)   128x64x192
-//     (ii)  D_S += U16 x KH (K-major)                        128x128x64
+//     operand of the Gram), KH[c][r] = Khat_p, PP[r][i] = P, WT[c][r] = -W^T,
+//     DT[m][r] = Dg^T, B1 = A_o -> N2 -> -M (row-major), NR = N -> T diag(beta)
+//     (row-major); fp32 diagonal blocks of A and of Dg; a ring of 16-token
+//     input slots filled by TMA.
+//   The products (all tcgen05.mma, fp16 operands, fp32 accumulation):
+//     Gram  D_G = [KT;QT] x KH                 M=128 N=64  K=128
+//     S1..4 D_W = DT x B1, NR x NR, B1 x DT, NR x B1 (accumulate)   M=64 N=64 K=64
+//     WY    D_W = KT x T,  D_U = V16 x T       M=128 N=64  K=64
+//     (i)   D_U += X16 x WT                    M=128 N=64  K=128
+//     (iii) D_O = X16 x QT + U16 x PP          M=128 N=64  K=128+64
+//     (ii)  D_S += U16 x KH                    M=128 N=128 K=64
 //
-// Warp roles (12 warps): 0 TMA producer, 1 MMA issuer (+ TMEM allocation),
-// 2-3 triangular solve (one column of T per thread), 4-7 "prep" warpgroup
-// (decay cumsum, operand tiles, Gram readout), 8-11 "state" warpgroup (W
-// conversion, U conversion, outputs, state rescale, snapshots).  Roles hand
-// work to each other through mbarriers; every wait is bounded.
+// Warp roles (16 warps): 0 TMA producer, 1 MMA issuer (+ TMEM allocation),
+// 2-3 the 16x16 diagonal-block inverses, 4-7 "prep" warpgroup (decay cumsum,
+// operand tiles, Gram readout), 8-11 "state" warpgroup (W and U conversion,
+// outputs, state rescale, snapshots), 12-15 "tri" warpgroup (readout of the
+// four inverse products).  Roles hand work to each other through mbarriers;
+// every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -53,90 +64,141 @@ namespace kda {
 namespace {
 using namespace sm100;
 
-constexpr int C = 64;     // chunk length
-constexpr int QR = 16;    // token rows per input slot
-constexpr int NTHREADS = 384;
+constexpr int C = 64;   // chunk length
+constexpr int QR = 16;  // token rows per input slot
+constexpr int NTHREADS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxExp2 = 15.0f;  // |g - ref| bound (log2 units) for fp16 operands
 
-// TMEM column map (512 columns allocated)
-constexpr uint32_t TM_S = 0, TM_X16 = 128, TM_U = 192, TM_U16 = 256, TM_O = 288, TM_G = 352, TM_W = 416,
-                   TM_V16 = 480;
-
-// MN-major descriptors: which field carries the stride between 64-element
-// atoms along M/N (the other carries the 1024-byte stride between 8-row groups).
-constexpr bool kMnAtomInLbo = true;
+// TMEM column map (512 columns allocated).  The fp16 U operand is written over
+// the first 32 columns of the U accumulator once that has been read out; V16
+// (the fp16 v^T operand) is double-buffered by chunk parity.
+constexpr uint32_t TM_S = 0, TM_X16 = 128, TM_U = 192, TM_U16 = 192, TM_O = 256, TM_G = 320, TM_W = 384,
+                   TM_V16 = 448;
 
 template <typename Tin>
 struct Cfg {
     static constexpr int ES = sizeof(Tin);
     static constexpr int NSLOT = ES == 2 ? 3 : 2;
+    static constexpr int NPP = ES == 2 ? 2 : 1;  // P buffers (fp32 inputs trade overlap for smem)
     static constexpr uint32_t SLOT_Q = 0;
     static constexpr uint32_t SLOT_K = QR * 128 * ES;
     static constexpr uint32_t SLOT_V = 2 * QR * 128 * ES;
     static constexpr uint32_t SLOT_LA = 3 * QR * 128 * ES;
     static constexpr uint32_t SLOT_BYTES = 3 * QR * 128 * ES + QR * 128 * 4;
     // shared memory map (offsets from a 1024-byte aligned base)
-    static constexpr uint32_t OFF_KQ = 0;            // [2] x (KT 16K | QT 16K)
-    static constexpr uint32_t OFF_KH = 65536;        // [2] x 16K
-    static constexpr uint32_t OFF_PP = 98304;        // [2] x 8K
-    static constexpr uint32_t OFF_TT = 114688;       // 8K
-    static constexpr uint32_t OFF_WT = 122880;       // 16K
-    static constexpr uint32_t OFF_AS = 139264;       // fp32 [64][68]
-    static constexpr uint32_t AS_STRIDE = 68;
-    static constexpr uint32_t OFF_RING = OFF_AS + 64 * AS_STRIDE * 4;  // 156672
+    static constexpr uint32_t OFF_KQ = 0;                    // [2] x (KT 16K | QT 16K)
+    static constexpr uint32_t OFF_KH = 65536;                // [2] x 16K
+    static constexpr uint32_t OFF_PP = 98304;                // [NPP] x 8K
+    static constexpr uint32_t OFF_WT = OFF_PP + NPP * 8192;  // 16K
+    static constexpr uint32_t OFF_DT = OFF_WT + 16384;       // 8K
+    static constexpr uint32_t OFF_B1 = OFF_DT + 8192;        // 8K
+    static constexpr uint32_t OFF_NR = OFF_B1 + 8192;        // 8K
+    static constexpr uint32_t OFF_LDG = OFF_NR + 8192;       // fp32 [4][16][17]
+    static constexpr uint32_t OFF_DFP = OFF_LDG + 4 * 16 * 17 * 4;  // fp32 [4][16][16]
+    static constexpr uint32_t OFF_RING = OFF_DFP + 4 * 16 * 16 * 4;
     static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[2][128], b[2][128]
-    static constexpr uint32_t OFF_BETA = OFF_VEC + 4 * 128 * 4;         // [2][64]
-    static constexpr uint32_t OFF_BAR = OFF_BETA + 2 * 64 * 4;
-    static constexpr uint32_t NBAR = 64;
+    static constexpr uint32_t OFF_BETA = OFF_VEC + 4 * 128 * 4;         // [4][64]
+    static constexpr uint32_t OFF_BAR = OFF_BETA + 4 * 64 * 4;
+    static constexpr uint32_t NBAR = 44;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 };
 static_assert(Cfg<__nv_bfloat16>::SMEM_BYTES <= 232448, "smem budget (bf16)");
 static_assert(Cfg<float>::SMEM_BYTES <= 232448, "smem budget (fp32)");
+static_assert(Cfg<__nv_bfloat16>::OFF_RING % 128 == 0 && Cfg<float>::OFF_RING % 128 == 0, "TMA destinations");
 
 // barrier indices
 enum {
-    B_FULL = 0,       // [NSLOT] (up to 3)
-    B_EMPTY = 4,      // [NSLOT]
-    B_PREPD = 8,      // [2] prep outputs (KT/QT/KH, vectors, beta) of a chunk ready
-    B_VRDY = 10,      // V16 written
-    B_GDONE = 11,     // Gram complete
-    B_P2D = 12,       // Gram read out (A scratch, PP written; D_G free)
-    B_AFREE = 13,     // solver finished reading the A scratch
-    B_TRDY = 14,      // TT written
-    B_WYDONE = 15,    // WY products complete
-    B_WRDY = 16,      // WT written, D_W free
-    B_XRDY = 17,      // X16 / D_S ready for the chunk
-    B_UIDONE = 18,    // (i) and (iii-a) complete
-    B_URDY = 19,      // U16 written, D_U free
-    B_SDONE = 20,     // (ii) and (iii-b) complete
-    B_KQFREE = 21,    // [2] chunk's KT/QT/KH/PP buffers free again
-    B_OFREE = 23,     // D_O read out
-    B_VFREE = 24,     // [2] vector buffers free again
-    B_DRAIN = 26,     // MMA drain on abort
-    B_COUNT = 27
+    B_FULL = 0,     // [NSLOT] input slot landed
+    B_EMPTY = 3,    // [NSLOT] input slot consumed
+    B_PREPD = 6,    // [2] KT/QT/KH, vectors, beta of a chunk ready
+    B_GDONE = 9,    // Gram complete
+    B_P2D = 10,     // Gram read out: D_G free; A blocks, A_o and P written
+    B_AFREE = 11,   // diagonal-block inverses done reading their input
+    B_DRDY = 12,    // DT and the fp32 diagonal inverses written
+    B_S1D = 13, B_C1 = 14, B_S2D = 15, B_C2 = 16, B_S3D = 17, B_C3 = 18,  // inverse products / readouts
+    B_TDONE = 19,   // last inverse product complete
+    B_TRDY = 20,    // T diag(beta) written
+    B_WYDONE = 21,  // WY products complete
+    B_WRDY = 22,    // WT written, D_W free
+    B_XRDY = 23,    // X16 / D_S ready for the chunk
+    B_UIDONE = 24,  // (i) and (iii-a) complete
+    B_URDY = 25,    // U16 written, D_U free
+    B_SDONE = 26,   // (ii) and (iii-b) complete
+    B_KQFREE = 27,  // [2] chunk's KT/QT/KH/PP buffers free again
+    B_OFREE = 29,   // D_O read out
+    B_VFREE = 30,   // [2] vector buffers free again
+    B_BFULL = 33,   // [4] beta of a chunk loaded (ring of 4, by chunk index mod 4)
+    B_STG = 37,     // output staging tile written by the whole state warpgroup
+    B_STGR = 38,    // output staging buffer free again (thread 0 -> state warpgroup)
+    B_BFREE = 39,   // [4] beta ring slot read by all its users
+    B_COUNT = 43
 };
 
+#ifdef KDA_TRACE
+// Debug timeline (compiled only with -DKDA_TRACE): clock64 stamps of each
+// role's milestones for the first 64 chunks of CTA 0.
+constexpr int kTrEv = 40;
+__device__ unsigned long long g_trace[64 * kTrEv];
+#define KDA_TR(n, ev)                                                                                    \
+    do {                                                                                                 \
+        if (blockIdx.x == 0 && (n) < 64) g_trace[(n) * kTrEv + (ev)] = (unsigned long long)clock64(); \
+    } while (0)
+#else
+#define KDA_TR(n, ev) \
+    do {              \
+    } while (0)
+#endif
 
 __device__ __forceinline__ float ld_in(const __nv_bfloat16* s, uint32_t idx) { return __bfloat162float(s[idx]); }
 __device__ __forceinline__ float ld_in(const float* s, uint32_t idx) { return s[idx]; }
+
+// Writes 64 fp32 values (r0: columns 0..31, r1: 32..63) as one 128-byte
+// swizzled fp16 row.
+__device__ __forceinline__ void store_row16(uint8_t* tile, uint32_t row, const uint32_t (&r0)[32],
+                                            const uint32_t (&r1)[32]) {
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16) {
+        const uint32_t* s = c16 < 4 ? &r0[8 * c16] : &r1[8 * (c16 - 4)];
+        *reinterpret_cast<uint4*>(tile + sw128(row, c16)) =
+            make_uint4(pack_half2(__uint_as_float(s[0]), __uint_as_float(s[1])),
+                       pack_half2(__uint_as_float(s[2]), __uint_as_float(s[3])),
+                       pack_half2(__uint_as_float(s[4]), __uint_as_float(s[5])),
+                       pack_half2(__uint_as_float(s[6]), __uint_as_float(s[7])));
+    }
+}
+
+// Adds the 16 values `d` to columns 16a .. 16a+15 of a 64-wide row held as (r0, r1).
+__device__ __forceinline__ void add_block16(uint32_t (&r0)[32], uint32_t (&r1)[32], int a, const float* d) {
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float dm = d[m];
+#pragma unroll
+        for (int aa = 0; aa < 4; ++aa)
+            if (aa == a) {
+                uint32_t& e = aa < 2 ? r0[16 * aa + m] : r1[16 * (aa - 2) + m];
+                e = __float_as_uint(__uint_as_float(e) + dm);
+            }
+    }
+}
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(NTHREADS, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
-                 const SeqProblem P) {
+                 const __grid_constant__ CUtensorMap tm_out, const SeqProblem P) {
     using L = Cfg<Tin>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
     Abort* ab = reinterpret_cast<Abort*>(sm + L::OFF_MISC + 16);
-    float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);            // [2][128]
-    float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 1024);     // [2][128]
-    float* sbeta = reinterpret_cast<float*>(sm + L::OFF_BETA);           // [2][64]
-    float* ascr = reinterpret_cast<float*>(sm + L::OFF_AS);
+    float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);         // [2][128]
+    float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 1024);  // [2][128]
+    float* sbeta = reinterpret_cast<float*>(sm + L::OFF_BETA);        // [4][64]
+    float* ldg = reinterpret_cast<float*>(sm + L::OFF_LDG);           // [4][16][17] diagonal blocks of A
+    float* dfp = reinterpret_cast<float*>(sm + L::OFF_DFP);           // [4][16][16] their inverses
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x;
@@ -157,25 +219,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&bar[B_FULL + i], 1);
             mbar_init(&bar[B_EMPTY + i], 128);
         }
-        mbar_init(&bar[B_PREPD], 128);
-        mbar_init(&bar[B_PREPD + 1], 128);
-        mbar_init(&bar[B_VRDY], 128);
-        mbar_init(&bar[B_GDONE], 1);
-        mbar_init(&bar[B_P2D], 128);
+        const int c128[] = {B_PREPD, B_PREPD + 1, B_P2D, B_C1, B_C2, B_C3, B_TRDY, B_WRDY, B_XRDY, B_URDY,
+                            B_OFREE, B_VFREE, B_VFREE + 1};
+        for (int i : c128) mbar_init(&bar[i], 128);
+        const int c1[] = {B_GDONE, B_S1D, B_S2D, B_S3D, B_TDONE, B_WYDONE, B_UIDONE, B_SDONE, B_KQFREE, B_KQFREE + 1};
+        for (int i : c1) mbar_init(&bar[i], 1);
         mbar_init(&bar[B_AFREE], 64);
-        mbar_init(&bar[B_TRDY], 64);
-        mbar_init(&bar[B_WYDONE], 1);
-        mbar_init(&bar[B_WRDY], 128);
-        mbar_init(&bar[B_XRDY], 128);
-        mbar_init(&bar[B_UIDONE], 1);
-        mbar_init(&bar[B_URDY], 128);
-        mbar_init(&bar[B_SDONE], 1);
-        mbar_init(&bar[B_KQFREE], 1);
-        mbar_init(&bar[B_KQFREE + 1], 1);
-        mbar_init(&bar[B_OFREE], 128);
-        mbar_init(&bar[B_VFREE], 128);
-        mbar_init(&bar[B_VFREE + 1], 128);
-        mbar_init(&bar[B_DRAIN], 1);
+        mbar_init(&bar[B_DRDY], 64);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&bar[B_BFULL + i], 32);
+            mbar_init(&bar[B_BFREE + i], 64 + 128);
+        }
+        mbar_init(&bar[B_STG], 128);
+        mbar_init(&bar[B_STGR], 1);
         ab->flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -187,15 +243,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int* status = P.status;
 
     const uint32_t sm_base = smem_u32(sm);
-    auto mn_desc = [&](uint32_t addr, uint32_t atom_stride) -> uint64_t {
-        return kMnAtomInLbo ? sdesc(addr, atom_stride, 1024) : sdesc(addr, 1024, atom_stride);
-    };
+    // MN-major operand: the stride between 64-element atoms along M/N goes in
+    // the leading-byte-offset field, the 1024-byte stride between 8-row groups
+    // in the stride field.  K-major operand: only the 8-row group stride.
+    auto mn_desc = [&](uint32_t addr, uint32_t atom_stride) -> uint64_t { return sdesc(addr, atom_stride, 1024); };
     auto k_desc = [&](uint32_t addr) -> uint64_t { return sdesc(addr, 16, 1024); };
+    constexpr uint32_t ID_G = idesc_f16(128, 64, 1, 1);
+    constexpr uint32_t ID_MN = idesc_f16(128, 64, 0, 1);
+    constexpr uint32_t ID_KK = idesc_f16(128, 64, 0, 0);
+    constexpr uint32_t ID_S = idesc_f16(128, 128, 0, 0);
+    constexpr uint32_t ID_T1 = idesc_f16(64, 64, 1, 1);
+    constexpr uint32_t ID_T2 = idesc_f16(64, 64, 0, 1);
+    constexpr uint32_t ID_T3 = idesc_f16(64, 64, 0, 0);
+    const uint32_t sdt = sm_base + L::OFF_DT, sb1 = sm_base + L::OFF_B1, snr = sm_base + L::OFF_NR;
+    // Every product group is issued by thread 0 of the role that completes its last
+    // input, after waiting for that input and for the previous reader of its
+    // accumulator; the commits below are what the other roles wait on.
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_la);
+            prefetch_tmap(&tm_out);
             int issued = 0;
             bool ok = true;
             for (int n = 0; n < nch && ok; ++n)
@@ -209,6 +278,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tma_load_3d(slot + L::SLOT_K, &tm_k, &bar[B_FULL + sl], 0, h, z);
                     tma_load_3d(slot + L::SLOT_V, &tm_v, &bar[B_FULL + sl], 0, h, z);
                     tma_load_3d(slot + L::SLOT_LA, &tm_la, &bar[B_FULL + sl], 0, h, z);
+                    KDA_TR(n, 32 + q);
                     ++issued;
                 }
             if (!ok) {  // let the copies already issued land before the CTA can exit
@@ -221,136 +291,83 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t ID_G = idesc_f16(128, 64, 1, 1);
-            constexpr uint32_t ID_MN = idesc_f16(128, 64, 0, 1);
-            constexpr uint32_t ID_S = idesc_f16(128, 128, 0, 0);
-            constexpr uint32_t ID_P = idesc_f16(128, 64, 0, 0);
-            auto gram = [&](int n) {
-                const uint32_t kq = sm_base + L::OFF_KQ + (n & 1) * 32768, kh = sm_base + L::OFF_KH + (n & 1) * 16384;
-                for (int st = 0; st < 8; ++st)
-                    mma_ss(tmem + TM_G, mn_desc(kq + st * 2048, 16384), mn_desc(kh + st * 2048, 8192), ID_G, st > 0);
-                mma_commit(&bar[B_GDONE]);
-            };
-            bool ok = mbar_wait(&bar[B_PREPD], 0, ab, status);
-            if (ok) { tc_fence_after(); gram(0); }
-            for (int n = 0; n < nch && ok; ++n) {
-                const int b = n & 1;
-                // B(n): Gram of the next chunk
-                if (n + 1 < nch) {
-                    if (!(ok = mbar_wait(&bar[B_PREPD + ((n + 1) & 1)], ((n + 1) >> 1) & 1, ab, status))) break;
-                    if (!(ok = mbar_wait(&bar[B_P2D], n & 1, ab, status))) break;
-                    tc_fence_after();
-                    gram(n + 1);
-                }
-                // A(n): WY products
-                if (!(ok = mbar_wait(&bar[B_TRDY], n & 1, ab, status))) break;
-                if (!(ok = mbar_wait(&bar[B_VRDY], n & 1, ab, status))) break;
-                tc_fence_after();
-                {
-                    const uint32_t kt = sm_base + L::OFF_KQ + b * 32768, tt = sm_base + L::OFF_TT;
-                    for (int st = 0; st < 4; ++st) {
-                        const uint64_t bd = mn_desc(tt + st * 2048, 8192);
-                        mma_ss(tmem + TM_W, k_desc(kt + st * 32), bd, ID_MN, st > 0);
-                        mma_ts(tmem + TM_U, tmem + TM_V16 + st * 8, bd, ID_MN, st > 0);
-                    }
-                    mma_commit(&bar[B_WYDONE]);
-                }
-                // C(n): U = U' - W S0 and O = Qtil S0
-                if (!(ok = mbar_wait(&bar[B_WRDY], n & 1, ab, status))) break;
-                if (!(ok = mbar_wait(&bar[B_XRDY], n & 1, ab, status))) break;
-                if (n > 0 && !(ok = mbar_wait(&bar[B_OFREE], (n - 1) & 1, ab, status))) break;
-                tc_fence_after();
-                {
-                    const uint32_t wt = sm_base + L::OFF_WT, qt = sm_base + L::OFF_KQ + b * 32768 + 16384;
-                    for (int st = 0; st < 8; ++st)
-                        mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, mn_desc(wt + st * 2048, 8192), ID_MN, 1);
-                    for (int st = 0; st < 8; ++st)
-                        mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, mn_desc(qt + st * 2048, 8192), ID_MN, st > 0);
-                    mma_commit(&bar[B_UIDONE]);
-                }
-                // D(n): state update and the intra-chunk part of the output
-                if (!(ok = mbar_wait(&bar[B_URDY], n & 1, ab, status))) break;
-                tc_fence_after();
-                {
-                    const uint32_t kh = sm_base + L::OFF_KH + b * 16384, pp = sm_base + L::OFF_PP + b * 8192;
-                    for (int st = 0; st < 4; ++st)
-                        mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, k_desc(kh + st * 32), ID_S, 1);
-                    for (int st = 0; st < 4; ++st)
-                        mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, k_desc(pp + st * 32), ID_P, 1);
-                    mma_commit(&bar[B_SDONE]);
-                    mma_commit(&bar[B_KQFREE + b]);
-                }
-            }
-            if (!ok) {  // wait for every MMA already issued before the CTA can release TMEM
-                mma_commit(&bar[B_DRAIN]);
-                const long long tstart = clock64();
-                while (!mbar_try_wait(&bar[B_DRAIN], 0) && clock64() - tstart < kWaitCycles) {
-                }
-            }
+        // ------------------------------------------------------------ beta loader
+        // beta of chunk m into ring slot m % 4 (0 past the sequence end).  Plain loads in a
+        // warp of their own, so that no other role's barrier arrive or proxy fence waits on
+        // them.  (This warp also owns the TMEM allocation.)
+        for (int m = 0; m < nch; ++m) {
+            const int k4 = m & 3;
+            if (m >= 4 && !mbar_wait(&bar[B_BFREE + k4], ((m - 4) >> 2) & 1, ab, status)) break;
+            const int64_t vld = len - (int64_t)C * m;
+            for (int i = lane; i < C; i += 32)
+                sbeta[k4 * 64 + i] = i < vld ? P.beta[(size_t)(t0 + (int64_t)C * m + i) * P.H + h] : 0.f;
+            mbar_arrive(&bar[B_BFULL + k4]);
         }
     } else if (warp < 4) {
-        // ------------------------------------------------------------ triangular solve
-        // Thread j owns column j of T = (I + A)^-1 (A strictly lower triangular):
-        // x_j = 1, x_r = -sum_{i<r} A[r][i] x_i for r > j, x_r = 0 for r < j.
-        const int j = tid - 64;
+        // ------------------------------------------------------------ 16x16 diagonal-block inverses
+        // Thread (a, jj) solves column jj of (I + A_aa)^-1 by right-looking substitution.
+        const int t = tid - 64, a = t >> 4, jj = t & 15;
+        const float* blk = ldg + a * 16 * 17;
         for (int n = 0; n < nch; ++n) {
             if (!mbar_wait(&bar[B_P2D], n & 1, ab, status)) break;
-            float x[C];
+            float x[16];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float acc = 0.f;
-                const float4* row = reinterpret_cast<const float4*>(ascr + r * L::AS_STRIDE);
+            for (int i = 0; i < 16; ++i) x[i] = 0.f;
 #pragma unroll
-                for (int i4 = 0; i4 < (r + 3) / 4; ++i4) {
-                    const float4 a = row[i4];
-                    acc += a.x * x[4 * i4];
-                    if (4 * i4 + 1 < r) acc += a.y * x[4 * i4 + 1];
-                    if (4 * i4 + 2 < r) acc += a.z * x[4 * i4 + 2];
-                    if (4 * i4 + 3 < r) acc += a.w * x[4 * i4 + 3];
-                }
-                x[r] = (r == j) ? 1.f : (r > j ? -acc : 0.f);
+            for (int r = 0; r < 16; ++r) {
+                const float xr = (r == jj) ? 1.f : (r > jj ? x[r] : 0.f);
+                x[r] = xr;
+#pragma unroll
+                for (int i = r + 1; i < 16; ++i) x[i] -= blk[i * 17 + r] * xr;
             }
             mbar_arrive(&bar[B_AFREE]);
-            if (n > 0 && !mbar_wait(&bar[B_WYDONE], (n - 1) & 1, ab, status)) break;
-            const float bj = sbeta[(n & 1) * 64 + j];
-            uint8_t* tt = sm + L::OFF_TT;
+            if (n > 0 && !mbar_wait(&bar[B_TRDY], (n - 1) & 1, ab, status)) break;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dfp[(a * 16 + i) * 16 + jj] = x[i];
+            uint8_t* dt = sm + L::OFF_DT;  // row (16a + jj) holds column 16a+jj of Dg
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16) {
-                uint4 w;
-                w.x = pack_half2(x[8 * c16 + 0] * bj, x[8 * c16 + 1] * bj);
-                w.y = pack_half2(x[8 * c16 + 2] * bj, x[8 * c16 + 3] * bj);
-                w.z = pack_half2(x[8 * c16 + 4] * bj, x[8 * c16 + 5] * bj);
-                w.w = pack_half2(x[8 * c16 + 6] * bj, x[8 * c16 + 7] * bj);
-                *reinterpret_cast<uint4*>(tt + sw128(j, c16)) = w;
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (c16 == 2 * a)
+                    w = make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
+                                   pack_half2(x[6], x[7]));
+                if (c16 == 2 * a + 1)
+                    w = make_uint4(pack_half2(x[8], x[9]), pack_half2(x[10], x[11]), pack_half2(x[12], x[13]),
+                                   pack_half2(x[14], x[15]));
+                *reinterpret_cast<uint4*>(dt + sw128(16 * a + jj, c16)) = w;
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bar[B_TRDY]);
+            mbar_arrive(&bar[B_DRDY]);
+            KDA_TR(n, 7);
+            if (t == 0) {  // S1: D_W = Dg A_o, once D_W's previous contents (W of chunk n-1) were read
+                if (!mbar_wait(&bar[B_DRDY], n & 1, ab, status)) break;
+                if (n > 0 && !mbar_wait(&bar[B_WRDY], (n - 1) & 1, ab, status)) break;
+                tc_fence_after();
+                for (int st = 0; st < 4; ++st)
+                    mma_ss(tmem + TM_W, mn_desc(sdt + st * 2048, 8192), mn_desc(sb1 + st * 2048, 8192), ID_T1, st > 0);
+                mma_commit(&bar[B_S1D]);
+                KDA_TR(n, 12);
+            }
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------ prep warpgroup
         const int c = tid - 128;  // key channel (and TMEM lane) of this thread
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        bool range_bad = false;
-        uint32_t v16[32];  // this channel's 64 values of v as packed fp16 (V16 row c)
-        float beta_next = 0.f;
-        auto load_beta = [&](int n) -> float {
-            const int64_t vld = len - (int64_t)C * n;
-            return (c < 64 && c < vld) ? P.beta[(size_t)(t0 + (int64_t)C * n + c) * P.H + h] : 0.f;
-        };
-        beta_next = load_beta(0);
+        float max_x = 0.f;  // largest |g - ref| seen (log2 units), for the range check
 
-        // prep1(n): decay cumsum, operand tiles KT/QT/KH, vectors, beta.
+        // prep1(n): decay cumsum, operand tiles KT/QT/KH, V16, vectors, beta.
+        // Rows past the end of a sequence get log alpha = 0 and k = 0 (their beta
+        // is 0 too), which makes them identity steps; q and v of such rows only
+        // reach outputs that are never stored.
         auto prep1 = [&](int n) -> bool {
             const int b = n & 1;
+            if (c == 0) KDA_TR(n, 0);
             if (n >= 2) {
                 if (!mbar_wait(&bar[B_KQFREE + b], ((n - 2) >> 1) & 1, ab, status)) return false;
                 if (!mbar_wait(&bar[B_VFREE + b], ((n - 2) >> 1) & 1, ab, status)) return false;
             }
+            tc_fence_after();  // V16[b] was last read by the WY product of chunk n - 2
             const int valid = (int)((len - (int64_t)C * n) < C ? (len - (int64_t)C * n) : C);
-            if (c < 64) sbeta[b * 64 + c] = beta_next;
-            if (n + 1 < nch) beta_next = load_beta(n + 1);
             uint8_t* kt = sm + L::OFF_KQ + b * 32768;
             uint8_t* qt = kt + 16384;
             uint8_t* kh = sm + L::OFF_KH + b * 16384;
@@ -361,6 +378,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             };
             // pass A over rows 0..31: the reference ref = g_31
             if (!wait_slot(0) || !wait_slot(1)) return false;
+            if (c == 0) KDA_TR(n, 1);
             float g2 = 0.f;
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
@@ -369,140 +387,175 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 g2 += (r < valid) ? la * kLog2e : 0.f;
             }
             const float ref = g2;
-            // pass B: operand rows
+            // pass B, one 16-row quarter at a time
             g2 = 0.f;
-            uint32_t pk[4], pq[4], ph[4];
-            float kprev = 0.f, qprev = 0.f, hprev = 0.f, vprev = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                if (q >= 2 && !wait_slot(q)) return false;
+                if (c == 0) KDA_TR(n, 34 + q);
+                const uint8_t* sl = slot_ptr(q);
+                const float* sla = reinterpret_cast<const float*>(sl + L::SLOT_LA);
+                const Tin* sk = reinterpret_cast<const Tin*>(sl + L::SLOT_K);
+                const Tin* sq = reinterpret_cast<const Tin*>(sl + L::SLOT_Q);
+                const Tin* sv = reinterpret_cast<const Tin*>(sl + L::SLOT_V);
+                const int vq = valid - QR * q;  // rows of this quarter inside the sequence
+                uint32_t pk[8], pq[8], ph[8], pv[8];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                if (r == 32) {  // rows 0..31 consumed: release their slots, fetch rows 32..47
-                    mbar_arrive(&bar[B_EMPTY + (4 * n + 0) % L::NSLOT]);
-                    mbar_arrive(&bar[B_EMPTY + (4 * n + 1) % L::NSLOT]);
-                    if (!wait_slot(2)) return false;
+                for (int rp = 0; rp < QR / 2; ++rp) {
+                    float kv2[2], qv2[2], hv2[2], vv2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int rr = 2 * rp + e;
+                        const bool on = rr < vq;
+                        const float la = on ? sla[rr * 128 + c] : 0.f;
+                        const float kk = on ? ld_in(sk, rr * 128 + c) : 0.f;
+                        const float qq = ld_in(sq, rr * 128 + c);
+                        vv2[e] = ld_in(sv, rr * 128 + c);
+                        g2 = fmaf(la, kLog2e, g2);
+                        const float x = g2 - ref;
+                        max_x = fmaxf(max_x, fabsf(x));
+                        const float e1 = fast_exp2(x), e2 = fast_exp2(-x);
+                        kv2[e] = kk * e1;
+                        qv2[e] = qq * e1;
+                        hv2[e] = kk * e2;
+                    }
+                    pk[rp] = pack_half2(kv2[0], kv2[1]);
+                    pq[rp] = pack_half2(qv2[0], qv2[1]);
+                    ph[rp] = pack_half2(hv2[0], hv2[1]);
+                    pv[rp] = pack_half2(vv2[0], vv2[1]);
                 }
-                if (r == 48) {
-                    mbar_arrive(&bar[B_EMPTY + (4 * n + 2) % L::NSLOT]);
-                    if (!wait_slot(3)) return false;
+                mbar_arrive(&bar[B_EMPTY + (4 * n + q) % L::NSLOT]);
+#pragma unroll
+                for (int g8 = 0; g8 < 2; ++g8) {
+                    const uint32_t off = sw128(c, 2 * q + g8);
+                    *reinterpret_cast<uint4*>(kt + off) = make_uint4(pk[4 * g8], pk[4 * g8 + 1], pk[4 * g8 + 2], pk[4 * g8 + 3]);
+                    *reinterpret_cast<uint4*>(qt + off) = make_uint4(pq[4 * g8], pq[4 * g8 + 1], pq[4 * g8 + 2], pq[4 * g8 + 3]);
+                    *reinterpret_cast<uint4*>(kh + off) = make_uint4(ph[4 * g8], ph[4 * g8 + 1], ph[4 * g8 + 2], ph[4 * g8 + 3]);
                 }
-                const uint8_t* sl = slot_ptr(r >> 4);
-                const int rr = r & 15;
-                const bool on = r < valid;
-                const float la = on ? reinterpret_cast<const float*>(sl + L::SLOT_LA)[rr * 128 + c] : 0.f;
-                const float kk = on ? ld_in(reinterpret_cast<const Tin*>(sl + L::SLOT_K), rr * 128 + c) : 0.f;
-                const float qq = on ? ld_in(reinterpret_cast<const Tin*>(sl + L::SLOT_Q), rr * 128 + c) : 0.f;
-                const float vv = on ? ld_in(reinterpret_cast<const Tin*>(sl + L::SLOT_V), rr * 128 + c) : 0.f;
-                g2 += la * kLog2e;
-                const float x = g2 - ref;
-                range_bad |= fabsf(x) > kMaxExp2;
-                const float e1 = exp2f(x), e2 = exp2f(-x);
-                const float kv = kk * e1, qv = qq * e1, hv = kk * e2;
-                if (r & 1) {
-                    pk[(r >> 1) & 3] = pack_half2(kprev, kv);
-                    pq[(r >> 1) & 3] = pack_half2(qprev, qv);
-                    ph[(r >> 1) & 3] = pack_half2(hprev, hv);
-                    v16[r >> 1] = pack_half2(vprev, vv);
-                } else {
-                    kprev = kv; qprev = qv; hprev = hv; vprev = vv;
-                }
-                if ((r & 7) == 7) {
-                    const uint32_t off = sw128(c, r >> 3);
-                    *reinterpret_cast<uint4*>(kt + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4*>(qt + off) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
-                    *reinterpret_cast<uint4*>(kh + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                }
+                tmem_st8(tmem + lane_base + TM_V16 + b * 32 + q * 8, pv);
+                if (c == 0) KDA_TR(n, 22 + q);
             }
-            mbar_arrive(&bar[B_EMPTY + (4 * n + 3) % L::NSLOT]);
-            vec_a[b * 128 + c] = exp2f(ref);
-            vec_b[b * 128 + c] = exp2f(g2 - ref);
-            fence_proxy_async_smem();
-            mbar_arrive(&bar[B_PREPD + b]);
-            return true;
-        };
-        // prep2(n): V16 into TMEM once the previous chunk's WY product has read it
-        auto prep2 = [&](int n) -> bool {
-            if (n > 0 && !mbar_wait(&bar[B_WYDONE], (n - 1) & 1, ab, status)) return false;
-            tc_fence_after();
-            tmem_st32(tmem + lane_base + TM_V16, v16);
+            const float an = fast_exp2(ref);
+            vec_a[b * 128 + c] = an;
+            vec_b[b * 128 + c] = fast_exp2(g2 - ref);
             tmem_st_wait();
+            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bar[B_VRDY]);
+            mbar_arrive(&bar[B_PREPD + b]);
+            if (c == 0) {  // the Gram of this chunk, once all operand rows and D_G (read by P2(n-1)) are ready
+                KDA_TR(n, 2);
+                if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) return false;
+                if (n > 0 && !mbar_wait(&bar[B_P2D], (n - 1) & 1, ab, status)) return false;
+                tc_fence_after();
+                const uint32_t kq = sm_base + L::OFF_KQ + b * 32768, khb = sm_base + L::OFF_KH + b * 16384;
+                for (int st = 0; st < 8; ++st)
+                    mma_ss(tmem + TM_G, mn_desc(kq + st * 2048, 16384), mn_desc(khb + st * 2048, 8192), ID_G, st > 0);
+                mma_commit(&bar[B_GDONE]);
+                KDA_TR(n, 8);
+            }
             return true;
         };
-        // P2(n): read the Gram accumulator: A rows to the solver's scratch, P rows to PP
+        // P2(n): read the Gram accumulator.  Rows 0..63 (A, beta_r applied): the
+        // 16x16 diagonal blocks (fp32) and A_o (fp16); rows 64..127: P (fp16).
         auto p2 = [&](int n) -> bool {
             const int b = n & 1;
             if (!mbar_wait(&bar[B_GDONE], n & 1, ab, status)) return false;
+            if (!mbar_wait(&bar[B_BFULL + (n & 3)], (n >> 2) & 1, ab, status)) return false;
             tc_fence_after();
+            if (c == 0) KDA_TR(n, 3);
             uint32_t r0[32], r1[32];
             tmem_ld32(tmem + lane_base + TM_G, r0);
             tmem_ld32(tmem + lane_base + TM_G + 32, r1);
             tmem_ld_wait();
-            if (c < 64) {  // row r = c of A (beta_r applied here)
-                if (n > 0 && !mbar_wait(&bar[B_AFREE], (n - 1) & 1, ab, status)) return false;
-                const float br = sbeta[b * 64 + c];
-                float* row = ascr + c * L::AS_STRIDE;
-#pragma unroll
-                for (int i4 = 0; i4 < 16; ++i4) {
-                    float4 w;
-                    const uint32_t* src = i4 < 8 ? &r0[4 * i4] : &r1[4 * (i4 - 8)];
-                    w.x = (4 * i4 + 0 < c) ? br * __uint_as_float(src[0]) : 0.f;
-                    w.y = (4 * i4 + 1 < c) ? br * __uint_as_float(src[1]) : 0.f;
-                    w.z = (4 * i4 + 2 < c) ? br * __uint_as_float(src[2]) : 0.f;
-                    w.w = (4 * i4 + 3 < c) ? br * __uint_as_float(src[3]) : 0.f;
-                    reinterpret_cast<float4*>(row)[i4] = w;
+            if (c == 0) KDA_TR(n, 29);
+            if (c < 64) {  // row r = c of A
+                if (n > 0) {
+                    if (!mbar_wait(&bar[B_AFREE], (n - 1) & 1, ab, status)) return false;
+                    if (!mbar_wait(&bar[B_TDONE], (n - 1) & 1, ab, status)) return false;
                 }
+
+                const float br = c < len - (int64_t)C * n ? sbeta[(n & 3) * 64 + c] : 0.f;
+                const int a = c >> 4, i = c & 15;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    r0[e] = __float_as_uint(e < c ? br * __uint_as_float(r0[e]) : 0.f);
+                    r1[e] = __float_as_uint(e + 32 < c ? br * __uint_as_float(r1[e]) : 0.f);
+                }
+                // row i of diagonal block a: columns 16a .. 16a+15
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int aa = 0; aa < 4; ++aa)
+                        if (aa == a) v = __uint_as_float(aa < 2 ? r0[16 * aa + m] : r1[16 * (aa - 2) + m]);
+                    ldg[(a * 16 + i) * 17 + m] = v;
+                }
+
+                mbar_arrive(&bar[B_BFREE + (n & 3)]);
+                // A_o: keep the columns left of the diagonal block
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    if (e >= 16 * a) r0[e] = 0u;
+                    if (e + 32 >= 16 * a) r1[e] = 0u;
+                }
+                store_row16(sm + L::OFF_B1, c, r0, r1);
+                if (c == 0) KDA_TR(n, 26);
             } else {  // row r = c - 64 of P (lower triangle including the diagonal)
-                if (n >= 2 && !mbar_wait(&bar[B_KQFREE + b], ((n - 2) >> 1) & 1, ab, status)) return false;
-                const int r = c - 64;
-                uint8_t* pp = sm + L::OFF_PP + b * 8192;
-#pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = 8 * c16 + e;
-                        const uint32_t u = i < 32 ? r0[i] : r1[i - 32];
-                        f[e] = (i <= r) ? __uint_as_float(u) : 0.f;
-                    }
-                    *reinterpret_cast<uint4*>(pp + sw128(r, c16)) =
-                        make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
-                                   pack_half2(f[6], f[7]));
+                if (n >= L::NPP) {
+                    const int m = n - L::NPP;
+                    if (!mbar_wait(&bar[B_KQFREE + (m & 1)], (m >> 1) & 1, ab, status)) return false;
                 }
-                fence_proxy_async_smem();
+                const int r = c - 64;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    if (e > r) r0[e] = 0u;
+                    if (e + 32 > r) r1[e] = 0u;
+                }
+                store_row16(sm + L::OFF_PP + (n % L::NPP) * 8192, r, r0, r1);
             }
+            fence_proxy_async_smem();
+            if (c == 0) KDA_TR(n, 27);
             tc_fence_before();
             mbar_arrive(&bar[B_P2D]);
+            if (c == 0) KDA_TR(n, 4);
             return true;
         };
-        bool ok = prep1(0) && prep2(0) && p2(0);
-        for (int n = 0; n + 1 < nch && ok; ++n) ok = prep1(n + 1) && p2(n + 1) && prep2(n + 1);
-        if (range_bad) atomicCAS(status, 0, (int)KDA_STATUS_GATE_RANGE);
-    } else {
+        for (int n = 0; n < nch; ++n)
+            if (!prep1(n) || !p2(n)) break;
+        if (max_x > kMaxExp2) atomicCAS(status, 0, (int)KDA_STATUS_GATE_RANGE);
+    } else if (warp < 12) {
         // ------------------------------------------------------------ state warpgroup
         const int j = tid - 256;  // value column (and TMEM lane) of this thread
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         Tout* out = static_cast<Tout*>(P.out);
         bool ok = true;
+        // Staging buffer hand-offs within the warpgroup (every thread follows the same
+        // sequence, so the phase counters agree).  Thread 0 owns the bulk stores.
+        uint32_t ph_stg = 0, ph_rd = 0;
+        auto staging_free = [&](bool all_read) -> bool {  // wait until WT may be rewritten
+            if (j == 0) {
+                if (all_read) bulk_wait_read<0>(); else bulk_wait_read<1>();
+                mbar_arrive(&bar[B_STGR]);
+            }
+            return mbar_wait(&bar[B_STGR], (ph_rd++) & 1, ab, status);
+        };
         {  // X_0 = Diag(a_0) S_0 into D_S and X16
             if (!(ok = mbar_wait(&bar[B_PREPD], 0, ab, status))) goto state_done;
-            const float* a0 = vec_a;
-            uint32_t x16[64];
-#pragma unroll
+#pragma unroll 1
             for (int piece = 0; piece < 4; ++piece) {
-                uint32_t xs[32];
+                uint32_t xs[32], x16[16];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int cc = piece * 32 + e;
                     const float s0 = P.init ? P.init[sbase + (size_t)cc * kD + j] : 0.f;
-                    xs[e] = __float_as_uint(s0 * a0[cc]);
+                    xs[e] = __float_as_uint(s0 * vec_a[cc]);
                 }
-                tmem_st32(tmem + lane_base + TM_S + piece * 32, xs);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    x16[piece * 16 + e] = pack_half2(__uint_as_float(xs[2 * e]), __uint_as_float(xs[2 * e + 1]));
+                    x16[e] = pack_half2(__uint_as_float(xs[2 * e]), __uint_as_float(xs[2 * e + 1]));
+                tmem_st32(tmem + lane_base + TM_S + piece * 32, xs);
+                tmem_st16(tmem + lane_base + TM_X16 + piece * 16, x16);
             }
-            tmem_st32(tmem + lane_base + TM_X16, *reinterpret_cast<uint32_t(*)[32]>(&x16[0]));
-            tmem_st32(tmem + lane_base + TM_X16 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x16[32]));
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar[B_XRDY]);
@@ -510,31 +563,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int n = 0; n < nch; ++n) {
             const int b = n & 1;
             const int valid = (int)((len - (int64_t)C * n) < C ? (len - (int64_t)C * n) : C);
-            // P4(n): WT = -W^T as fp16
+            // P4(n): WT = -W^T as fp16 (WT also stages the previous chunk's outputs)
+            if (!(ok = staging_free(true))) break;
             if (!(ok = mbar_wait(&bar[B_WYDONE], n & 1, ab, status))) break;
             tc_fence_after();
+            if (j == 0) KDA_TR(n, 16);
             {
                 uint32_t r0[32], r1[32];
                 tmem_ld32(tmem + lane_base + TM_W, r0);
                 tmem_ld32(tmem + lane_base + TM_W + 32, r1);
                 tmem_ld_wait();
-                uint8_t* wt = sm + L::OFF_WT;
 #pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16) {
-                    const uint32_t* src = c16 < 4 ? &r0[8 * c16] : &r1[8 * (c16 - 4)];
-                    *reinterpret_cast<uint4*>(wt + sw128(j, c16)) = make_uint4(
-                        pack_half2(-__uint_as_float(src[0]), -__uint_as_float(src[1])),
-                        pack_half2(-__uint_as_float(src[2]), -__uint_as_float(src[3])),
-                        pack_half2(-__uint_as_float(src[4]), -__uint_as_float(src[5])),
-                        pack_half2(-__uint_as_float(src[6]), -__uint_as_float(src[7])));
+                for (int e = 0; e < 32; ++e) {
+                    r0[e] ^= 0x80000000u;
+                    r1[e] ^= 0x80000000u;
                 }
+                store_row16(sm + L::OFF_WT, j, r0, r1);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&bar[B_WRDY]);
+                if (j == 0) {  // C: U = U' - W S0 and O = Qtil S0
+                    KDA_TR(n, 17);
+                    if (!(ok = mbar_wait(&bar[B_WRDY], n & 1, ab, status))) break;
+                    if (!(ok = mbar_wait(&bar[B_XRDY], n & 1, ab, status))) break;
+                    if (n > 0 && !(ok = mbar_wait(&bar[B_OFREE], (n - 1) & 1, ab, status))) break;
+                    tc_fence_after();
+                    const uint32_t wt = sm_base + L::OFF_WT, qt = sm_base + L::OFF_KQ + (n & 1) * 32768 + 16384;
+                    for (int st = 0; st < 8; ++st)
+                        mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, mn_desc(wt + st * 2048, 8192), ID_MN, 1);
+                    for (int st = 0; st < 8; ++st)
+                        mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, mn_desc(qt + st * 2048, 8192), ID_MN, st > 0);
+                    mma_commit(&bar[B_UIDONE]);
+                    KDA_TR(n, 10);
+                }
             }
             // S2(n): U16 = fp16(U^T)
             if (!(ok = mbar_wait(&bar[B_UIDONE], n & 1, ab, status))) break;
             tc_fence_after();
+            if (j == 0) KDA_TR(n, 18);
             {
                 uint32_t r0[32], r1[32], u16[32];
                 tmem_ld32(tmem + lane_base + TM_U, r0);
@@ -549,80 +615,273 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bar[B_URDY]);
+                if (j == 0) {  // D: state update and the intra-chunk part of the output
+                    if (!(ok = mbar_wait(&bar[B_URDY], n & 1, ab, status))) break;
+                    tc_fence_after();
+                    const uint32_t kh = sm_base + L::OFF_KH + b * 16384, pp = sm_base + L::OFF_PP + (n % L::NPP) * 8192;
+                    for (int st = 0; st < 4; ++st)
+                        mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, k_desc(kh + st * 32), ID_S, 1);
+                    for (int st = 0; st < 4; ++st)
+                        mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, k_desc(pp + st * 32), ID_KK, 1);
+                    mma_commit(&bar[B_SDONE]);
+                    mma_commit(&bar[B_KQFREE + b]);
+                    KDA_TR(n, 11);
+                }
+                if (j == 0) KDA_TR(n, 19);
             }
-            // S3(n): outputs, state, snapshots, next X
+            // S3(n): outputs and state.  Order: rows 0..31 of the output (staged and
+            // stored), the state (snapshots, next X: the chain continues from there),
+            // then rows 32..63.  No 32-wide register array stays live across the state
+            // update, which keeps it free of register spills.
             if (!(ok = mbar_wait(&bar[B_SDONE], n & 1, ab, status))) break;
             tc_fence_after();
-            {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem + lane_base + TM_O, r0);
-                tmem_ld32(tmem + lane_base + TM_O + 32, r1);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&bar[B_OFREE]);
-                const size_t obase = ((size_t)(t0 + (int64_t)C * n) * P.H + h) * kD + j;
-                const size_t ostride = (size_t)P.H * kD;
+            if (j == 0) KDA_TR(n, 20);
+            constexpr uint32_t QB = QR * kD * sizeof(Tout);  // one 16-row output quarter
+            const bool full = valid == C;
+            // Writes rows 32*half .. 32*half+31 of the output: staged through WT and
+            // stored by bulk tensor copies for full chunks, plain stores otherwise.
+            auto emit_half = [&](const uint32_t (&o)[32], int half) -> bool {
+                if (!full) {
+                    const size_t obase = ((size_t)(t0 + (int64_t)C * n) * P.H + h) * kD + j;
+                    const size_t ostride = (size_t)P.H * kD;
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
-                    if (r < valid) {
-                        const float o = __uint_as_float(r < 32 ? r0[r] : r1[r - 32]);
+                    for (int e = 0; e < 32; ++e) {
+                        const int r = 32 * half + e;
+                        if (r < valid) {
+                            if constexpr (sizeof(Tout) == 2)
+                                out[obase + r * ostride] = __float2bfloat16_rn(__uint_as_float(o[e]));
+                            else
+                                out[obase + r * ostride] = __uint_as_float(o[e]);
+                        }
+                    }
+                    return true;
+                }
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int q = 2 * half + qq;
+                    Tout* buf = reinterpret_cast<Tout*>(sm + L::OFF_WT + qq * QB);
+                    if (half == 1 && !staging_free(false)) return false;
+#pragma unroll
+                    for (int rr = 0; rr < QR; ++rr) {
+                        const float v = __uint_as_float(o[QR * qq + rr]);
                         if constexpr (sizeof(Tout) == 2)
-                            out[obase + r * ostride] = __float2bfloat16_rn(o);
+                            buf[rr * kD + j] = __float2bfloat16_rn(v);
                         else
-                            out[obase + r * ostride] = o;
+                            buf[rr * kD + j] = v;
+                    }
+                    // Every thread waits, so no thread can arrive for the next quarter
+                    // before all have arrived for this one.
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bar[B_STG]);
+                    if (!mbar_wait(&bar[B_STG], (ph_stg++) & 1, ab, status)) return false;
+                    if (j == 0) {
+                        tma_store_3d(&tm_out, buf, 0, h, (int)(t0 + (int64_t)C * n + QR * q));
+                        bulk_commit();
                     }
                 }
+                return true;
+            };
+            {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_base + TM_O, o);
+                tmem_ld_wait();
+                if (!(ok = emit_half(o, 0))) break;
             }
+            if (j == 0) KDA_TR(n, 5);
             {
                 const bool last = (n + 1 == nch);
                 const int64_t end_pos = (int64_t)C * n + valid;  // tokens of the sequence consumed so far
                 float* snap = nullptr;
-                if (P.snap_interval > 0 && valid == C && end_pos % P.snap_interval == 0)
+                if (P.snap_interval > 0 && full && end_pos % P.snap_interval == 0)
                     snap = P.snapshots + ((size_t)(P.snap_offsets[s] + end_pos / P.snap_interval - 1) * P.H + h) *
                                              kD * kD;
                 float* fin = (last && P.final_state) ? P.final_state + sbase : nullptr;
                 if (!last && !(ok = mbar_wait(&bar[B_PREPD + ((n + 1) & 1)], ((n + 1) >> 1) & 1, ab, status)))
                     break;
                 const float* bv = vec_b + b * 128;
-                const float* an = vec_a + ((n + 1) & 1) * 128;
-                uint32_t x16[64];
+                if (snap || fin) {  // true state S = Diag(b_n) D, at snapshot positions and the end
+#pragma unroll 1
+                    for (int piece = 0; piece < 4; ++piece) {
+                        uint32_t d[32];
+                        tmem_ld32(tmem + lane_base + TM_S + piece * 32, d);
+                        tmem_ld_wait();
 #pragma unroll
-                for (int piece = 0; piece < 4; ++piece) {
-                    uint32_t d[32];
-                    tmem_ld32(tmem + lane_base + TM_S + piece * 32, d);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int cc = piece * 32 + e;
-                        const float sv = __uint_as_float(d[e]) * bv[cc];  // true state S[cc][j]
-                        if (snap) snap[(size_t)cc * kD + j] = sv;
-                        if (fin) fin[(size_t)cc * kD + j] = sv;
-                        d[e] = __float_as_uint(last ? 0.f : sv * an[cc]);
-                    }
-                    if (!last) {
-                        tmem_st32(tmem + lane_base + TM_S + piece * 32, d);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            x16[piece * 16 + e] =
-                                pack_half2(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
+                        for (int e = 0; e < 32; ++e) {
+                            const int cc = piece * 32 + e;
+                            const float sv = __uint_as_float(d[e]) * bv[cc];
+                            if (snap) snap[(size_t)cc * kD + j] = sv;
+                            if (fin) fin[(size_t)cc * kD + j] = sv;
+                        }
                     }
                 }
+                if (!last) {  // X_{n+1} = Diag(a_{n+1}) (Diag(b_n) D) into D_S (fp32) and X16 (fp16)
+                    // (the same two roundings as a run resumed from the returned state)
+                    const float* an = vec_a + ((n + 1) & 1) * 128;
+                    uint32_t da[32], db[32];
+                    tmem_ld32(tmem + lane_base + TM_S, da);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int piece = 0; piece < 4; ++piece) {
+                        uint32_t(&d)[32] = (piece & 1) ? db : da;
+                        uint32_t(&dn)[32] = (piece & 1) ? da : db;
+                        if (piece < 3) tmem_ld32(tmem + lane_base + TM_S + (piece + 1) * 32, dn);
+                        uint32_t x16[16];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            d[e] = __float_as_uint(__uint_as_float(d[e]) * bv[piece * 32 + e] * an[piece * 32 + e]);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            x16[e] = pack_half2(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
+                        tmem_st32(tmem + lane_base + TM_S + piece * 32, d);
+                        tmem_st16(tmem + lane_base + TM_X16 + piece * 16, x16);
+                        if (piece < 3) tmem_ld_wait();
+                    }
+                }
+                if (j == 0) KDA_TR(n, 30);
                 if (!last) {
-                    tmem_st32(tmem + lane_base + TM_X16, *reinterpret_cast<uint32_t(*)[32]>(&x16[0]));
-                    tmem_st32(tmem + lane_base + TM_X16 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x16[32]));
                     tmem_st_wait();
+                    if (j == 0) KDA_TR(n, 31);
                     tc_fence_before();
                     mbar_arrive(&bar[B_XRDY]);
                 }
                 mbar_arrive(&bar[B_VFREE + b]);
+                if (j == 0) KDA_TR(n, 21);
+            }
+            {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_base + TM_O + 32, o);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&bar[B_OFREE]);
+                if (!(ok = emit_half(o, 1))) break;
+            }
+            if (j == 0) KDA_TR(n, 28);
+        }
+        if (j == 0) bulk_wait_all();  // the CTA's shared memory must outlive the bulk stores
+    state_done:;
+    } else {
+        // ------------------------------------------------------------ tri warpgroup
+        // Reads the four M = 64 products of the inverse (row r of a product sits in
+        // TMEM lane 32*(r/16) + r%16, so lanes 0..15 of each warp hold rows).
+        const int q = warp & 3, r = 16 * q + (lane & 15);
+        const bool act = lane < 16;
+        const int a = r >> 4;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        uint8_t* b1 = sm + L::OFF_B1;
+        uint8_t* nr = sm + L::OFF_NR;
+        const float* dblk = dfp + r * 16;  // row r of its 16x16 diagonal inverse block
+        for (int n = 0; n < nch; ++n) {
+            uint32_t r0[32], r1[32];
+            // readout 1: N -> NR
+            if (!mbar_wait(&bar[B_S1D], n & 1, ab, status)) break;
+            tc_fence_after();
+            tmem_ld32(tmem + lane_base + TM_W, r0);
+            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
+            tmem_ld_wait();
+            if (act) store_row16(nr, r, r0, r1);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar[B_C1]);
+            if (tid == 384) {  // S2: D_W = N N
+                if (!mbar_wait(&bar[B_C1], n & 1, ab, status)) break;
+                tc_fence_after();
+                for (int st = 0; st < 4; ++st)
+                    mma_ss(tmem + TM_W, k_desc(snr + st * 32), mn_desc(snr + st * 2048, 8192), ID_T2, st > 0);
+                mma_commit(&bar[B_S2D]);
+                KDA_TR(n, 13);
+            }
+            // readout 2: N2 -> B1
+            if (!mbar_wait(&bar[B_S2D], n & 1, ab, status)) break;
+            tc_fence_after();
+            tmem_ld32(tmem + lane_base + TM_W, r0);
+            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
+            tmem_ld_wait();
+            if (act) store_row16(b1, r, r0, r1);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar[B_C2]);
+            if (tid == 384) {  // S3: D_W = N2 Dg
+                if (!mbar_wait(&bar[B_C2], n & 1, ab, status)) break;
+                tc_fence_after();
+                for (int st = 0; st < 4; ++st)
+                    mma_ss(tmem + TM_W, k_desc(sb1 + st * 32), k_desc(sdt + st * 32), ID_T3, st > 0);
+                mma_commit(&bar[B_S3D]);
+                KDA_TR(n, 14);
+            }
+            // readout 3: M = Dg + N2 Dg; -M -> B1
+            if (!mbar_wait(&bar[B_S3D], n & 1, ab, status)) break;
+            tc_fence_after();
+            tmem_ld32(tmem + lane_base + TM_W, r0);
+            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
+            tmem_ld_wait();
+            if (act) {
+                add_block16(r0, r1, a, dblk);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    r0[e] ^= 0x80000000u;
+                    r1[e] ^= 0x80000000u;
+                }
+                store_row16(b1, r, r0, r1);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar[B_C3]);
+            if (tid == 384) {  // S4: D_W += N (-M)
+                if (!mbar_wait(&bar[B_C3], n & 1, ab, status)) break;
+                tc_fence_after();
+                for (int st = 0; st < 4; ++st)
+                    mma_ss(tmem + TM_W, k_desc(snr + st * 32), mn_desc(sb1 + st * 2048, 8192), ID_T2, 1);
+                mma_commit(&bar[B_TDONE]);
+                KDA_TR(n, 15);
+            }
+            // readout 4: T = Dg + (N2 Dg - N M); T diag(beta) -> NR (K-major B of the WY products)
+            if (!mbar_wait(&bar[B_TDONE], n & 1, ab, status)) break;
+            tc_fence_after();
+            tmem_ld32(tmem + lane_base + TM_W, r0);
+            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
+            tmem_ld_wait();
+            if (!mbar_wait(&bar[B_BFULL + (n & 3)], (n >> 2) & 1, ab, status)) break;
+            if (act) {
+                add_block16(r0, r1, a, dblk);
+                const float* bt = sbeta + (n & 3) * 64;
+                const int64_t vld = len - (int64_t)C * n;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    r0[e] = __float_as_uint(e < vld ? __uint_as_float(r0[e]) * bt[e] : 0.f);
+                    r1[e] = __float_as_uint(e + 32 < vld ? __uint_as_float(r1[e]) * bt[e + 32] : 0.f);
+                }
+                store_row16(nr, r, r0, r1);
+            }
+            mbar_arrive(&bar[B_BFREE + (n & 3)]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar[B_TRDY]);
+            KDA_TR(n, 6);
+            if (tid == 384) {  // WY products, once U16 of chunk n-1 (over D_U) has been consumed
+                if (!mbar_wait(&bar[B_TRDY], n & 1, ab, status)) break;
+                if (!mbar_wait(&bar[B_PREPD + (n & 1)], (n >> 1) & 1, ab, status)) break;
+                if (n > 0 && !mbar_wait(&bar[B_SDONE], (n - 1) & 1, ab, status)) break;
+                tc_fence_after();
+                const uint32_t kt = sm_base + L::OFF_KQ + (n & 1) * 32768, v16 = TM_V16 + (n & 1) * 32;
+                for (int st = 0; st < 4; ++st) {
+                    const uint64_t bd = k_desc(snr + st * 32);
+                    mma_ss(tmem + TM_W, k_desc(kt + st * 32), bd, ID_KK, st > 0);
+                    mma_ts(tmem + TM_U, tmem + v16 + st * 8, bd, ID_KK, st > 0);
+                }
+                mma_commit(&bar[B_WYDONE]);
+                KDA_TR(n, 9);
             }
         }
-    state_done:;
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (ab->flag) {  // aborted: let any product group still in flight drain before TMEM goes away
+        const long long tstart = clock64();
+        while (clock64() - tstart < 2000000) {
+        }
+    }
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -656,24 +915,33 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, 
 
 template <typename Tin, typename Tout>
 cudaError_t launch_t(const SeqProblem& p, cudaStream_t st) {
-    CUtensorMap mq, mk, mv, ml;
+    CUtensorMap mq, mk, mv, ml, mo;
     const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int64_t Tt = p.T_total > 0 ? p.T_total : 1;
     if (Tt > (int64_t)0x7FFFFFFF - 2 * C) return cudaErrorInvalidValue;  // tensor-map coordinates are 32-bit
     if (!make_map(&mq, p.q, dt, sizeof(Tin), Tt, p.H) || !make_map(&mk, p.k, dt, sizeof(Tin), Tt, p.H) ||
         !make_map(&mv, p.v, dt, sizeof(Tin), Tt, p.H) ||
-        !make_map(&ml, p.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Tt, p.H))
+        !make_map(&ml, p.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Tt, p.H) ||
+        !make_map(&mo, p.out, sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  sizeof(Tout), Tt, p.H))
         return cudaErrorInvalidValue;
     auto kern = chunk_kernel<Tin, Tout>;
     const int smem = (int)Cfg<Tin>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((int64_t)p.N * p.H);
-    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, p);
+    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+#ifdef KDA_TRACE
+extern "C" int kda_trace_read(unsigned long long* host, int n) {
+    const size_t cnt = (size_t)(n < 64 * kTrEv ? n : 64 * kTrEv);
+    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * cnt) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 size_t chunk_prefill_workspace(int N, int H) {
     (void)N;
