@@ -42,9 +42,13 @@
  *     from run to run on the same GPU.
  *   - Numerics of the chunk = 64 path: tensor-core products take fp16 operands
  *     with fp32 accumulation; the state and every carry are fp32.  Inputs must
- *     stay inside the fp16 range after gating (|q|,|k|,|v| well below 6.5e4)
- *     and each chunk's cumulative log-decay must be >= -20 per key channel
- *     (otherwise KDA_STATUS_GATE_RANGE is raised in the device status word).
+ *     stay inside the fp16 range after gating: decay factors are taken
+ *     relative to the log-decay after a chunk's first 32 tokens, so within
+ *     every 64-token chunk the summed log_alpha of tokens 1..31 and of
+ *     tokens 32..63 must each be >= -15 ln 2 (about -10.4) per key channel
+ *     (otherwise KDA_STATUS_GATE_RANGE is raised in the device status word),
+ *     and q, k elements are then scaled by at most 2^15, which L2-normalised
+ *     rows (|q_c|, |k_c| <= 1) always satisfy.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -68,7 +72,7 @@ typedef enum {
     KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
     KDA_ERR_TIMEOUT = 5,     /* device status: a bounded wait inside a kernel expired */
     KDA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than kda_workspace_size() */
-    KDA_STATUS_GATE_RANGE = 7 /* device status: a chunk's cumulative log-decay was below -20 */
+    KDA_STATUS_GATE_RANGE = 7 /* device status: a half-chunk's summed log-decay was below -15 ln 2 */
 } kda_status;
 
 /* Operation selector of kda_workspace_size(). */

@@ -63,7 +63,7 @@ const char* kda_status_string(int status) {
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel expired";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
-        case KDA_STATUS_GATE_RANGE: return "KDA_STATUS_GATE_RANGE: a chunk's cumulative log-decay is below -20";
+        case KDA_STATUS_GATE_RANGE: return "KDA_STATUS_GATE_RANGE: a half-chunk's summed log-decay is below -15 ln 2";
         default: return "unknown kda status";
     }
 }
