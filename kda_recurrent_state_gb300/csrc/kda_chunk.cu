@@ -20,39 +20,38 @@
 // as X = Diag(e^{ref}) S0 (what the products with Ktil_p / Qtil_p need), and the
 // state accumulator holds D = X + Khat_p^T U, so S_C = Diag(e^{g_63 - ref}) D.
 //
-// The triangular inverse on the tensor cores: split A = A_d + A_o into its
-// 16x16 diagonal blocks and the rest.  With Dg = (I + A_d)^-1 (four small
-// inverses, CUDA cores) and N = Dg A_o (strictly block-lower, N^4 = 0):
-//   I + A = (I + A_d)(I + N)   =>   T = (I + N)^-1 Dg = (I - N)(I + N^2) Dg,
-// evaluated as four 64x64x64 products: N = Dg A_o, N2 = N N, M = Dg + N2 Dg,
-// T = M - N M.
+// The triangular inverse (the WY solve of §六) runs on CUDA cores in fp32:
+// A is split into 16x16 blocks; the diagonal blocks are inverted by
+// substitution (Dg_a = (I + A_aa)^-1, one thread per column), and the blocks
+// below the diagonal follow block column by block column from
+//   T_ab = -Dg_a sum_{k=b}^{a-1} A_ak T_kb      (T_bb = Dg_b),
+// one warp per (half) block column.  Only T diag(beta) is rounded to fp16, as
+// the operand of the WY products.
 //
 // Data layout on chip (one CTA = one (sequence, head), all of d_v = 128):
 //   TMEM (fp32 accumulators, lanes = the M rows):
 //     D_S [j][c] state (128 cols)   X16 [j][c] fp16 A operand   D_U [j][r] U'/U
 //     U16 [j][r] fp16 A operand (over D_U)   D_O [j][r] output   D_G [r|64+r][i] Gram
-//     D_W [c][r] W^T, and before that the four M = 64 products of the inverse
-//     V16 [2][j][i] fp16 A operand (v^T), by chunk parity
-//   SMEM (fp16, 128-byte swizzled rows of 64 elements):
+//     D_W [c][r] W^T    V16 [2][j][i] fp16 A operand (v^T), by chunk parity
+//   SMEM (fp16 operand tiles, 128-byte swizzled rows of 64 elements):
 //     KT[c][r] = Ktil_p, QT[c][r] = Qtil_p (adjacent: together the M = 128 A
-//     operand of the Gram), KH[c][r] = Khat_p, PP[r][i] = P, WT[c][r] = -W^T,
-//     DT[m][r] = Dg^T, B1 = A_o -> N2 -> -M (row-major), NR = N -> T diag(beta)
-//     (row-major); fp32 diagonal blocks of A and of Dg; a ring of 16-token
-//     input slots filled by TMA.
+//     operand of the Gram; once a chunk's products are done the pair stages
+//     its output for the TMA store), KH[c][r] = Khat_p, PP[r][i] = P,
+//     WT[c][r] = -W^T, NR[r][i] = T diag(beta); fp32 16x16 blocks of A and T;
+//     a ring of 16-token input slots filled by TMA.
 //   The products (all tcgen05.mma, fp16 operands, fp32 accumulation):
 //     Gram  D_G = [KT;QT] x KH                 M=128 N=64  K=128
-//     S1..4 D_W = DT x B1, NR x NR, B1 x DT, NR x B1 (accumulate)   M=64 N=64 K=64
-//     WY    D_W = KT x T,  D_U = V16 x T       M=128 N=64  K=64
+//     WY    D_W = KT x NR,  D_U = V16 x NR     M=128 N=64  K=64
 //     (i)   D_U += X16 x WT                    M=128 N=64  K=128
-//     (iii) D_O = X16 x QT + U16 x PP          M=128 N=64  K=128+64
+//     (iii) D_O = X16 x QT, D_O += U16 x PP    M=128 N=64  K=128, 64
 //     (ii)  D_S += U16 x KH                    M=128 N=128 K=64
 //
-// Warp roles (16 warps): 0 TMA producer, 1 MMA issuer (+ TMEM allocation),
-// 2-3 the 16x16 diagonal-block inverses, 4-7 "prep" warpgroup (decay cumsum,
-// operand tiles, Gram readout), 8-11 "state" warpgroup (W and U conversion,
-// outputs, state rescale, snapshots), 12-15 "tri" warpgroup (readout of the
-// four inverse products).  Roles hand work to each other through mbarriers;
-// every wait is bounded.
+// Warp roles (16 warps): 0 TMA producer, 1 beta loader (+ TMEM allocation),
+// 4-7 "prep" warpgroup (decay cumsum, operand tiles, issues the Gram), 8-11
+// "state" warpgroup (U conversion, state rescale, snapshots, outputs; issues
+// (i)-(iii)), 12-15 "tri" warpgroup (Gram readout, the inverse, W readout;
+// issues WY).  Warps 2-3 have no role.  Roles hand work to each other through
+// mbarriers; every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -69,6 +68,8 @@ constexpr int QR = 16;  // token rows per input slot
 constexpr int NTHREADS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxExp2 = 15.0f;  // |g - ref| bound (log2 units) for fp16 operands
+constexpr int kBS = 20;            // row stride (floats) of a 16x16 fp32 block of A or T
+constexpr int kBlk = 16 * kBS;     // floats per block
 
 // TMEM column map (512 columns allocated).  The fp16 U operand is written over
 // the first 32 columns of the U accumulator once that has been read out; V16
@@ -87,20 +88,17 @@ struct Cfg {
     static constexpr uint32_t SLOT_LA = 3 * QR * 128 * ES;
     static constexpr uint32_t SLOT_BYTES = 3 * QR * 128 * ES + QR * 128 * 4;
     // shared memory map (offsets from a 1024-byte aligned base)
-    static constexpr uint32_t OFF_KQ = 0;                    // [2] x (KT 16K | QT 16K)
+    static constexpr uint32_t OFF_KQ = 0;                    // [2] x (KT 16K | QT 16K); then output staging
     static constexpr uint32_t OFF_KH = 65536;                // [2] x 16K
     static constexpr uint32_t OFF_PP = 98304;                // [NPP] x 8K
     static constexpr uint32_t OFF_WT = OFF_PP + NPP * 8192;  // 16K
-    static constexpr uint32_t OFF_DT = OFF_WT + 16384;       // 8K
-    static constexpr uint32_t OFF_B1 = OFF_DT + 8192;        // 8K
-    static constexpr uint32_t OFF_NR = OFF_B1 + 8192;        // 8K
-    static constexpr uint32_t OFF_LDG = OFF_NR + 8192;       // fp32 [4][16][17]
-    static constexpr uint32_t OFF_DFP = OFF_LDG + 4 * 16 * 17 * 4;  // fp32 [4][16][16]
-    static constexpr uint32_t OFF_RING = OFF_DFP + 4 * 16 * 16 * 4;
-    static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[2][128], b[2][128]
-    static constexpr uint32_t OFF_BETA = OFF_VEC + 4 * 128 * 4;         // [4][64]
+    static constexpr uint32_t OFF_NR = OFF_WT + 16384;       // 8K
+    static constexpr uint32_t OFF_INV = OFF_NR + 8192;       // 17 fp32 blocks: A (10), Dg (4), T10, T21, T20
+    static constexpr uint32_t OFF_RING = OFF_INV + 17 * kBlk * 4;
+    static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[4][128], b[4][128]
+    static constexpr uint32_t OFF_BETA = OFF_VEC + 8 * 128 * 4;         // [4][64]
     static constexpr uint32_t OFF_BAR = OFF_BETA + 4 * 64 * 4;
-    static constexpr uint32_t NBAR = 44;
+    static constexpr uint32_t NBAR = 40;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 };
@@ -110,36 +108,34 @@ static_assert(Cfg<__nv_bfloat16>::OFF_RING % 128 == 0 && Cfg<float>::OFF_RING % 
 
 // barrier indices
 enum {
-    B_FULL = 0,     // [NSLOT] input slot landed
-    B_EMPTY = 3,    // [NSLOT] input slot consumed
-    B_PREPD = 6,    // [2] KT/QT/KH, vectors, beta of a chunk ready
-    B_GDONE = 9,    // Gram complete
-    B_P2D = 10,     // Gram read out: D_G free; A blocks, A_o and P written
-    B_AFREE = 11,   // diagonal-block inverses done reading their input
-    B_DRDY = 12,    // DT and the fp32 diagonal inverses written
-    B_S1D = 13, B_C1 = 14, B_S2D = 15, B_C2 = 16, B_S3D = 17, B_C3 = 18,  // inverse products / readouts
-    B_TDONE = 19,   // last inverse product complete
-    B_TRDY = 20,    // T diag(beta) written
-    B_WYDONE = 21,  // WY products complete
-    B_WRDY = 22,    // WT written, D_W free
-    B_XRDY = 23,    // X16 / D_S ready for the chunk
-    B_UIDONE = 24,  // (i) and (iii-a) complete
-    B_URDY = 25,    // U16 written, D_U free
-    B_SDONE = 26,   // (ii) and (iii-b) complete
-    B_KQFREE = 27,  // [2] chunk's KT/QT/KH/PP buffers free again
-    B_OFREE = 29,   // D_O read out
-    B_VFREE = 30,   // [2] vector buffers free again
-    B_BFULL = 33,   // [4] beta of a chunk loaded (ring of 4, by chunk index mod 4)
-    B_STG = 37,     // output staging tile written by the whole state warpgroup
-    B_STGR = 38,    // output staging buffer free again (thread 0 -> state warpgroup)
-    B_BFREE = 39,   // [4] beta ring slot read by all its users
-    B_COUNT = 43
+    B_FULL = 0,      // [3] input slot landed
+    B_EMPTY = 3,     // [3] input slot consumed
+    B_PREPD = 6,     // [2] KT/QT/KH, V16, vectors of a chunk ready
+    B_GDONE = 8,     // Gram complete
+    B_P2D = 9,       // Gram read out: D_G free
+    B_TB = 10,       // tri warpgroup's own barrier
+    B_WYDONE = 11,   // WY products complete
+    B_V16FREE = 12,  // [2] V16 of a chunk consumed (WY complete)
+    B_WRDY = 14,     // WT and PP written
+    B_XRDY = 15,     // X16 / D_S ready for the chunk
+    B_UIDONE = 16,   // (i) complete: U readable, WT free
+    B_URDY = 17,     // U16 written
+    B_SDONE = 18,    // (ii) and (iii) complete
+    B_KQFREE = 19,   // [2] KH and PP of a chunk consumed
+    B_OFREE = 21,    // D_O read out
+    B_STG = 22,      // output staging tile written by the whole state warpgroup
+    B_STGFREE = 23,  // [2] KT/QT pair free again (staged output read by the bulk store)
+    B_BFULL = 25,    // [4] beta of a chunk loaded (ring of 4, by chunk index mod 4)
+    B_BFREE = 29,    // [4] beta ring slot consumed
+    B_VFREE = 33,    // [4] decay vectors of a chunk consumed
+    B_COUNT = 37
 };
+static_assert(B_COUNT <= (int)Cfg<float>::NBAR, "barrier space");
 
 #ifdef KDA_TRACE
 // Debug timeline (compiled only with -DKDA_TRACE): clock64 stamps of each
 // role's milestones for the first 64 chunks of CTA 0.
-constexpr int kTrEv = 40;
+constexpr int kTrEv = 24;
 __device__ unsigned long long g_trace[64 * kTrEv];
 #define KDA_TR(n, ev)                                                                                    \
     do {                                                                                                 \
@@ -169,18 +165,76 @@ __device__ __forceinline__ void store_row16(uint8_t* tile, uint32_t row, const u
     }
 }
 
-// Adds the 16 values `d` to columns 16a .. 16a+15 of a 64-wide row held as (r0, r1).
-__device__ __forceinline__ void add_block16(uint32_t (&r0)[32], uint32_t (&r1)[32], int a, const float* d) {
+// Writes 32 packed fp16 pairs (columns 0..63) as one 128-byte swizzled row.
+__device__ __forceinline__ void store_row16_packed(uint8_t* tile, uint32_t row, const uint32_t (&p)[32]) {
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16)
+        *reinterpret_cast<uint4*>(tile + sw128(row, c16)) =
+            make_uint4(p[4 * c16], p[4 * c16 + 1], p[4 * c16 + 2], p[4 * c16 + 3]);
+}
+
+// acc[q] += sum_m arow[m] * bcol[m * kBS + q]  (one row of a 16x16 block times
+// four columns of another; both fp32 in shared memory, 16-byte aligned).
+__device__ __forceinline__ void mac16(const float* arow, const float* bcol, float (&acc)[4]) {
+    float a[16];
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 t = *reinterpret_cast<const float4*>(arow + 4 * k4);
+        a[4 * k4] = t.x;
+        a[4 * k4 + 1] = t.y;
+        a[4 * k4 + 2] = t.z;
+        a[4 * k4 + 3] = t.w;
+    }
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        const float dm = d[m];
-#pragma unroll
-        for (int aa = 0; aa < 4; ++aa)
-            if (aa == a) {
-                uint32_t& e = aa < 2 ? r0[16 * aa + m] : r1[16 * (aa - 2) + m];
-                e = __float_as_uint(__uint_as_float(e) + dm);
-            }
+        const float4 bv = *reinterpret_cast<const float4*>(bcol + m * kBS);
+        acc[0] = fmaf(a[m], bv.x, acc[0]);
+        acc[1] = fmaf(a[m], bv.y, acc[1]);
+        acc[2] = fmaf(a[m], bv.z, acc[2]);
+        acc[3] = fmaf(a[m], bv.w, acc[3]);
     }
+}
+// The same for two / three rows of different left blocks sharing the right block.
+__device__ __forceinline__ void mac16x2(const float* a0, const float* a1, const float* bcol, float (&c0)[4],
+                                        float (&c1)[4]) {
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 x0 = *reinterpret_cast<const float4*>(a0 + 4 * m4);
+        const float4 x1 = *reinterpret_cast<const float4*>(a1 + 4 * m4);
+        const float u0[4] = {x0.x, x0.y, x0.z, x0.w}, u1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 bv = *reinterpret_cast<const float4*>(bcol + (4 * m4 + k) * kBS);
+            c0[0] = fmaf(u0[k], bv.x, c0[0]); c0[1] = fmaf(u0[k], bv.y, c0[1]);
+            c0[2] = fmaf(u0[k], bv.z, c0[2]); c0[3] = fmaf(u0[k], bv.w, c0[3]);
+            c1[0] = fmaf(u1[k], bv.x, c1[0]); c1[1] = fmaf(u1[k], bv.y, c1[1]);
+            c1[2] = fmaf(u1[k], bv.z, c1[2]); c1[3] = fmaf(u1[k], bv.w, c1[3]);
+        }
+    }
+}
+__device__ __forceinline__ void mac16x3(const float* a0, const float* a1, const float* a2, const float* bcol,
+                                        float (&c0)[4], float (&c1)[4], float (&c2)[4]) {
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 x0 = *reinterpret_cast<const float4*>(a0 + 4 * m4);
+        const float4 x1 = *reinterpret_cast<const float4*>(a1 + 4 * m4);
+        const float4 x2 = *reinterpret_cast<const float4*>(a2 + 4 * m4);
+        const float u0[4] = {x0.x, x0.y, x0.z, x0.w}, u1[4] = {x1.x, x1.y, x1.z, x1.w},
+                    u2[4] = {x2.x, x2.y, x2.z, x2.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 bv = *reinterpret_cast<const float4*>(bcol + (4 * m4 + k) * kBS);
+            c0[0] = fmaf(u0[k], bv.x, c0[0]); c0[1] = fmaf(u0[k], bv.y, c0[1]);
+            c0[2] = fmaf(u0[k], bv.z, c0[2]); c0[3] = fmaf(u0[k], bv.w, c0[3]);
+            c1[0] = fmaf(u1[k], bv.x, c1[0]); c1[1] = fmaf(u1[k], bv.y, c1[1]);
+            c1[2] = fmaf(u1[k], bv.z, c1[2]); c1[3] = fmaf(u1[k], bv.w, c1[3]);
+            c2[0] = fmaf(u2[k], bv.x, c2[0]); c2[1] = fmaf(u2[k], bv.y, c2[1]);
+            c2[2] = fmaf(u2[k], bv.z, c2[2]); c2[3] = fmaf(u2[k], bv.w, c2[3]);
+        }
+    }
+}
+__device__ __forceinline__ void st4(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
 template <typename Tin, typename Tout>
@@ -194,11 +248,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
     Abort* ab = reinterpret_cast<Abort*>(sm + L::OFF_MISC + 16);
-    float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);         // [2][128]
-    float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 1024);  // [2][128]
+    float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);         // [4][128] e^{ref}
+    float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 2048);  // [4][128] e^{g_63 - ref}
     float* sbeta = reinterpret_cast<float*>(sm + L::OFF_BETA);        // [4][64]
-    float* ldg = reinterpret_cast<float*>(sm + L::OFF_LDG);           // [4][16][17] diagonal blocks of A
-    float* dfp = reinterpret_cast<float*>(sm + L::OFF_DFP);           // [4][16][16] their inverses
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x;
@@ -219,19 +271,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&bar[B_FULL + i], 1);
             mbar_init(&bar[B_EMPTY + i], 128);
         }
-        const int c128[] = {B_PREPD, B_PREPD + 1, B_P2D, B_C1, B_C2, B_C3, B_TRDY, B_WRDY, B_XRDY, B_URDY,
-                            B_OFREE, B_VFREE, B_VFREE + 1};
+        const int c128[] = {B_PREPD, B_PREPD + 1, B_P2D, B_TB, B_WRDY, B_XRDY, B_URDY, B_OFREE, B_STG};
         for (int i : c128) mbar_init(&bar[i], 128);
-        const int c1[] = {B_GDONE, B_S1D, B_S2D, B_S3D, B_TDONE, B_WYDONE, B_UIDONE, B_SDONE, B_KQFREE, B_KQFREE + 1};
+        const int c1[] = {B_GDONE,  B_WYDONE,   B_V16FREE,    B_V16FREE + 1, B_UIDONE,
+                          B_SDONE,  B_KQFREE,   B_KQFREE + 1, B_STGFREE,     B_STGFREE + 1};
         for (int i : c1) mbar_init(&bar[i], 1);
-        mbar_init(&bar[B_AFREE], 64);
-        mbar_init(&bar[B_DRDY], 64);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bar[B_BFULL + i], 32);
-            mbar_init(&bar[B_BFREE + i], 64 + 128);
+            mbar_init(&bar[B_BFREE + i], 128);
+            mbar_init(&bar[B_VFREE + i], 128);
         }
-        mbar_init(&bar[B_STG], 128);
-        mbar_init(&bar[B_STGR], 1);
         ab->flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -252,10 +301,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr uint32_t ID_MN = idesc_f16(128, 64, 0, 1);
     constexpr uint32_t ID_KK = idesc_f16(128, 64, 0, 0);
     constexpr uint32_t ID_S = idesc_f16(128, 128, 0, 0);
-    constexpr uint32_t ID_T1 = idesc_f16(64, 64, 1, 1);
-    constexpr uint32_t ID_T2 = idesc_f16(64, 64, 0, 1);
-    constexpr uint32_t ID_T3 = idesc_f16(64, 64, 0, 0);
-    const uint32_t sdt = sm_base + L::OFF_DT, sb1 = sm_base + L::OFF_B1, snr = sm_base + L::OFF_NR;
     // Every product group is issued by thread 0 of the role that completes its last
     // input, after waiting for that input and for the previous reader of its
     // accumulator; the commits below are what the other roles wait on.
@@ -267,9 +312,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             prefetch_tmap(&tm_out);
             int issued = 0;
             bool ok = true;
+            // The ring holds only a few slots, so every tile is first pulled into L2
+            // kPf quarters ahead of its load (DRAM latency would otherwise stall prep).
+            constexpr int kPf = 8;
+            const int nq = (int)((len + QR - 1) / QR);
+            auto prefetch = [&](int g) {
+                const int z = (int)(t0 + (int64_t)QR * g);
+                tma_prefetch_3d(&tm_q, 0, h, z);
+                tma_prefetch_3d(&tm_k, 0, h, z);
+                tma_prefetch_3d(&tm_v, 0, h, z);
+                tma_prefetch_3d(&tm_la, 0, h, z);
+            };
+            for (int g = L::NSLOT; g < kPf && g < nq; ++g) prefetch(g);
             for (int n = 0; n < nch && ok; ++n)
                 for (int q = 0; q < 4 && ok; ++q) {
                     const int g = 4 * n + q, sl = g % L::NSLOT, use = g / L::NSLOT;
+                    if (g + kPf < nq) prefetch(g + kPf);
                     if (use > 0 && !(ok = mbar_wait(&bar[B_EMPTY + sl], (use - 1) & 1, ab, status))) break;
                     uint8_t* slot = sm + L::OFF_RING + sl * L::SLOT_BYTES;
                     mbar_arrive_expect_tx(&bar[B_FULL + sl], L::SLOT_BYTES);
@@ -278,7 +336,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tma_load_3d(slot + L::SLOT_K, &tm_k, &bar[B_FULL + sl], 0, h, z);
                     tma_load_3d(slot + L::SLOT_V, &tm_v, &bar[B_FULL + sl], 0, h, z);
                     tma_load_3d(slot + L::SLOT_LA, &tm_la, &bar[B_FULL + sl], 0, h, z);
-                    KDA_TR(n, 32 + q);
                     ++issued;
                 }
             if (!ok) {  // let the copies already issued land before the CTA can exit
@@ -304,69 +361,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive(&bar[B_BFULL + k4]);
         }
     } else if (warp < 4) {
-        // ------------------------------------------------------------ 16x16 diagonal-block inverses
-        // Thread (a, jj) solves column jj of (I + A_aa)^-1 by right-looking substitution.
-        const int t = tid - 64, a = t >> 4, jj = t & 15;
-        const float* blk = ldg + a * 16 * 17;
-        for (int n = 0; n < nch; ++n) {
-            if (!mbar_wait(&bar[B_P2D], n & 1, ab, status)) break;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = 0.f;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const float xr = (r == jj) ? 1.f : (r > jj ? x[r] : 0.f);
-                x[r] = xr;
-#pragma unroll
-                for (int i = r + 1; i < 16; ++i) x[i] -= blk[i * 17 + r] * xr;
-            }
-            mbar_arrive(&bar[B_AFREE]);
-            if (n > 0 && !mbar_wait(&bar[B_TRDY], (n - 1) & 1, ab, status)) break;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) dfp[(a * 16 + i) * 16 + jj] = x[i];
-            uint8_t* dt = sm + L::OFF_DT;  // row (16a + jj) holds column 16a+jj of Dg
-#pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) {
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (c16 == 2 * a)
-                    w = make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
-                                   pack_half2(x[6], x[7]));
-                if (c16 == 2 * a + 1)
-                    w = make_uint4(pack_half2(x[8], x[9]), pack_half2(x[10], x[11]), pack_half2(x[12], x[13]),
-                                   pack_half2(x[14], x[15]));
-                *reinterpret_cast<uint4*>(dt + sw128(16 * a + jj, c16)) = w;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&bar[B_DRDY]);
-            KDA_TR(n, 7);
-            if (t == 0) {  // S1: D_W = Dg A_o, once D_W's previous contents (W of chunk n-1) were read
-                if (!mbar_wait(&bar[B_DRDY], n & 1, ab, status)) break;
-                if (n > 0 && !mbar_wait(&bar[B_WRDY], (n - 1) & 1, ab, status)) break;
-                tc_fence_after();
-                for (int st = 0; st < 4; ++st)
-                    mma_ss(tmem + TM_W, mn_desc(sdt + st * 2048, 8192), mn_desc(sb1 + st * 2048, 8192), ID_T1, st > 0);
-                mma_commit(&bar[B_S1D]);
-                KDA_TR(n, 12);
-            }
-        }
+        // no role
     } else if (warp < 8) {
         // ------------------------------------------------------------ prep warpgroup
         const int c = tid - 128;  // key channel (and TMEM lane) of this thread
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         float max_x = 0.f;  // largest |g - ref| seen (log2 units), for the range check
 
-        // prep1(n): decay cumsum, operand tiles KT/QT/KH, V16, vectors, beta.
+        // prep1(n): decay cumsum, operand tiles KT/QT/KH, V16, decay vectors.
         // Rows past the end of a sequence get log alpha = 0 and k = 0 (their beta
         // is 0 too), which makes them identity steps; q and v of such rows only
         // reach outputs that are never stored.
         auto prep1 = [&](int n) -> bool {
-            const int b = n & 1;
+            const int b = n & 1, v4 = n & 3;
             if (c == 0) KDA_TR(n, 0);
-            if (n >= 2) {
-                if (!mbar_wait(&bar[B_KQFREE + b], ((n - 2) >> 1) & 1, ab, status)) return false;
-                if (!mbar_wait(&bar[B_VFREE + b], ((n - 2) >> 1) & 1, ab, status)) return false;
+            if (n >= 2) {  // the buffers of chunk n - 2
+                const uint32_t par = ((n - 2) >> 1) & 1;
+                if (!mbar_wait(&bar[B_KQFREE + b], par, ab, status)) return false;   // KH (D products)
+                if (c == 0) KDA_TR(n, 18);
+                if (!mbar_wait(&bar[B_STGFREE + b], par, ab, status)) return false;  // KT/QT (staged output)
+                if (c == 0) KDA_TR(n, 19);
+                if (!mbar_wait(&bar[B_V16FREE + b], par, ab, status)) return false;  // V16 (WY products)
+                if (c == 0) KDA_TR(n, 20);
             }
-            tc_fence_after();  // V16[b] was last read by the WY product of chunk n - 2
+            if (n >= 4 && !mbar_wait(&bar[B_VFREE + v4], ((n - 4) >> 2) & 1, ab, status)) return false;
+            if (c == 0) KDA_TR(n, 21);
+            tc_fence_after();
             const int valid = (int)((len - (int64_t)C * n) < C ? (len - (int64_t)C * n) : C);
             uint8_t* kt = sm + L::OFF_KQ + b * 32768;
             uint8_t* qt = kt + 16384;
@@ -392,7 +412,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
                 if (q >= 2 && !wait_slot(q)) return false;
-                if (c == 0) KDA_TR(n, 34 + q);
                 const uint8_t* sl = slot_ptr(q);
                 const float* sla = reinterpret_cast<const float*>(sl + L::SLOT_LA);
                 const Tin* sk = reinterpret_cast<const Tin*>(sl + L::SLOT_K);
@@ -433,17 +452,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     *reinterpret_cast<uint4*>(kh + off) = make_uint4(ph[4 * g8], ph[4 * g8 + 1], ph[4 * g8 + 2], ph[4 * g8 + 3]);
                 }
                 tmem_st8(tmem + lane_base + TM_V16 + b * 32 + q * 8, pv);
-                if (c == 0) KDA_TR(n, 22 + q);
             }
-            const float an = fast_exp2(ref);
-            vec_a[b * 128 + c] = an;
-            vec_b[b * 128 + c] = fast_exp2(g2 - ref);
+            vec_a[v4 * 128 + c] = fast_exp2(ref);
+            vec_b[v4 * 128 + c] = fast_exp2(g2 - ref);
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar[B_PREPD + b]);
-            if (c == 0) {  // the Gram of this chunk, once all operand rows and D_G (read by P2(n-1)) are ready
-                KDA_TR(n, 2);
+            if (c == 0) KDA_TR(n, 2);
+            if (c == 0) {  // the Gram of this chunk, once all operand rows and D_G (read by the tri warps) are ready
                 if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) return false;
                 if (n > 0 && !mbar_wait(&bar[B_P2D], (n - 1) & 1, ab, status)) return false;
                 tc_fence_after();
@@ -451,77 +468,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int st = 0; st < 8; ++st)
                     mma_ss(tmem + TM_G, mn_desc(kq + st * 2048, 16384), mn_desc(khb + st * 2048, 8192), ID_G, st > 0);
                 mma_commit(&bar[B_GDONE]);
-                KDA_TR(n, 8);
+                KDA_TR(n, 3);
             }
-            return true;
-        };
-        // P2(n): read the Gram accumulator.  Rows 0..63 (A, beta_r applied): the
-        // 16x16 diagonal blocks (fp32) and A_o (fp16); rows 64..127: P (fp16).
-        auto p2 = [&](int n) -> bool {
-            const int b = n & 1;
-            if (!mbar_wait(&bar[B_GDONE], n & 1, ab, status)) return false;
-            if (!mbar_wait(&bar[B_BFULL + (n & 3)], (n >> 2) & 1, ab, status)) return false;
-            tc_fence_after();
-            if (c == 0) KDA_TR(n, 3);
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tmem + lane_base + TM_G, r0);
-            tmem_ld32(tmem + lane_base + TM_G + 32, r1);
-            tmem_ld_wait();
-            if (c == 0) KDA_TR(n, 29);
-            if (c < 64) {  // row r = c of A
-                if (n > 0) {
-                    if (!mbar_wait(&bar[B_AFREE], (n - 1) & 1, ab, status)) return false;
-                    if (!mbar_wait(&bar[B_TDONE], (n - 1) & 1, ab, status)) return false;
-                }
-
-                const float br = c < len - (int64_t)C * n ? sbeta[(n & 3) * 64 + c] : 0.f;
-                const int a = c >> 4, i = c & 15;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    r0[e] = __float_as_uint(e < c ? br * __uint_as_float(r0[e]) : 0.f);
-                    r1[e] = __float_as_uint(e + 32 < c ? br * __uint_as_float(r1[e]) : 0.f);
-                }
-                // row i of diagonal block a: columns 16a .. 16a+15
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    float v = 0.f;
-#pragma unroll
-                    for (int aa = 0; aa < 4; ++aa)
-                        if (aa == a) v = __uint_as_float(aa < 2 ? r0[16 * aa + m] : r1[16 * (aa - 2) + m]);
-                    ldg[(a * 16 + i) * 17 + m] = v;
-                }
-
-                mbar_arrive(&bar[B_BFREE + (n & 3)]);
-                // A_o: keep the columns left of the diagonal block
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    if (e >= 16 * a) r0[e] = 0u;
-                    if (e + 32 >= 16 * a) r1[e] = 0u;
-                }
-                store_row16(sm + L::OFF_B1, c, r0, r1);
-                if (c == 0) KDA_TR(n, 26);
-            } else {  // row r = c - 64 of P (lower triangle including the diagonal)
-                if (n >= L::NPP) {
-                    const int m = n - L::NPP;
-                    if (!mbar_wait(&bar[B_KQFREE + (m & 1)], (m >> 1) & 1, ab, status)) return false;
-                }
-                const int r = c - 64;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    if (e > r) r0[e] = 0u;
-                    if (e + 32 > r) r1[e] = 0u;
-                }
-                store_row16(sm + L::OFF_PP + (n % L::NPP) * 8192, r, r0, r1);
-            }
-            fence_proxy_async_smem();
-            if (c == 0) KDA_TR(n, 27);
-            tc_fence_before();
-            mbar_arrive(&bar[B_P2D]);
-            if (c == 0) KDA_TR(n, 4);
             return true;
         };
         for (int n = 0; n < nch; ++n)
-            if (!prep1(n) || !p2(n)) break;
+            if (!prep1(n)) break;
         if (max_x > kMaxExp2) atomicCAS(status, 0, (int)KDA_STATUS_GATE_RANGE);
     } else if (warp < 12) {
         // ------------------------------------------------------------ state warpgroup
@@ -529,15 +481,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         Tout* out = static_cast<Tout*>(P.out);
         bool ok = true;
-        // Staging buffer hand-offs within the warpgroup (every thread follows the same
-        // sequence, so the phase counters agree).  Thread 0 owns the bulk stores.
-        uint32_t ph_stg = 0, ph_rd = 0;
-        auto staging_free = [&](bool all_read) -> bool {  // wait until WT may be rewritten
-            if (j == 0) {
-                if (all_read) bulk_wait_read<0>(); else bulk_wait_read<1>();
-                mbar_arrive(&bar[B_STGR]);
-            }
-            return mbar_wait(&bar[B_STGR], (ph_rd++) & 1, ab, status);
+        uint32_t ph_stg = 0;    // phase of the staging barrier (every thread waits on it)
+        bool u_issued = false;  // (i) of the coming chunk already issued (thread 0)
+        // (i): U += X16 x WT for chunk m, once X_m and WT(m) are ready (thread 0)
+        auto issue_u = [&](int m) -> bool {
+            if (!mbar_wait(&bar[B_XRDY], m & 1, ab, status)) return false;
+            if (!mbar_wait(&bar[B_WRDY], m & 1, ab, status)) return false;
+            tc_fence_after();
+            const uint32_t wt = sm_base + L::OFF_WT;
+            for (int st = 0; st < 8; ++st)
+                mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, mn_desc(wt + st * 2048, 8192), ID_MN, 1);
+            mma_commit(&bar[B_UIDONE]);
+            KDA_TR(m, 10);
+            return true;
+        };
+        // (iii-a): O = X16 x QT for chunk m, once O of chunk m - 1 has been read out (thread 0)
+        auto issue_o = [&](int m) -> bool {
+            if (m > 0 && !mbar_wait(&bar[B_OFREE], (m - 1) & 1, ab, status)) return false;
+            tc_fence_after();
+            const uint32_t qt = sm_base + L::OFF_KQ + (m & 1) * 32768 + 16384;
+            for (int st = 0; st < 8; ++st)
+                mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, mn_desc(qt + st * 2048, 8192), ID_MN, st > 0);
+            KDA_TR(m, 11);
+            return true;
         };
         {  // X_0 = Diag(a_0) S_0 into D_S and X16
             if (!(ok = mbar_wait(&bar[B_PREPD], 0, ab, status))) goto state_done;
@@ -559,48 +525,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar[B_XRDY]);
+            if (j == 0 && !(ok = issue_u(0) && issue_o(0))) goto state_done;
         }
         for (int n = 0; n < nch; ++n) {
             const int b = n & 1;
             const int valid = (int)((len - (int64_t)C * n) < C ? (len - (int64_t)C * n) : C);
-            // P4(n): WT = -W^T as fp16 (WT also stages the previous chunk's outputs)
-            if (!(ok = staging_free(true))) break;
-            if (!(ok = mbar_wait(&bar[B_WYDONE], n & 1, ab, status))) break;
-            tc_fence_after();
-            if (j == 0) KDA_TR(n, 16);
-            {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem + lane_base + TM_W, r0);
-                tmem_ld32(tmem + lane_base + TM_W + 32, r1);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    r0[e] ^= 0x80000000u;
-                    r1[e] ^= 0x80000000u;
-                }
-                store_row16(sm + L::OFF_WT, j, r0, r1);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(&bar[B_WRDY]);
-                if (j == 0) {  // C: U = U' - W S0 and O = Qtil S0
-                    KDA_TR(n, 17);
-                    if (!(ok = mbar_wait(&bar[B_WRDY], n & 1, ab, status))) break;
-                    if (!(ok = mbar_wait(&bar[B_XRDY], n & 1, ab, status))) break;
-                    if (n > 0 && !(ok = mbar_wait(&bar[B_OFREE], (n - 1) & 1, ab, status))) break;
-                    tc_fence_after();
-                    const uint32_t wt = sm_base + L::OFF_WT, qt = sm_base + L::OFF_KQ + (n & 1) * 32768 + 16384;
-                    for (int st = 0; st < 8; ++st)
-                        mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, mn_desc(wt + st * 2048, 8192), ID_MN, 1);
-                    for (int st = 0; st < 8; ++st)
-                        mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, mn_desc(qt + st * 2048, 8192), ID_MN, st > 0);
-                    mma_commit(&bar[B_UIDONE]);
-                    KDA_TR(n, 10);
-                }
+            const bool last = (n + 1 == nch);
+            // S2(n): U16 = fp16(U^T).  Thread 0 first hands back the KT/QT pair that
+            // staged the previous chunk's output, once the bulk store has read it, and
+            // issues (i) of this chunk if WT was not ready earlier.
+            if (j == 0 && n > 0) {
+                bulk_wait_read<0>();
+                mbar_arrive(&bar[B_STGFREE + ((n - 1) & 1)]);
+                if (!u_issued && !(ok = issue_u(n))) break;
+                u_issued = false;
             }
-            // S2(n): U16 = fp16(U^T)
             if (!(ok = mbar_wait(&bar[B_UIDONE], n & 1, ab, status))) break;
             tc_fence_after();
-            if (j == 0) KDA_TR(n, 18);
+            if (j == 0) KDA_TR(n, 12);
             {
                 uint32_t r0[32], r1[32], u16[32];
                 tmem_ld32(tmem + lane_base + TM_U, r0);
@@ -615,7 +557,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bar[B_URDY]);
-                if (j == 0) {  // D: state update and the intra-chunk part of the output
+                if (j == 0) {  // (ii) state update and (iii-b) the intra-chunk part of the output
                     if (!(ok = mbar_wait(&bar[B_URDY], n & 1, ab, status))) break;
                     tc_fence_after();
                     const uint32_t kh = sm_base + L::OFF_KH + b * 16384, pp = sm_base + L::OFF_PP + (n % L::NPP) * 8192;
@@ -625,80 +567,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, k_desc(pp + st * 32), ID_KK, 1);
                     mma_commit(&bar[B_SDONE]);
                     mma_commit(&bar[B_KQFREE + b]);
-                    KDA_TR(n, 11);
+                    KDA_TR(n, 13);
                 }
-                if (j == 0) KDA_TR(n, 19);
             }
-            // S3(n): outputs and state.  Order: rows 0..31 of the output (staged and
-            // stored), the state (snapshots, next X: the chain continues from there),
-            // then rows 32..63.  No 32-wide register array stays live across the state
-            // update, which keeps it free of register spills.
+            // S3(n): the state (snapshots, final state, next X: the chain continues from
+            // there), then the output of the chunk.
             if (!(ok = mbar_wait(&bar[B_SDONE], n & 1, ab, status))) break;
             tc_fence_after();
-            if (j == 0) KDA_TR(n, 20);
-            constexpr uint32_t QB = QR * kD * sizeof(Tout);  // one 16-row output quarter
-            const bool full = valid == C;
-            // Writes rows 32*half .. 32*half+31 of the output: staged through WT and
-            // stored by bulk tensor copies for full chunks, plain stores otherwise.
-            auto emit_half = [&](const uint32_t (&o)[32], int half) -> bool {
-                if (!full) {
-                    const size_t obase = ((size_t)(t0 + (int64_t)C * n) * P.H + h) * kD + j;
-                    const size_t ostride = (size_t)P.H * kD;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int r = 32 * half + e;
-                        if (r < valid) {
-                            if constexpr (sizeof(Tout) == 2)
-                                out[obase + r * ostride] = __float2bfloat16_rn(__uint_as_float(o[e]));
-                            else
-                                out[obase + r * ostride] = __uint_as_float(o[e]);
-                        }
-                    }
-                    return true;
-                }
-#pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const int q = 2 * half + qq;
-                    Tout* buf = reinterpret_cast<Tout*>(sm + L::OFF_WT + qq * QB);
-                    if (half == 1 && !staging_free(false)) return false;
-#pragma unroll
-                    for (int rr = 0; rr < QR; ++rr) {
-                        const float v = __uint_as_float(o[QR * qq + rr]);
-                        if constexpr (sizeof(Tout) == 2)
-                            buf[rr * kD + j] = __float2bfloat16_rn(v);
-                        else
-                            buf[rr * kD + j] = v;
-                    }
-                    // Every thread waits, so no thread can arrive for the next quarter
-                    // before all have arrived for this one.
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bar[B_STG]);
-                    if (!mbar_wait(&bar[B_STG], (ph_stg++) & 1, ab, status)) return false;
-                    if (j == 0) {
-                        tma_store_3d(&tm_out, buf, 0, h, (int)(t0 + (int64_t)C * n + QR * q));
-                        bulk_commit();
-                    }
-                }
-                return true;
-            };
+            if (j == 0) KDA_TR(n, 14);
             {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + TM_O, o);
-                tmem_ld_wait();
-                if (!(ok = emit_half(o, 0))) break;
-            }
-            if (j == 0) KDA_TR(n, 5);
-            {
-                const bool last = (n + 1 == nch);
                 const int64_t end_pos = (int64_t)C * n + valid;  // tokens of the sequence consumed so far
                 float* snap = nullptr;
-                if (P.snap_interval > 0 && full && end_pos % P.snap_interval == 0)
+                if (P.snap_interval > 0 && valid == C && end_pos % P.snap_interval == 0)
                     snap = P.snapshots + ((size_t)(P.snap_offsets[s] + end_pos / P.snap_interval - 1) * P.H + h) *
                                              kD * kD;
                 float* fin = (last && P.final_state) ? P.final_state + sbase : nullptr;
-                if (!last && !(ok = mbar_wait(&bar[B_PREPD + ((n + 1) & 1)], ((n + 1) >> 1) & 1, ab, status)))
-                    break;
-                const float* bv = vec_b + b * 128;
+                const float* bv = vec_b + (n & 3) * 128;
                 if (snap || fin) {  // true state S = Diag(b_n) D, at snapshot positions and the end
 #pragma unroll 1
                     for (int piece = 0; piece < 4; ++piece) {
@@ -716,7 +600,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 if (!last) {  // X_{n+1} = Diag(a_{n+1}) (Diag(b_n) D) into D_S (fp32) and X16 (fp16)
                     // (the same two roundings as a run resumed from the returned state)
-                    const float* an = vec_a + ((n + 1) & 1) * 128;
+                    if (!(ok = mbar_wait(&bar[B_PREPD + ((n + 1) & 1)], ((n + 1) >> 1) & 1, ab, status))) break;
+                    const float* an = vec_a + ((n + 1) & 3) * 128;
                     uint32_t da[32], db[32];
                     tmem_ld32(tmem + lane_base + TM_S, da);
                     tmem_ld_wait();
@@ -727,8 +612,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         if (piece < 3) tmem_ld32(tmem + lane_base + TM_S + (piece + 1) * 32, dn);
                         uint32_t x16[16];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            d[e] = __float_as_uint(__uint_as_float(d[e]) * bv[piece * 32 + e] * an[piece * 32 + e]);
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 b4 = *reinterpret_cast<const float4*>(bv + piece * 32 + 4 * e4);
+                            const float4 a4 = *reinterpret_cast<const float4*>(an + piece * 32 + 4 * e4);
+                            const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                d[4 * e4 + q] = __float_as_uint(__uint_as_float(d[4 * e4 + q]) * bb[q] * aa[q]);
+                        }
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             x16[e] = pack_half2(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
@@ -736,141 +627,304 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         tmem_st16(tmem + lane_base + TM_X16 + piece * 16, x16);
                         if (piece < 3) tmem_ld_wait();
                     }
-                }
-                if (j == 0) KDA_TR(n, 30);
-                if (!last) {
                     tmem_st_wait();
-                    if (j == 0) KDA_TR(n, 31);
                     tc_fence_before();
                     mbar_arrive(&bar[B_XRDY]);
+                    if (j == 0) KDA_TR(n, 15);
                 }
-                mbar_arrive(&bar[B_VFREE + b]);
-                if (j == 0) KDA_TR(n, 21);
+                mbar_arrive(&bar[B_VFREE + (n & 3)]);
+                // (i) of the next chunk now if its inputs are ready; otherwise after this
+                // chunk's output is out (so that the output never waits on WT)
+                if (!last && j == 0 && mbar_test(&bar[B_XRDY], (n + 1) & 1) &&
+                    mbar_test(&bar[B_WRDY], (n + 1) & 1)) {
+                    if (!(ok = issue_u(n + 1))) break;
+                    u_issued = true;
+                }
             }
-            {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + TM_O + 32, o);
+            {  // O(n): read out, hand D_O back to (iii-a) of the next chunk, store
+                uint32_t o0[32], o1[32];
+                tmem_ld32(tmem + lane_base + TM_O, o0);
+                tmem_ld32(tmem + lane_base + TM_O + 32, o1);
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&bar[B_OFREE]);
-                if (!(ok = emit_half(o, 1))) break;
+                if (j == 0) KDA_TR(n, 16);
+                if (valid == C) {  // staged through the chunk's KT/QT pair, stored by the TMA
+                    Tout* stg = reinterpret_cast<Tout*>(sm + L::OFF_KQ + b * 32768);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if constexpr (sizeof(Tout) == 2) {
+                            stg[e * kD + j] = __float2bfloat16_rn(__uint_as_float(o0[e]));
+                            stg[(32 + e) * kD + j] = __float2bfloat16_rn(__uint_as_float(o1[e]));
+                        } else {
+                            stg[e * kD + j] = __uint_as_float(o0[e]);
+                            stg[(32 + e) * kD + j] = __uint_as_float(o1[e]);
+                        }
+                    }
+                    // Every thread waits, so no thread can arrive for the next chunk before
+                    // all have arrived for this one.
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bar[B_STG]);
+                    if (!(ok = mbar_wait(&bar[B_STG], (ph_stg++) & 1, ab, status))) break;
+                    if (j == 0) {
+                        for (int q = 0; q < 4; ++q)
+                            tma_store_3d(&tm_out, stg + q * QR * kD, 0, h, (int)(t0 + (int64_t)C * n + QR * q));
+                        bulk_commit();
+                    }
+                } else {  // partial last chunk: plain stores of the rows inside the sequence
+                    const size_t obase = ((size_t)(t0 + (int64_t)C * n) * P.H + h) * kD + j;
+                    const size_t ostride = (size_t)P.H * kD;
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) {
+                        const float v = __uint_as_float(e < 32 ? o0[e] : o1[e - 32]);
+                        if (e < valid) {
+                            if constexpr (sizeof(Tout) == 2)
+                                out[obase + e * ostride] = __float2bfloat16_rn(v);
+                            else
+                                out[obase + e * ostride] = v;
+                        }
+                    }
+                }
+                if (j == 0) KDA_TR(n, 17);
             }
-            if (j == 0) KDA_TR(n, 28);
+            if (!last && j == 0 && !(ok = issue_o(n + 1))) break;  // (iii-a) of the next chunk
         }
         if (j == 0) bulk_wait_all();  // the CTA's shared memory must outlive the bulk stores
     state_done:;
     } else {
         // ------------------------------------------------------------ tri warpgroup
-        // Reads the four M = 64 products of the inverse (row r of a product sits in
-        // TMEM lane 32*(r/16) + r%16, so lanes 0..15 of each warp hold rows).
-        const int q = warp & 3, r = 16 * q + (lane & 15);
-        const bool act = lane < 16;
-        const int a = r >> 4;
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        uint8_t* b1 = sm + L::OFF_B1;
+        const int c = tid - 384;  // TMEM lane: Gram row / key channel
+        const int wi = warp - 12;
+        const uint32_t lane_base = (uint32_t)(wi * 32) << 16;
+        float* inv = reinterpret_cast<float*>(sm + L::OFF_INV);
+        auto Ab = [&](int a, int bb) { return inv + (a * (a + 1) / 2 + bb) * kBlk; };  // A_ab, b <= a
+        float* Tg = inv + 10 * kBlk;  // Dg_0..3, then T_10, T_21, T_20
+        float* T10 = Tg + 4 * kBlk;
+        float* T21 = Tg + 5 * kBlk;
+        float* T20 = Tg + 6 * kBlk;
         uint8_t* nr = sm + L::OFF_NR;
-        const float* dblk = dfp + r * 16;  // row r of its 16x16 diagonal inverse block
+        uint32_t ph_tb = 0;
+        auto wg_sync = [&]() -> bool {
+            tc_fence_before();
+            mbar_arrive(&bar[B_TB]);
+            const bool r = mbar_wait(&bar[B_TB], (ph_tb++) & 1, ab, status);
+            tc_fence_after();
+            return r;
+        };
+        // NR blocks above the diagonal are never written again: zero them once.
+        for (int i = c; i < 8192 / 16; i += 128) reinterpret_cast<uint4*>(nr)[i] = make_uint4(0u, 0u, 0u, 0u);
+        const int r = lane >> 1;  // block row of this lane in the column stage
         for (int n = 0; n < nch; ++n) {
-            uint32_t r0[32], r1[32];
-            // readout 1: N -> NR
-            if (!mbar_wait(&bar[B_S1D], n & 1, ab, status)) break;
-            tc_fence_after();
-            tmem_ld32(tmem + lane_base + TM_W, r0);
-            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
-            tmem_ld_wait();
-            if (act) store_row16(nr, r, r0, r1);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar[B_C1]);
-            if (tid == 384) {  // S2: D_W = N N
-                if (!mbar_wait(&bar[B_C1], n & 1, ab, status)) break;
-                tc_fence_after();
-                for (int st = 0; st < 4; ++st)
-                    mma_ss(tmem + TM_W, k_desc(snr + st * 32), mn_desc(snr + st * 2048, 8192), ID_T2, st > 0);
-                mma_commit(&bar[B_S2D]);
-                KDA_TR(n, 13);
-            }
-            // readout 2: N2 -> B1
-            if (!mbar_wait(&bar[B_S2D], n & 1, ab, status)) break;
-            tc_fence_after();
-            tmem_ld32(tmem + lane_base + TM_W, r0);
-            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
-            tmem_ld_wait();
-            if (act) store_row16(b1, r, r0, r1);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar[B_C2]);
-            if (tid == 384) {  // S3: D_W = N2 Dg
-                if (!mbar_wait(&bar[B_C2], n & 1, ab, status)) break;
-                tc_fence_after();
-                for (int st = 0; st < 4; ++st)
-                    mma_ss(tmem + TM_W, k_desc(sb1 + st * 32), k_desc(sdt + st * 32), ID_T3, st > 0);
-                mma_commit(&bar[B_S3D]);
-                KDA_TR(n, 14);
-            }
-            // readout 3: M = Dg + N2 Dg; -M -> B1
-            if (!mbar_wait(&bar[B_S3D], n & 1, ab, status)) break;
-            tc_fence_after();
-            tmem_ld32(tmem + lane_base + TM_W, r0);
-            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
-            tmem_ld_wait();
-            if (act) {
-                add_block16(r0, r1, a, dblk);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    r0[e] ^= 0x80000000u;
-                    r1[e] ^= 0x80000000u;
-                }
-                store_row16(b1, r, r0, r1);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar[B_C3]);
-            if (tid == 384) {  // S4: D_W += N (-M)
-                if (!mbar_wait(&bar[B_C3], n & 1, ab, status)) break;
-                tc_fence_after();
-                for (int st = 0; st < 4; ++st)
-                    mma_ss(tmem + TM_W, k_desc(snr + st * 32), mn_desc(sb1 + st * 2048, 8192), ID_T2, 1);
-                mma_commit(&bar[B_TDONE]);
-                KDA_TR(n, 15);
-            }
-            // readout 4: T = Dg + (N2 Dg - N M); T diag(beta) -> NR (K-major B of the WY products)
-            if (!mbar_wait(&bar[B_TDONE], n & 1, ab, status)) break;
-            tc_fence_after();
-            tmem_ld32(tmem + lane_base + TM_W, r0);
-            tmem_ld32(tmem + lane_base + TM_W + 32, r1);
-            tmem_ld_wait();
+            const int b = n & 1;
+            const float* bt = sbeta + (n & 3) * 64;
+            // T diag(beta)[16 rb + r][cb + q] for q < 4 into NR (fp16)
+            auto nr_store = [&](int row, int col, const float (&t)[4]) {
+                const uint32_t w0 = pack_half2(t[0] * bt[col], t[1] * bt[col + 1]);
+                const uint32_t w1 = pack_half2(t[2] * bt[col + 2], t[3] * bt[col + 3]);
+                *reinterpret_cast<uint2*>(nr + sw128(row, col >> 3) + (col & 7) * 2) = make_uint2(w0, w1);
+            };
+            // ---- P2: read the Gram; rows 0..63 -> A (beta_r applied, strictly lower, fp32
+            // blocks), rows 64..127 -> P (lower triangle including the diagonal, fp16)
+            if (!mbar_wait(&bar[B_GDONE], n & 1, ab, status)) break;
             if (!mbar_wait(&bar[B_BFULL + (n & 3)], (n >> 2) & 1, ab, status)) break;
-            if (act) {
-                add_block16(r0, r1, a, dblk);
-                const float* bt = sbeta + (n & 3) * 64;
-                const int64_t vld = len - (int64_t)C * n;
+            tc_fence_after();
+            if (c == 0) KDA_TR(n, 4);
+            uint32_t pr[32];  // P row (c >= 64), packed fp16, written after the WY issue
+            {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + lane_base + TM_G, r0);
+                tmem_ld32(tmem + lane_base + TM_G + 32, r1);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&bar[B_P2D]);
+                if (c < 64) {
+                    const float br = bt[c];
+                    const int a = c >> 4, i = c & 15;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    r0[e] = __float_as_uint(e < vld ? __uint_as_float(r0[e]) * bt[e] : 0.f);
-                    r1[e] = __float_as_uint(e + 32 < vld ? __uint_as_float(r1[e]) * bt[e + 32] : 0.f);
+                    for (int bb = 0; bb < 4; ++bb) {
+                        if (bb <= a) {
+                            float* dst = Ab(a, bb) + i * kBS;
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                float w[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const int e = 16 * bb + 4 * e4 + q;
+                                    const float gv = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
+                                    w[q] = e < c ? br * gv : 0.f;
+                                }
+                                st4(dst + 4 * e4, w);
+                            }
+                        }
+                    }
+                } else {
+                    const int rr = c - 64;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int e0 = 2 * e, e1 = 2 * e + 1;
+                        const float v0 = __uint_as_float(e0 < 32 ? r0[e0] : r1[e0 - 32]);
+                        const float v1 = __uint_as_float(e1 < 32 ? r0[e1] : r1[e1 - 32]);
+                        pr[e] = pack_half2(e0 <= rr ? v0 : 0.f, e1 <= rr ? v1 : 0.f);
+                    }
                 }
-                store_row16(nr, r, r0, r1);
             }
-            mbar_arrive(&bar[B_BFREE + (n & 3)]);
+            if (!wg_sync()) break;  // A written
+            if (c == 0) KDA_TR(n, 5);
+            // ---- diagonal blocks: Dg_wi column `lane` by right-looking substitution
+            if (lane < 16) {
+                const float* blk = Ab(wi, wi);
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
+#pragma unroll
+                for (int rr = 0; rr < 15; ++rr) {
+                    const float xr = x[rr];
+#pragma unroll
+                    for (int i = rr + 1; i < 16; ++i) x[i] = fmaf(-blk[i * kBS + rr], xr, x[i]);
+                }
+                float* dg = Tg + wi * kBlk;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) dg[i * kBS + lane] = x[i];
+            }
+            if (!wg_sync()) break;  // Dg written; the A diagonal blocks are free as scratch
+            if (c == 0) KDA_TR(n, 6);
+            // ---- blocks below the diagonal, by block column (T_ab = -Dg_a Z_ab)
+            {
+                float t[4];
+                auto zero = [](float (&v)[4]) { v[0] = v[1] = v[2] = v[3] = 0.f; };
+                auto neg = [](float (&v)[4]) { v[0] = -v[0]; v[1] = -v[1]; v[2] = -v[2]; v[3] = -v[3]; };
+                // Dg_wi itself into NR
+                {
+                    const int hf = lane & 1;
+                    const float* src = Tg + wi * kBlk + r * kBS + 8 * hf;
+                    const int col = 16 * wi + 8 * hf;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_half2(src[2 * e] * bt[col + 2 * e], src[2 * e + 1] * bt[col + 2 * e + 1]);
+                    *reinterpret_cast<uint4*>(nr + sw128(16 * wi + r, col >> 3)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                if (wi < 2) {  // block column 0, columns c0 .. c0+3
+                    const int c0 = 8 * wi + 4 * (lane & 1);
+                    float* zs = Ab(0, 0);
+                    float z10[4] = {0.f, 0.f, 0.f, 0.f}, z20[4] = {0.f, 0.f, 0.f, 0.f}, z30[4] = {0.f, 0.f, 0.f, 0.f};
+                    mac16x3(Ab(1, 0) + r * kBS, Ab(2, 0) + r * kBS, Ab(3, 0) + r * kBS, Tg + c0, z10, z20, z30);
+                    // T_10
+                    st4(zs + r * kBS + c0, z10);
+                    __syncwarp();
+                    zero(t);
+                    mac16(Tg + 1 * kBlk + r * kBS, zs + c0, t);
+                    neg(t);
+                    st4(T10 + r * kBS + c0, t);
+                    nr_store(16 + r, c0, t);
+                    __syncwarp();
+                    // T_20
+                    mac16x2(Ab(2, 1) + r * kBS, Ab(3, 1) + r * kBS, T10 + c0, z20, z30);
+                    st4(zs + r * kBS + c0, z20);
+                    __syncwarp();
+                    zero(t);
+                    mac16(Tg + 2 * kBlk + r * kBS, zs + c0, t);
+                    neg(t);
+                    st4(T20 + r * kBS + c0, t);
+                    nr_store(32 + r, c0, t);
+                    __syncwarp();
+                    // T_30
+                    mac16(Ab(3, 2) + r * kBS, T20 + c0, z30);
+                    st4(zs + r * kBS + c0, z30);
+                    __syncwarp();
+                    zero(t);
+                    mac16(Tg + 3 * kBlk + r * kBS, zs + c0, t);
+                    neg(t);
+                    nr_store(48 + r, c0, t);
+                } else {  // block column 1 (columns c0 .. c0+3); warp 15 also block column 2
+                    const int c0 = 8 * (wi - 2) + 4 * (lane & 1);
+                    const int c2 = 8 * (lane & 1);  // T_32: columns c2 .. c2+7 (warp 15)
+                    float* zs = Ab(1, 1);
+                    float* zs2 = Ab(2, 2);
+                    float z21[4] = {0.f, 0.f, 0.f, 0.f}, z31[4] = {0.f, 0.f, 0.f, 0.f};
+                    mac16x2(Ab(2, 1) + r * kBS, Ab(3, 1) + r * kBS, Tg + 1 * kBlk + c0, z21, z31);
+                    if (wi == 3) {
+                        float za[4] = {0.f, 0.f, 0.f, 0.f}, zb[4] = {0.f, 0.f, 0.f, 0.f};
+                        mac16(Ab(3, 2) + r * kBS, Tg + 2 * kBlk + c2, za);
+                        mac16(Ab(3, 2) + r * kBS, Tg + 2 * kBlk + c2 + 4, zb);
+                        st4(zs2 + r * kBS + c2, za);
+                        st4(zs2 + r * kBS + c2 + 4, zb);
+                    }
+                    // T_21 (and T_32)
+                    st4(zs + r * kBS + c0, z21);
+                    __syncwarp();
+                    zero(t);
+                    mac16(Tg + 2 * kBlk + r * kBS, zs + c0, t);
+                    neg(t);
+                    st4(T21 + r * kBS + c0, t);
+                    nr_store(32 + r, 16 + c0, t);
+                    if (wi == 3) {
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            zero(t);
+                            mac16(Tg + 3 * kBlk + r * kBS, zs2 + c2 + 4 * h2, t);
+                            neg(t);
+                            nr_store(48 + r, 32 + c2 + 4 * h2, t);
+                        }
+                    }
+                    __syncwarp();
+                    // T_31
+                    mac16(Ab(3, 2) + r * kBS, T21 + c0, z31);
+                    st4(zs + r * kBS + c0, z31);
+                    __syncwarp();
+                    zero(t);
+                    mac16(Tg + 3 * kBlk + r * kBS, zs + c0, t);
+                    neg(t);
+                    nr_store(48 + r, 16 + c0, t);
+                }
+            }
             fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar[B_TRDY]);
-            KDA_TR(n, 6);
-            if (tid == 384) {  // WY products, once U16 of chunk n-1 (over D_U) has been consumed
-                if (!mbar_wait(&bar[B_TRDY], n & 1, ab, status)) break;
-                if (!mbar_wait(&bar[B_PREPD + (n & 1)], (n >> 1) & 1, ab, status)) break;
+            if (!wg_sync()) break;  // NR = T diag(beta) complete
+            if (c == 0) KDA_TR(n, 7);
+            mbar_arrive(&bar[B_BFREE + (n & 3)]);
+            if (c == 0) {  // WY products, once V16/KT of the chunk are ready and D(n-1) has consumed U16
+                if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) break;
                 if (n > 0 && !mbar_wait(&bar[B_SDONE], (n - 1) & 1, ab, status)) break;
                 tc_fence_after();
-                const uint32_t kt = sm_base + L::OFF_KQ + (n & 1) * 32768, v16 = TM_V16 + (n & 1) * 32;
+                const uint32_t kt = sm_base + L::OFF_KQ + b * 32768, v16 = TM_V16 + b * 32;
+                const uint32_t snr = sm_base + L::OFF_NR;
                 for (int st = 0; st < 4; ++st) {
                     const uint64_t bd = k_desc(snr + st * 32);
                     mma_ss(tmem + TM_W, k_desc(kt + st * 32), bd, ID_KK, st > 0);
                     mma_ts(tmem + TM_U, tmem + v16 + st * 8, bd, ID_KK, st > 0);
                 }
                 mma_commit(&bar[B_WYDONE]);
-                KDA_TR(n, 9);
+                mma_commit(&bar[B_V16FREE + b]);
+                KDA_TR(n, 8);
             }
+            if (c >= 64) {  // P of this chunk, once the D products of chunk n - NPP are done with PP
+                if (n >= L::NPP) {
+                    const int m = n - L::NPP;
+                    if (!mbar_wait(&bar[B_KQFREE + (m & 1)], (m >> 1) & 1, ab, status)) break;
+                }
+                store_row16_packed(sm + L::OFF_PP + (n % L::NPP) * 8192, c - 64, pr);
+            }
+            // ---- P4: WT = -W^T (fp16), once the WY products are complete and (i) of
+            // chunk n - 1 has consumed the previous WT
+            if (!mbar_wait(&bar[B_WYDONE], n & 1, ab, status)) break;
+            tc_fence_after();
+            {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + lane_base + TM_W, r0);
+                tmem_ld32(tmem + lane_base + TM_W + 32, r1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    r0[e] ^= 0x80000000u;
+                    r1[e] ^= 0x80000000u;
+                }
+                if (n > 0 && !mbar_wait(&bar[B_UIDONE], (n - 1) & 1, ab, status)) break;
+                store_row16(sm + L::OFF_WT, c, r0, r1);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar[B_WRDY]);
+            if (c == 0) KDA_TR(n, 9);
         }
     }
 
