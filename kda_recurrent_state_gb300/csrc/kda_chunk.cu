@@ -55,6 +55,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
@@ -68,8 +69,7 @@ constexpr int QR = 16;  // token rows per input slot
 constexpr int NTHREADS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxExp2 = 15.0f;  // |g - ref| bound (log2 units) for fp16 operands
-constexpr int kBS = 20;            // row stride (floats) of a 16x16 fp32 block of A or T
-constexpr int kBlk = 16 * kBS;     // floats per block
+constexpr int kBlk = 256;          // floats per 16x16 fp32 block of A or T (see bsw)
 
 // TMEM column map (512 columns allocated).  The fp16 U operand is written over
 // the first 32 columns of the U accumulator once that has been read out; V16
@@ -80,36 +80,49 @@ constexpr uint32_t TM_S = 0, TM_X16 = 128, TM_U = 192, TM_U16 = 192, TM_O = 256,
 template <typename Tin>
 struct Cfg {
     static constexpr int ES = sizeof(Tin);
-    static constexpr int NSLOT = ES == 2 ? 3 : 2;
-    static constexpr int NPP = ES == 2 ? 2 : 1;  // P buffers (fp32 inputs trade overlap for smem)
+#ifndef KDA_CFG_NSLOT
+#define KDA_CFG_NSLOT 2
+#endif
+#ifndef KDA_CFG_STG_OWN
+#define KDA_CFG_STG_OWN 1
+#endif
+    static constexpr int NSLOT = ES == 2 ? KDA_CFG_NSLOT : 2;  // input ring slots (tiles are pulled into L2 ahead)
+    static constexpr int NPP = 1;                              // P buffers
+    static constexpr bool STG_OWN = ES == 2 && KDA_CFG_STG_OWN;  // own staging buffer for the output (else KT/QT)
     static constexpr uint32_t SLOT_Q = 0;
     static constexpr uint32_t SLOT_K = QR * 128 * ES;
     static constexpr uint32_t SLOT_V = 2 * QR * 128 * ES;
     static constexpr uint32_t SLOT_LA = 3 * QR * 128 * ES;
     static constexpr uint32_t SLOT_BYTES = 3 * QR * 128 * ES + QR * 128 * 4;
     // shared memory map (offsets from a 1024-byte aligned base)
-    static constexpr uint32_t OFF_KQ = 0;                    // [2] x (KT 16K | QT 16K); then output staging
+    static constexpr uint32_t OFF_KQ = 0;                    // [2] x (KT 16K | QT 16K)
     static constexpr uint32_t OFF_KH = 65536;                // [2] x 16K
     static constexpr uint32_t OFF_PP = 98304;                // [NPP] x 8K
     static constexpr uint32_t OFF_WT = OFF_PP + NPP * 8192;  // 16K
     static constexpr uint32_t OFF_NR = OFF_WT + 16384;       // 8K
-    static constexpr uint32_t OFF_INV = OFF_NR + 8192;       // 17 fp32 blocks: A (10), Dg (4), T10, T21, T20
-    static constexpr uint32_t OFF_RING = OFF_INV + 17 * kBlk * 4;
-    static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[4][128], b[4][128]
-    static constexpr uint32_t OFF_BETA = OFF_VEC + 8 * 128 * 4;         // [4][64]
+    static constexpr uint32_t OFF_INV = OFF_NR + 8192;       // 17 fp32 blocks: A (10), Dg (4), T10, T20, T21
+    static constexpr uint32_t OFF_STG = OFF_INV + 17 * kBlk * 4;              // 64 output rows (STG_OWN)
+    static constexpr uint32_t OFF_RING = OFF_STG + (STG_OWN ? 64 * 128 * 4 : 0);
+    static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[3][128], b[3][128]
+    static constexpr uint32_t OFF_BETA = OFF_VEC + 6 * 128 * 4;         // [4][64]
     static constexpr uint32_t OFF_BAR = OFF_BETA + 4 * 64 * 4;
     static constexpr uint32_t NBAR = 40;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+#ifdef KDA_TRACE
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 32 * 24 * 4 + 1024;
+#else
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+#endif
 };
 static_assert(Cfg<__nv_bfloat16>::SMEM_BYTES <= 232448, "smem budget (bf16)");
 static_assert(Cfg<float>::SMEM_BYTES <= 232448, "smem budget (fp32)");
 static_assert(Cfg<__nv_bfloat16>::OFF_RING % 128 == 0 && Cfg<float>::OFF_RING % 128 == 0, "TMA destinations");
+static_assert(Cfg<__nv_bfloat16>::OFF_STG % 128 == 0, "TMA store source");
 
 // barrier indices
 enum {
-    B_FULL = 0,      // [3] input slot landed
-    B_EMPTY = 3,     // [3] input slot consumed
+    B_FULL = 0,      // [NSLOT] input slot landed
+    B_EMPTY = 3,     // [NSLOT] input slot consumed
     B_PREPD = 6,     // [2] KT/QT/KH, V16, vectors of a chunk ready
     B_GDONE = 8,     // Gram complete
     B_P2D = 9,       // Gram read out: D_G free
@@ -124,22 +137,28 @@ enum {
     B_KQFREE = 19,   // [2] KH and PP of a chunk consumed
     B_OFREE = 21,    // D_O read out
     B_STG = 22,      // output staging tile written by the whole state warpgroup
-    B_STGFREE = 23,  // [2] KT/QT pair free again (staged output read by the bulk store)
+    B_STGFREE = 23,  // [2] KT/QT pair free again (staged output read by the bulk store; !STG_OWN)
     B_BFULL = 25,    // [4] beta of a chunk loaded (ring of 4, by chunk index mod 4)
     B_BFREE = 29,    // [4] beta ring slot consumed
-    B_VFREE = 33,    // [4] decay vectors of a chunk consumed
+    B_VFREE = 33,    // [3] decay vectors of a chunk consumed (ring of 3, by chunk index mod 3)
+    B_STGR = 36,     // own staging buffer read by the previous bulk store (STG_OWN)
     B_COUNT = 37
 };
 static_assert(B_COUNT <= (int)Cfg<float>::NBAR, "barrier space");
 
 #ifdef KDA_TRACE
-// Debug timeline (compiled only with -DKDA_TRACE): clock64 stamps of each
-// role's milestones for the first 64 chunks of CTA 0.
-constexpr int kTrEv = 24;
-__device__ unsigned long long g_trace[64 * kTrEv];
-#define KDA_TR(n, ev)                                                                                    \
-    do {                                                                                                 \
-        if (blockIdx.x == 0 && (n) < 64) g_trace[(n) * kTrEv + (ev)] = (unsigned long long)clock64(); \
+// Debug timeline (compiled only with -DKDA_TRACE): clock() stamps of each role's
+// milestones for chunks 16..47 of CTA 0, kept in shared memory (a global store
+// would delay the next barrier arrive) and copied out when the CTA ends.
+#ifndef KDA_TRACE_FIRST
+#define KDA_TRACE_FIRST 16
+#endif
+constexpr int kTrEv = 32, kTrN0 = KDA_TRACE_FIRST, kTrN = 24;
+__device__ unsigned int g_trace[kTrN * kTrEv];
+#define KDA_TR(n, ev)                                                                       \
+    do {                                                                                    \
+        if (blockIdx.x == 0 && (n) >= kTrN0 && (n) < kTrN0 + kTrN)                          \
+            trace_sm[((n) - kTrN0) * kTrEv + (ev)] = (unsigned int)clock();                 \
     } while (0)
 #else
 #define KDA_TR(n, ev) \
@@ -173,13 +192,30 @@ __device__ __forceinline__ void store_row16_packed(uint8_t* tile, uint32_t row, 
             make_uint4(p[4 * c16], p[4 * c16 + 1], p[4 * c16 + 2], p[4 * c16 + 3]);
 }
 
-// acc[q] += sum_m arow[m] * bcol[m * kBS + q]  (one row of a 16x16 block times
-// four columns of another; both fp32 in shared memory, 16-byte aligned).
-__device__ __forceinline__ void mac16(const float* arow, const float* bcol, float (&acc)[4]) {
+// fp32 16x16 blocks of A and T in shared memory: row r holds its 16 values as four
+// 16-byte chunks, chunk k stored at position k ^ ((r >> 1) & 3), so that the sixteen
+// rows of a block read at the same chunk index fall in distinct bank groups.
+__device__ __forceinline__ int bsw(int r, int k4) { return r * 16 + ((k4 ^ ((r >> 1) & 3)) << 2); }
+
+// Four columns 4*c4 .. 4*c4+3 of a block, as per-row-group base pointers
+// (row m reads p[(m >> 1) & 3] + 16 m).
+struct BCol {
+    const float* p[4];
+};
+__device__ __forceinline__ BCol bcol(const float* blk, int c4) {
+    BCol b;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) b.p[s] = blk + ((c4 ^ s) << 2);
+    return b;
+}
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// acc[q] += sum_m A[r][m] * B[m][4 c4 + q] with row r of A given by its chunk offsets.
+__device__ __forceinline__ void mac16(const float* A, const int (&aoff)[4], const BCol& B, float (&acc)[4]) {
     float a[16];
 #pragma unroll
     for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 t = *reinterpret_cast<const float4*>(arow + 4 * k4);
+        const float4 t = ld4(A + aoff[k4]);
         a[4 * k4] = t.x;
         a[4 * k4 + 1] = t.y;
         a[4 * k4 + 2] = t.z;
@@ -187,50 +223,11 @@ __device__ __forceinline__ void mac16(const float* arow, const float* bcol, floa
     }
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        const float4 bv = *reinterpret_cast<const float4*>(bcol + m * kBS);
+        const float4 bv = ld4(B.p[(m >> 1) & 3] + 16 * m);
         acc[0] = fmaf(a[m], bv.x, acc[0]);
         acc[1] = fmaf(a[m], bv.y, acc[1]);
         acc[2] = fmaf(a[m], bv.z, acc[2]);
         acc[3] = fmaf(a[m], bv.w, acc[3]);
-    }
-}
-// The same for two / three rows of different left blocks sharing the right block.
-__device__ __forceinline__ void mac16x2(const float* a0, const float* a1, const float* bcol, float (&c0)[4],
-                                        float (&c1)[4]) {
-#pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 x0 = *reinterpret_cast<const float4*>(a0 + 4 * m4);
-        const float4 x1 = *reinterpret_cast<const float4*>(a1 + 4 * m4);
-        const float u0[4] = {x0.x, x0.y, x0.z, x0.w}, u1[4] = {x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 bv = *reinterpret_cast<const float4*>(bcol + (4 * m4 + k) * kBS);
-            c0[0] = fmaf(u0[k], bv.x, c0[0]); c0[1] = fmaf(u0[k], bv.y, c0[1]);
-            c0[2] = fmaf(u0[k], bv.z, c0[2]); c0[3] = fmaf(u0[k], bv.w, c0[3]);
-            c1[0] = fmaf(u1[k], bv.x, c1[0]); c1[1] = fmaf(u1[k], bv.y, c1[1]);
-            c1[2] = fmaf(u1[k], bv.z, c1[2]); c1[3] = fmaf(u1[k], bv.w, c1[3]);
-        }
-    }
-}
-__device__ __forceinline__ void mac16x3(const float* a0, const float* a1, const float* a2, const float* bcol,
-                                        float (&c0)[4], float (&c1)[4], float (&c2)[4]) {
-#pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 x0 = *reinterpret_cast<const float4*>(a0 + 4 * m4);
-        const float4 x1 = *reinterpret_cast<const float4*>(a1 + 4 * m4);
-        const float4 x2 = *reinterpret_cast<const float4*>(a2 + 4 * m4);
-        const float u0[4] = {x0.x, x0.y, x0.z, x0.w}, u1[4] = {x1.x, x1.y, x1.z, x1.w},
-                    u2[4] = {x2.x, x2.y, x2.z, x2.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 bv = *reinterpret_cast<const float4*>(bcol + (4 * m4 + k) * kBS);
-            c0[0] = fmaf(u0[k], bv.x, c0[0]); c0[1] = fmaf(u0[k], bv.y, c0[1]);
-            c0[2] = fmaf(u0[k], bv.z, c0[2]); c0[3] = fmaf(u0[k], bv.w, c0[3]);
-            c1[0] = fmaf(u1[k], bv.x, c1[0]); c1[1] = fmaf(u1[k], bv.y, c1[1]);
-            c1[2] = fmaf(u1[k], bv.z, c1[2]); c1[3] = fmaf(u1[k], bv.w, c1[3]);
-            c2[0] = fmaf(u2[k], bv.x, c2[0]); c2[1] = fmaf(u2[k], bv.y, c2[1]);
-            c2[2] = fmaf(u2[k], bv.z, c2[2]); c2[3] = fmaf(u2[k], bv.w, c2[3]);
-        }
     }
 }
 __device__ __forceinline__ void st4(float* p, const float (&v)[4]) {
@@ -248,9 +245,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
     Abort* ab = reinterpret_cast<Abort*>(sm + L::OFF_MISC + 16);
-    float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);         // [4][128] e^{ref}
-    float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 2048);  // [4][128] e^{g_63 - ref}
+    float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);         // [3][128] e^{ref}
+    float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 1536);  // [3][128] e^{g_63 - ref}
     float* sbeta = reinterpret_cast<float*>(sm + L::OFF_BETA);        // [4][64]
+#ifdef KDA_TRACE
+    unsigned int* trace_sm = reinterpret_cast<unsigned int*>(sm + L::OFF_MISC + 64);
+#endif
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x;
@@ -279,8 +279,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bar[B_BFULL + i], 32);
             mbar_init(&bar[B_BFREE + i], 128);
-            mbar_init(&bar[B_VFREE + i], 128);
         }
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[B_VFREE + i], 128);
+        mbar_init(&bar[B_STGR], 1);
         ab->flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -373,18 +374,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // is 0 too), which makes them identity steps; q and v of such rows only
         // reach outputs that are never stored.
         auto prep1 = [&](int n) -> bool {
-            const int b = n & 1, v4 = n & 3;
+            const int b = n & 1, v3 = n % 3;
             if (c == 0) KDA_TR(n, 0);
             if (n >= 2) {  // the buffers of chunk n - 2
                 const uint32_t par = ((n - 2) >> 1) & 1;
-                if (!mbar_wait(&bar[B_KQFREE + b], par, ab, status)) return false;   // KH (D products)
+                if (!mbar_wait(&bar[B_KQFREE + b], par, ab, status)) return false;  // KT/QT/KH (products)
                 if (c == 0) KDA_TR(n, 18);
-                if (!mbar_wait(&bar[B_STGFREE + b], par, ab, status)) return false;  // KT/QT (staged output)
+                if constexpr (!L::STG_OWN)  // KT/QT also staged the output of chunk n - 2
+                    if (!mbar_wait(&bar[B_STGFREE + b], par, ab, status)) return false;
                 if (c == 0) KDA_TR(n, 19);
                 if (!mbar_wait(&bar[B_V16FREE + b], par, ab, status)) return false;  // V16 (WY products)
                 if (c == 0) KDA_TR(n, 20);
             }
-            if (n >= 4 && !mbar_wait(&bar[B_VFREE + v4], ((n - 4) >> 2) & 1, ab, status)) return false;
+            if (n >= 3 && !mbar_wait(&bar[B_VFREE + v3], ((n - 3) / 3) & 1, ab, status)) return false;
             if (c == 0) KDA_TR(n, 21);
             tc_fence_after();
             const int valid = (int)((len - (int64_t)C * n) < C ? (len - (int64_t)C * n) : C);
@@ -399,19 +401,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // pass A over rows 0..31: the reference ref = g_31
             if (!wait_slot(0) || !wait_slot(1)) return false;
             if (c == 0) KDA_TR(n, 1);
-            float g2 = 0.f;
+            const bool full = valid == C;
+            float ref = 0.f;
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
                 const uint8_t* sl = slot_ptr(r >> 4);
                 const float la = reinterpret_cast<const float*>(sl + L::SLOT_LA)[(r & 15) * 128 + c];
-                g2 += (r < valid) ? la * kLog2e : 0.f;
+                ref += (full || r < valid) ? la : 0.f;
             }
-            const float ref = g2;
-            // pass B, one 16-row quarter at a time
-            g2 = 0.f;
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                if (q >= 2 && !wait_slot(q)) return false;
+            ref *= kLog2e;
+            if (c == 0) KDA_TR(n, 28);
+            // pass B, one 16-row quarter at a time.  g decreases monotonically (log alpha
+            // <= 0), so |g - ref| is largest at the chunk's first or last row: the range
+            // check looks at those two.
+            float g2 = 0.f;
+            auto quarter = [&](int q, auto full_chunk) {
+                constexpr bool FULL = decltype(full_chunk)::value;
                 const uint8_t* sl = slot_ptr(q);
                 const float* sla = reinterpret_cast<const float*>(sl + L::SLOT_LA);
                 const Tin* sk = reinterpret_cast<const Tin*>(sl + L::SLOT_K);
@@ -421,26 +426,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 uint32_t pk[8], pq[8], ph[8], pv[8];
 #pragma unroll
                 for (int rp = 0; rp < QR / 2; ++rp) {
-                    float kv2[2], qv2[2], hv2[2], vv2[2];
+                    float kk[2], qq[2], e1[2], e2[2], vv2[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int rr = 2 * rp + e;
-                        const bool on = rr < vq;
+                        const bool on = FULL || rr < vq;
                         const float la = on ? sla[rr * 128 + c] : 0.f;
-                        const float kk = on ? ld_in(sk, rr * 128 + c) : 0.f;
-                        const float qq = ld_in(sq, rr * 128 + c);
+                        kk[e] = on ? ld_in(sk, rr * 128 + c) : 0.f;
+                        qq[e] = ld_in(sq, rr * 128 + c);
                         vv2[e] = ld_in(sv, rr * 128 + c);
                         g2 = fmaf(la, kLog2e, g2);
                         const float x = g2 - ref;
-                        max_x = fmaxf(max_x, fabsf(x));
-                        const float e1 = fast_exp2(x), e2 = fast_exp2(-x);
-                        kv2[e] = kk * e1;
-                        qv2[e] = qq * e1;
-                        hv2[e] = kk * e2;
+                        if (rr == 0 || rr == QR - 1) max_x = fmaxf(max_x, fabsf(x));
+                        e1[e] = fast_exp2(x);
+                        e2[e] = fast_exp2(-x);
                     }
-                    pk[rp] = pack_half2(kv2[0], kv2[1]);
-                    pq[rp] = pack_half2(qv2[0], qv2[1]);
-                    ph[rp] = pack_half2(hv2[0], hv2[1]);
+                    pk[rp] = pack_half2(kk[0] * e1[0], kk[1] * e1[1]);
+                    pq[rp] = pack_half2(qq[0] * e1[0], qq[1] * e1[1]);
+                    ph[rp] = pack_half2(kk[0] * e2[0], kk[1] * e2[1]);
                     pv[rp] = pack_half2(vv2[0], vv2[1]);
                 }
                 mbar_arrive(&bar[B_EMPTY + (4 * n + q) % L::NSLOT]);
@@ -452,9 +455,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     *reinterpret_cast<uint4*>(kh + off) = make_uint4(ph[4 * g8], ph[4 * g8 + 1], ph[4 * g8 + 2], ph[4 * g8 + 3]);
                 }
                 tmem_st8(tmem + lane_base + TM_V16 + b * 32 + q * 8, pv);
+            };
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                if (q >= 2 && !wait_slot(q)) return false;
+                if (full)
+                    quarter(q, std::true_type{});
+                else
+                    quarter(q, std::false_type{});
+                if (c == 0 && q == 1) KDA_TR(n, 29);
             }
-            vec_a[v4 * 128 + c] = fast_exp2(ref);
-            vec_b[v4 * 128 + c] = fast_exp2(g2 - ref);
+            vec_a[v3 * 128 + c] = fast_exp2(ref);
+            vec_b[v3 * 128 + c] = fast_exp2(g2 - ref);
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -464,9 +476,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) return false;
                 if (n > 0 && !mbar_wait(&bar[B_P2D], (n - 1) & 1, ab, status)) return false;
                 tc_fence_after();
-                const uint32_t kq = sm_base + L::OFF_KQ + b * 32768, khb = sm_base + L::OFF_KH + b * 16384;
-                for (int st = 0; st < 8; ++st)
-                    mma_ss(tmem + TM_G, mn_desc(kq + st * 2048, 16384), mn_desc(khb + st * 2048, 8192), ID_G, st > 0);
+                const uint64_t da = mn_desc(sm_base + L::OFF_KQ + b * 32768, 16384);
+                const uint64_t db = mn_desc(sm_base + L::OFF_KH + b * 16384, 8192);
+#pragma unroll
+                for (int st = 0; st < 8; ++st) mma_ss(tmem + TM_G, da + 128u * st, db + 128u * st, ID_G, st > 0);
                 mma_commit(&bar[B_GDONE]);
                 KDA_TR(n, 3);
             }
@@ -488,9 +501,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!mbar_wait(&bar[B_XRDY], m & 1, ab, status)) return false;
             if (!mbar_wait(&bar[B_WRDY], m & 1, ab, status)) return false;
             tc_fence_after();
-            const uint32_t wt = sm_base + L::OFF_WT;
-            for (int st = 0; st < 8; ++st)
-                mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, mn_desc(wt + st * 2048, 8192), ID_MN, 1);
+            KDA_TR(m, 24);
+            const uint64_t db = mn_desc(sm_base + L::OFF_WT, 8192);
+#pragma unroll
+            for (int st = 0; st < 8; ++st) mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, db + 128u * st, ID_MN, 1);
             mma_commit(&bar[B_UIDONE]);
             KDA_TR(m, 10);
             return true;
@@ -499,9 +513,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto issue_o = [&](int m) -> bool {
             if (m > 0 && !mbar_wait(&bar[B_OFREE], (m - 1) & 1, ab, status)) return false;
             tc_fence_after();
-            const uint32_t qt = sm_base + L::OFF_KQ + (m & 1) * 32768 + 16384;
-            for (int st = 0; st < 8; ++st)
-                mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, mn_desc(qt + st * 2048, 8192), ID_MN, st > 0);
+            const uint64_t db = mn_desc(sm_base + L::OFF_KQ + (m & 1) * 32768 + 16384, 8192);
+#pragma unroll
+            for (int st = 0; st < 8; ++st) mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, db + 128u * st, ID_MN, st > 0);
             KDA_TR(m, 11);
             return true;
         };
@@ -531,12 +545,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int b = n & 1;
             const int valid = (int)((len - (int64_t)C * n) < C ? (len - (int64_t)C * n) : C);
             const bool last = (n + 1 == nch);
-            // S2(n): U16 = fp16(U^T).  Thread 0 first hands back the KT/QT pair that
-            // staged the previous chunk's output, once the bulk store has read it, and
-            // issues (i) of this chunk if WT was not ready earlier.
+            // S2(n): U16 = fp16(U^T).  Thread 0 first hands back the buffer that staged
+            // the previous chunk's output, once the bulk store has read it, and issues
+            // (i) of this chunk if WT was not ready earlier.
             if (j == 0 && n > 0) {
                 bulk_wait_read<0>();
-                mbar_arrive(&bar[B_STGFREE + ((n - 1) & 1)]);
+                if constexpr (L::STG_OWN)
+                    mbar_arrive(&bar[B_STGR]);
+                else
+                    mbar_arrive(&bar[B_STGFREE + ((n - 1) & 1)]);
                 if (!u_issued && !(ok = issue_u(n))) break;
                 u_issued = false;
             }
@@ -548,6 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld32(tmem + lane_base + TM_U, r0);
                 tmem_ld32(tmem + lane_base + TM_U + 32, r1);
                 tmem_ld_wait();
+                if (j == 0) KDA_TR(n, 25);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     u16[e] = pack_half2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1]));
@@ -560,11 +578,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j == 0) {  // (ii) state update and (iii-b) the intra-chunk part of the output
                     if (!(ok = mbar_wait(&bar[B_URDY], n & 1, ab, status))) break;
                     tc_fence_after();
-                    const uint32_t kh = sm_base + L::OFF_KH + b * 16384, pp = sm_base + L::OFF_PP + (n % L::NPP) * 8192;
-                    for (int st = 0; st < 4; ++st)
-                        mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, k_desc(kh + st * 32), ID_S, 1);
-                    for (int st = 0; st < 4; ++st)
-                        mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, k_desc(pp + st * 32), ID_KK, 1);
+                    const uint64_t dkh = k_desc(sm_base + L::OFF_KH + b * 16384);
+                    const uint64_t dpp = k_desc(sm_base + L::OFF_PP + (n % L::NPP) * 8192);
+#pragma unroll
+                    for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, dkh + 2u * st, ID_S, 1);
+#pragma unroll
+                    for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, dpp + 2u * st, ID_KK, 1);
                     mma_commit(&bar[B_SDONE]);
                     mma_commit(&bar[B_KQFREE + b]);
                     KDA_TR(n, 13);
@@ -582,7 +601,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     snap = P.snapshots + ((size_t)(P.snap_offsets[s] + end_pos / P.snap_interval - 1) * P.H + h) *
                                              kD * kD;
                 float* fin = (last && P.final_state) ? P.final_state + sbase : nullptr;
-                const float* bv = vec_b + (n & 3) * 128;
+                const float* bv = vec_b + (n % 3) * 128;
                 if (snap || fin) {  // true state S = Diag(b_n) D, at snapshot positions and the end
 #pragma unroll 1
                     for (int piece = 0; piece < 4; ++piece) {
@@ -601,38 +620,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!last) {  // X_{n+1} = Diag(a_{n+1}) (Diag(b_n) D) into D_S (fp32) and X16 (fp16)
                     // (the same two roundings as a run resumed from the returned state)
                     if (!(ok = mbar_wait(&bar[B_PREPD + ((n + 1) & 1)], ((n + 1) >> 1) & 1, ab, status))) break;
-                    const float* an = vec_a + ((n + 1) & 3) * 128;
+                    const float* an = vec_a + ((n + 1) % 3) * 128;
                     uint32_t da[32], db[32];
-                    tmem_ld32(tmem + lane_base + TM_S, da);
-                    tmem_ld_wait();
+#pragma unroll 1
+                    for (int pp = 0; pp < 4; pp += 2) {
+                        tmem_ld32(tmem + lane_base + TM_S + pp * 32, da);
+                        tmem_ld32(tmem + lane_base + TM_S + (pp + 1) * 32, db);
+                        tmem_ld_wait();
+                        if (j == 0 && pp == 0) KDA_TR(n, 26);
 #pragma unroll
-                    for (int piece = 0; piece < 4; ++piece) {
-                        uint32_t(&d)[32] = (piece & 1) ? db : da;
-                        uint32_t(&dn)[32] = (piece & 1) ? da : db;
-                        if (piece < 3) tmem_ld32(tmem + lane_base + TM_S + (piece + 1) * 32, dn);
-                        uint32_t x16[16];
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t(&d)[32] = half ? db : da;
+                            const int piece = pp + half;
+                            uint32_t x16[16];
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 b4 = *reinterpret_cast<const float4*>(bv + piece * 32 + 4 * e4);
-                            const float4 a4 = *reinterpret_cast<const float4*>(an + piece * 32 + 4 * e4);
-                            const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 b4 = *reinterpret_cast<const float4*>(bv + piece * 32 + 4 * e4);
+                                const float4 a4 = *reinterpret_cast<const float4*>(an + piece * 32 + 4 * e4);
+                                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                d[4 * e4 + q] = __float_as_uint(__uint_as_float(d[4 * e4 + q]) * bb[q] * aa[q]);
+                                for (int q = 0; q < 4; ++q)
+                                    d[4 * e4 + q] = __float_as_uint(__uint_as_float(d[4 * e4 + q]) * bb[q] * aa[q]);
+                            }
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                x16[e] = pack_half2(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
+                            tmem_st32(tmem + lane_base + TM_S + piece * 32, d);
+                            tmem_st16(tmem + lane_base + TM_X16 + piece * 16, x16);
                         }
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            x16[e] = pack_half2(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
-                        tmem_st32(tmem + lane_base + TM_S + piece * 32, d);
-                        tmem_st16(tmem + lane_base + TM_X16 + piece * 16, x16);
-                        if (piece < 3) tmem_ld_wait();
                     }
+                    if (j == 0) KDA_TR(n, 27);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&bar[B_XRDY]);
                     if (j == 0) KDA_TR(n, 15);
                 }
-                mbar_arrive(&bar[B_VFREE + (n & 3)]);
+                mbar_arrive(&bar[B_VFREE + (n % 3)]);
                 // (i) of the next chunk now if its inputs are ready; otherwise after this
                 // chunk's output is out (so that the output never waits on WT)
                 if (!last && j == 0 && mbar_test(&bar[B_XRDY], (n + 1) & 1) &&
@@ -649,8 +672,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_before();
                 mbar_arrive(&bar[B_OFREE]);
                 if (j == 0) KDA_TR(n, 16);
-                if (valid == C) {  // staged through the chunk's KT/QT pair, stored by the TMA
-                    Tout* stg = reinterpret_cast<Tout*>(sm + L::OFF_KQ + b * 32768);
+                {  // staged in shared memory; full chunks are stored by the TMA
+                    Tout* stg = reinterpret_cast<Tout*>(sm + (L::STG_OWN ? L::OFF_STG : L::OFF_KQ + b * 32768));
+                    if constexpr (L::STG_OWN)  // the previous chunk's bulk store has read the buffer
+                        if (n > 0 && !(ok = mbar_wait(&bar[B_STGR], (n - 1) & 1, ab, status))) break;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         if constexpr (sizeof(Tout) == 2) {
@@ -661,28 +686,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             stg[(32 + e) * kD + j] = __uint_as_float(o1[e]);
                         }
                     }
-                    // Every thread waits, so no thread can arrive for the next chunk before
-                    // all have arrived for this one.
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bar[B_STG]);
-                    if (!(ok = mbar_wait(&bar[B_STG], (ph_stg++) & 1, ab, status))) break;
-                    if (j == 0) {
-                        for (int q = 0; q < 4; ++q)
-                            tma_store_3d(&tm_out, stg + q * QR * kD, 0, h, (int)(t0 + (int64_t)C * n + QR * q));
-                        bulk_commit();
-                    }
-                } else {  // partial last chunk: plain stores of the rows inside the sequence
-                    const size_t obase = ((size_t)(t0 + (int64_t)C * n) * P.H + h) * kD + j;
-                    const size_t ostride = (size_t)P.H * kD;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        const float v = __uint_as_float(e < 32 ? o0[e] : o1[e - 32]);
-                        if (e < valid) {
-                            if constexpr (sizeof(Tout) == 2)
-                                out[obase + e * ostride] = __float2bfloat16_rn(v);
-                            else
-                                out[obase + e * ostride] = v;
+                    if (valid == C) {
+                        // Every thread waits, so no thread can arrive for the next chunk before
+                        // all have arrived for this one.
+                        fence_proxy_async_smem();
+                        mbar_arrive(&bar[B_STG]);
+                        if (!(ok = mbar_wait(&bar[B_STG], (ph_stg++) & 1, ab, status))) break;
+                        if (j == 0) {
+                            for (int q = 0; q < 4; ++q)
+                                tma_store_3d(&tm_out, stg + q * QR * kD, 0, h, (int)(t0 + (int64_t)C * n + QR * q));
+                            bulk_commit();
                         }
+                    } else {  // partial last chunk: this thread's column of the rows inside the sequence
+                        Tout* dst = out + ((size_t)(t0 + (int64_t)C * n) * P.H + h) * kD + j;
+#pragma unroll 1
+                        for (int e = 0; e < valid; ++e) dst[(size_t)e * P.H * kD] = stg[e * kD + j];
                     }
                 }
                 if (j == 0) KDA_TR(n, 17);
@@ -697,11 +715,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int wi = warp - 12;
         const uint32_t lane_base = (uint32_t)(wi * 32) << 16;
         float* inv = reinterpret_cast<float*>(sm + L::OFF_INV);
-        auto Ab = [&](int a, int bb) { return inv + (a * (a + 1) / 2 + bb) * kBlk; };  // A_ab, b <= a
-        float* Tg = inv + 10 * kBlk;  // Dg_0..3, then T_10, T_21, T_20
-        float* T10 = Tg + 4 * kBlk;
-        float* T21 = Tg + 5 * kBlk;
-        float* T20 = Tg + 6 * kBlk;
+        // 16x16 fp32 blocks: A_ab (b <= a) at block a(a+1)/2 + b; Dg_a = T_aa at 10 + a; the
+        // T_ab that later blocks read (a = 1, 2) at 14 + a(a-1)/2 + b
+        auto Ab = [&](int a, int bb) { return inv + (a * (a + 1) / 2 + bb) * kBlk; };
+        auto Tb = [&](int a, int bb) { return inv + (a == bb ? 10 + a : 14 + a * (a - 1) / 2 + bb) * kBlk; };
         uint8_t* nr = sm + L::OFF_NR;
         uint32_t ph_tb = 0;
         auto wg_sync = [&]() -> bool {
@@ -714,6 +731,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // NR blocks above the diagonal are never written again: zero them once.
         for (int i = c; i < 8192 / 16; i += 128) reinterpret_cast<uint4*>(nr)[i] = make_uint4(0u, 0u, 0u, 0u);
         const int r = lane >> 1;  // block row of this lane in the column stage
+        int aoff[4];              // float offsets of the four chunks of block row r
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) aoff[k4] = bsw(r, k4);
         for (int n = 0; n < nch; ++n) {
             const int b = n & 1;
             const float* bt = sbeta + (n & 3) * 64;
@@ -735,26 +755,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld32(tmem + lane_base + TM_G, r0);
                 tmem_ld32(tmem + lane_base + TM_G + 32, r1);
                 tmem_ld_wait();
+                if (c == 0) KDA_TR(n, 30);
                 tc_fence_before();
                 mbar_arrive(&bar[B_P2D]);
                 if (c < 64) {
+                    // Row c of A = beta_c G[c][:].  Only entries left of the diagonal are ever
+                    // read, so the row is stored unmasked; its parts right of the diagonal
+                    // block land in T_10's block (rewritten later in the chunk).
                     const float br = bt[c];
                     const int a = c >> 4, i = c & 15;
 #pragma unroll
                     for (int bb = 0; bb < 4; ++bb) {
-                        if (bb <= a) {
-                            float* dst = Ab(a, bb) + i * kBS;
+                        float* dst = bb <= a ? Ab(a, bb) : Tb(1, 0);
 #pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4) {
-                                float w[4];
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            float w[4];
 #pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    const int e = 16 * bb + 4 * e4 + q;
-                                    const float gv = __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
-                                    w[q] = e < c ? br * gv : 0.f;
-                                }
-                                st4(dst + 4 * e4, w);
+                            for (int q = 0; q < 4; ++q) {
+                                const int e = 16 * bb + 4 * e4 + q;
+                                w[q] = br * __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
                             }
+                            st4(dst + bsw(i, e4), w);
                         }
                     }
                 } else {
@@ -780,102 +801,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int rr = 0; rr < 15; ++rr) {
                     const float xr = x[rr];
 #pragma unroll
-                    for (int i = rr + 1; i < 16; ++i) x[i] = fmaf(-blk[i * kBS + rr], xr, x[i]);
+                    for (int i = rr + 1; i < 16; ++i) x[i] = fmaf(-blk[bsw(i, rr >> 2) + (rr & 3)], xr, x[i]);
                 }
-                float* dg = Tg + wi * kBlk;
+                float* dg = Tb(wi, wi);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) dg[i * kBS + lane] = x[i];
+                for (int i = 0; i < 16; ++i) dg[bsw(i, lane >> 2) + (lane & 3)] = x[i];
             }
             if (!wg_sync()) break;  // Dg written; the A diagonal blocks are free as scratch
             if (c == 0) KDA_TR(n, 6);
-            // ---- blocks below the diagonal, by block column (T_ab = -Dg_a Z_ab)
+            // ---- blocks below the diagonal, block column by block column:
+            //   T_ab = -Dg_a Z_ab,  Z_ab = sum_{k=b}^{a-1} A_ak T_kb  (T_bb = Dg_b)
+            // Warps 12-13 take block column 0 (columns 8 wi .. 8 wi + 7); warps 14-15 take
+            // columns 8 (wi - 2) .. of block columns 1 and 2.  Lane (r, lane & 1) computes
+            // row r, four columns.  The dead A diagonal blocks hold each column's Z.
             {
-                float t[4];
-                auto zero = [](float (&v)[4]) { v[0] = v[1] = v[2] = v[3] = 0.f; };
-                auto neg = [](float (&v)[4]) { v[0] = -v[0]; v[1] = -v[1]; v[2] = -v[2]; v[3] = -v[3]; };
-                // Dg_wi itself into NR
+                // Dg_wi itself into NR: row r, columns 8 hf .. 8 hf + 7
                 {
                     const int hf = lane & 1;
-                    const float* src = Tg + wi * kBlk + r * kBS + 8 * hf;
+                    const float* blk = Tb(wi, wi);
+                    const float4 u = ld4(blk + bsw(r, 2 * hf)), v = ld4(blk + bsw(r, 2 * hf + 1));
+                    const float x8[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
                     const int col = 16 * wi + 8 * hf;
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        w[e] = pack_half2(src[2 * e] * bt[col + 2 * e], src[2 * e + 1] * bt[col + 2 * e + 1]);
+                        w[e] = pack_half2(x8[2 * e] * bt[col + 2 * e], x8[2 * e + 1] * bt[col + 2 * e + 1]);
                     *reinterpret_cast<uint4*>(nr + sw128(16 * wi + r, col >> 3)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                if (wi < 2) {  // block column 0, columns c0 .. c0+3
-                    const int c0 = 8 * wi + 4 * (lane & 1);
-                    float* zs = Ab(0, 0);
-                    float z10[4] = {0.f, 0.f, 0.f, 0.f}, z20[4] = {0.f, 0.f, 0.f, 0.f}, z30[4] = {0.f, 0.f, 0.f, 0.f};
-                    mac16x3(Ab(1, 0) + r * kBS, Ab(2, 0) + r * kBS, Ab(3, 0) + r * kBS, Tg + c0, z10, z20, z30);
-                    // T_10
-                    st4(zs + r * kBS + c0, z10);
-                    __syncwarp();
-                    zero(t);
-                    mac16(Tg + 1 * kBlk + r * kBS, zs + c0, t);
-                    neg(t);
-                    st4(T10 + r * kBS + c0, t);
-                    nr_store(16 + r, c0, t);
-                    __syncwarp();
-                    // T_20
-                    mac16x2(Ab(2, 1) + r * kBS, Ab(3, 1) + r * kBS, T10 + c0, z20, z30);
-                    st4(zs + r * kBS + c0, z20);
-                    __syncwarp();
-                    zero(t);
-                    mac16(Tg + 2 * kBlk + r * kBS, zs + c0, t);
-                    neg(t);
-                    st4(T20 + r * kBS + c0, t);
-                    nr_store(32 + r, c0, t);
-                    __syncwarp();
-                    // T_30
-                    mac16(Ab(3, 2) + r * kBS, T20 + c0, z30);
-                    st4(zs + r * kBS + c0, z30);
-                    __syncwarp();
-                    zero(t);
-                    mac16(Tg + 3 * kBlk + r * kBS, zs + c0, t);
-                    neg(t);
-                    nr_store(48 + r, c0, t);
-                } else {  // block column 1 (columns c0 .. c0+3); warp 15 also block column 2
-                    const int c0 = 8 * (wi - 2) + 4 * (lane & 1);
-                    const int c2 = 8 * (lane & 1);  // T_32: columns c2 .. c2+7 (warp 15)
-                    float* zs = Ab(1, 1);
-                    float* zs2 = Ab(2, 2);
-                    float z21[4] = {0.f, 0.f, 0.f, 0.f}, z31[4] = {0.f, 0.f, 0.f, 0.f};
-                    mac16x2(Ab(2, 1) + r * kBS, Ab(3, 1) + r * kBS, Tg + 1 * kBlk + c0, z21, z31);
-                    if (wi == 3) {
-                        float za[4] = {0.f, 0.f, 0.f, 0.f}, zb[4] = {0.f, 0.f, 0.f, 0.f};
-                        mac16(Ab(3, 2) + r * kBS, Tg + 2 * kBlk + c2, za);
-                        mac16(Ab(3, 2) + r * kBS, Tg + 2 * kBlk + c2 + 4, zb);
-                        st4(zs2 + r * kBS + c2, za);
-                        st4(zs2 + r * kBS + c2 + 4, zb);
-                    }
-                    // T_21 (and T_32)
-                    st4(zs + r * kBS + c0, z21);
-                    __syncwarp();
-                    zero(t);
-                    mac16(Tg + 2 * kBlk + r * kBS, zs + c0, t);
-                    neg(t);
-                    st4(T21 + r * kBS + c0, t);
-                    nr_store(32 + r, 16 + c0, t);
-                    if (wi == 3) {
+                const int c4 = 2 * (wi & 1) + (lane & 1);  // column quad inside the block column
+                const int b0 = wi < 2 ? 0 : 1, b1 = wi < 2 ? 0 : 2;
+#pragma unroll 1
+                for (int bc = b0; bc <= b1; ++bc) {
+                    float* zs = Ab(bc, bc);
+#pragma unroll 1
+                    for (int a = bc + 1; a < 4; ++a) {
+                        float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                        for (int k = bc; k < a; ++k) mac16(Ab(a, k), aoff, bcol(Tb(k, bc), c4), z);
+                        st4(zs + bsw(r, c4), z);
+                        __syncwarp();
+                        float t[4] = {0.f, 0.f, 0.f, 0.f};
+                        mac16(Tb(a, a), aoff, bcol(zs, c4), t);
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            zero(t);
-                            mac16(Tg + 3 * kBlk + r * kBS, zs2 + c2 + 4 * h2, t);
-                            neg(t);
-                            nr_store(48 + r, 32 + c2 + 4 * h2, t);
-                        }
+                        for (int q = 0; q < 4; ++q) t[q] = -t[q];
+                        if (a < 3) st4(Tb(a, bc) + bsw(r, c4), t);
+                        const int col = 16 * bc + 4 * c4;
+                        const uint32_t w0 = pack_half2(t[0] * bt[col], t[1] * bt[col + 1]);
+                        const uint32_t w1 = pack_half2(t[2] * bt[col + 2], t[3] * bt[col + 3]);
+                        *reinterpret_cast<uint2*>(nr + sw128(16 * a + r, col >> 3) + (col & 7) * 2) = make_uint2(w0, w1);
+                        __syncwarp();
                     }
-                    __syncwarp();
-                    // T_31
-                    mac16(Ab(3, 2) + r * kBS, T21 + c0, z31);
-                    st4(zs + r * kBS + c0, z31);
-                    __syncwarp();
-                    zero(t);
-                    mac16(Tg + 3 * kBlk + r * kBS, zs + c0, t);
-                    neg(t);
-                    nr_store(48 + r, 16 + c0, t);
                 }
             }
             fence_proxy_async_smem();
@@ -886,12 +861,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) break;
                 if (n > 0 && !mbar_wait(&bar[B_SDONE], (n - 1) & 1, ab, status)) break;
                 tc_fence_after();
-                const uint32_t kt = sm_base + L::OFF_KQ + b * 32768, v16 = TM_V16 + b * 32;
-                const uint32_t snr = sm_base + L::OFF_NR;
+                KDA_TR(n, 22);
+                const uint64_t dkt = k_desc(sm_base + L::OFF_KQ + b * 32768), dnr = k_desc(sm_base + L::OFF_NR);
+                const uint32_t v16 = tmem + TM_V16 + b * 32;
+#pragma unroll
                 for (int st = 0; st < 4; ++st) {
-                    const uint64_t bd = k_desc(snr + st * 32);
-                    mma_ss(tmem + TM_W, k_desc(kt + st * 32), bd, ID_KK, st > 0);
-                    mma_ts(tmem + TM_U, tmem + v16 + st * 8, bd, ID_KK, st > 0);
+                    mma_ss(tmem + TM_W, dkt + 2u * st, dnr + 2u * st, ID_KK, st > 0);
+                    mma_ts(tmem + TM_U, v16 + st * 8, dnr + 2u * st, ID_KK, st > 0);
                 }
                 mma_commit(&bar[B_WYDONE]);
                 mma_commit(&bar[B_V16FREE + b]);
@@ -913,6 +889,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld32(tmem + lane_base + TM_W, r0);
                 tmem_ld32(tmem + lane_base + TM_W + 32, r1);
                 tmem_ld_wait();
+                if (c == 0) KDA_TR(n, 23);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     r0[e] ^= 0x80000000u;
@@ -937,6 +914,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     if (warp == 1) tmem_dealloc(tmem, 512);
+#ifdef KDA_TRACE
+    if (blockIdx.x == 0)
+        for (int i = tid; i < kTrN * kTrEv; i += NTHREADS) g_trace[i] = trace_sm[i];
+#endif
 }
 
 // ---------------------------------------------------------------- host side
@@ -991,9 +972,9 @@ cudaError_t launch_t(const SeqProblem& p, cudaStream_t st) {
 }  // namespace
 
 #ifdef KDA_TRACE
-extern "C" int kda_trace_read(unsigned long long* host, int n) {
-    const size_t cnt = (size_t)(n < 64 * kTrEv ? n : 64 * kTrEv);
-    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * cnt) == cudaSuccess ? 0 : 1;
+extern "C" int kda_trace_read(unsigned int* host, int n) {
+    const size_t cnt = (size_t)(n < kTrN * kTrEv ? n : kTrN * kTrEv);
+    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned int) * cnt) == cudaSuccess ? 0 : 1;
 }
 #endif
 

@@ -30,11 +30,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
+#ifdef KDA_WAIT_HINT_NS
+    // with a suspend-time hint: a waiting thread sleeps until the phase completes
+    // (or the hint expires) instead of re-polling
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.b32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(KDA_WAIT_HINT_NS)
+        : "memory");
+#else
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.b32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
+#endif
     return ok != 0;
 }
 
@@ -63,8 +73,9 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: far beyond any legitim
 
 // Waits for phase `parity` of `bar`.  Returns false (and raises the abort flag
 // and the device status) if the deadline passes or another role aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait, kept out of line so that the many wait sites stay small
+// in the instruction cache.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
     const long long t0 = clock64();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -77,6 +88,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort*
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, ab, status);
 }
 
 // 4-byte asynchronous global -> shared copy, and an arrive on `bar` that fires
@@ -219,6 +234,22 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// ---------------------------------------------------------------- packed fp32 (sm_100 f32x2)
+// {d0, d1} += {a0, a1} * {b0, b1} and {d0, d1} = {a0, a1} * {b0, b1}: one instruction
+// for two lanes' worth of fp32 arithmetic, each result rounded as its scalar form.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n.reg .b64 ra, rb, rc;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\nmov.b64 rc, {%0, %1};\n"
+        "fma.rn.f32x2 rc, ra, rb, rc;\nmov.b64 {%0, %1}, rc;\n}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n.reg .b64 ra, rb, rc;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+        "mul.rn.f32x2 rc, ra, rb;\nmov.b64 {%0, %1}, rc;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // ---------------------------------------------------------------- conversions
