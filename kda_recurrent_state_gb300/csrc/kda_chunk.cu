@@ -171,16 +171,17 @@ __device__ __forceinline__ float ld_in(const float* s, uint32_t idx) { return s[
 
 // Writes 64 fp32 values (r0: columns 0..31, r1: 32..63) as one 128-byte
 // swizzled fp16 row.
+// `sign` is XORed into every packed pair (0x80008000 negates both halves).
 __device__ __forceinline__ void store_row16(uint8_t* tile, uint32_t row, const uint32_t (&r0)[32],
-                                            const uint32_t (&r1)[32]) {
+                                            const uint32_t (&r1)[32], uint32_t sign = 0u) {
 #pragma unroll
     for (int c16 = 0; c16 < 8; ++c16) {
         const uint32_t* s = c16 < 4 ? &r0[8 * c16] : &r1[8 * (c16 - 4)];
         *reinterpret_cast<uint4*>(tile + sw128(row, c16)) =
-            make_uint4(pack_half2(__uint_as_float(s[0]), __uint_as_float(s[1])),
-                       pack_half2(__uint_as_float(s[2]), __uint_as_float(s[3])),
-                       pack_half2(__uint_as_float(s[4]), __uint_as_float(s[5])),
-                       pack_half2(__uint_as_float(s[6]), __uint_as_float(s[7])));
+            make_uint4(pack_half2(__uint_as_float(s[0]), __uint_as_float(s[1])) ^ sign,
+                       pack_half2(__uint_as_float(s[2]), __uint_as_float(s[3])) ^ sign,
+                       pack_half2(__uint_as_float(s[4]), __uint_as_float(s[5])) ^ sign,
+                       pack_half2(__uint_as_float(s[6]), __uint_as_float(s[7])) ^ sign);
     }
 }
 
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (c == 0) KDA_TR(n, 1);
             const bool full = valid == C;
             float ref = 0.f;
-#pragma unroll
+#pragma unroll 8
             for (int r = 0; r < 32; ++r) {
                 const uint8_t* sl = slot_ptr(r >> 4);
                 const float la = reinterpret_cast<const float*>(sl + L::SLOT_LA)[(r & 15) * 128 + c];
@@ -791,21 +792,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             if (!wg_sync()) break;  // A written
             if (c == 0) KDA_TR(n, 5);
-            // ---- diagonal blocks: Dg_wi column `lane` by right-looking substitution
-            if (lane < 16) {
-                const float* blk = Ab(wi, wi);
+            if (c < 64) {
+                // ---- diagonal blocks: column jj of Dg_a = (I + A_aa)^-1 (thread c = 16 a + jj)
+                // by right-looking substitution
+                const int a = c >> 4, jj = c & 15;
+                const float* blk = Ab(a, a);
                 float x[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
+                for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.f : 0.f;
 #pragma unroll
                 for (int rr = 0; rr < 15; ++rr) {
                     const float xr = x[rr];
 #pragma unroll
                     for (int i = rr + 1; i < 16; ++i) x[i] = fmaf(-blk[bsw(i, rr >> 2) + (rr & 3)], xr, x[i]);
                 }
-                float* dg = Tb(wi, wi);
+                float* dg = Tb(a, a);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) dg[bsw(i, lane >> 2) + (lane & 3)] = x[i];
+                for (int i = 0; i < 16; ++i) dg[bsw(i, jj >> 2) + (jj & 3)] = x[i];
             }
             if (!wg_sync()) break;  // Dg written; the A diagonal blocks are free as scratch
             if (c == 0) KDA_TR(n, 6);
@@ -890,13 +893,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld32(tmem + lane_base + TM_W + 32, r1);
                 tmem_ld_wait();
                 if (c == 0) KDA_TR(n, 23);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    r0[e] ^= 0x80000000u;
-                    r1[e] ^= 0x80000000u;
-                }
                 if (n > 0 && !mbar_wait(&bar[B_UIDONE], (n - 1) & 1, ab, status)) break;
-                store_row16(sm + L::OFF_WT, c, r0, r1);
+                store_row16(sm + L::OFF_WT, c, r0, r1, 0x80008000u);  // -W^T
             }
             fence_proxy_async_smem();
             tc_fence_before();
