@@ -17,8 +17,10 @@ repository) on a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -39,6 +41,25 @@ PREFILL_FLOP = 6 * D * D + CHUNK * (3 * D + 2 * D)
 # decode: state read + written (2 x 65,536 B) + q,k,v bf16, log_alpha, beta, out fp32 per session-head
 DEC_BYTES = 2 * D * D * 4 + 3 * 256 + 512 + 4 + 512
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_chunk_prefill_B1_H16_T32768.md")
+CHUNK_SRC = os.path.join(ROOT, "kda_recurrent_state_gb300", "csrc", "kda_chunk.cu")
+
+
+def measured_traffic_per_token_head():
+    """DRAM bytes per token-head of the chunked prefill from the committed ncu summary, or
+    None when that summary was taken on a different version of the kernel source."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+        sha = hashlib.sha256(open(CHUNK_SRC, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m = re.search(r"kernel source sha256: ([0-9a-f]{64})", text)
+    t = re.search(r"dram bytes per token-head: ([0-9.]+)", text)
+    if not m or not t or m.group(1) != sha:
+        return None
+    return float(t.group(1))
 
 
 def load_peaks():
@@ -88,7 +109,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -208,6 +229,10 @@ def run_ours(args):
     out_b = 512 if out_dtype == torch.float32 else 256
     alg_bytes = B * T * H * (PREFILL_IN_BYTES + out_b)
     achieved = alg_bytes / kern_s / 1e9
+    if args.traffic is None:
+        tph = measured_traffic_per_token_head()
+        if tph is not None:
+            args.traffic = tph * B * T * H
     flops = B * T * H * PREFILL_FLOP
     line = {
         "metric": "KDA prefill tokens/s at H=96,T=128K (% tensor roofline); decode state GB/s",
@@ -329,10 +354,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_case():
+    """Small workload for ncu captures: inputs (0.9 GB) larger than L2, two launches."""
+    import torch
+
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    x = synth.prefill_inputs(1, 32768, 16, seed=synth.SEED_BASE + 5, device="cuda")
+    for _ in range(2):
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, chunk=64)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    print("profile case done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk", type=int, default=64, choices=[1, 64])
@@ -341,10 +381,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="dram bytes per launch of the prefill kernel from an ncu capture (null if unknown)")
+                    help="dram bytes per launch of the prefill kernel (default: from the committed ncu summary "
+                         "when it matches the kernel source, else null)")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run two launches of the chunked prefill on B=1,H=16,T=32768 (fp32 out) and exit: the "
+                         "small case the committed ncu summaries are captured on")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case()
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
