@@ -20,13 +20,15 @@
 // as X = Diag(e^{ref}) S0 (what the products with Ktil_p / Qtil_p need), and the
 // state accumulator holds D = X + Khat_p^T U, so S_C = Diag(e^{g_63 - ref}) D.
 //
-// The triangular inverse (the WY solve of §六) runs on CUDA cores in fp32:
-// A is split into 16x16 blocks; the diagonal blocks are inverted by
-// substitution (Dg_a = (I + A_aa)^-1, one thread per column), and the blocks
-// below the diagonal follow block column by block column from
+// The triangular inverse (the WY solve of §六) is a blocked substitution: A is
+// split into 16x16 blocks; the diagonal blocks are inverted in fp32 on CUDA cores
+// (Dg_a = (I + A_aa)^-1, one thread per column), and the blocks below the diagonal
+// follow block column by block column from
 //   T_ab = -Dg_a sum_{k=b}^{a-1} A_ak T_kb      (T_bb = Dg_b),
-// one warp per (half) block column.  Only T diag(beta) is rounded to fp16, as
-// the operand of the WY products.
+// as warp-level 16x16 products (fp16 operands, fp32 accumulation), one warp per
+// block column.  They are computed transposed, S_ba = T_ab^T, so that every result
+// is directly the left operand of the next product.  T diag(beta) is rounded to
+// fp16 as the operand of the WY products.
 //
 // Data layout on chip (one CTA = one (sequence, head), all of d_v = 128):
 //   TMEM (fp32 accumulators, lanes = the M rows):
@@ -37,7 +39,8 @@
 //     KT[c][r] = Ktil_p, QT[c][r] = Qtil_p (adjacent: together the M = 128 A
 //     operand of the Gram; once a chunk's products are done the pair stages
 //     its output for the TMA store), KH[c][r] = Khat_p, PP[r][i] = P,
-//     WT[c][r] = -W^T, NR[r][i] = T diag(beta); fp32 16x16 blocks of A and T;
+//     WT[c][r] = -W^T, NR[r][i] = T diag(beta); the 16x16 blocks of A (diagonal
+//     ones fp32, the rest fp16) and of Dg (fp16);
 //     a ring of 16-token input slots filled by TMA.
 //   The products (all tcgen05.mma, fp16 operands, fp32 accumulation):
 //     Gram  D_G = [KT;QT] x KH                 M=128 N=64  K=128
@@ -69,7 +72,8 @@ constexpr int QR = 16;  // token rows per input slot
 constexpr int NTHREADS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxExp2 = 15.0f;  // |g - ref| bound (log2 units) for fp16 operands
-constexpr int kBlk = 256;          // floats per 16x16 fp32 block of A or T (see bsw)
+constexpr int kRowH = 48;          // row stride (bytes) of a 16x16 fp16 block (ldmatrix: no bank conflicts)
+constexpr int kBlkH = 16 * kRowH;  // bytes per fp16 block
 
 // TMEM column map (512 columns allocated).  The fp16 U operand is written over
 // the first 32 columns of the U accumulator once that has been read out; V16
@@ -100,8 +104,9 @@ struct Cfg {
     static constexpr uint32_t OFF_PP = 98304;                // [NPP] x 8K
     static constexpr uint32_t OFF_WT = OFF_PP + NPP * 8192;  // 16K
     static constexpr uint32_t OFF_NR = OFF_WT + 16384;       // 8K
-    static constexpr uint32_t OFF_INV = OFF_NR + 8192;       // 17 fp32 blocks: A (10), Dg (4), T10, T20, T21
-    static constexpr uint32_t OFF_STG = OFF_INV + 17 * kBlk * 4;              // 64 output rows (STG_OWN)
+    static constexpr uint32_t OFF_INV = OFF_NR + 8192;  // A diagonal blocks (fp32), A below them and Dg (fp16)
+    static constexpr uint32_t INV_BYTES = 4 * 1024 + 10 * kBlkH;
+    static constexpr uint32_t OFF_STG = OFF_INV + INV_BYTES;  // 64 output rows (STG_OWN)
     static constexpr uint32_t OFF_RING = OFF_STG + (STG_OWN ? 64 * 128 * 4 : 0);
     static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[3][128], b[3][128]
     static constexpr uint32_t OFF_BETA = OFF_VEC + 6 * 128 * 4;         // [4][64]
@@ -193,46 +198,92 @@ __device__ __forceinline__ void store_row16_packed(uint8_t* tile, uint32_t row, 
             make_uint4(p[4 * c16], p[4 * c16 + 1], p[4 * c16 + 2], p[4 * c16 + 3]);
 }
 
-// fp32 16x16 blocks of A and T in shared memory: row r holds its 16 values as four
-// 16-byte chunks, chunk k stored at position k ^ ((r >> 1) & 3), so that the sixteen
-// rows of a block read at the same chunk index fall in distinct bank groups.
+// fp32 16x16 diagonal blocks of A (read by the substitution): row r holds its 16
+// values as four 16-byte chunks, chunk k stored at position k ^ ((r >> 1) & 3).
 __device__ __forceinline__ int bsw(int r, int k4) { return r * 16 + ((k4 ^ ((r >> 1) & 3)) << 2); }
 
-// Four columns 4*c4 .. 4*c4+3 of a block, as per-row-group base pointers
-// (row m reads p[(m >> 1) & 3] + 16 m).
-struct BCol {
-    const float* p[4];
-};
-__device__ __forceinline__ BCol bcol(const float* blk, int c4) {
-    BCol b;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) b.p[s] = blk + ((c4 ^ s) << 2);
-    return b;
+// Warp-level 16x16 block products of the triangular solve (fp16 in, fp32 accumulate).
+// ldmatrix: lanes 8m .. 8m+7 give the rows of 8x8 matrix m; .trans delivers its transpose.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr)
+                 : "memory");
 }
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
-// acc[q] += sum_m A[r][m] * B[m][4 c4 + q] with row r of A given by its chunk offsets.
-__device__ __forceinline__ void mac16(const float* A, const int (&aoff)[4], const BCol& B, float (&acc)[4]) {
-    float a[16];
-#pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 t = ld4(A + aoff[k4]);
-        a[4 * k4] = t.x;
-        a[4 * k4 + 1] = t.y;
-        a[4 * k4 + 2] = t.z;
-        a[4 * k4 + 3] = t.w;
-    }
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const float4 bv = ld4(B.p[(m >> 1) & 3] + 16 * m);
-        acc[0] = fmaf(a[m], bv.x, acc[0]);
-        acc[1] = fmaf(a[m], bv.y, acc[1]);
-        acc[2] = fmaf(a[m], bv.z, acc[2]);
-        acc[3] = fmaf(a[m], bv.w, acc[3]);
-    }
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr)
+                 : "memory");
+}
+// d (16x8 fp32) += a (16x16 fp16, row-major fragment) x b (16x8 fp16, column fragment)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ void st4(float* p, const float (&v)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void st_half(uint8_t* p, float v) {
+    *reinterpret_cast<__half*>(p) = __float2half_rn(v);
+}
+
+// One block column B of T = (I + A)^-1 (T_aa = Dg_a), with T_aB = -Dg_a sum_{k=B}^{a-1} A_ak T_kB,
+// computed transposed, S_Ba = T_aB^T = -(sum_k S_Bk A_ak^T) Dg_a^T, so that each result's
+// accumulator fragment is directly the A fragment of the next product.  The blocks
+// below the diagonal go to NR as T diag(beta) (fp16, 128-byte swizzled rows).  One warp.
+template <int B>
+__device__ __forceinline__ void tri_column(uint32_t a16, uint32_t dg16, uint8_t* nr, const float* bt, int lane) {
+    // lane l supplies the row address (l & 7) + 8 (l >> 4), column half (l >> 3) & 1 of a block
+    const uint32_t lrow = (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * kRowH + 16 * ((lane >> 3) & 1));
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t sf[4][4];
+    {  // S_BB = Dg_B^T: matrices (rows 0-7 | 8-15) x (cols 0-7 | 8-15) of Dg_B, transposed
+        const uint32_t trow = (uint32_t)(((lane & 7) + 8 * ((lane >> 4) & 1)) * kRowH + 16 * ((lane >> 3) & 1));
+        uint32_t m[4];
+        ldsm_x4_t(m, dg16 + B * kBlkH + trow);
+        // fragment order: (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15)
+        sf[B][0] = m[0];
+        sf[B][1] = m[1];
+        sf[B][2] = m[2];
+        sf[B][3] = m[3];
+    }
+    const float bg = bt[16 * B + g], bg8 = bt[16 * B + g + 8];
+#pragma unroll
+    for (int a = B + 1; a < 4; ++a) {
+        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = B; k < a; ++k) {  // Z += S_Bk A_ak^T
+            uint32_t bA[4];
+            ldsm_x4(bA, a16 + (a * (a - 1) / 2 + k) * kBlkH + lrow);
+            mma16816(z0, sf[k], bA[0], bA[1]);
+            mma16816(z1, sf[k], bA[2], bA[3]);
+        }
+        const uint32_t zf[4] = {pack_half2(z0[0], z0[1]), pack_half2(z0[2], z0[3]), pack_half2(z1[0], z1[1]),
+                                pack_half2(z1[2], z1[3])};
+        uint32_t bD[4];
+        ldsm_x4(bD, dg16 + a * kBlkH + lrow);
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(s0, zf, bD[0], bD[1]);
+        mma16816(s1, zf, bD[2], bD[3]);
+        if (a < 3) {  // S_Ba = -Z Dg_a^T, kept as the A fragment of later levels
+            sf[a][0] = pack_half2(-s0[0], -s0[1]);
+            sf[a][1] = pack_half2(-s0[2], -s0[3]);
+            sf[a][2] = pack_half2(-s1[0], -s1[1]);
+            sf[a][3] = pack_half2(-s1[2], -s1[3]);
+        }
+        // S_Ba[i][r] = T_aB[r][i]: this lane holds i in {g, g+8}, r in {2t, 2t+1, 2t+8, 2t+9}
+        const int row = 16 * a + 2 * t, col = 16 * B + g;
+        st_half(nr + sw128(row, col >> 3) + (col & 7) * 2, -s0[0] * bg);
+        st_half(nr + sw128(row + 1, col >> 3) + (col & 7) * 2, -s0[1] * bg);
+        st_half(nr + sw128(row, (col + 8) >> 3) + (col & 7) * 2, -s0[2] * bg8);
+        st_half(nr + sw128(row + 1, (col + 8) >> 3) + (col & 7) * 2, -s0[3] * bg8);
+        st_half(nr + sw128(row + 8, col >> 3) + (col & 7) * 2, -s1[0] * bg);
+        st_half(nr + sw128(row + 9, col >> 3) + (col & 7) * 2, -s1[1] * bg);
+        st_half(nr + sw128(row + 8, (col + 8) >> 3) + (col & 7) * 2, -s1[2] * bg8);
+        st_half(nr + sw128(row + 9, (col + 8) >> 3) + (col & 7) * 2, -s1[3] * bg8);
+    }
 }
 
 template <typename Tin, typename Tout>
@@ -715,11 +766,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int c = tid - 384;  // TMEM lane: Gram row / key channel
         const int wi = warp - 12;
         const uint32_t lane_base = (uint32_t)(wi * 32) << 16;
-        float* inv = reinterpret_cast<float*>(sm + L::OFF_INV);
-        // 16x16 fp32 blocks: A_ab (b <= a) at block a(a+1)/2 + b; Dg_a = T_aa at 10 + a; the
-        // T_ab that later blocks read (a = 1, 2) at 14 + a(a-1)/2 + b
-        auto Ab = [&](int a, int bb) { return inv + (a * (a + 1) / 2 + bb) * kBlk; };
-        auto Tb = [&](int a, int bb) { return inv + (a == bb ? 10 + a : 14 + a * (a - 1) / 2 + bb) * kBlk; };
+        // Workspace of the inverse: the diagonal blocks A_aa in fp32 (for the substitution),
+        // the blocks below them A_ab (b < a, block a(a-1)/2 + b) and Dg_a in fp16 rows of
+        // kRowH bytes (for the warp-level products).
+        float* adiag = reinterpret_cast<float*>(sm + L::OFF_INV);
+        uint8_t* a16p = sm + L::OFF_INV + 4096;
+        uint8_t* dg16p = a16p + 6 * kBlkH;
         uint8_t* nr = sm + L::OFF_NR;
         uint32_t ph_tb = 0;
         auto wg_sync = [&]() -> bool {
@@ -731,19 +783,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         };
         // NR blocks above the diagonal are never written again: zero them once.
         for (int i = c; i < 8192 / 16; i += 128) reinterpret_cast<uint4*>(nr)[i] = make_uint4(0u, 0u, 0u, 0u);
-        const int r = lane >> 1;  // block row of this lane in the column stage
-        int aoff[4];              // float offsets of the four chunks of block row r
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) aoff[k4] = bsw(r, k4);
         for (int n = 0; n < nch; ++n) {
             const int b = n & 1;
             const float* bt = sbeta + (n & 3) * 64;
-            // T diag(beta)[16 rb + r][cb + q] for q < 4 into NR (fp16)
-            auto nr_store = [&](int row, int col, const float (&t)[4]) {
-                const uint32_t w0 = pack_half2(t[0] * bt[col], t[1] * bt[col + 1]);
-                const uint32_t w1 = pack_half2(t[2] * bt[col + 2], t[3] * bt[col + 3]);
-                *reinterpret_cast<uint2*>(nr + sw128(row, col >> 3) + (col & 7) * 2) = make_uint2(w0, w1);
-            };
             // ---- P2: read the Gram; rows 0..63 -> A (beta_r applied, strictly lower, fp32
             // blocks), rows 64..127 -> P (lower triangle including the diagonal, fp16)
             if (!mbar_wait(&bar[B_GDONE], n & 1, ab, status)) break;
@@ -760,23 +802,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_before();
                 mbar_arrive(&bar[B_P2D]);
                 if (c < 64) {
-                    // Row c of A = beta_c G[c][:].  Only entries left of the diagonal are ever
-                    // read, so the row is stored unmasked; its parts right of the diagonal
-                    // block land in T_10's block (rewritten later in the chunk).
+                    // Row c of A = beta_c G[c][:]: the blocks left of the diagonal in fp16, the
+                    // diagonal block in fp32.  Only entries left of the diagonal are ever read,
+                    // so nothing is masked.
                     const float br = bt[c];
                     const int a = c >> 4, i = c & 15;
 #pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-                        float* dst = bb <= a ? Ab(a, bb) : Tb(1, 0);
+                    for (int bb = 0; bb < 3; ++bb) {
+                        if (bb < a) {
+                            uint32_t h[8];
 #pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) {
-                            float w[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int e = 16 * bb + 4 * e4 + q;
-                                w[q] = br * __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
+                            for (int e = 0; e < 8; ++e) {
+                                const int e0 = 16 * bb + 2 * e;
+                                h[e] = pack_half2(br * __uint_as_float(e0 < 32 ? r0[e0] : r1[e0 - 32]),
+                                                  br * __uint_as_float(e0 + 1 < 32 ? r0[e0 + 1] : r1[e0 + 1 - 32]));
                             }
-                            st4(dst + bsw(i, e4), w);
+                            uint8_t* dst = a16p + (a * (a - 1) / 2 + bb) * kBlkH + i * kRowH;
+                            *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+                            *reinterpret_cast<uint4*>(dst + 16) = make_uint4(h[4], h[5], h[6], h[7]);
+                        }
+                    }
+#pragma unroll
+                    for (int aa = 0; aa < 4; ++aa) {
+                        if (aa == a) {
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                float w[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const int e = 16 * aa + 4 * e4 + q;
+                                    w[q] = br * __uint_as_float(e < 32 ? r0[e] : r1[e - 32]);
+                                }
+                                st4(adiag + aa * 256 + bsw(i, e4), w);
+                            }
                         }
                     }
                 } else {
@@ -796,7 +854,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // ---- diagonal blocks: column jj of Dg_a = (I + A_aa)^-1 (thread c = 16 a + jj)
                 // by right-looking substitution
                 const int a = c >> 4, jj = c & 15;
-                const float* blk = Ab(a, a);
+                const float* blk = adiag + a * 256;
                 float x[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.f : 0.f;
@@ -806,55 +864,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int i = rr + 1; i < 16; ++i) x[i] = fmaf(-blk[bsw(i, rr >> 2) + (rr & 3)], xr, x[i]);
                 }
-                float* dg = Tb(a, a);
+                // Dg_a in fp16 for the block products, and T diag(beta) of the diagonal block
+                const int col = 16 * a + jj;
+                const float bcol = bt[col];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) dg[bsw(i, jj >> 2) + (jj & 3)] = x[i];
+                for (int i = 0; i < 16; ++i) {
+                    st_half(dg16p + a * kBlkH + i * kRowH + jj * 2, x[i]);
+                    st_half(nr + sw128(16 * a + i, col >> 3) + (col & 7) * 2, x[i] * bcol);
+                }
             }
-            if (!wg_sync()) break;  // Dg written; the A diagonal blocks are free as scratch
+            if (!wg_sync()) break;  // Dg written
             if (c == 0) KDA_TR(n, 6);
-            // ---- blocks below the diagonal, block column by block column:
-            //   T_ab = -Dg_a Z_ab,  Z_ab = sum_{k=b}^{a-1} A_ak T_kb  (T_bb = Dg_b)
-            // Warps 12-13 take block column 0 (columns 8 wi .. 8 wi + 7); warps 14-15 take
-            // columns 8 (wi - 2) .. of block columns 1 and 2.  Lane (r, lane & 1) computes
-            // row r, four columns.  The dead A diagonal blocks hold each column's Z.
+            // ---- blocks below the diagonal: warp 12 + B takes block column B (warp-level products)
             {
-                // Dg_wi itself into NR: row r, columns 8 hf .. 8 hf + 7
-                {
-                    const int hf = lane & 1;
-                    const float* blk = Tb(wi, wi);
-                    const float4 u = ld4(blk + bsw(r, 2 * hf)), v = ld4(blk + bsw(r, 2 * hf + 1));
-                    const float x8[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-                    const int col = 16 * wi + 8 * hf;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack_half2(x8[2 * e] * bt[col + 2 * e], x8[2 * e + 1] * bt[col + 2 * e + 1]);
-                    *reinterpret_cast<uint4*>(nr + sw128(16 * wi + r, col >> 3)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                const int c4 = 2 * (wi & 1) + (lane & 1);  // column quad inside the block column
-                const int b0 = wi < 2 ? 0 : 1, b1 = wi < 2 ? 0 : 2;
-#pragma unroll 1
-                for (int bc = b0; bc <= b1; ++bc) {
-                    float* zs = Ab(bc, bc);
-#pragma unroll 1
-                    for (int a = bc + 1; a < 4; ++a) {
-                        float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                        for (int k = bc; k < a; ++k) mac16(Ab(a, k), aoff, bcol(Tb(k, bc), c4), z);
-                        st4(zs + bsw(r, c4), z);
-                        __syncwarp();
-                        float t[4] = {0.f, 0.f, 0.f, 0.f};
-                        mac16(Tb(a, a), aoff, bcol(zs, c4), t);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) t[q] = -t[q];
-                        if (a < 3) st4(Tb(a, bc) + bsw(r, c4), t);
-                        const int col = 16 * bc + 4 * c4;
-                        const uint32_t w0 = pack_half2(t[0] * bt[col], t[1] * bt[col + 1]);
-                        const uint32_t w1 = pack_half2(t[2] * bt[col + 2], t[3] * bt[col + 3]);
-                        *reinterpret_cast<uint2*>(nr + sw128(16 * a + r, col >> 3) + (col & 7) * 2) = make_uint2(w0, w1);
-                        __syncwarp();
-                    }
-                }
+                const uint32_t a16 = smem_u32(a16p), dg16 = smem_u32(dg16p);
+                if (wi == 0)
+                    tri_column<0>(a16, dg16, nr, bt, lane);
+                else if (wi == 1)
+                    tri_column<1>(a16, dg16, nr, bt, lane);
+                else if (wi == 2)
+                    tri_column<2>(a16, dg16, nr, bt, lane);
+                if (c == 0) KDA_TR(n, 31);
             }
             fence_proxy_async_smem();
             if (!wg_sync()) break;  // NR = T diag(beta) complete
