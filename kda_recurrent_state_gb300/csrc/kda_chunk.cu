@@ -378,8 +378,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             };
             for (int g = L::NSLOT; g < kPf && g < nq; ++g) prefetch(g);
             for (int n = 0; n < nch && ok; ++n)
-                for (int q = 0; q < 4 && ok; ++q) {
-                    const int g = 4 * n + q, sl = g % L::NSLOT, use = g / L::NSLOT;
+                for (int i = 0; i < 4 && ok; ++i) {
+                    const int q = i < 2 ? 1 - i : i;  // the order prep consumes them: 1, 0, 2, 3
+                    const int g = 4 * n + i, sl = g % L::NSLOT, use = g / L::NSLOT;
                     if (g + kPf < nq) prefetch(g + kPf);
                     if (use > 0 && !(ok = mbar_wait(&bar[B_EMPTY + sl], (use - 1) & 1, ab, status))) break;
                     uint8_t* slot = sm + L::OFF_RING + sl * L::SLOT_BYTES;
@@ -445,31 +446,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint8_t* kt = sm + L::OFF_KQ + b * 32768;
             uint8_t* qt = kt + 16384;
             uint8_t* kh = sm + L::OFF_KH + b * 16384;
-            auto slot_ptr = [&](int q) { return sm + L::OFF_RING + ((4 * n + q) % L::NSLOT) * L::SLOT_BYTES; };
-            auto wait_slot = [&](int q) {
-                const int g = 4 * n + q;
+            // Quarters in the order 1, 0 (rows 31 down to 0), 2, 3 (rows 32 up to 63), one ring
+            // slot each.  Relative to ref = g_31: rows r <= 31 use x_r = g_r - ref =
+            // -(L_{r+1} + .. + L_31), accumulated downwards from row 31 (which also yields
+            // ref = L_0 + .. + L_31); rows r >= 32 use x_r = L_32 + .. + L_r (L = log2 alpha).
+            auto wait_slot = [&](int i) {
+                const int g = 4 * n + i;
                 return mbar_wait(&bar[B_FULL + g % L::NSLOT], (g / L::NSLOT) & 1, ab, status);
             };
-            // pass A over rows 0..31: the reference ref = g_31
-            if (!wait_slot(0) || !wait_slot(1)) return false;
-            if (c == 0) KDA_TR(n, 1);
             const bool full = valid == C;
-            float ref = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) {
-                const uint8_t* sl = slot_ptr(r >> 4);
-                const float la = reinterpret_cast<const float*>(sl + L::SLOT_LA)[(r & 15) * 128 + c];
-                ref += (full || r < valid) ? la : 0.f;
-            }
-            ref *= kLog2e;
-            if (c == 0) KDA_TR(n, 28);
-            // pass B, one 16-row quarter at a time.  g decreases monotonically (log alpha
-            // <= 0), so |g - ref| is largest at the chunk's first or last row: the range
-            // check looks at those two.
-            float g2 = 0.f;
-            auto quarter = [&](int q, auto full_chunk) {
-                constexpr bool FULL = decltype(full_chunk)::value;
-                const uint8_t* sl = slot_ptr(q);
+            float x = 0.f;
+            // g decreases monotonically (log alpha <= 0), so |x| is largest at a quarter's
+            // first or last row: the range check looks at those.
+            auto quarter = [&](int i, auto full_chunk, auto reverse) {
+                constexpr bool FULL = decltype(full_chunk)::value, REV = decltype(reverse)::value;
+                const int q = REV ? 1 - i : i;
+                const uint8_t* sl = sm + L::OFF_RING + ((4 * n + i) % L::NSLOT) * L::SLOT_BYTES;
                 const float* sla = reinterpret_cast<const float*>(sl + L::SLOT_LA);
                 const Tin* sk = reinterpret_cast<const Tin*>(sl + L::SLOT_K);
                 const Tin* sq = reinterpret_cast<const Tin*>(sl + L::SLOT_Q);
@@ -477,28 +469,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int vq = valid - QR * q;  // rows of this quarter inside the sequence
                 uint32_t pk[8], pq[8], ph[8], pv[8];
 #pragma unroll
-                for (int rp = 0; rp < QR / 2; ++rp) {
+                for (int ps = 0; ps < QR / 2; ++ps) {
+                    const int rp = REV ? QR / 2 - 1 - ps : ps;
                     float kk[2], qq[2], e1[2], e2[2], vv2[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
+                    for (int es = 0; es < 2; ++es) {
+                        const int e = REV ? 1 - es : es;
                         const int rr = 2 * rp + e;
                         const bool on = FULL || rr < vq;
                         const float la = on ? sla[rr * 128 + c] : 0.f;
                         kk[e] = on ? ld_in(sk, rr * 128 + c) : 0.f;
                         qq[e] = ld_in(sq, rr * 128 + c);
                         vv2[e] = ld_in(sv, rr * 128 + c);
-                        g2 = fmaf(la, kLog2e, g2);
-                        const float x = g2 - ref;
-                        if (rr == 0 || rr == QR - 1) max_x = fmaxf(max_x, fabsf(x));
-                        e1[e] = fast_exp2(x);
-                        e2[e] = fast_exp2(-x);
+                        float xu;
+                        if (REV) {
+                            xu = x;
+                            x = fmaf(-la, kLog2e, x);
+                        } else {
+                            x = fmaf(la, kLog2e, x);
+                            xu = x;
+                        }
+                        if ((ps == 0 && es == 0) || (ps == QR / 2 - 1 && es == 1)) max_x = fmaxf(max_x, fabsf(xu));
+                        e1[e] = fast_exp2(xu);
+                        e2[e] = fast_exp2(-xu);
                     }
                     pk[rp] = pack_half2(kk[0] * e1[0], kk[1] * e1[1]);
                     pq[rp] = pack_half2(qq[0] * e1[0], qq[1] * e1[1]);
                     ph[rp] = pack_half2(kk[0] * e2[0], kk[1] * e2[1]);
                     pv[rp] = pack_half2(vv2[0], vv2[1]);
                 }
-                mbar_arrive(&bar[B_EMPTY + (4 * n + q) % L::NSLOT]);
+                mbar_arrive(&bar[B_EMPTY + (4 * n + i) % L::NSLOT]);
 #pragma unroll
                 for (int g8 = 0; g8 < 2; ++g8) {
                     const uint32_t off = sw128(c, 2 * q + g8);
@@ -508,17 +508,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tmem_st8(tmem + lane_base + TM_V16 + b * 32 + q * 8, pv);
             };
+            float ref = 0.f;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                if (q >= 2 && !wait_slot(q)) return false;
-                if (full)
-                    quarter(q, std::true_type{});
-                else
-                    quarter(q, std::false_type{});
-                if (c == 0 && q == 1) KDA_TR(n, 29);
+            for (int i = 0; i < 4; ++i) {
+                if (!wait_slot(i)) return false;
+                if (i == 2) {  // first half done: ref = -x, and the second half restarts at row 32
+                    ref = -x;
+                    x = 0.f;
+                }
+                if (i < 2) {
+                    if (full)
+                        quarter(i, std::true_type{}, std::true_type{});
+                    else
+                        quarter(i, std::false_type{}, std::true_type{});
+                } else {
+                    if (full)
+                        quarter(i, std::true_type{}, std::false_type{});
+                    else
+                        quarter(i, std::false_type{}, std::false_type{});
+                }
+                if (c == 0 && i == 1) KDA_TR(n, 29);
             }
             vec_a[v3 * 128 + c] = fast_exp2(ref);
-            vec_b[v3 * 128 + c] = fast_exp2(g2 - ref);
+            vec_b[v3 * 128 + c] = fast_exp2(x);  // e^{g_63 - ref}
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
