@@ -277,6 +277,39 @@ def run_ours(args):
     line["gpu_launches"] += DEC_STEPS + 3
     del d, st, dout
 
+    # ---- varlen prefix-cache workload: 16 packed sequences (log-uniform 1024..65536 tokens), H=64,
+    # every other sequence resuming from a state, snapshots every 16384 tokens (reported, not the metric)
+    lengths = synth.varlen_lengths(16, 1024, 65536, seed=synth.SEED_BASE + 4)
+    xv = synth.varlen_inputs(lengths, 64, seed=synth.SEED_BASE + 4, device=dev)
+    cu_h = xv["cu_seqlens"].cpu()
+    vout = torch.empty(xv["q"].shape, dtype=torch.float32, device=dev)
+    vfin = torch.empty_like(xv["init_states"])
+    varlen = lambda: kda.kda_varlen_fwd(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], xv["cu_seqlens"],
+                                        xv["init_states"], snapshot_interval=16384, cu_seqlens_host=cu_h, out=vout,
+                                        final_states=vfin)
+    vsnaps = varlen()[2]
+    for _ in range(2):
+        varlen()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(5):
+        kda.kda_varlen_fwd(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], xv["cu_seqlens"],
+                           xv["init_states"], snapshot_interval=16384, cu_seqlens_host=cu_h, out=vout,
+                           final_states=vfin, snapshots=vsnaps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    vt = e0.elapsed_time(e1) / 1e3 / 5
+    ttot = int(sum(lengths))
+    n_state = (16 + 8 + int(vsnaps.shape[0])) * 64  # final + resumed initial + snapshot states, per head
+    vbytes = ttot * 64 * (PREFILL_IN_BYTES + 512) + n_state * D * D * 4
+    line["varlen"] = {"tokens_per_s": ttot / vt, "ms_per_call": vt * 1e3, "GB_per_s": vbytes / vt / 1e9,
+                      "frac_of_hbm": vbytes / vt / 1e9 / peaks["hbm_gbs"],
+                      "workload": f"16 packed sequences ({ttot} tokens, log-uniform 1024..65536), H=64, chunk 64, "
+                                  f"8 resumed from a state, {int(vsnaps.shape[0])} snapshots every 16384 tokens, "
+                                  f"fp32 out"}
+    line["gpu_launches"] += 8
+    del xv, vout, vfin, vsnaps
+
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
         line["e2e"] = e2e(args, x, out, fin, ws, dev, out_dtype)
