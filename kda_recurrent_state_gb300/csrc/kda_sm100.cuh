@@ -30,21 +30,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
-#ifdef KDA_WAIT_HINT_NS
-    // with a suspend-time hint: a waiting thread sleeps until the phase completes
-    // (or the hint expires) instead of re-polling
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.b32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "n"(KDA_WAIT_HINT_NS)
-        : "memory");
-#else
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.b32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
-#endif
     return ok != 0;
 }
 
@@ -57,11 +47,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
-}
-
-// Named barrier over `nthreads` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Abort state shared by the CTA: set when any bounded wait expires.
@@ -92,16 +77,6 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, Abor
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, ab, status);
-}
-
-// 4-byte asynchronous global -> shared copy, and an arrive on `bar` that fires
-// once every cp.async of this thread issued so far has landed (the barrier's
-// expected count must include this arrival).
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ---------------------------------------------------------------- fences
@@ -234,22 +209,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-// ---------------------------------------------------------------- packed fp32 (sm_100 f32x2)
-// {d0, d1} += {a0, a1} * {b0, b1} and {d0, d1} = {a0, a1} * {b0, b1}: one instruction
-// for two lanes' worth of fp32 arithmetic, each result rounded as its scalar form.
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-    asm("{\n.reg .b64 ra, rb, rc;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\nmov.b64 rc, {%0, %1};\n"
-        "fma.rn.f32x2 rc, ra, rb, rc;\nmov.b64 {%0, %1}, rc;\n}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-    asm("{\n.reg .b64 ra, rb, rc;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
-        "mul.rn.f32x2 rc, ra, rb;\nmov.b64 {%0, %1}, rc;\n}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // ---------------------------------------------------------------- conversions
