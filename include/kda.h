@@ -153,6 +153,21 @@ int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);
 int kda_snapshot_offsets(const int64_t* cu_seqlens_host, int N, int64_t interval, int64_t* offsets_host);
 
 /*
+ * Host helper for resuming a sequence from its snapshots (the prefix-cache use of
+ * state snapshots, "Kimi K3 混合线性注意力", hubwiz.com, §5): the latest snapshot of
+ * sequence `seq` that covers at most `prefix_len` of its tokens.  `offsets_host`
+ * [N+1] is the output of kda_snapshot_offsets for the same `interval`.  Returns the
+ * snapshot's index into the packed snapshot array and writes the tokens it covers
+ * (m * interval) to *covered_host; a run resumed from it continues at that token
+ * (kda_chunk_fwd / kda_varlen_fwd with the snapshot as initial state reproduce the
+ * unsplit run bit for bit).  Returns -1 with *covered_host = 0 when the prefix is
+ * shorter than one interval (resume from the sequence's initial state), -2 on
+ * invalid arguments (null pointers, seq outside [0, N), interval <= 0, prefix_len < 0).
+ */
+int64_t kda_snapshot_lookup(const int64_t* offsets_host, int N, int seq, int64_t interval, int64_t prefix_len,
+                            int64_t* covered_host);
+
+/*
  * Bytes of device workspace the call `op` needs for these sizes (T = T_total
  * and B = N for KDA_OP_VARLEN).  0 means the workspace may be NULL.
  */

@@ -45,6 +45,8 @@ def lib() -> ctypes.CDLL:
         L.kda_snapshot_count.argtypes = [I64, I64]
         L.kda_snapshot_count.restype = I64
         L.kda_snapshot_offsets.argtypes = [P, I, I64, P]
+        L.kda_snapshot_lookup.argtypes = [P, I, I, I64, I64, P]
+        L.kda_snapshot_lookup.restype = I64
         L.kda_workspace_size.argtypes = [I, I, I64, I, I, I, I]
         L.kda_workspace_size.restype = SZ
         L.kda_status_string.argtypes = [I]
@@ -101,6 +103,18 @@ def kda_snapshot_offsets(cu_seqlens_host, interval: int) -> torch.Tensor:
     off = torch.empty(N + 1, dtype=torch.int64)
     _check(lib().kda_snapshot_offsets(_ptr(cu), N, int(interval), _ptr(off)), "kda_snapshot_offsets")
     return off
+
+
+def kda_snapshot_lookup(offsets_host, seq: int, interval: int, prefix_len: int):
+    """(index, covered): the latest snapshot of sequence `seq` covering at most `prefix_len`
+    tokens (index into the packed snapshots, tokens it covers), or (-1, 0) if there is none."""
+    off = torch.as_tensor(offsets_host, dtype=torch.int64).cpu().contiguous()
+    cov = ctypes.c_int64(0)
+    idx = lib().kda_snapshot_lookup(_ptr(off), off.numel() - 1, int(seq), int(interval), int(prefix_len),
+                                    ctypes.byref(cov))
+    if idx == -2:
+        raise KdaError(KDA_ERR_INVALID_ARG, "kda_snapshot_lookup")
+    return int(idx), int(cov.value)
 
 
 def kda_workspace_size(op: int, B: int, T: int, H: int, dk: int = 128, dv: int = 128, chunk: int = 64) -> int:

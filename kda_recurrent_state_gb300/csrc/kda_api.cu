@@ -85,6 +85,16 @@ int kda_snapshot_offsets(const int64_t* cu_seqlens_host, int N, int64_t interval
     return KDA_OK;
 }
 
+int64_t kda_snapshot_lookup(const int64_t* offsets_host, int N, int seq, int64_t interval, int64_t prefix_len,
+                            int64_t* covered_host) {
+    if (!offsets_host || !covered_host || seq < 0 || seq >= N || interval <= 0 || prefix_len < 0) return -2;
+    const int64_t have = offsets_host[seq + 1] - offsets_host[seq];
+    int64_t m = prefix_len / interval;
+    if (m > have) m = have;
+    *covered_host = m * interval;
+    return m > 0 ? offsets_host[seq] + m - 1 : -1;
+}
+
 size_t kda_workspace_size(int op, int B, int64_t T, int H, int dk, int dv, int chunk) {
     (void)T; (void)dk; (void)dv;
     if (op == KDA_OP_DECODE || B <= 0 || H <= 0 || chunk != 64) return 0;

@@ -70,6 +70,7 @@ using namespace sm100;
 constexpr int C = 64;   // chunk length
 constexpr int QR = 16;  // token rows per input slot
 constexpr int NTHREADS = 512;
+constexpr int kLptMax = 256;  // most packed sequences the kernel orders by length itself
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxExp2 = 15.0f;  // |g - ref| bound (log2 units) for fp16 operands
 constexpr int kRowH = 48;          // row stride (bytes) of a 16x16 fp16 block (ldmatrix: no bank conflicts)
@@ -306,7 +307,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x;
-    const int h = unit % P.H, s = unit / P.H;
+    const int h = unit % P.H;
+    // Packed sequences of different lengths: CTAs are handed out longest sequence first
+    // (CTA u takes the sequence of length rank u / H), so that the longest chains start
+    // first and the short ones fill in behind them.  Every CTA ranks the lengths itself
+    // (up to kLptMax sequences; beyond that, in order of appearance).
+    int s = unit / P.H;
+    if (P.cu_seqlens && P.N > 1 && P.N <= kLptMax) {
+        int64_t* cul = reinterpret_cast<int64_t*>(sm + L::OFF_RING);  // scratch before the ring is used
+        int* pick = reinterpret_cast<int*>(sm + L::OFF_RING + 8 * (kLptMax + 1));
+        for (int i = threadIdx.x; i <= P.N; i += NTHREADS) cul[i] = P.cu_seqlens[i];
+        __syncthreads();
+        for (int i = threadIdx.x; i < P.N; i += NTHREADS) {
+            const int64_t li = cul[i + 1] - cul[i];
+            int rank = 0;
+            for (int q = 0; q < P.N; ++q) {
+                const int64_t lq = cul[q + 1] - cul[q];
+                rank += (lq > li) || (lq == li && q < i);
+            }
+            if (rank == s) *pick = i;
+        }
+        __syncthreads();
+        s = *pick;
+        __syncthreads();
+    }
     int64_t t0, len;
     seq_bounds(P, s, t0, len);
     const int nch = (int)((len + C - 1) / C);

@@ -44,6 +44,21 @@ def test_snapshot_helpers(L):
         b.kda_snapshot_offsets([0, 100, 50], 64)  # decreasing cu_seqlens
 
 
+def test_snapshot_lookup(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    off = b.kda_snapshot_offsets([0, 1000, 1700, 1830], 128)  # 7, 5 and 1 snapshots
+    assert off.tolist() == [0, 7, 12, 13]
+    assert b.kda_snapshot_lookup(off, 0, 128, 700) == (4, 640)    # snapshot 5 of sequence 0
+    assert b.kda_snapshot_lookup(off, 0, 128, 5000) == (6, 896)   # clamped to its last snapshot
+    assert b.kda_snapshot_lookup(off, 1, 128, 256) == (8, 256)    # exactly on an interval
+    assert b.kda_snapshot_lookup(off, 2, 128, 100) == (-1, 0)     # shorter than one interval
+    assert b.kda_snapshot_lookup(off, 2, 128, 130) == (12, 128)
+    for bad in [(3, 128, 10), (-1, 128, 10), (0, 0, 10), (0, 128, -1)]:
+        with pytest.raises(b.KdaError):
+            b.kda_snapshot_lookup(off, *bad)
+
+
 def test_status_strings(L):
     from kda_recurrent_state_gb300 import binding as b
 

@@ -99,3 +99,27 @@ def test_varlen_full_size_sampled(chunk):
     longest = int(np.argmax(lengths))
     for s, heads in [(longest, [0, 63]), (0, [5]), (1, [17]), (7, [40]), (15, [62])]:
         _check_seq(x, s, heads, out, fin, snaps, off, 16384, "full")
+
+
+@pytest.mark.parametrize("prefix", [700, 1000])
+def test_resume_from_snapshot(prefix):
+    """Prefix reuse: the latest snapshot covering a request's prefix, used as the initial
+    state of a run over the remaining tokens, reproduces the unsplit run bit for bit
+    (outputs after the snapshot and the final state)."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    lengths = [1000, 700, 130]
+    x = synth.varlen_inputs(lengths, 3, seed=synth.SEED_BASE + 13, device="cuda", gate="slow")
+    out, fin, snaps = _run(x, 64, interval=128)
+    off = kda.kda_snapshot_offsets(x["cu_seqlens"].cpu(), 128)
+    idx, covered = kda.kda_snapshot_lookup(off, 0, 128, prefix)
+    assert covered == (prefix // 128) * 128 and idx == off[0].item() + prefix // 128 - 1
+    rest = {n: x[n][covered:lengths[0]].unsqueeze(0).contiguous() for n in ("q", "k", "v", "log_alpha", "beta")}
+    o2, f2 = kda.kda_chunk_fwd(rest["q"], rest["k"], rest["v"], rest["log_alpha"], rest["beta"],
+                               snaps[idx].unsqueeze(0).contiguous(), chunk=64)
+    torch.cuda.synchronize()
+    assert torch.equal(o2[0], out[covered:lengths[0]])
+    assert torch.equal(f2[0], fin[0])
+    assert kda.kda_snapshot_lookup(off, 2, 128, 100) == (-1, 0)
+
