@@ -30,6 +30,12 @@
  * (special cases with closed forms, the pages' overwrite example, brute
  * force matrix products on tiny inputs, and recurrent == chunked).
  *
+ * bf16-stored state ("Kimi K3 混合线性注意力", §3 sizes the state in bf16): the
+ * variant kda_oracle_recurrent_bf16state keeps every step's arithmetic in fp64
+ * but rounds the state to bf16 (round to nearest, ties to even) after each
+ * token's update and read, as a decode step that stores its state in bf16
+ * does.  kda_oracle_round_bf16 exposes that rounding.
+ *
  * Layouts (all contiguous, head-major; "n" = independent heads):
  *   q, k, log_alpha : [n][T][dk]  double  (bf16 / fp32 inputs upcast exactly)
  *   v               : [n][T][dv]  double
@@ -62,11 +68,24 @@ typedef struct {
     int64_t interval;
     double* snaps;
     int colblk; /* value columns per work unit */
+    int state_bf16; /* round the state to bf16 after every token */
     int64_t n_units;
     int64_t next; /* shared unit counter, guarded by mu */
     pthread_mutex_t mu;
     int err;
 } job_t;
+
+/* Nearest bf16 value (8 significant bits, fp32's exponent range), ties to even. */
+static double round_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    frexp(x, &e); /* |x| in [2^(e-1), 2^e) */
+    if (e < -125) e = -125; /* below 2^-126 the spacing stays 2^-133 (subnormals) */
+    const double quantum = ldexp(1.0, e - 8);
+    const double y = nearbyint(x / quantum) * quantum; /* default rounding: to nearest, ties to even */
+    if (fabs(y) > 3.3895313892515355e38) return copysign(INFINITY, x); /* beyond the largest bf16 */
+    return y;
+}
 
 static int64_t grab_unit(job_t* J) {
     pthread_mutex_lock(&J->mu);
@@ -129,6 +148,8 @@ static void recurrent_unit(job_t* J, int64_t h, int j0, int nj) {
         }
         double* ot = J->out + ((size_t)h * T + t) * dv + j0;
         for (int j = 0; j < nj; ++j) ot[j] = o[j];
+        if (J->state_bf16) /* the state is stored in bf16 between tokens */
+            for (size_t i = 0; i < (size_t)dk * nj; ++i) S[i] = round_bf16(S[i]);
 
         if (J->snaps && J->interval > 0 && (t + 1) % J->interval == 0) {
             const int64_t m = (t + 1) / J->interval - 1;
@@ -325,6 +346,26 @@ int kda_oracle_recurrent(int64_t n, int64_t T, int dk, int dv, const double* q, 
     J.colblk = 16;
     J.n_units = n * (int64_t)((dv + J.colblk - 1) / J.colblk);
     return run(&J, n_threads);
+}
+
+/* The same with the state rounded to bf16 after every token (S0 should hold bf16 values). */
+int kda_oracle_recurrent_bf16state(int64_t n, int64_t T, int dk, int dv, const double* q, const double* k,
+                                   const double* v, const double* log_alpha, const double* beta, const double* S0,
+                                   double* out, double* S_final, int n_threads) {
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.n = n; J.T = T; J.dk = dk; J.dv = dv; J.C = 0;
+    J.q = q; J.k = k; J.v = v; J.la = log_alpha; J.beta = beta; J.S0 = S0;
+    J.out = out; J.S_final = S_final;
+    J.colblk = 16;
+    J.state_bf16 = 1;
+    J.n_units = n * (int64_t)((dv + J.colblk - 1) / J.colblk);
+    return run(&J, n_threads);
+}
+
+/* round_bf16 over an array (exposed so that the rounding itself can be checked). */
+void kda_oracle_round_bf16(const double* x, double* y, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) y[i] = round_bf16(x[i]);
 }
 
 /* Naive chunked rewrite in fp64 (chunk length C >= 1). Returns 0 on success. */

@@ -48,6 +48,10 @@ def _bind(path: str):
     lib.kda_oracle_recurrent.restype = ctypes.c_int
     lib.kda_oracle_chunked.argtypes = [i64, i64, i32, i32, i32, f, f, f, f, f, d, d, d, i64, d, i32]
     lib.kda_oracle_chunked.restype = ctypes.c_int
+    lib.kda_oracle_recurrent_bf16state.argtypes = [i64, i64, i32, i32, f, f, f, f, f, d, d, d, i32]
+    lib.kda_oracle_recurrent_bf16state.restype = ctypes.c_int
+    lib.kda_oracle_round_bf16.argtypes = [d, d, i64]
+    lib.kda_oracle_round_bf16.restype = None
     return lib
 
 
@@ -101,6 +105,32 @@ def _run(which, q, k, v, log_alpha, beta, S0, chunk, snap_interval, threads, lib
 def recurrent(q, k, v, log_alpha, beta, S0=None, snap_interval: int = 0, threads: int | None = None, lib=None):
     """Per-token fp64 recurrence.  Returns (out [n,T,dv], S_final [n,dk,dv][, snaps])."""
     return _run("recurrent", q, k, v, log_alpha, beta, S0, 0, snap_interval, threads, lib)
+
+
+def recurrent_bf16state(q, k, v, log_alpha, beta, S0=None, threads: int | None = None, lib=None):
+    """Per-token recurrence (fp64 arithmetic) with the state rounded to bf16 after every token,
+    as stored by a decode step that keeps its state in bf16.  Returns (out, S_final)."""
+    lib = lib or load()
+    q, k, v, la, be = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(beta)
+    n, T, dk = q.shape
+    dv = v.shape[2]
+    s0 = None if S0 is None else np.ascontiguousarray(np.asarray(S0, dtype=np.float64))
+    out = np.zeros((n, T, dv), dtype=np.float64)
+    Sf = np.zeros((n, dk, dv), dtype=np.float64)
+    rc = lib.kda_oracle_recurrent_bf16state(n, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(be), _ptr(s0),
+                                            _ptr(out), _ptr(Sf), int(threads or os.cpu_count() or 1))
+    if rc != 0:
+        raise RuntimeError(f"oracle recurrent_bf16state failed (rc={rc})")
+    return out, Sf
+
+
+def round_bf16(x, lib=None) -> np.ndarray:
+    """The oracle's bf16 rounding (to nearest, ties to even) of fp64 values."""
+    lib = lib or load()
+    x = _f64(x)
+    y = np.empty_like(x)
+    lib.kda_oracle_round_bf16(_ptr(x), _ptr(y), x.size)
+    return y
 
 
 def chunked(q, k, v, log_alpha, beta, S0=None, chunk: int = 64, snap_interval: int = 0,

@@ -276,3 +276,69 @@ def test_planted_mistakes_are_caught(mutant, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"mutant {mutant} passed every pin"
+
+
+# --------------------------------------------------------------------------- bf16-stored state
+def test_round_bf16_matches_torch():
+    """The oracle's bf16 rounding equals torch's fp32 -> bf16 conversion (round to nearest,
+    ties to even) on fp32 values: random magnitudes, exact ties, subnormals, values near
+    the largest bf16 and beyond it."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal(20000) * np.exp2(rng.uniform(-140, 127, 20000))
+    ties = (1.0 + (2 * rng.integers(0, 128, 2000) + 1) * 2.0 ** -8) * np.exp2(rng.integers(-120, 120, 2000))
+    special = np.array([0.0, -0.0, 1.0, 3.3895313892515355e38, 3.3961e38, -3.3961e38, 2.0 ** -133, 2.0 ** -134,
+                        3 * 2.0 ** -135, 1e-45, 2.0 ** -126 * (1 - 2.0 ** -9)])
+    x32 = np.concatenate([x, ties, -ties, special]).astype(np.float32)
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(x32.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_bf16state_overwrite_reads_before_rounding():
+    """alpha = 1, beta = 1, unit key e_1: the step overwrites row 1 of the state with v.
+    The read o = S^T e_1 returns v exactly (taken before the state is rounded); the stored
+    row is v rounded to bf16, the other rows (bf16 values) are unchanged."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(22)
+    dk, dv = 8, 5
+    S0 = torch.from_numpy(rng.standard_normal((1, dk, dv)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    v = (1.0 + rng.integers(1, 2 ** 20, (1, 1, dv)) * 2.0 ** -21).astype(np.float32).astype(np.float64)
+    e1 = np.zeros((1, 1, dk))
+    e1[0, 0, 1] = 1.0
+    out, S = oracle.recurrent_bf16state(e1, e1, v, np.zeros((1, 1, dk)), np.ones((1, 1)), S0)
+    np.testing.assert_array_equal(out[0, 0], v[0, 0])
+    want_row = torch.from_numpy(v[0, 0].astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(S[0, 1], want_row)
+    rest = [i for i in range(dk) if i != 1]
+    np.testing.assert_array_equal(S[0, rest], S0[0, rest])
+
+
+def test_bf16state_equals_fp64_when_exact():
+    """Orthonormal basis keys, alpha = 1, beta = 1 and bf16-valued v: every state stays
+    exactly representable in bf16, so the rounding variant equals the fp64 recurrence."""
+    rng = np.random.default_rng(23)
+    dk, dv, T = 8, 6, 12
+    idx = rng.integers(0, dk, T)
+    k = np.zeros((1, T, dk))
+    k[0, np.arange(T), idx] = 1.0
+    q = np.zeros((1, T, dk))
+    q[0, np.arange(T), rng.integers(0, dk, T)] = 1.0
+    v = (rng.integers(-127, 128, (1, T, dv)) / 16.0)
+    la = np.zeros((1, T, dk))
+    b = np.ones((1, T))
+    o1, S1 = oracle.recurrent(q, k, v, la, b)
+    o2, S2 = oracle.recurrent_bf16state(q, k, v, la, b)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+
+
+def test_bf16state_error_bounded():
+    """With general inputs the stored state differs from the fp64 recurrence by no more than
+    bf16 rounding can explain: relative error of the final state well below 2^-6 over 64 steps."""
+    rng = np.random.default_rng(24)
+    q, k, v, la, b = _inputs(rng, 2, 64, 16, 8)
+    o1, S1 = oracle.recurrent(q, k, v, la, b)
+    o2, S2 = oracle.recurrent_bf16state(q, k, v, la, b)
+    assert 0 < rel(S2, S1) < 2.0 ** -6
+    assert 0 < rel(o2, o1) < 2.0 ** -6
