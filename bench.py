@@ -38,7 +38,8 @@ PREFILL_IN_BYTES = 3 * 256 + 512 + 4
 # flops per token-head of the chunked form at C = 64 (triangles counted half):
 # 6 dk dv + C (3 dk + 2 dv)
 PREFILL_FLOP = 6 * D * D + CHUNK * (3 * D + 2 * D)
-# decode: state read + written (2 x 65,536 B) + q,k,v bf16, log_alpha, beta, out fp32 per session-head
+# decode: fp32 state read + written (2 x 65,536 B; half that for a bf16 state) + q,k,v bf16,
+# log_alpha, beta, out fp32 per session-head
 DEC_BYTES = 2 * D * D * 4 + 3 * 256 + 512 + 4 + 512
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -254,28 +255,33 @@ def run_ours(args):
         "gpu_launches": args.steps,
     }
 
-    # ---- decode: 256 sessions x 96 heads, 64 steps with the state updated in place
+    # ---- decode: 256 sessions x 96 heads, 64 steps with the state updated in place, the state
+    # stored in fp32 (kda_decode_step) and in bf16 (kda_decode_step_bf16state)
     d = synth.decode_inputs(DEC_SESSIONS, H, seed=synth.SEED_BASE + 3, steps=DEC_STEPS, device=dev)
-    st = d["state"]
     dout = torch.empty(DEC_SESSIONS, H, D, dtype=torch.float32, device=dev)
-    dec = lambda s: kda.kda_decode_step(d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s], d["beta"][s], st, dout)
-    for s in range(3):
-        dec(s)
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for s in range(DEC_STEPS):
-        dec(s)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    dt = e0.elapsed_time(e1) / 1e3 / DEC_STEPS
-    dgbs = DEC_SESSIONS * H * DEC_BYTES / dt / 1e9
-    line["decode"] = {"session_steps_per_s": DEC_SESSIONS / dt, "GB_per_s": dgbs, "us_per_step": dt * 1e6,
-                      "roofline": {"bound": "hbm", "achieved": dgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                   "frac": dgbs / peaks["hbm_gbs"]},
-                      "workload": "256 sessions x 96 heads, fp32 state in place, 64 steps, bf16 q/k/v, fp32 out"}
-    line["gpu_launches"] += DEC_STEPS + 3
-    del d, st, dout
+    for key, fn, st, state_bytes in (("decode", kda.kda_decode_step, d["state"], 4),
+                                     ("decode_bf16state", kda.kda_decode_step_bf16state,
+                                      d["state"].to(torch.bfloat16), 2)):
+        dec = lambda s: fn(d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s], d["beta"][s], st, dout)
+        for s in range(3):
+            dec(s)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for s in range(DEC_STEPS):
+            dec(s)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dt = e0.elapsed_time(e1) / 1e3 / DEC_STEPS
+        dgbs = DEC_SESSIONS * H * (DEC_BYTES - 2 * D * D * (4 - state_bytes)) / dt / 1e9
+        line[key] = {"session_steps_per_s": DEC_SESSIONS / dt, "GB_per_s": dgbs, "us_per_step": dt * 1e6,
+                     "roofline": {"bound": "hbm", "achieved": dgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": dgbs / peaks["hbm_gbs"]},
+                     "workload": f"256 sessions x 96 heads, {'fp32' if state_bytes == 4 else 'bf16'} state in "
+                                 f"place, 64 steps, bf16 q/k/v, fp32 out"}
+        line["gpu_launches"] += DEC_STEPS + 3
+        del st
+    del d, dout
 
     # ---- varlen prefix-cache workload: 16 packed sequences (log-uniform 1024..65536 tokens), H=64,
     # every other sequence resuming from a state, snapshots every 16384 tokens (reported, not the metric)

@@ -31,7 +31,7 @@
  *     KDA_ERR_UNSUPPORTED.
  *   - Alignment (KDA_ERR_MISALIGNED otherwise): q, k, v, log_alpha, out and
  *     every state/snapshot pointer of the prefill calls 16 bytes (tensor-map
- *     loads); the state of kda_decode_step 16 bytes; beta 4 bytes; cu_seqlens
+ *     loads); the state of both decode calls 16 bytes; beta 4 bytes; cu_seqlens
  *     and snap_offsets 8 bytes; the other decode operands their element size.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  A return of KDA_OK means the work was enqueued.
@@ -140,6 +140,20 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log
 int kda_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
                     float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
                     void* stream);
+
+/*
+ * kda_decode_step with the state STORED in bf16 (halving the state bytes each
+ * step moves; the state is the whole memory of a session, "Kimi K3 混合线性注意力",
+ * hubwiz.com, §3, so its storage precision is a serving choice).  Arguments as
+ * for kda_decode_step except
+ *   state [B, H, dk, dv] bf16 (raw 16-bit storage), read and overwritten.
+ * Each element is widened exactly to fp32, the whole step runs in fp32, o_t is
+ * read from the updated state BEFORE rounding, and the new state is then stored
+ * rounded to nearest-even bf16.
+ */
+int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const float* log_alpha,
+                              const float* beta, void* state, void* out, int B, int H, int dk, int dv,
+                              int in_dtype, int out_dtype, void* stream);
 
 /* Number of snapshots of a sequence: floor(seqlen / interval); 0 if interval <= 0 or seqlen < 0. */
 int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);

@@ -42,6 +42,7 @@ def lib() -> ctypes.CDLL:
         L.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I, P, SZ, P]
         L.kda_varlen_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, P, P, I64, P, P, P, I, I, P, SZ, P]
         L.kda_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+        L.kda_decode_step_bf16state.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
         L.kda_snapshot_count.argtypes = [I64, I64]
         L.kda_snapshot_count.restype = I64
         L.kda_snapshot_offsets.argtypes = [P, I, I64, P]
@@ -52,7 +53,8 @@ def lib() -> ctypes.CDLL:
         L.kda_status_string.argtypes = [I]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_get_device_status.argtypes = [P]
-        for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_snapshot_offsets,
+        for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
+                  L.kda_snapshot_offsets,
                   L.kda_get_device_status):
             f.restype = I
         _lib = L
@@ -181,14 +183,28 @@ def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, ch
     return out, final_states, (snapshots if snapshot_interval else None)
 
 
-def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=torch.float32):
-    """One token per session: q,k [B,H,dk], v [B,H,dv], log_alpha [B,H,dk], beta [B,H];
-    state [B,H,dk,dv] fp32 is updated in place.  Returns out [B,H,dv]."""
+def _decode(fn, name, state_dtype, q, k, v, log_alpha, beta, state, out, out_dtype):
+    if state.dtype != state_dtype:
+        raise TypeError(f"{name}: state must be {state_dtype}, got {state.dtype}")
     B, H, dk = q.shape
     dv = v.shape[-1]
     if out is None:
         out = torch.empty(B, H, dv, dtype=out_dtype, device=q.device)
-    rc = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(state), _ptr(out), B, H,
-                               dk, dv, _dt(q), _dt(out), _stream(q.device))
-    _check(rc, "kda_decode_step")
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(state), _ptr(out), B, H, dk, dv, _dt(q),
+            _dt(out), _stream(q.device))
+    _check(rc, name)
     return out
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=torch.float32):
+    """One token per session: q,k [B,H,dk], v [B,H,dv], log_alpha [B,H,dk], beta [B,H];
+    state [B,H,dk,dv] fp32 is updated in place.  Returns out [B,H,dv]."""
+    return _decode(lib().kda_decode_step, "kda_decode_step", torch.float32, q, k, v, log_alpha, beta, state, out,
+                   out_dtype)
+
+
+def kda_decode_step_bf16state(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=torch.float32):
+    """kda_decode_step with a bf16-stored state [B,H,dk,dv] (updated in place; the step
+    itself runs in fp32 and the output is read before the state is rounded)."""
+    return _decode(lib().kda_decode_step_bf16state, "kda_decode_step_bf16state", torch.bfloat16, q, k, v, log_alpha,
+                   beta, state, out, out_dtype)

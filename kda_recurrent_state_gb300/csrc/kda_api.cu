@@ -187,9 +187,9 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log
     return run_prefill(p, chunk, in_dtype, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-int kda_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
-                    float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
-                    void* stream) {
+static int decode_common(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                         void* state, int state_dtype, void* out, int B, int H, int dk, int dv, int in_dtype,
+                         int out_dtype, void* stream) {
     if (B < 0 || H < 0) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return KDA_ERR_INVALID_ARG;
     if (dk != kD || dv != kD) return KDA_ERR_UNSUPPORTED;
@@ -199,9 +199,23 @@ int kda_decode_step(const void* q, const void* k, const void* v, const float* lo
     if (!aligned16(state) || !aligned(q, in_al) || !aligned(k, in_al) || !aligned(v, in_al) ||
         !aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned(out, out_al))
         return KDA_ERR_MISALIGNED;
-    DecodeProblem p{q, k, v, log_alpha, beta, state, out, B, H};
-    return launch_decode(p, in_dtype, out_dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
-                                                                                               : KDA_ERR_CUDA;
+    DecodeProblem p{q, k, v, log_alpha, beta, state, out, B, H, status_ptr()};
+    if (!p.status) return KDA_ERR_CUDA;
+    return launch_decode(p, in_dtype, out_dtype, state_dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
+int kda_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                    float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
+                    void* stream) {
+    return decode_common(q, k, v, log_alpha, beta, state, KDA_F32, out, B, H, dk, dv, in_dtype, out_dtype, stream);
+}
+
+int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const float* log_alpha,
+                              const float* beta, void* state, void* out, int B, int H, int dk, int dv,
+                              int in_dtype, int out_dtype, void* stream) {
+    return decode_common(q, k, v, log_alpha, beta, state, KDA_BF16, out, B, H, dk, dv, in_dtype, out_dtype, stream);
 }
 
 }  // extern "C"

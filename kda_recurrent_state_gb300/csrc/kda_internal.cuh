@@ -41,10 +41,11 @@ struct DecodeProblem {
     const void* v;
     const float* log_alpha;
     const float* beta;
-    float* state;
+    void* state;  // [B, H, D, D] fp32 or bf16
     void* out;
     int B;
     int H;
+    int* status;  // device status word
 };
 
 __host__ __device__ inline void seq_bounds(const SeqProblem& p, int s, int64_t& start, int64_t& len) {
@@ -58,7 +59,7 @@ __host__ __device__ inline void seq_bounds(const SeqProblem& p, int s, int64_t& 
 }
 
 // Launchers (return a cudaError_t from the launch).
-cudaError_t launch_decode(const DecodeProblem& p, int in_dtype, int out_dtype, cudaStream_t st);
+cudaError_t launch_decode(const DecodeProblem& p, int in_dtype, int out_dtype, int state_dtype, cudaStream_t st);
 cudaError_t launch_serial_prefill(const SeqProblem& p, int in_dtype, int out_dtype, cudaStream_t st);
 cudaError_t launch_chunk_prefill(const SeqProblem& p, int in_dtype, int out_dtype, void* workspace,
                                  size_t ws_bytes, cudaStream_t st);

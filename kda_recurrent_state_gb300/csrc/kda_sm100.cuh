@@ -60,7 +60,7 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s: far beyond any legitim
 // and the device status) if the deadline passes or another role aborted.
 // Slow path of mbar_wait, kept out of line so that the many wait sites stay small
 // in the instruction cache.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
     const long long t0 = clock64();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -107,6 +107,14 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+// Contiguous bulk copy global -> shared (async proxy), completion counted on `bar`.
+// Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

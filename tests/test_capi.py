@@ -100,6 +100,12 @@ def test_argument_validation(L):
                              None) == b.KDA_ERR_MISALIGNED
     assert L.kda_decode_step(P(16), P(16), P(16), P(16), P(0x1002), P(16), P(16), 2, 2, 128, 128, 0, 1,
                              None) == b.KDA_ERR_MISALIGNED  # beta needs 4 bytes
+    assert L.kda_decode_step_bf16state(P(16), P(16), P(16), P(16), P(16), P(16), P(16), 2, 2, 128, 96, 0, 1,
+                                       None) == b.KDA_ERR_UNSUPPORTED
+    assert L.kda_decode_step_bf16state(P(16), P(16), P(16), P(16), P(16), P(0x1008), P(16), 2, 2, 128, 128, 0,
+                                       1, None) == b.KDA_ERR_MISALIGNED  # the state needs 16 bytes
+    assert L.kda_decode_step_bf16state(P(16), P(16), P(16), P(16), P(16), P(16), P(16), 0, 2, 128, 128, 0, 1,
+                                       None) == b.KDA_OK  # B = 0: nothing to do
 
 
 def test_workspace_size(L):

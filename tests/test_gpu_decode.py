@@ -1,24 +1,27 @@
-"""GPU parity of kda_decode_step against the fp64 oracle (through the C ABI)."""
+"""GPU parity of kda_decode_step and kda_decode_step_bf16state against the fp64 oracle
+(through the C ABI)."""
 import numpy as np
 import pytest
 import torch
 
-from kda_testutil import assert_close, np64
+from kda_testutil import assert_close, errors, np64
 from oracle import oracle
 
 pytestmark = pytest.mark.gpu
 
 
-def _oracle_steps(d, pairs, steps):
-    """Oracle over `steps` tokens for the listed (b,h) pairs, starting from d['state']."""
+def _oracle_steps(d, pairs, steps, fn=oracle.recurrent, state=None):
+    """Oracle over `steps` tokens for the listed (b,h) pairs, starting from `state`
+    (default d['state'])."""
+    state = d["state"] if state is None else state
     col = lambda t, b, h: np64(t[:steps, b, h])
     q = np.stack([col(d["q"], b, h) for b, h in pairs])
     k = np.stack([col(d["k"], b, h) for b, h in pairs])
     v = np.stack([col(d["v"], b, h) for b, h in pairs])
     la = np.stack([col(d["log_alpha"], b, h) for b, h in pairs])
     be = np.stack([col(d["beta"], b, h) for b, h in pairs])
-    S0 = np.stack([np64(d["state"][b, h]) for b, h in pairs])
-    return oracle.recurrent(q, k, v, la, be, S0)
+    S0 = np.stack([np64(state[b, h]) for b, h in pairs])
+    return fn(q, k, v, la, be, S0)
 
 
 @pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
@@ -71,3 +74,96 @@ def test_decode_empty_is_noop():
     st = torch.empty(0, 4, 128, 128, device="cuda")
     out = kda.kda_decode_step(z, z, z, z.float(), torch.empty(0, 4, device="cuda"), st)
     assert out.shape == (0, 4, 128)
+
+
+# ---- bf16-stored state -------------------------------------------------------------
+
+
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
+def test_decode_bf16state_small(in_dtype):
+    """Several steps on a bf16 state against the oracle that rounds its fp64 state to bf16
+    after every token (the output is read before the rounding)."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    B, H, steps = 5, 3, 6
+    d = synth.decode_inputs(B, H, seed=211, steps=steps, device="cuda", in_dtype=in_dtype)
+    state = d["state"].to(torch.bfloat16)
+    s0 = state.clone()
+    outs = [kda.kda_decode_step_bf16state(d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s], d["beta"][s], state)
+            for s in range(steps)]
+    torch.cuda.synchronize()
+    pairs = [(b, h) for b in range(B) for h in range(H)]
+    ro, rs = _oracle_steps(d, pairs, steps, oracle.recurrent_bf16state, s0)
+    got_o = np.stack([np.stack([np64(outs[s][b, h]) for s in range(steps)]) for b, h in pairs])
+    assert_close(got_o, ro, "bf16-state decode outputs")
+    assert_close(np.stack([np64(state[b, h]) for b, h in pairs]), rs, "bf16-state decode state")
+    assert kda.kda_get_device_status() == 0
+
+
+def test_decode_bf16state_rounding_one_step():
+    """One step from a bf16 state: the stored state is the fp32 update rounded to nearest
+    bf16, so it equals the oracle's rounded fp64 update except where the two sides'
+    unrounded values straddle a rounding boundary (then they differ by one bf16 unit, or
+    by the fp32 rounding of the update's terms where an entry cancels to near zero).
+    Truncation instead of rounding would change about half of the elements."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    B, H = 8, 16
+    d = synth.decode_inputs(B, H, seed=223, steps=1, device="cuda")
+    state = d["state"].to(torch.bfloat16)
+    s0 = state.clone()
+    kda.kda_decode_step_bf16state(d["q"][0], d["k"][0], d["v"][0], d["log_alpha"][0], d["beta"][0], state)
+    torch.cuda.synchronize()
+    pairs = [(b, h) for b in range(B) for h in range(H)]
+    _, rs = _oracle_steps(d, pairs, 1, oracle.recurrent_bf16state, s0)
+    got = np.stack([np64(state[b, h]) for b, h in pairs])
+    diff = got != rs
+    ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(rs), 1e-30))[1] - 8)  # bf16 spacing at |rs|
+    # fp32 rounding of the update's terms (a few units of 2^-24 of the head's largest entry)
+    # can exceed the bf16 spacing of an entry that cancels to near zero
+    slack = ulp + 2.0 ** -19 * np.abs(rs).max(axis=(1, 2), keepdims=True)
+    err = np.abs(got - rs)
+    w = np.unravel_index(np.argmax(err / slack), err.shape)
+    assert np.all(err <= slack), f"stored state at {w}: {got[w]!r} vs {rs[w]!r} (bf16 unit {ulp[w]:.3e})"
+    assert diff.mean() < 1e-3, f"{diff.mean():.2e} of the stored elements differ from round-to-nearest"
+
+
+def test_decode_bf16state_full_size_sampled():
+    """256 sessions x 96 heads with a bf16 state, 64 successive in-place steps; sampled
+    (session, head) pairs against the rounding oracle, and the drift from the fp64-state
+    recurrence stays within what bf16 storage implies."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    Bs, H, steps = 256, 96, 64
+    d = synth.decode_inputs(Bs, H, seed=synth.SEED_BASE + 3, steps=steps, device="cuda")
+    state = d["state"].to(torch.bfloat16)
+    s0 = state.clone()
+    pairs = [(0, 0), (255, 95), (17, 40), (128, 3), (200, 77), (63, 64)]
+    outs = torch.empty(steps, len(pairs), 128, device="cuda")
+    for s in range(steps):
+        o = kda.kda_decode_step_bf16state(d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s], d["beta"][s], state)
+        for i, (b, h) in enumerate(pairs):
+            outs[s, i] = o[b, h]
+    torch.cuda.synchronize()
+    got_o = np64(outs).transpose(1, 0, 2)
+    got_s = np.stack([np64(state[b, h]) for b, h in pairs])
+    ro, rs = _oracle_steps(d, pairs, steps, oracle.recurrent_bf16state, s0)
+    assert_close(got_o, ro, "bf16-state decode outputs")
+    assert_close(got_s, rs, "bf16-state decode state")
+    fo, fs = _oracle_steps(d, pairs, steps, oracle.recurrent, s0)  # same start, state kept in fp64
+    rel_o, _ = errors(got_o, fo)
+    rel_s, _ = errors(got_s, fs)
+    assert rel_o < 3e-2 and rel_s < 3e-2, (rel_o, rel_s)
+    assert kda.kda_get_device_status() == 0
+
+
+def test_decode_bf16state_rejects_fp32_state():
+    import kda_recurrent_state_gb300 as kda
+
+    z = torch.zeros(1, 1, 128, device="cuda")
+    with pytest.raises(TypeError):
+        kda.kda_decode_step_bf16state(z, z, z, z, torch.zeros(1, 1, device="cuda"), torch.zeros(1, 1, 128, 128,
+                                                                                                  device="cuda"))
