@@ -255,11 +255,35 @@ def run_ours(args):
         "gpu_launches": args.steps,
     }
 
+    # ---- the same prefill with one gate per (token, head) (Gated DeltaNet) and with none
+    # (DeltaNet): 508 fewer gate bytes per token-head
+    la_h = synth.head_gates((B, T), H, seed=synth.SEED_BASE + 5, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for key, gate, gate_b in (("gdn_prefill", la_h, 4), ("deltanet_prefill", None, 0)):
+        run = lambda: kda.kda_gdn_chunk_fwd(x["q"], x["k"], x["v"], gate, x["beta"], None, out, fin,
+                                            chunk=args.chunk, workspace=ws)
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(5):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        gt = e0.elapsed_time(e1) / 1e3 / 5
+        gbytes = B * T * H * (PREFILL_IN_BYTES - 512 + gate_b + out_b)
+        line[key] = {"tokens_per_s": B * T / gt, "ms_per_call": gt * 1e3, "GB_per_s": gbytes / gt / 1e9,
+                     "frac_of_hbm": gbytes / gt / 1e9 / peaks["hbm_gbs"],
+                     "workload": f"B={B} H={H} T={T}, bf16 q/k/v, "
+                                 + ("one fp32 log-decay per token-head" if gate_b else "no decay") + f", {args.out_dtype} out"}
+        line["gpu_launches"] += 7
+    assert kda.kda_get_device_status() == 0, "device status raised by the scalar-gate prefill"
+    del la_h
+
     # ---- decode: 256 sessions x 96 heads, 64 steps with the state updated in place, the state
     # stored in fp32 (kda_decode_step) and in bf16 (kda_decode_step_bf16state)
     d = synth.decode_inputs(DEC_SESSIONS, H, seed=synth.SEED_BASE + 3, steps=DEC_STEPS, device=dev)
     dout = torch.empty(DEC_SESSIONS, H, D, dtype=torch.float32, device=dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for key, fn, st, state_bytes in (("decode", kda.kda_decode_step, d["state"], 4),
                                      ("decode_bf16state", kda.kda_decode_step_bf16state,
                                       d["state"].to(torch.bfloat16), 2)):

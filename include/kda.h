@@ -155,6 +155,35 @@ int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const
                               const float* beta, void* state, void* out, int B, int H, int dk, int dv,
                               int in_dtype, int out_dtype, void* stream);
 
+/*
+ * The same three operations with a coarser gate.  "Kimi K3" article, §四: Gated
+ * DeltaNet decays the whole state of a head by ONE scalar alpha_t per token,
+ *     S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+ * which KDA refines into one alpha per key channel; with a scalar, decaying
+ * before or after the delta step is the same operator.  §三: with no gate at
+ * all (alpha_t = 1) the update is the plain delta rule (DeltaNet).
+ *   log_alpha  float32 with ONE value per (token, head): [B, T, H] for
+ *              kda_gdn_chunk_fwd, [T_total, H] for kda_gdn_varlen_fwd, [B, H] for
+ *              kda_gdn_decode_step; 4-byte aligned; finite and <= 0.
+ *              NULL selects DeltaNet (alpha = 1 everywhere).
+ * Every other argument, the layouts, the snapshot rules, the results' bit-exact
+ * reproducibility and the error codes are those of kda_chunk_fwd,
+ * kda_varlen_fwd and kda_decode_step.  The per-half-chunk gate range of
+ * kda_chunk_fwd applies to the scalar gate in the same way.
+ */
+int kda_gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                      const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
+                      int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
+                      void* stream);
+int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                       const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv, int chunk,
+                       const float* init_states, float* final_states, int64_t snapshot_interval,
+                       const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
+                       void* workspace, size_t ws_bytes, void* stream);
+int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                        float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
+                        void* stream);
+
 /* Number of snapshots of a sequence: floor(seqlen / interval); 0 if interval <= 0 or seqlen < 0. */
 int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);
 

@@ -43,6 +43,9 @@ def lib() -> ctypes.CDLL:
         L.kda_varlen_fwd.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, P, P, I64, P, P, P, I, I, P, SZ, P]
         L.kda_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
         L.kda_decode_step_bf16state.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+        L.kda_gdn_chunk_fwd.argtypes = L.kda_chunk_fwd.argtypes
+        L.kda_gdn_varlen_fwd.argtypes = L.kda_varlen_fwd.argtypes
+        L.kda_gdn_decode_step.argtypes = L.kda_decode_step.argtypes
         L.kda_snapshot_count.argtypes = [I64, I64]
         L.kda_snapshot_count.restype = I64
         L.kda_snapshot_offsets.argtypes = [P, I, I64, P]
@@ -54,7 +57,7 @@ def lib() -> ctypes.CDLL:
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_get_device_status.argtypes = [P]
         for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
-                  L.kda_snapshot_offsets,
+                  L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_snapshot_offsets,
                   L.kda_get_device_status):
             f.restype = I
         _lib = L
@@ -135,10 +138,8 @@ def _workspace(op, B, T, H, dk, dv, chunk, device, workspace):
     return workspace, (workspace.numel() * workspace.element_size() if workspace is not None else 0)
 
 
-def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, out=None, final_state=None, *, chunk: int = 64,
-                  out_dtype=torch.float32, return_final_state: bool = True, workspace=None):
-    """Batched prefill.  q,k [B,T,H,dk], v [B,T,H,dv] (bf16/fp32), log_alpha [B,T,H,dk] fp32,
-    beta [B,T,H] fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state)."""
+def _chunk(name, q, k, v, log_alpha, beta, init_state, out, final_state, chunk, out_dtype, return_final_state,
+           workspace):
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     if out is None:
@@ -146,18 +147,31 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, out=None, final_sta
     if final_state is None and return_final_state:
         final_state = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
     ws, ws_bytes = _workspace(KDA_OP_CHUNK, B, T, H, dk, dv, chunk, q.device, workspace)
-    rc = lib().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(out),
-                             _ptr(final_state), B, T, H, dk, dv, int(chunk), _dt(q), _dt(out), _ptr(ws), ws_bytes,
-                             _stream(q.device))
-    _check(rc, "kda_chunk_fwd")
+    rc = getattr(lib(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(out),
+                              _ptr(final_state), B, T, H, dk, dv, int(chunk), _dt(q), _dt(out), _ptr(ws), ws_bytes,
+                              _stream(q.device))
+    _check(rc, name)
     return out, final_state
 
 
-def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, chunk: int = 64,
-                   snapshot_interval: int = 0, cu_seqlens_host=None, out=None, final_states=None,
-                   snapshots=None, out_dtype=torch.float32, workspace=None):
-    """Packed sequences.  q,k [Ttot,H,dk], v [Ttot,H,dv], log_alpha [Ttot,H,dk], beta [Ttot,H];
-    cu_seqlens int64 [N+1] on the device.  Returns (out, final_states, snapshots or None)."""
+def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, out=None, final_state=None, *, chunk: int = 64,
+                  out_dtype=torch.float32, return_final_state: bool = True, workspace=None):
+    """Batched prefill.  q,k [B,T,H,dk], v [B,T,H,dv] (bf16/fp32), log_alpha [B,T,H,dk] fp32,
+    beta [B,T,H] fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state)."""
+    return _chunk("kda_chunk_fwd", q, k, v, log_alpha, beta, init_state, out, final_state, chunk, out_dtype,
+                  return_final_state, workspace)
+
+
+def kda_gdn_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, out=None, final_state=None, *, chunk: int = 64,
+                      out_dtype=torch.float32, return_final_state: bool = True, workspace=None):
+    """kda_chunk_fwd with one log-decay per (token, head): log_alpha [B,T,H] fp32 (Gated
+    DeltaNet), or None for no decay (DeltaNet)."""
+    return _chunk("kda_gdn_chunk_fwd", q, k, v, log_alpha, beta, init_state, out, final_state, chunk, out_dtype,
+                  return_final_state, workspace)
+
+
+def _varlen(name, q, k, v, log_alpha, beta, cu_seqlens, init_states, chunk, snapshot_interval, cu_seqlens_host,
+            out, final_states, snapshots, out_dtype, workspace):
     Ttot, H, dk = q.shape
     dv = v.shape[-1]
     N = cu_seqlens.numel() - 1
@@ -173,14 +187,31 @@ def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, ch
         if snapshots is None:
             snapshots = torch.empty(max(int(off_h[-1]), 1), H, dk, dv, dtype=torch.float32, device=q.device)
     ws, ws_bytes = _workspace(KDA_OP_VARLEN, N, Ttot, H, dk, dv, chunk, q.device, workspace)
-    rc = lib().kda_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), N, Ttot, H,
-                              dk, dv, int(chunk), _ptr(init_states), _ptr(final_states), int(snapshot_interval),
+    rc = getattr(lib(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), N, Ttot,
+                              H, dk, dv, int(chunk), _ptr(init_states), _ptr(final_states), int(snapshot_interval),
                               _ptr(snap_off), _ptr(snapshots) if snapshot_interval else None, _ptr(out), _dt(q),
                               _dt(out), _ptr(ws), ws_bytes, _stream(q.device))
-    _check(rc, "kda_varlen_fwd")
+    _check(rc, name)
     if snapshot_interval and snapshots is not None:
         snapshots = snapshots[: int(snap_off[-1].item())] if snapshots.shape[0] > 0 else snapshots
     return out, final_states, (snapshots if snapshot_interval else None)
+
+
+def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, chunk: int = 64,
+                   snapshot_interval: int = 0, cu_seqlens_host=None, out=None, final_states=None,
+                   snapshots=None, out_dtype=torch.float32, workspace=None):
+    """Packed sequences.  q,k [Ttot,H,dk], v [Ttot,H,dv], log_alpha [Ttot,H,dk], beta [Ttot,H];
+    cu_seqlens int64 [N+1] on the device.  Returns (out, final_states, snapshots or None)."""
+    return _varlen("kda_varlen_fwd", q, k, v, log_alpha, beta, cu_seqlens, init_states, chunk, snapshot_interval,
+                   cu_seqlens_host, out, final_states, snapshots, out_dtype, workspace)
+
+
+def kda_gdn_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, chunk: int = 64,
+                       snapshot_interval: int = 0, cu_seqlens_host=None, out=None, final_states=None,
+                       snapshots=None, out_dtype=torch.float32, workspace=None):
+    """kda_varlen_fwd with log_alpha [Ttot,H] (Gated DeltaNet) or None (DeltaNet)."""
+    return _varlen("kda_gdn_varlen_fwd", q, k, v, log_alpha, beta, cu_seqlens, init_states, chunk,
+                   snapshot_interval, cu_seqlens_host, out, final_states, snapshots, out_dtype, workspace)
 
 
 def _decode(fn, name, state_dtype, q, k, v, log_alpha, beta, state, out, out_dtype):
@@ -208,3 +239,9 @@ def kda_decode_step_bf16state(q, k, v, log_alpha, beta, state, out=None, *, out_
     itself runs in fp32 and the output is read before the state is rounded)."""
     return _decode(lib().kda_decode_step_bf16state, "kda_decode_step_bf16state", torch.bfloat16, q, k, v, log_alpha,
                    beta, state, out, out_dtype)
+
+
+def kda_gdn_decode_step(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=torch.float32):
+    """kda_decode_step with log_alpha [B,H] (Gated DeltaNet) or None (DeltaNet); fp32 state."""
+    return _decode(lib().kda_gdn_decode_step, "kda_gdn_decode_step", torch.float32, q, k, v, log_alpha, beta, state,
+                   out, out_dtype)

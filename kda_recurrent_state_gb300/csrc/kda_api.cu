@@ -40,10 +40,10 @@ int check_common(int dk, int dv, int chunk, int in_dtype, int out_dtype) {
     return KDA_OK;
 }
 
-int run_prefill(const SeqProblem& p, int chunk, int in_dtype, int out_dtype, void* ws, size_t ws_bytes,
+int run_prefill(const SeqProblem& p, int gate, int chunk, int in_dtype, int out_dtype, void* ws, size_t ws_bytes,
                 cudaStream_t st) {
-    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, in_dtype, out_dtype, st)
-                                 : launch_chunk_prefill(p, in_dtype, out_dtype, ws, ws_bytes, st);
+    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, gate, in_dtype, out_dtype, st)
+                                 : launch_chunk_prefill(p, gate, in_dtype, out_dtype, ws, ws_bytes, st);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -112,10 +112,19 @@ int kda_get_device_status(void* stream) {
     return host;
 }
 
-int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
-                  const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
-                  int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
-                  void* stream) {
+// The gates: per channel (16-byte aligned, TMA), per head (4-byte aligned) or none (null).
+static bool gate_ok(const float* log_alpha, int gate, bool required) {
+    if (gate == kGateNone) return log_alpha == nullptr;
+    return log_alpha ? true : !required;
+}
+static bool gate_aligned(const float* log_alpha, int gate) {
+    return !log_alpha || (gate == kGateChannel ? aligned16(log_alpha) : aligned(log_alpha, 4));
+}
+
+static int chunk_common(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
+                        const float* beta, const float* init_state, void* out, float* final_state, int B,
+                        int64_t T, int H, int dk, int dv, int chunk, int in_dtype, int out_dtype, void* workspace,
+                        size_t ws_bytes, void* stream) {
     if (B < 0 || T < 0 || H < 0) return KDA_ERR_INVALID_ARG;
     int rc = check_common(dk, dv, chunk, in_dtype, out_dtype);
     if (rc != KDA_OK) return rc;
@@ -132,11 +141,11 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
                                    : cudaMemsetAsync(final_state, 0, state_bytes, st);
         return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
-    if (!q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, log_alpha, init_state, out, final_state};
+    if (!q || !k || !v || !gate_ok(log_alpha, gate, true) || !beta || !out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, init_state, out, final_state};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
-    if (!aligned(beta, 4)) return KDA_ERR_MISALIGNED;
+    if (!aligned(beta, 4) || !gate_aligned(log_alpha, gate)) return KDA_ERR_MISALIGNED;
     const size_t need = kda_workspace_size(KDA_OP_CHUNK, B, T, H, dk, dv, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
     if (workspace && !aligned16(workspace)) return KDA_ERR_MISALIGNED;
@@ -149,28 +158,46 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
     p.snap_interval = 0; p.snap_offsets = nullptr; p.snapshots = nullptr;
     p.status = status_ptr();
     if (!p.status) return KDA_ERR_CUDA;
-    return run_prefill(p, chunk, in_dtype, out_dtype, workspace, ws_bytes, st);
+    return run_prefill(p, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes, st);
 }
 
-int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
-                   const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv, int chunk,
-                   const float* init_states, float* final_states, int64_t snapshot_interval,
-                   const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
-                   void* workspace, size_t ws_bytes, void* stream) {
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                  const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
+                  int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
+                  void* stream) {
+    return chunk_common(q, k, v, log_alpha, kGateChannel, beta, init_state, out, final_state, B, T, H, dk, dv,
+                        chunk, in_dtype, out_dtype, workspace, ws_bytes, stream);
+}
+
+int kda_gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                      const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
+                      int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
+                      void* stream) {
+    return chunk_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, init_state, out, final_state,
+                        B, T, H, dk, dv, chunk, in_dtype, out_dtype, workspace, ws_bytes, stream);
+}
+
+static int varlen_common(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
+                         const float* beta, const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk,
+                         int dv, int chunk, const float* init_states, float* final_states,
+                         int64_t snapshot_interval, const int64_t* snap_offsets, float* snapshots, void* out,
+                         int in_dtype, int out_dtype, void* workspace, size_t ws_bytes, void* stream) {
     if (N < 0 || T_total < 0 || H < 0 || snapshot_interval < 0) return KDA_ERR_INVALID_ARG;
     int rc = check_common(dk, dv, chunk, in_dtype, out_dtype);
     if (rc != KDA_OK) return rc;
     if (N == 0 || H == 0) return KDA_OK;
     if (!cu_seqlens || !final_states) return KDA_ERR_INVALID_ARG;
-    if (T_total > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    if (!gate_ok(log_alpha, gate, T_total > 0)) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !beta || !out)) return KDA_ERR_INVALID_ARG;
     if (snapshot_interval > 0) {
         if (snapshot_interval % chunk != 0) return KDA_ERR_INVALID_ARG;
         if (!snap_offsets) return KDA_ERR_INVALID_ARG;
     }
-    const void* ptrs[] = {q, k, v, log_alpha, init_states, final_states, snapshots, out};
+    const void* ptrs[] = {q, k, v, init_states, final_states, snapshots, out};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
-    if ((beta && !aligned(beta, 4)) || !aligned(cu_seqlens, 8) || (snap_offsets && !aligned(snap_offsets, 8)))
+    if ((beta && !aligned(beta, 4)) || !gate_aligned(log_alpha, gate) || !aligned(cu_seqlens, 8) ||
+        (snap_offsets && !aligned(snap_offsets, 8)))
         return KDA_ERR_MISALIGNED;
     const size_t need = kda_workspace_size(KDA_OP_VARLEN, N, T_total, H, dk, dv, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
@@ -184,22 +211,42 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log
     p.snap_interval = snapshot_interval; p.snap_offsets = snap_offsets; p.snapshots = snapshots;
     p.status = status_ptr();
     if (!p.status) return KDA_ERR_CUDA;
-    return run_prefill(p, chunk, in_dtype, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+    return run_prefill(p, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-static int decode_common(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
-                         void* state, int state_dtype, void* out, int B, int H, int dk, int dv, int in_dtype,
-                         int out_dtype, void* stream) {
+int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                   const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv, int chunk,
+                   const float* init_states, float* final_states, int64_t snapshot_interval,
+                   const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
+                   void* workspace, size_t ws_bytes, void* stream) {
+    return varlen_common(q, k, v, log_alpha, kGateChannel, beta, cu_seqlens, N, T_total, H, dk, dv, chunk,
+                         init_states, final_states, snapshot_interval, snap_offsets, snapshots, out, in_dtype,
+                         out_dtype, workspace, ws_bytes, stream);
+}
+
+int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                       const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv, int chunk,
+                       const float* init_states, float* final_states, int64_t snapshot_interval,
+                       const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
+                       void* workspace, size_t ws_bytes, void* stream) {
+    return varlen_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, cu_seqlens, N, T_total, H,
+                         dk, dv, chunk, init_states, final_states, snapshot_interval, snap_offsets, snapshots, out,
+                         in_dtype, out_dtype, workspace, ws_bytes, stream);
+}
+
+static int decode_common(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
+                         const float* beta, void* state, int state_dtype, void* out, int B, int H, int dk, int dv,
+                         int in_dtype, int out_dtype, void* stream) {
     if (B < 0 || H < 0) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return KDA_ERR_INVALID_ARG;
     if (dk != kD || dv != kD) return KDA_ERR_UNSUPPORTED;
     if (B == 0 || H == 0) return KDA_OK;
-    if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !gate_ok(log_alpha, gate, true) || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
     const uintptr_t in_al = in_dtype == KDA_BF16 ? 2 : 4, out_al = out_dtype == KDA_BF16 ? 2 : 4;
     if (!aligned16(state) || !aligned(q, in_al) || !aligned(k, in_al) || !aligned(v, in_al) ||
-        !aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned(out, out_al))
+        (log_alpha && !aligned(log_alpha, 4)) || !aligned(beta, 4) || !aligned(out, out_al))
         return KDA_ERR_MISALIGNED;
-    DecodeProblem p{q, k, v, log_alpha, beta, state, out, B, H, status_ptr()};
+    DecodeProblem p{q, k, v, log_alpha, beta, state, out, B, H, status_ptr(), gate};
     if (!p.status) return KDA_ERR_CUDA;
     return launch_decode(p, in_dtype, out_dtype, state_dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KDA_OK
@@ -209,13 +256,22 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
 int kda_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
                     float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
                     void* stream) {
-    return decode_common(q, k, v, log_alpha, beta, state, KDA_F32, out, B, H, dk, dv, in_dtype, out_dtype, stream);
+    return decode_common(q, k, v, log_alpha, kGateChannel, beta, state, KDA_F32, out, B, H, dk, dv, in_dtype,
+                         out_dtype, stream);
+}
+
+int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                        float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
+                        void* stream) {
+    return decode_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, state, KDA_F32, out, B, H,
+                         dk, dv, in_dtype, out_dtype, stream);
 }
 
 int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const float* log_alpha,
                               const float* beta, void* state, void* out, int B, int H, int dk, int dv,
                               int in_dtype, int out_dtype, void* stream) {
-    return decode_common(q, k, v, log_alpha, beta, state, KDA_BF16, out, B, H, dk, dv, in_dtype, out_dtype, stream);
+    return decode_common(q, k, v, log_alpha, kGateChannel, beta, state, KDA_BF16, out, B, H, dk, dv, in_dtype,
+                         out_dtype, stream);
 }
 
 }  // extern "C"

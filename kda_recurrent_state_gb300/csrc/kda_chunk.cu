@@ -111,7 +111,8 @@ struct Cfg {
     static constexpr uint32_t OFF_RING = OFF_STG + (STG_OWN ? 64 * 128 * 4 : 0);
     static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[3][128], b[3][128]
     static constexpr uint32_t OFF_BETA = OFF_VEC + 6 * 128 * 4;         // [4][64]
-    static constexpr uint32_t OFF_BAR = OFF_BETA + 4 * 64 * 4;
+    static constexpr uint32_t OFF_GATE = OFF_BETA + 4 * 64 * 4;         // [4][64] scalar gates
+    static constexpr uint32_t OFF_BAR = OFF_GATE + 4 * 64 * 4;
     static constexpr uint32_t NBAR = 40;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 #ifdef KDA_TRACE
@@ -287,7 +288,10 @@ __device__ __forceinline__ void tri_column(uint32_t a16, uint32_t dg16, uint8_t*
     }
 }
 
-template <typename Tin, typename Tout>
+// SG: one log-decay per (token, head) (the scalar gate of Gated DeltaNet), or none at
+// all (DeltaNet, alpha = 1) when P.log_alpha is null.  The gates then come in with beta
+// through the beta loader, and the TMA ring carries q, k and v only.
+template <typename Tin, typename Tout, bool SG>
 __global__ void __launch_bounds__(NTHREADS, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
@@ -301,6 +305,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);         // [3][128] e^{ref}
     float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 1536);  // [3][128] e^{g_63 - ref}
     float* sbeta = reinterpret_cast<float*>(sm + L::OFF_BETA);        // [4][64]
+    float* sgate = reinterpret_cast<float*>(sm + L::OFF_GATE);        // [4][64] (SG)
 #ifdef KDA_TRACE
     unsigned int* trace_sm = reinterpret_cast<unsigned int*>(sm + L::OFF_MISC + 64);
 #endif
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i : c1) mbar_init(&bar[i], 1);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&bar[B_BFULL + i], 32);
-            mbar_init(&bar[B_BFREE + i], 128);
+            mbar_init(&bar[B_BFREE + i], SG ? 256 : 128);  // SG: prep reads the gates too
         }
         for (int i = 0; i < 3; ++i) mbar_init(&bar[B_VFREE + i], 128);
         mbar_init(&bar[B_STGR], 1);
@@ -385,7 +390,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_la);
+            prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
+            if constexpr (!SG) prefetch_tmap(&tm_la);
             prefetch_tmap(&tm_out);
             int issued = 0;
             bool ok = true;
@@ -398,7 +404,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tma_prefetch_3d(&tm_q, 0, h, z);
                 tma_prefetch_3d(&tm_k, 0, h, z);
                 tma_prefetch_3d(&tm_v, 0, h, z);
-                tma_prefetch_3d(&tm_la, 0, h, z);
+                if constexpr (!SG) tma_prefetch_3d(&tm_la, 0, h, z);
             };
             for (int g = L::NSLOT; g < kPf && g < nq; ++g) prefetch(g);
             for (int n = 0; n < nch && ok; ++n)
@@ -408,12 +414,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (g + kPf < nq) prefetch(g + kPf);
                     if (use > 0 && !(ok = mbar_wait(&bar[B_EMPTY + sl], (use - 1) & 1, ab, status))) break;
                     uint8_t* slot = sm + L::OFF_RING + sl * L::SLOT_BYTES;
-                    mbar_arrive_expect_tx(&bar[B_FULL + sl], L::SLOT_BYTES);
+                    mbar_arrive_expect_tx(&bar[B_FULL + sl], SG ? L::SLOT_LA : L::SLOT_BYTES);
                     const int z = (int)(t0 + (int64_t)C * n + QR * q);
                     tma_load_3d(slot + L::SLOT_Q, &tm_q, &bar[B_FULL + sl], 0, h, z);
                     tma_load_3d(slot + L::SLOT_K, &tm_k, &bar[B_FULL + sl], 0, h, z);
                     tma_load_3d(slot + L::SLOT_V, &tm_v, &bar[B_FULL + sl], 0, h, z);
-                    tma_load_3d(slot + L::SLOT_LA, &tm_la, &bar[B_FULL + sl], 0, h, z);
+                    if constexpr (!SG) tma_load_3d(slot + L::SLOT_LA, &tm_la, &bar[B_FULL + sl], 0, h, z);
                     ++issued;
                 }
             if (!ok) {  // let the copies already issued land before the CTA can exit
@@ -434,8 +440,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int k4 = m & 3;
             if (m >= 4 && !mbar_wait(&bar[B_BFREE + k4], ((m - 4) >> 2) & 1, ab, status)) break;
             const int64_t vld = len - (int64_t)C * m;
-            for (int i = lane; i < C; i += 32)
-                sbeta[k4 * 64 + i] = i < vld ? P.beta[(size_t)(t0 + (int64_t)C * m + i) * P.H + h] : 0.f;
+            for (int i = lane; i < C; i += 32) {
+                const size_t row = (size_t)(t0 + (int64_t)C * m + i) * P.H + h;
+                sbeta[k4 * 64 + i] = i < vld ? P.beta[row] : 0.f;
+                if constexpr (SG) sgate[k4 * 64 + i] = (i < vld && P.log_alpha) ? P.log_alpha[row] : 0.f;
+            }
             mbar_arrive(&bar[B_BFULL + k4]);
         }
     } else if (warp < 4) {
@@ -474,6 +483,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // slot each.  Relative to ref = g_31: rows r <= 31 use x_r = g_r - ref =
             // -(L_{r+1} + .. + L_31), accumulated downwards from row 31 (which also yields
             // ref = L_0 + .. + L_31); rows r >= 32 use x_r = L_32 + .. + L_r (L = log2 alpha).
+            const float* sg = sgate + (n & 3) * 64;  // SG: this chunk's gates
+            if constexpr (SG)
+                if (!mbar_wait(&bar[B_BFULL + (n & 3)], (n >> 2) & 1, ab, status)) return false;
             auto wait_slot = [&](int i) {
                 const int g = 4 * n + i;
                 return mbar_wait(&bar[B_FULL + g % L::NSLOT], (g / L::NSLOT) & 1, ab, status);
@@ -501,7 +513,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const int e = REV ? 1 - es : es;
                         const int rr = 2 * rp + e;
                         const bool on = FULL || rr < vq;
-                        const float la = on ? sla[rr * 128 + c] : 0.f;
+                        float la;
+                        if constexpr (SG)
+                            la = on ? sg[QR * q + rr] : 0.f;
+                        else
+                            la = on ? sla[rr * 128 + c] : 0.f;
                         kk[e] = on ? ld_in(sk, rr * 128 + c) : 0.f;
                         qq[e] = ld_in(sq, rr * 128 + c);
                         vv2[e] = ld_in(sv, rr * 128 + c);
@@ -553,6 +569,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 if (c == 0 && i == 1) KDA_TR(n, 29);
             }
+            if constexpr (SG) mbar_arrive(&bar[B_BFREE + (n & 3)]);  // done with this chunk's gates
             vec_a[v3 * 128 + c] = fast_exp2(ref);
             vec_b[v3 * 128 + c] = fast_exp2(x);  // e^{g_63 - ref}
             tmem_st_wait();
@@ -1012,7 +1029,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool SG>
 cudaError_t launch_t(const SeqProblem& p, cudaStream_t st) {
     CUtensorMap mq, mk, mv, ml, mo;
     const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -1020,11 +1037,12 @@ cudaError_t launch_t(const SeqProblem& p, cudaStream_t st) {
     if (Tt > (int64_t)0x7FFFFFFF - 2 * C) return cudaErrorInvalidValue;  // tensor-map coordinates are 32-bit
     if (!make_map(&mq, p.q, dt, sizeof(Tin), Tt, p.H) || !make_map(&mk, p.k, dt, sizeof(Tin), Tt, p.H) ||
         !make_map(&mv, p.v, dt, sizeof(Tin), Tt, p.H) ||
-        !make_map(&ml, p.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Tt, p.H) ||
+        (!SG && !make_map(&ml, p.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Tt, p.H)) ||
         !make_map(&mo, p.out, sizeof(Tout) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                   sizeof(Tout), Tt, p.H))
         return cudaErrorInvalidValue;
-    auto kern = chunk_kernel<Tin, Tout>;
+    if (SG) ml = mq;  // not read
+    auto kern = chunk_kernel<Tin, Tout, SG>;
     const int smem = (int)Cfg<Tin>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -1048,15 +1066,21 @@ size_t chunk_prefill_workspace(int N, int H) {
     return 0;
 }
 
-cudaError_t launch_chunk_prefill(const SeqProblem& p, int in_dtype, int out_dtype, void* workspace,
+cudaError_t launch_chunk_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, void* workspace,
                                  size_t ws_bytes, cudaStream_t st) {
     (void)workspace;
     (void)ws_bytes;
     if ((int64_t)p.N * p.H == 0) return cudaSuccess;
-    if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16>(p, st);
-    if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float>(p, st);
-    if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16>(p, st);
-    return launch_t<float, float>(p, st);
+    if (gate != kGateChannel) {
+        if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, true>(p, st);
+        if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, true>(p, st);
+        if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, true>(p, st);
+        return launch_t<float, float, true>(p, st);
+    }
+    if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, false>(p, st);
+    if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, false>(p, st);
+    if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, false>(p, st);
+    return launch_t<float, float, false>(p, st);
 }
 
 }  // namespace kda

@@ -35,6 +35,12 @@ __device__ __forceinline__ float ldin(const __nv_bfloat16* p, size_t i) { return
 __device__ __forceinline__ float ldin(const float* p, size_t i) { return p[i]; }
 __device__ __forceinline__ void stout(__nv_bfloat16* p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void stout(float* p, size_t i, float x) { p[i] = x; }
+// alpha of key channel c: per channel (KDA), one per head (Gated DeltaNet) or 1 (DeltaNet).
+__device__ __forceinline__ float gate_alpha(const DecodeProblem& p, int bh, int c) {
+    if (p.gate == kGateChannel) return expf(p.log_alpha[(size_t)bh * kD + c]);
+    if (p.gate == kGateHead) return expf(p.log_alpha[bh]);
+    return 1.f;
+}
 // Four bf16 (two packed words) widened exactly to fp32.
 __device__ __forceinline__ float4 widen_bf16x4(uint2 w) {
     return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
@@ -65,7 +71,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeProblem p) {
         s_q[tid] = ldin(q, tid);
         s_k[tid] = ldin(k, tid);
         s_v[tid] = ldin(v, tid);
-        s_a[tid] = expf(p.log_alpha[(size_t)bh * kD + tid]);
+        s_a[tid] = gate_alpha(p, bh, tid);
     }
     if (tid == 0) s_beta = p.beta[bh];
     __syncthreads();
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(256, 5) decode_bf16state_kernel(DecodeProblem 
     const Tin* v = static_cast<const Tin*>(p.v) + (size_t)bh * kD;
     float qk = 0.f;
     if (tid < kD) {
-        const float qq = ldin(q, tid), kk = ldin(k, tid), a = expf(p.log_alpha[(size_t)bh * kD + tid]);
+        const float qq = ldin(q, tid), kk = ldin(k, tid), a = gate_alpha(p, bh, tid);
         s_k[tid] = kk;
         s_v[tid] = ldin(v, tid);
         s_a[tid] = a;

@@ -12,6 +12,12 @@ namespace kda {
 
 constexpr int kD = 128;  // d_k = d_v supported by every kernel
 
+// Layout of the decay gates log_alpha:
+//   kGateChannel: one per key channel, [.., H, d_k] (KDA)
+//   kGateHead:    one per head, [.., H] (Gated DeltaNet's scalar gate)
+//   kGateNone:    no gates, alpha = 1 (DeltaNet); log_alpha is null
+enum GateMode { kGateChannel = 0, kGateHead = 1, kGateNone = 2 };
+
 // One prefill problem: N sequences x H heads.  Sequence s covers packed tokens
 // [start(s), start(s) + len(s)).  With cu_seqlens == nullptr the sequences are
 // uniform: start = s * T_uniform, len = T_uniform (the batched [B, T] layout).
@@ -46,6 +52,7 @@ struct DecodeProblem {
     int B;
     int H;
     int* status;  // device status word
+    int gate;     // GateMode
 };
 
 __host__ __device__ inline void seq_bounds(const SeqProblem& p, int s, int64_t& start, int64_t& len) {
@@ -60,8 +67,10 @@ __host__ __device__ inline void seq_bounds(const SeqProblem& p, int s, int64_t& 
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_decode(const DecodeProblem& p, int in_dtype, int out_dtype, int state_dtype, cudaStream_t st);
-cudaError_t launch_serial_prefill(const SeqProblem& p, int in_dtype, int out_dtype, cudaStream_t st);
-cudaError_t launch_chunk_prefill(const SeqProblem& p, int in_dtype, int out_dtype, void* workspace,
+// `gate` (a GateMode) travels beside the problem: the chunk kernel takes it as a template
+// argument, so it is not part of the kernel's parameter block.
+cudaError_t launch_serial_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, cudaStream_t st);
+cudaError_t launch_chunk_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, void* workspace,
                                  size_t ws_bytes, cudaStream_t st);
 size_t chunk_prefill_workspace(int N, int H);
 

@@ -9,7 +9,8 @@
 // Per token: decay, column prediction p = S'^T k (a cross-warp reduction),
 // u = beta (v - p), rank-one write, read o = S^T q (a second reduction).
 // Snapshots (hubwiz.com "Kimi K3 混合线性注意力", §5) are taken after every
-// `interval` tokens of a sequence.
+// `interval` tokens of a sequence.  The decay is per key channel (KDA), one
+// scalar per head (Gated DeltaNet) or absent (DeltaNet, alpha = 1).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -24,7 +25,7 @@ __device__ __forceinline__ void stout(__nv_bfloat16* p, size_t i, float x) { p[i
 __device__ __forceinline__ void stout(float* p, size_t i, float x) { p[i] = x; }
 
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(256) serial_kernel(SeqProblem p) {
+__global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, int gate) {
     const int nblk = kD / NJ;
     const int jb = blockIdx.x % nblk;
     const int h = (blockIdx.x / nblk) % p.H;
@@ -56,7 +57,9 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p) {
                 const size_t off = ((size_t)(t0 + tb + r) * p.H + h) * kD + c;
                 sk[r][c] = ldin(k, off);
                 sq[r][c] = ldin(q, off);
-                sa[r][c] = expf(p.log_alpha[off]);
+                sa[r][c] = gate == kGateChannel ? expf(p.log_alpha[off])
+                           : gate == kGateHead  ? expf(p.log_alpha[(size_t)(t0 + tb + r) * p.H + h])
+                                                : 1.f;
             }
         }
         for (int idx = threadIdx.x; idx < TB * NJ; idx += blockDim.x) {
@@ -112,18 +115,18 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p) {
 
 }  // namespace
 
-cudaError_t launch_serial_prefill(const SeqProblem& p, int in_dtype, int out_dtype, cudaStream_t st) {
+cudaError_t launch_serial_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, cudaStream_t st) {
     const int64_t units = (int64_t)p.N * p.H * (kD / NJ);
     if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)units;
     if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16)
-        serial_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(p);
+        serial_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(p, gate);
     else if (in_dtype == KDA_BF16)
-        serial_kernel<__nv_bfloat16, float><<<grid, 256, 0, st>>>(p);
+        serial_kernel<__nv_bfloat16, float><<<grid, 256, 0, st>>>(p, gate);
     else if (out_dtype == KDA_BF16)
-        serial_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(p);
+        serial_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(p, gate);
     else
-        serial_kernel<float, float><<<grid, 256, 0, st>>>(p);
+        serial_kernel<float, float><<<grid, 256, 0, st>>>(p, gate);
     return cudaGetLastError();
 }
 

@@ -10,7 +10,8 @@ Distributions (per tensor, i.i.d. unless stated):
               operator does not normalise.
   v         ~ N(0, 1)
   beta      = sigmoid(N(0, 1))                           (fp32)
-  log_alpha = -Uniform(0.001, 0.1) per key channel     (fp32, "config" gates)
+  log_alpha = -Uniform(0.001, 0.1) per key channel     (fp32, "config" gates;
+              head_gates draws one per (token, head) the same way)
               -Uniform(1e-5, 1e-3)                       ("slow" gates: the
               initial state and the chunk carry stay visible for thousands
               of tokens, so they are actually tested)
@@ -39,6 +40,12 @@ def _gates(shape, g, device, gate: str) -> torch.Tensor:
     lo, hi = {"config": (0.001, 0.1), "slow": (1e-5, 1e-3)}[gate]
     u = torch.rand(shape, generator=g, device=device, dtype=torch.float32)
     return -(lo + (hi - lo) * u)
+
+
+def head_gates(lead: tuple, H: int, *, seed: int, device="cpu", gate: str = "config") -> torch.Tensor:
+    """One log-decay per (token, head), ``lead + (H,)`` fp32, from the same distribution as the
+    per-channel gates (the scalar gate of Gated DeltaNet)."""
+    return _gates((*lead, H), _gen(device, seed), device, gate)
 
 
 def token_tensors(lead: tuple, H: int, dk: int, dv: int, g, device, in_dtype, gate: str):

@@ -108,6 +108,30 @@ def test_argument_validation(L):
                                        None) == b.KDA_OK  # B = 0: nothing to do
 
 
+def test_gate_validation(L):
+    """Per-channel gates are required and 16-byte aligned; scalar gates (Gated DeltaNet) need
+    4 bytes; a null gate selects DeltaNet in the scalar entry points only."""
+    from kda_recurrent_state_gb300 import binding as b
+
+    P = ctypes.c_void_p
+
+    def chunk(fn, la, dk=128):
+        return fn(P(16), P(16), P(16), la, P(16), None, P(16), None, 1, 8, 1, dk, 128, 64, 0, 1, None, 0, None)
+
+    assert chunk(L.kda_chunk_fwd, None) == b.KDA_ERR_INVALID_ARG
+    assert chunk(L.kda_chunk_fwd, P(0x1004)) == b.KDA_ERR_MISALIGNED
+    assert chunk(L.kda_gdn_chunk_fwd, P(0x1002)) == b.KDA_ERR_MISALIGNED
+    assert chunk(L.kda_gdn_chunk_fwd, None, dk=64) == b.KDA_ERR_UNSUPPORTED
+    assert L.kda_gdn_varlen_fwd(P(16), P(16), P(16), P(0x1002), P(16), P(16), 2, 100, 1, 128, 128, 64, None,
+                                P(16), 0, None, None, P(16), 0, 1, None, 0, None) == b.KDA_ERR_MISALIGNED
+    assert L.kda_gdn_varlen_fwd(P(16), P(16), P(16), None, P(16), P(16), 2, 100, 1, 128, 128, 64, None,
+                                None, 0, None, None, P(16), 0, 1, None, 0, None) == b.KDA_ERR_INVALID_ARG
+    assert L.kda_gdn_decode_step(P(16), P(16), P(16), P(0x1002), P(16), P(16), P(16), 2, 2, 128, 128, 0, 1,
+                                 None) == b.KDA_ERR_MISALIGNED
+    assert L.kda_decode_step(P(16), P(16), P(16), None, P(16), P(16), P(16), 2, 2, 128, 128, 0, 1,
+                             None) == b.KDA_ERR_INVALID_ARG
+
+
 def test_workspace_size(L):
     from kda_recurrent_state_gb300 import binding as b
 
