@@ -72,11 +72,16 @@ typedef enum {
     KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
     KDA_ERR_TIMEOUT = 5,     /* device status: a bounded wait inside a kernel expired */
     KDA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than kda_workspace_size() */
-    KDA_STATUS_GATE_RANGE = 7 /* device status: a half-chunk's summed log-decay was below -15 ln 2 */
+    KDA_STATUS_GATE_RANGE = 7, /* device status: a half-chunk's summed log-decay was below -15 ln 2 */
+    KDA_STATUS_SLOT_RANGE = 8  /* device status: a state-pool slot index outside [-1, pool_slots) was skipped */
 } kda_status;
 
 /* Operation selector of kda_workspace_size(). */
 typedef enum { KDA_OP_CHUNK = 0, KDA_OP_VARLEN = 1, KDA_OP_DECODE = 2 } kda_op;
+
+/* Layout of log_alpha for kda_varlen_fwd_pool: one value per key channel (KDA), one per head
+   (Gated DeltaNet), or none (DeltaNet, log_alpha NULL).  See kda_gdn_chunk_fwd. */
+typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_HEAD = 1, KDA_GATE_NONE = 2 } kda_gate;
 
 /*
  * Batched prefill: B independent sequences of T tokens, H heads each.
@@ -119,7 +124,8 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
  *               state bit for bit.
  *   snap_offsets device int64 [N+1] from kda_snapshot_offsets() (copied to the
  *               device by the caller); NULL when snapshot_interval = 0.
- *   snapshots   float32 [snap_offsets[N], H, dk, dv]; NULL when no snapshot.
+ *   snapshots   float32 [snap_offsets[N], H, dk, dv]; NULL when no snapshot (a NULL
+ *               array with snapshot positions present stores nothing).
  * Chunks are aligned to each sequence's first token; each sequence's result
  * is bit-identical to running that sequence alone through this function.
  */
@@ -184,6 +190,36 @@ int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float
                         float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
                         void* stream);
 
+/*
+ * Packed variable-length prefill over a caller-owned STATE POOL, for prefix reuse in
+ * serving ("Kimi K3 混合线性注意力", hubwiz.com, §5: restartable state snapshots at a
+ * fixed token interval; a prompt that shares a prefix resumes from the nearest snapshot
+ * instead of recomputing it, with the snapshot block size decoupled from the
+ * granularity of prefix matching).  Arguments as for kda_varlen_fwd, except:
+ *   gate        kda_gate: the layout of log_alpha ([T_total, H, dk], [T_total, H] or NULL).
+ *   pool        float32 [pool_slots, H, dk, dv], 16-byte aligned; slot i holds the states
+ *               of all H heads at one position of one sequence.
+ *   init_slots  device int64 [N] or NULL: sequence s starts from slot init_slots[s]
+ *               (-1: zero state).  NULL: every sequence starts from zeros.
+ *   snap_slots  device int64 [snap_offsets[N]], required when snapshot_interval > 0:
+ *               snapshot m of sequence s (as in kda_varlen_fwd) is stored into slot
+ *               snap_slots[snap_offsets[s] + m - 1]; -1 means "not stored" (for example
+ *               because that prefix is already in the pool).
+ * final_states stays a dense [N, H, dk, dv] array.  Snapshot slots written by one call
+ * must be distinct, and no slot written by a call may be an initial-state slot of the
+ * same call.  A slot index outside [-1, pool_slots) is not dereferenced: the state is
+ * taken as zero, or the snapshot is dropped, and KDA_STATUS_SLOT_RANGE is raised in the
+ * device status word.  Results are bit-identical to kda_varlen_fwd (or
+ * kda_gdn_varlen_fwd) with the same states gathered into packed arrays; with
+ * kda_snapshot_lookup, a resumed sequence reproduces the unsplit run bit for bit.
+ */
+int kda_varlen_fwd_pool(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
+                        const float* beta, const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
+                        int chunk, float* pool, int64_t pool_slots, const int64_t* init_slots,
+                        int64_t snapshot_interval, const int64_t* snap_offsets, const int64_t* snap_slots,
+                        float* final_states, void* out, int in_dtype, int out_dtype, void* workspace,
+                        size_t ws_bytes, void* stream);
+
 /* Number of snapshots of a sequence: floor(seqlen / interval); 0 if interval <= 0 or seqlen < 0. */
 int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);
 
@@ -221,7 +257,7 @@ const char* kda_status_string(int status);
 
 /*
  * Waits for `stream`, then reads and clears the device status word of the
- * current device: KDA_OK, KDA_ERR_TIMEOUT or KDA_STATUS_GATE_RANGE (the first
+ * current device: KDA_OK, KDA_ERR_TIMEOUT, KDA_STATUS_GATE_RANGE or KDA_STATUS_SLOT_RANGE (the first
  * fault recorded since the last read).  Returns KDA_ERR_CUDA if the read fails.
  */
 int kda_get_device_status(void* stream);

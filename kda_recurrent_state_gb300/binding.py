@@ -20,7 +20,9 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 KDA_BF16, KDA_F32 = 0, 1
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_MISALIGNED = 0, 1, 2, 3
 KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_WORKSPACE, KDA_STATUS_GATE_RANGE = 4, 5, 6, 7
+KDA_STATUS_SLOT_RANGE = 8
 KDA_OP_CHUNK, KDA_OP_VARLEN, KDA_OP_DECODE = 0, 1, 2
+KDA_GATE_CHANNEL, KDA_GATE_HEAD, KDA_GATE_NONE = 0, 1, 2
 
 _lib = None
 
@@ -46,6 +48,8 @@ def lib() -> ctypes.CDLL:
         L.kda_gdn_chunk_fwd.argtypes = L.kda_chunk_fwd.argtypes
         L.kda_gdn_varlen_fwd.argtypes = L.kda_varlen_fwd.argtypes
         L.kda_gdn_decode_step.argtypes = L.kda_decode_step.argtypes
+        L.kda_varlen_fwd_pool.argtypes = [P, P, P, P, I, P, P, I, I64, I, I, I, I, P, I64, P, I64, P, P, P, P, I, I,
+                                          P, SZ, P]
         L.kda_snapshot_count.argtypes = [I64, I64]
         L.kda_snapshot_count.restype = I64
         L.kda_snapshot_offsets.argtypes = [P, I, I64, P]
@@ -57,7 +61,8 @@ def lib() -> ctypes.CDLL:
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_get_device_status.argtypes = [P]
         for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
-                  L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_snapshot_offsets,
+                  L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_varlen_fwd_pool,
+                  L.kda_snapshot_offsets,
                   L.kda_get_device_status):
             f.restype = I
         _lib = L
@@ -204,6 +209,39 @@ def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, ch
     cu_seqlens int64 [N+1] on the device.  Returns (out, final_states, snapshots or None)."""
     return _varlen("kda_varlen_fwd", q, k, v, log_alpha, beta, cu_seqlens, init_states, chunk, snapshot_interval,
                    cu_seqlens_host, out, final_states, snapshots, out_dtype, workspace)
+
+
+def kda_varlen_fwd_pool(q, k, v, log_alpha, beta, cu_seqlens, pool, init_slots=None, snap_slots=None, *,
+                        gate: int = KDA_GATE_CHANNEL, chunk: int = 64, snapshot_interval: int = 0,
+                        cu_seqlens_host=None, out=None, final_states=None, out_dtype=torch.float32, workspace=None):
+    """Packed sequences over a state pool [pool_slots,H,dk,dv] fp32: sequence s starts from slot
+    init_slots[s] (-1: zeros; None: all zeros) and snapshot m of sequence s goes to slot
+    snap_slots[offsets[s] + m - 1] (-1: not stored).  log_alpha's layout is given by `gate`.
+    Returns (out, final_states); the snapshots are in the pool."""
+    Ttot, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty(Ttot, H, dv, dtype=out_dtype, device=q.device)
+    if final_states is None:
+        final_states = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    if pool.dtype != torch.float32 or tuple(pool.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"pool must be float32 [slots, {H}, {dk}, {dv}]")
+    snap_off = None
+    if snapshot_interval:
+        cu_h = cu_seqlens.cpu() if cu_seqlens_host is None else torch.as_tensor(cu_seqlens_host)
+        snap_off = kda_snapshot_offsets(cu_h, snapshot_interval).to(q.device)
+    for name, t in (("init_slots", init_slots), ("snap_slots", snap_slots)):
+        if t is not None and t.dtype != torch.int64:
+            raise TypeError(f"{name} must be int64")
+    ws, ws_bytes = _workspace(KDA_OP_VARLEN, N, Ttot, H, dk, dv, chunk, q.device, workspace)
+    rc = lib().kda_varlen_fwd_pool(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), int(gate), _ptr(beta),
+                                   _ptr(cu_seqlens), N, Ttot, H, dk, dv, int(chunk), _ptr(pool), pool.shape[0],
+                                   _ptr(init_slots), int(snapshot_interval), _ptr(snap_off), _ptr(snap_slots),
+                                   _ptr(final_states), _ptr(out), _dt(q), _dt(out), _ptr(ws), ws_bytes,
+                                   _stream(q.device))
+    _check(rc, "kda_varlen_fwd_pool")
+    return out, final_states
 
 
 def kda_gdn_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, chunk: int = 64,

@@ -40,10 +40,10 @@ int check_common(int dk, int dv, int chunk, int in_dtype, int out_dtype) {
     return KDA_OK;
 }
 
-int run_prefill(const SeqProblem& p, int gate, int chunk, int in_dtype, int out_dtype, void* ws, size_t ws_bytes,
-                cudaStream_t st) {
-    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, gate, in_dtype, out_dtype, st)
-                                 : launch_chunk_prefill(p, gate, in_dtype, out_dtype, ws, ws_bytes, st);
+int run_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int chunk, int in_dtype, int out_dtype,
+                void* ws, size_t ws_bytes, cudaStream_t st) {
+    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, pool, gate, in_dtype, out_dtype, st)
+                                 : launch_chunk_prefill(p, pool, gate, in_dtype, out_dtype, ws, ws_bytes, st);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -64,6 +64,7 @@ const char* kda_status_string(int status) {
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel expired";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
         case KDA_STATUS_GATE_RANGE: return "KDA_STATUS_GATE_RANGE: a half-chunk's summed log-decay is below -15 ln 2";
+        case KDA_STATUS_SLOT_RANGE: return "KDA_STATUS_SLOT_RANGE: a state-pool slot index was out of range and skipped";
         default: return "unknown kda status";
     }
 }
@@ -158,7 +159,7 @@ static int chunk_common(const void* q, const void* k, const void* v, const float
     p.snap_interval = 0; p.snap_offsets = nullptr; p.snapshots = nullptr;
     p.status = status_ptr();
     if (!p.status) return KDA_ERR_CUDA;
-    return run_prefill(p, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes, st);
+    return run_prefill(p, PoolSlots{nullptr, nullptr, 0}, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes, st);
 }
 
 int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
@@ -177,11 +178,14 @@ int kda_gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* 
                         B, T, H, dk, dv, chunk, in_dtype, out_dtype, workspace, ws_bytes, stream);
 }
 
+// `pool.init_slots` / `pool.snap_slots` select the pool layout: init_states and snapshots
+// are then the same pool of pool.n_slots slots.
 static int varlen_common(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
                          const float* beta, const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk,
                          int dv, int chunk, const float* init_states, float* final_states,
                          int64_t snapshot_interval, const int64_t* snap_offsets, float* snapshots, void* out,
-                         int in_dtype, int out_dtype, void* workspace, size_t ws_bytes, void* stream) {
+                         int in_dtype, int out_dtype, void* workspace, size_t ws_bytes, void* stream,
+                         const PoolSlots& pool) {
     if (N < 0 || T_total < 0 || H < 0 || snapshot_interval < 0) return KDA_ERR_INVALID_ARG;
     int rc = check_common(dk, dv, chunk, in_dtype, out_dtype);
     if (rc != KDA_OK) return rc;
@@ -197,7 +201,8 @@ static int varlen_common(const void* q, const void* k, const void* v, const floa
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
     if ((beta && !aligned(beta, 4)) || !gate_aligned(log_alpha, gate) || !aligned(cu_seqlens, 8) ||
-        (snap_offsets && !aligned(snap_offsets, 8)))
+        (snap_offsets && !aligned(snap_offsets, 8)) || (pool.init_slots && !aligned(pool.init_slots, 8)) ||
+        (pool.snap_slots && !aligned(pool.snap_slots, 8)))
         return KDA_ERR_MISALIGNED;
     const size_t need = kda_workspace_size(KDA_OP_VARLEN, N, T_total, H, dk, dv, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
@@ -211,7 +216,8 @@ static int varlen_common(const void* q, const void* k, const void* v, const floa
     p.snap_interval = snapshot_interval; p.snap_offsets = snap_offsets; p.snapshots = snapshots;
     p.status = status_ptr();
     if (!p.status) return KDA_ERR_CUDA;
-    return run_prefill(p, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+    return run_prefill(p, pool, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
@@ -221,7 +227,7 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log
                    void* workspace, size_t ws_bytes, void* stream) {
     return varlen_common(q, k, v, log_alpha, kGateChannel, beta, cu_seqlens, N, T_total, H, dk, dv, chunk,
                          init_states, final_states, snapshot_interval, snap_offsets, snapshots, out, in_dtype,
-                         out_dtype, workspace, ws_bytes, stream);
+                         out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0});
 }
 
 int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
@@ -231,7 +237,25 @@ int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float*
                        void* workspace, size_t ws_bytes, void* stream) {
     return varlen_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, cu_seqlens, N, T_total, H,
                          dk, dv, chunk, init_states, final_states, snapshot_interval, snap_offsets, snapshots, out,
-                         in_dtype, out_dtype, workspace, ws_bytes, stream);
+                         in_dtype, out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0});
+}
+
+int kda_varlen_fwd_pool(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
+                        const float* beta, const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
+                        int chunk, float* pool, int64_t pool_slots, const int64_t* init_slots,
+                        int64_t snapshot_interval, const int64_t* snap_offsets, const int64_t* snap_slots,
+                        float* final_states, void* out, int in_dtype, int out_dtype, void* workspace,
+                        size_t ws_bytes, void* stream) {
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE) return KDA_ERR_INVALID_ARG;
+    if (pool_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (snapshot_interval > 0 && !snap_slots) return KDA_ERR_INVALID_ARG;
+    if ((init_slots || snapshot_interval > 0) && !pool) return KDA_ERR_INVALID_ARG;
+    if (gate == KDA_GATE_HEAD && !log_alpha && T_total > 0) return KDA_ERR_INVALID_ARG;
+    const int g = gate == KDA_GATE_CHANNEL ? kGateChannel : gate == KDA_GATE_HEAD ? kGateHead : kGateNone;
+    return varlen_common(q, k, v, log_alpha, g, beta, cu_seqlens, N, T_total, H, dk, dv, chunk,
+                         init_slots ? pool : nullptr, final_states, snapshot_interval, snap_offsets,
+                         snapshot_interval > 0 ? pool : nullptr, out, in_dtype, out_dtype, workspace, ws_bytes, stream,
+                         PoolSlots{init_slots, snapshot_interval > 0 ? snap_slots : nullptr, pool_slots});
 }
 
 static int decode_common(const void* q, const void* k, const void* v, const float* log_alpha, int gate,

@@ -295,7 +295,7 @@ template <typename Tin, typename Tout, bool SG>
 __global__ void __launch_bounds__(NTHREADS, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
-                 const __grid_constant__ CUtensorMap tm_out, const SeqProblem P) {
+                 const __grid_constant__ CUtensorMap tm_out, const SeqProblem P, const PoolSlots pool) {
     using L = Cfg<Tin>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -340,10 +340,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     seq_bounds(P, s, t0, len);
     const int nch = (int)((len + C - 1) / C);
     const size_t sbase = ((size_t)s * P.H + h) * kD * kD;
+    // this unit's initial state (null: zeros), looked up where it is read
+    auto init_state = [&]() -> const float* {
+        if (!pool.init_slots) return P.init ? P.init + sbase : nullptr;
+        const int64_t slot = checked_slot(pool.init_slots[s], pool.n_slots, P.status);
+        return slot >= 0 ? P.init + ((size_t)slot * P.H + h) * kD * kD : nullptr;
+    };
 
     if (nch == 0) {  // empty sequence: the final state is the initial state
-        if (P.final_state)
-            for (int i = tid; i < kD * kD; i += NTHREADS) P.final_state[sbase + i] = P.init ? P.init[sbase + i] : 0.f;
+        if (P.final_state) {
+            const float* S0 = init_state();
+            for (int i = tid; i < kD * kD; i += NTHREADS) P.final_state[sbase + i] = S0 ? S0[i] : 0.f;
+        }
         return;
     }
 
@@ -625,6 +633,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return true;
         };
         {  // X_0 = Diag(a_0) S_0 into D_S and X16
+            const float* S0 = init_state();
             if (!(ok = mbar_wait(&bar[B_PREPD], 0, ab, status))) goto state_done;
 #pragma unroll 1
             for (int piece = 0; piece < 4; ++piece) {
@@ -632,7 +641,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int cc = piece * 32 + e;
-                    const float s0 = P.init ? P.init[sbase + (size_t)cc * kD + j] : 0.f;
+                    const float s0 = S0 ? S0[(size_t)cc * kD + j] : 0.f;
                     xs[e] = __float_as_uint(s0 * vec_a[cc]);
                 }
 #pragma unroll
@@ -702,9 +711,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             {
                 const int64_t end_pos = (int64_t)C * n + valid;  // tokens of the sequence consumed so far
                 float* snap = nullptr;
-                if (P.snap_interval > 0 && valid == C && end_pos % P.snap_interval == 0)
-                    snap = P.snapshots + ((size_t)(P.snap_offsets[s] + end_pos / P.snap_interval - 1) * P.H + h) *
-                                             kD * kD;
+                if (P.snap_interval > 0 && valid == C && end_pos % P.snap_interval == 0) {
+                    int64_t slot = P.snap_offsets[s] + end_pos / P.snap_interval - 1;
+                    if (pool.snap_slots) slot = checked_slot(pool.snap_slots[slot], pool.n_slots, P.status);
+                    if (slot >= 0 && P.snapshots) snap = P.snapshots + ((size_t)slot * P.H + h) * kD * kD;
+                }
                 float* fin = (last && P.final_state) ? P.final_state + sbase : nullptr;
                 const float* bv = vec_b + (n % 3) * 128;
                 if (snap || fin) {  // true state S = Diag(b_n) D, at snapshot positions and the end
@@ -1030,7 +1041,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, 
 }
 
 template <typename Tin, typename Tout, bool SG>
-cudaError_t launch_t(const SeqProblem& p, cudaStream_t st) {
+cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, cudaStream_t st) {
     CUtensorMap mq, mk, mv, ml, mo;
     const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int64_t Tt = p.T_total > 0 ? p.T_total : 1;
@@ -1047,7 +1058,7 @@ cudaError_t launch_t(const SeqProblem& p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((int64_t)p.N * p.H);
-    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p);
+    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pool);
     return cudaGetLastError();
 }
 
@@ -1066,21 +1077,21 @@ size_t chunk_prefill_workspace(int N, int H) {
     return 0;
 }
 
-cudaError_t launch_chunk_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, void* workspace,
-                                 size_t ws_bytes, cudaStream_t st) {
+cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
+                                 void* workspace, size_t ws_bytes, cudaStream_t st) {
     (void)workspace;
     (void)ws_bytes;
     if ((int64_t)p.N * p.H == 0) return cudaSuccess;
     if (gate != kGateChannel) {
-        if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, true>(p, st);
-        if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, true>(p, st);
-        if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, true>(p, st);
-        return launch_t<float, float, true>(p, st);
+        if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, true>(p, pool, st);
+        if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, true>(p, pool, st);
+        if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, true>(p, pool, st);
+        return launch_t<float, float, true>(p, pool, st);
     }
-    if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, false>(p, st);
-    if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, false>(p, st);
-    if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, false>(p, st);
-    return launch_t<float, float, false>(p, st);
+    if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, false>(p, pool, st);
+    if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, false>(p, pool, st);
+    if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, false>(p, pool, st);
+    return launch_t<float, float, false>(p, pool, st);
 }
 
 }  // namespace kda

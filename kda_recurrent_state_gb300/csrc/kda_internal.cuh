@@ -37,9 +37,30 @@ struct SeqProblem {
     int H;
     int64_t snap_interval;        // 0 = none
     const int64_t* snap_offsets;  // device [N+1]
-    float* snapshots;             // [snap_offsets[N], H, D, D]
+    float* snapshots;             // [snap_offsets[N], H, D, D], or the pool when snap_slots is set
     int* status;                  // device status word
 };
+
+// State pool (both null for the packed layout): sequence s starts from pool slot
+// init_slots[s] of SeqProblem::init (-1: zeros), and its snapshot k = snap_offsets[s] + m - 1
+// goes to slot snap_slots[k] of SeqProblem::snapshots (-1: not stored).  A slot is [H, D, D].
+// Kept out of SeqProblem so that the chunk kernel's parameter block keeps its size.
+// A slot index outside [-1, n_slots) is skipped and raises KDA_STATUS_SLOT_RANGE.
+struct PoolSlots {
+    const int64_t* init_slots;
+    const int64_t* snap_slots;
+    int64_t n_slots;
+};
+
+// Pool slot `i` checked against the pool: -1 (none) passes through, anything else outside
+// [0, n) becomes -1 and records KDA_STATUS_SLOT_RANGE.
+__device__ inline int64_t checked_slot(int64_t i, int64_t n, int* status) {
+    if (i < -1 || i >= n) {
+        atomicCAS(status, 0, (int)KDA_STATUS_SLOT_RANGE);
+        return -1;
+    }
+    return i;
+}
 
 struct DecodeProblem {
     const void* q;
@@ -69,9 +90,10 @@ __host__ __device__ inline void seq_bounds(const SeqProblem& p, int s, int64_t& 
 cudaError_t launch_decode(const DecodeProblem& p, int in_dtype, int out_dtype, int state_dtype, cudaStream_t st);
 // `gate` (a GateMode) travels beside the problem: the chunk kernel takes it as a template
 // argument, so it is not part of the kernel's parameter block.
-cudaError_t launch_serial_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, cudaStream_t st);
-cudaError_t launch_chunk_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, void* workspace,
-                                 size_t ws_bytes, cudaStream_t st);
+cudaError_t launch_serial_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
+                                  cudaStream_t st);
+cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
+                                 void* workspace, size_t ws_bytes, cudaStream_t st);
 size_t chunk_prefill_workspace(int N, int H);
 
 }  // namespace kda

@@ -25,7 +25,7 @@ __device__ __forceinline__ void stout(__nv_bfloat16* p, size_t i, float x) { p[i
 __device__ __forceinline__ void stout(float* p, size_t i, float x) { p[i] = x; }
 
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, int gate) {
+__global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, PoolSlots pool, int gate) {
     const int nblk = kD / NJ;
     const int jb = blockIdx.x % nblk;
     const int h = (blockIdx.x / nblk) % p.H;
@@ -39,9 +39,14 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, int gate) {
     __shared__ float red[2][8][NJ];
 
     const size_t sbase = ((size_t)s * p.H + h) * kD * kD;
+    const float* S0 = p.init ? p.init + sbase : nullptr;
+    if (pool.init_slots) {
+        const int64_t slot = checked_slot(pool.init_slots[s], pool.n_slots, p.status);
+        S0 = slot >= 0 ? p.init + ((size_t)slot * p.H + h) * kD * kD : nullptr;
+    }
     float S[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) S[i] = p.init ? p.init[sbase + (size_t)(w * 16 + i) * kD + j] : 0.f;
+    for (int i = 0; i < 16; ++i) S[i] = S0 ? S0[(size_t)(w * 16 + i) * kD + j] : 0.f;
 
     const Tin* q = static_cast<const Tin*>(p.q);
     const Tin* k = static_cast<const Tin*>(p.k);
@@ -100,10 +105,13 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, int gate) {
                 stout(out, ((size_t)(t0 + t) * p.H + h) * kD + j, ot);
             }
             if (p.snap_interval > 0 && (t + 1) % p.snap_interval == 0) {
-                const int64_t m = (t + 1) / p.snap_interval - 1;
-                float* dst = p.snapshots + ((size_t)(p.snap_offsets[s] + m) * p.H + h) * kD * kD;
+                int64_t slot = p.snap_offsets[s] + (t + 1) / p.snap_interval - 1;
+                if (pool.snap_slots) slot = checked_slot(pool.snap_slots[slot], pool.n_slots, p.status);
+                if (slot >= 0 && p.snapshots) {
+                    float* dst = p.snapshots + ((size_t)slot * p.H + h) * kD * kD;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) dst[(size_t)(w * 16 + i) * kD + j] = S[i];
+                    for (int i = 0; i < 16; ++i) dst[(size_t)(w * 16 + i) * kD + j] = S[i];
+                }
             }
         }
     }
@@ -115,18 +123,19 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, int gate) {
 
 }  // namespace
 
-cudaError_t launch_serial_prefill(const SeqProblem& p, int gate, int in_dtype, int out_dtype, cudaStream_t st) {
+cudaError_t launch_serial_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
+                                  cudaStream_t st) {
     const int64_t units = (int64_t)p.N * p.H * (kD / NJ);
     if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)units;
     if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16)
-        serial_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(p, gate);
+        serial_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(p, pool, gate);
     else if (in_dtype == KDA_BF16)
-        serial_kernel<__nv_bfloat16, float><<<grid, 256, 0, st>>>(p, gate);
+        serial_kernel<__nv_bfloat16, float><<<grid, 256, 0, st>>>(p, pool, gate);
     else if (out_dtype == KDA_BF16)
-        serial_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(p, gate);
+        serial_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(p, pool, gate);
     else
-        serial_kernel<float, float><<<grid, 256, 0, st>>>(p, gate);
+        serial_kernel<float, float><<<grid, 256, 0, st>>>(p, pool, gate);
     return cudaGetLastError();
 }
 

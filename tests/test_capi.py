@@ -62,7 +62,7 @@ def test_snapshot_lookup(L):
 def test_status_strings(L):
     from kda_recurrent_state_gb300 import binding as b
 
-    for code in range(8):
+    for code in range(9):
         assert b.kda_status_string(code).startswith("KDA_")
     assert "unknown" in b.kda_status_string(99)
 
@@ -130,6 +130,29 @@ def test_gate_validation(L):
                                  None) == b.KDA_ERR_MISALIGNED
     assert L.kda_decode_step(P(16), P(16), P(16), None, P(16), P(16), P(16), 2, 2, 128, 128, 0, 1,
                              None) == b.KDA_ERR_INVALID_ARG
+
+
+def test_pool_validation(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+
+    def pool(gate=0, la=16, pool_ptr=16, slots=4, init=None, interval=0, snap_off=None, snap_slots=None):
+        return L.kda_varlen_fwd_pool(P(16), P(16), P(16), P(la) if la else None, gate, P(16), P(16), 2, 100, 1, 128,
+                                     128, 64, P(pool_ptr) if pool_ptr else None, slots, P(init) if init else None,
+                                     interval, P(snap_off) if snap_off else None,
+                                     P(snap_slots) if snap_slots else None, P(16), P(16), 0, 1, None, 0, None)
+
+    assert pool(gate=5) == b.KDA_ERR_INVALID_ARG
+    assert pool(slots=-1) == b.KDA_ERR_INVALID_ARG
+    assert pool(interval=64, snap_off=16) == b.KDA_ERR_INVALID_ARG        # snap_slots required
+    assert pool(pool_ptr=0, init=16) == b.KDA_ERR_INVALID_ARG             # a pool to read from
+    assert pool(gate=b.KDA_GATE_HEAD, la=0) == b.KDA_ERR_INVALID_ARG      # scalar gates required
+    assert pool(gate=b.KDA_GATE_NONE, la=16) == b.KDA_ERR_INVALID_ARG     # DeltaNet takes no gates
+    assert pool(init=0x1004) == b.KDA_ERR_MISALIGNED
+    assert pool(pool_ptr=0x1008, init=16) == b.KDA_ERR_MISALIGNED
+    assert pool(interval=96, snap_off=16, snap_slots=16) == b.KDA_ERR_INVALID_ARG  # not a chunk multiple
+    del I64
 
 
 def test_workspace_size(L):
