@@ -36,6 +36,13 @@
  * token's update and read, as a decode step that stores its state in bf16
  * does.  kda_oracle_round_bf16 exposes that rounding.
  *
+ * Backward (reverse mode of the same per-token recurrence; the pages give none, so it
+ * is derived here step by step from the forward definition above):
+ * kda_oracle_recurrent_bwd takes the loss L = sum_t <do_t, o_t> + <dS_T, S_T> and
+ * returns dL/dq, dL/dk, dL/dv, dL/dlog_alpha, dL/dbeta and dL/dS0.  It stores every
+ * state of the forward sweep and walks the tokens backwards, undoing one operation
+ * of the step at a time (read, rank-one write, error, prediction, decay).
+ *
  * Layouts (all contiguous, head-major; "n" = independent heads):
  *   q, k, log_alpha : [n][T][dk]  double  (bf16 / fp32 inputs upcast exactly)
  *   v               : [n][T][dv]  double
@@ -69,6 +76,10 @@ typedef struct {
     double* snaps;
     int colblk; /* value columns per work unit */
     int state_bf16; /* round the state to bf16 after every token */
+    /* backward: cotangents in, gradients out ([n][T][..] like the inputs) */
+    const double *dout, *dSf;
+    double *g_q, *g_k, *g_v, *g_la, *g_beta, *g_S0;
+    int bwd;
     int64_t n_units;
     int64_t next; /* shared unit counter, guarded by mu */
     pthread_mutex_t mu;
@@ -303,10 +314,128 @@ done:
     free(S); free(g); free(A); free(Tinv); free(QK); free(W); free(Up); free(U); free(Ke); free(P); free(Sn);
 }
 
+/* ------------------------------------------------------------------------
+ * Reverse mode of the per-token recurrence for head h.  Forward step t, from
+ * S = S_{t-1}:
+ *     a = exp(log_alpha_t)       S' = Diag(a) S        p = S'^T k
+ *     e = v - p                  u = beta e            S_t = S' + k u^T
+ *     o_t = S_t^T q
+ * Backward step t, with dS = dL/dS_t (from the later tokens) and do = dL/do_t:
+ *     o_t = S_t^T q        ->  dS += q do^T,            dq = S_t do
+ *     S_t = S' + k u^T     ->  dS' = dS,  dk = dS u,     du = dS^T k
+ *     u = beta e           ->  dbeta = du . e,           de = beta du
+ *     e = v - p            ->  dv = de,                  dp = -de
+ *     p = S'^T k           ->  dS' += k dp^T,            dk += S' dp
+ *     S' = Diag(a) S       ->  dS_{t-1} = Diag(a) dS',   dlog_alpha_i = a_i sum_j dS'_ij S_ij
+ * ---------------------------------------------------------------------- */
+static void backward_head(job_t* J, int64_t h) {
+    const int dk = J->dk, dv = J->dv;
+    const int64_t T = J->T;
+    const size_t sz_S = (size_t)dk * dv;
+    double* St = (double*)malloc(sizeof(double) * sz_S * (size_t)(T > 0 ? T : 1)); /* S_{t-1}, t = 0..T-1 */
+    double* S = (double*)malloc(sizeof(double) * sz_S);
+    double* Sp = (double*)malloc(sizeof(double) * sz_S);
+    double* dS = (double*)malloc(sizeof(double) * sz_S);
+    double* dSp = (double*)malloc(sizeof(double) * sz_S);
+    double* vec = (double*)malloc(sizeof(double) * (size_t)(3 * dk + 4 * dv));
+    if (!St || !S || !Sp || !dS || !dSp || !vec) { J->err = 1; goto done; }
+    double *a = vec, *p = a + dk, *e = p + dv, *u = e + dv, *du = u + dv, *gk = du + dv, *da = gk + dk;
+    (void)da;
+
+    for (size_t x = 0; x < sz_S; ++x) S[x] = J->S0 ? J->S0[(size_t)h * sz_S + x] : 0.0;
+    for (int64_t t = 0; t < T; ++t) { /* forward sweep, keeping S_{t-1} */
+        const size_t r = (size_t)h * T + t;
+        const double* kt = J->k + r * dk;
+        memcpy(St + (size_t)t * sz_S, S, sizeof(double) * sz_S);
+        for (int i = 0; i < dk; ++i) a[i] = exp(J->la[r * dk + i]);
+        for (int j = 0; j < dv; ++j) p[j] = 0.0;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) {
+                S[(size_t)i * dv + j] *= a[i];
+                p[j] += kt[i] * S[(size_t)i * dv + j];
+            }
+        for (int j = 0; j < dv; ++j) u[j] = J->beta[r] * (J->v[r * dv + j] - p[j]);
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += kt[i] * u[j];
+    }
+
+    for (size_t x = 0; x < sz_S; ++x) dS[x] = J->dSf ? J->dSf[(size_t)h * sz_S + x] : 0.0;
+    for (int64_t t = T - 1; t >= 0; --t) {
+        const size_t r = (size_t)h * T + t;
+        const double *qt = J->q + r * dk, *kt = J->k + r * dk, *vt = J->v + r * dv, *dot = J->dout + r * dv;
+        const double bt = J->beta[r];
+        const double* Sprev = St + (size_t)t * sz_S;
+        /* recompute the step */
+        for (int i = 0; i < dk; ++i) a[i] = exp(J->la[r * dk + i]);
+        for (int j = 0; j < dv; ++j) p[j] = 0.0;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) {
+                Sp[(size_t)i * dv + j] = a[i] * Sprev[(size_t)i * dv + j];
+                p[j] += kt[i] * Sp[(size_t)i * dv + j];
+            }
+        for (int j = 0; j < dv; ++j) {
+            e[j] = vt[j] - p[j];
+            u[j] = bt * e[j];
+        }
+        /* o_t = S_t^T q: dS += q do^T, dq = S_t do (S_t = S' + k u^T) */
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                dS[(size_t)i * dv + j] += qt[i] * dot[j];
+                acc += (Sp[(size_t)i * dv + j] + kt[i] * u[j]) * dot[j];
+            }
+            J->g_q[r * dk + i] = acc;
+        }
+        /* S_t = S' + k u^T: dS' = dS, dk = dS u, du = dS^T k */
+        for (int j = 0; j < dv; ++j) du[j] = 0.0;
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                const double d = dS[(size_t)i * dv + j];
+                dSp[(size_t)i * dv + j] = d;
+                acc += d * u[j];
+                du[j] += d * kt[i];
+            }
+            gk[i] = acc;
+        }
+        /* u = beta e, e = v - p */
+        double gb = 0.0;
+        for (int j = 0; j < dv; ++j) {
+            gb += du[j] * e[j];
+            J->g_v[r * dv + j] = bt * du[j];
+            p[j] = -bt * du[j]; /* p now holds dp */
+        }
+        J->g_beta[r] = gb;
+        /* p = S'^T k: dS' += k dp^T, dk += S' dp */
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                dSp[(size_t)i * dv + j] += kt[i] * p[j];
+                acc += Sp[(size_t)i * dv + j] * p[j];
+            }
+            J->g_k[r * dk + i] = MUT(6) ? gk[i] : gk[i] + acc;
+        }
+        /* S' = Diag(a) S_{t-1} */
+        for (int i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                acc += dSp[(size_t)i * dv + j] * Sprev[(size_t)i * dv + j];
+                dS[(size_t)i * dv + j] = MUT(7) ? dSp[(size_t)i * dv + j] : a[i] * dSp[(size_t)i * dv + j];
+            }
+            J->g_la[r * dk + i] = a[i] * acc;
+        }
+    }
+    if (J->g_S0) memcpy(J->g_S0 + (size_t)h * sz_S, dS, sizeof(double) * sz_S);
+done:
+    free(St); free(S); free(Sp); free(dS); free(dSp); free(vec);
+}
+
 static void* worker(void* arg) {
     job_t* J = (job_t*)arg;
     for (int64_t u; (u = grab_unit(J)) >= 0;) {
-        if (J->C > 0) {
+        if (J->bwd) {
+            backward_head(J, u);
+        } else if (J->C > 0) {
             chunked_head(J, u);
         } else {
             const int nblk = (J->dv + J->colblk - 1) / J->colblk;
@@ -380,5 +509,24 @@ int kda_oracle_chunked(int64_t n, int64_t T, int dk, int dv, int C, const double
     J.q = q; J.k = k; J.v = v; J.la = log_alpha; J.beta = beta; J.S0 = S0;
     J.out = out; J.S_final = S_final; J.interval = snap_interval; J.snaps = snaps;
     J.n_units = n;
+    return run(&J, n_threads);
+}
+
+/* Gradients of L = sum_t <dout_t, o_t> + <dS_final, S_T> (dS_final may be NULL) with
+ * respect to q, k, v, log_alpha, beta and S0, each in the layout of its input.  Holds
+ * T * dk * dv doubles per head in flight.  Returns 0 on success. */
+int kda_oracle_recurrent_bwd(int64_t n, int64_t T, int dk, int dv, const double* q, const double* k,
+                             const double* v, const double* log_alpha, const double* beta, const double* S0,
+                             const double* dout, const double* dS_final, double* dq, double* dk_out, double* dv_out,
+                             double* dlog_alpha, double* dbeta, double* dS0, int n_threads) {
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.n = n; J.T = T; J.dk = dk; J.dv = dv; J.C = 0;
+    J.q = q; J.k = k; J.v = v; J.la = log_alpha; J.beta = beta; J.S0 = S0;
+    J.dout = dout; J.dSf = dS_final;
+    J.g_q = dq; J.g_k = dk_out; J.g_v = dv_out; J.g_la = dlog_alpha; J.g_beta = dbeta; J.g_S0 = dS0;
+    J.bwd = 1;
+    J.n_units = n;
+    if (!dout || !dq || !dk_out || !dv_out || !dlog_alpha || !dbeta) return 1;
     return run(&J, n_threads);
 }

@@ -12,7 +12,9 @@ the read of §二.1, in fp64:
     o_t = S_t^T q_t,          alpha_t = exp(log_alpha_t) per key channel.
 
 ``recurrent`` runs it token by token; ``chunked`` runs the naive chunked
-rewrite of §六 (recurrent between chunks of C tokens, WY form inside).
+rewrite of §六 (recurrent between chunks of C tokens, WY form inside);
+``recurrent_bwd`` is the reverse mode of ``recurrent`` (the pages give no
+backward; it is derived step by step from the forward definition).
 """
 from __future__ import annotations
 
@@ -52,6 +54,8 @@ def _bind(path: str):
     lib.kda_oracle_recurrent_bf16state.restype = ctypes.c_int
     lib.kda_oracle_round_bf16.argtypes = [d, d, i64]
     lib.kda_oracle_round_bf16.restype = None
+    lib.kda_oracle_recurrent_bwd.argtypes = [i64, i64, i32, i32, f, f, f, f, f, d, d, d, d, d, d, d, d, d, i32]
+    lib.kda_oracle_recurrent_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -137,3 +141,27 @@ def chunked(q, k, v, log_alpha, beta, S0=None, chunk: int = 64, snap_interval: i
             threads: int | None = None, lib=None):
     """Naive chunked rewrite (WY form) in fp64.  Same returns as ``recurrent``."""
     return _run("chunked", q, k, v, log_alpha, beta, S0, chunk, snap_interval, threads, lib)
+
+
+def recurrent_bwd(q, k, v, log_alpha, beta, S0, dout, dS_final=None, threads: int | None = None, lib=None,
+                  mem_budget: int = 2 << 30) -> dict:
+    """Gradients of L = sum_t <dout_t, o_t> + <dS_final, S_T> through the per-token recurrence,
+    in fp64: dict with dq, dk, dv, dlog_alpha, dbeta (the inputs' layouts) and dS0 [n,dk,dv].
+    Each head keeps its T states in memory; threads are capped to stay near ``mem_budget`` bytes."""
+    lib = lib or load()
+    q, k, v, la, be, do = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(beta), _f64(dout)
+    n, T, dk = q.shape
+    dv = v.shape[2]
+    assert do.shape == (n, T, dv)
+    s0 = None if S0 is None else _f64(S0)
+    dsf = None if dS_final is None else _f64(dS_final)
+    g = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v), "dlog_alpha": np.zeros_like(la),
+         "dbeta": np.zeros_like(be), "dS0": np.zeros((n, dk, dv), dtype=np.float64)}
+    per_head = max(1, T) * dk * dv * 8
+    threads = max(1, min(threads or os.cpu_count() or 1, mem_budget // per_head or 1))
+    rc = lib.kda_oracle_recurrent_bwd(n, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(be), _ptr(s0), _ptr(do),
+                                      _ptr(dsf), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlog_alpha"]),
+                                      _ptr(g["dbeta"]), _ptr(g["dS0"]), int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle recurrent_bwd failed (rc={rc})")
+    return g

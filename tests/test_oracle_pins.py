@@ -342,3 +342,81 @@ def test_bf16state_error_bounded():
     o2, S2 = oracle.recurrent_bf16state(q, k, v, la, b)
     assert 0 < rel(S2, S1) < 2.0 ** -6
     assert 0 < rel(o2, o1) < 2.0 ** -6
+
+
+# --------------------------------------------------------------------------- backward
+def _loss_fd(lib, args, do, dSf, h=1e-6):
+    """Central finite differences of L = <do, o> + <dSf, S_T> through the forward oracle."""
+    def L(a):
+        o, Sf = oracle.recurrent(a["q"], a["k"], a["v"], a["la"], a["b"], a["S0"], lib=lib)
+        return float((o * do).sum() + (Sf * dSf).sum())
+    fd = {}
+    for name, x in args.items():
+        g = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            a = dict(args)
+            xp = x.copy(); xp[idx] += h; a[name] = xp; Lp = L(a)
+            xm = x.copy(); xm[idx] -= h; a[name] = xm; Lm = L(a)
+            g[idx] = (Lp - Lm) / (2 * h)
+        fd[name] = g
+    return fd
+
+
+BWD_NAMES = {"q": "dq", "k": "dk", "v": "dv", "la": "dlog_alpha", "b": "dbeta", "S0": "dS0"}
+
+
+def pin_bwd_finite_differences(lib):
+    """Every gradient of the reverse sweep equals central finite differences of the forward
+    oracle (an independent computation: no derivative is written down)."""
+    rng = np.random.default_rng(31)
+    for T, dSf_on in ((7, True), (4, False)):
+        q, k, v, la, b = _inputs(rng, 2, T, 5, 4, gate="slow")
+        la = la * 300  # decays of order e^-0.15 per token, so the gate gradient is not tiny
+        S0 = rng.standard_normal((2, 5, 4))
+        do = rng.standard_normal((2, T, 4))
+        dSf = rng.standard_normal((2, 5, 4)) if dSf_on else np.zeros((2, 5, 4))
+        g = oracle.recurrent_bwd(q, k, v, la, b, S0, do, dSf if dSf_on else None, lib=lib)
+        fd = _loss_fd(lib, {"q": q, "k": k, "v": v, "la": la, "b": b, "S0": S0}, do, dSf)
+        for name, want in fd.items():
+            got = g[BWD_NAMES[name]]
+            err = np.abs(got - want).max()
+            assert err <= 1e-6 * max(1.0, np.abs(want).max()), (name, T, err)
+
+
+def pin_bwd_closed_form_no_write(lib):
+    """alpha = 1, beta = 0: the state never changes (S_t = S0), so o_t = S0^T q_t and
+    dq_t = S0 do_t, dS0 = dS_T + sum_t q_t do_t^T, dk = dv = 0,
+    dlog_alpha_t = rowsum(G_t * S0) with G_t = dS_T + sum_{t' >= t} q_t' do_t'^T, and
+    dbeta_t = (G_t^T k_t) . (v_t - S0^T k_t)."""
+    rng = np.random.default_rng(32)
+    T, dk, dv = 6, 5, 4
+    q, k, v, _, _ = _inputs(rng, 1, T, dk, dv)
+    la, b = np.zeros((1, T, dk)), np.zeros((1, T))
+    S0, do, dSf = rng.standard_normal((1, dk, dv)), rng.standard_normal((1, T, dv)), rng.standard_normal((1, dk, dv))
+    g = oracle.recurrent_bwd(q, k, v, la, b, S0, do, dSf, lib=lib)
+    np.testing.assert_allclose(g["dq"][0], do[0] @ S0[0].T, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(g["dS0"][0], dSf[0] + q[0].T @ do[0], rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(g["dk"], 0.0)
+    np.testing.assert_array_equal(g["dv"], 0.0)
+    for t in range(T):
+        G = dSf[0] + q[0, t:].T @ do[0, t:]
+        np.testing.assert_allclose(g["dlog_alpha"][0, t], (G * S0[0]).sum(axis=1), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(g["dbeta"][0, t], (G.T @ k[0, t]) @ (v[0, t] - S0[0].T @ k[0, t]), rtol=0,
+                                   atol=1e-12)
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_closed_form_no_write]
+
+
+@pytest.mark.parametrize("pin", BWD_PINS, ids=[p.__name__ for p in BWD_PINS])
+def test_bwd_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+@pytest.mark.parametrize("mutant", [6, 7])
+def test_bwd_planted_mistakes_are_caught(mutant, tmp_path):
+    """Dropping the prediction's key-gradient term (6) or the decay on the carried state
+    gradient (7) fails the finite-difference pin."""
+    lib = oracle.load(oracle.build(str(tmp_path / f"mutant{mutant}.so"), mutant=mutant))
+    with pytest.raises(AssertionError):
+        pin_bwd_finite_differences(lib)
