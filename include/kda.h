@@ -77,7 +77,7 @@ typedef enum {
 } kda_status;
 
 /* Operation selector of kda_workspace_size(). */
-typedef enum { KDA_OP_CHUNK = 0, KDA_OP_VARLEN = 1, KDA_OP_DECODE = 2 } kda_op;
+typedef enum { KDA_OP_CHUNK = 0, KDA_OP_VARLEN = 1, KDA_OP_DECODE = 2, KDA_OP_BWD = 3 } kda_op;
 
 /* Layout of log_alpha for kda_varlen_fwd_pool: one value per key channel (KDA), one per head
    (Gated DeltaNet), or none (DeltaNet, log_alpha NULL).  See kda_gdn_chunk_fwd. */
@@ -219,6 +219,32 @@ int kda_varlen_fwd_pool(const void* q, const void* k, const void* v, const float
                         int64_t snapshot_interval, const int64_t* snap_offsets, const int64_t* snap_slots,
                         float* final_states, void* out, int in_dtype, int out_dtype, void* workspace,
                         size_t ws_bytes, void* stream);
+
+/*
+ * Gradients for training ("Kimi Linear 最多砍掉 75% KV Cache", ai.concitech.org: the
+ * chunkwise kernel serves training; the pages give no backward).  For the loss
+ *     L = sum_t <d_out_t, o_t> + sum_s <d_final_states_s, S_final_s>
+ * through the recurrence of kda_chunk_fwd (gate layout `gate`, as in kda_varlen_fwd_pool),
+ * returns dL/dq, dL/dk, dL/dv, dL/dlog_alpha, dL/dbeta and dL/dinit_states, each in the
+ * layout of its input, in float32.  Derived as the reverse mode of the per-token step.
+ *   cu_seqlens  NULL: N sequences of T tokens each, batched [N, T, H, ..] layout;
+ *               else device int64 [N+1] of packed sequences and T = T_total.
+ *   init_states [N, H, dk, dv] float32 or NULL (zeros); d_final_states likewise (no
+ *               loss on the final state); d_init_states may be NULL (not returned).
+ *   d_out       [.., H, dv] float32.  q, k, v in in_dtype; everything else float32.
+ *   dlog_alpha  [.., H, dk] (KDA_GATE_CHANNEL), [.., H] (KDA_GATE_HEAD), NULL (KDA_GATE_NONE).
+ *   workspace   device, kda_workspace_size(KDA_OP_BWD, N, T_total, H, dk, dv, 64) bytes,
+ *               16-byte aligned: a state checkpoint every 64 tokens of every head, and
+ *               a small per-(sequence, head) recomputation area.
+ * Evaluated token by token in fp32 (the state and its gradient of each (sequence,
+ * head) stay in one CTA's registers), with states recomputed from the checkpoints;
+ * deterministic.  Alignment: 16 bytes for the state arrays and the workspace, element
+ * size for the rest.
+ */
+int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
+            const float* init_states, const float* d_out, const float* d_final_states, const int64_t* cu_seqlens,
+            int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
+            float* dbeta, float* d_init_states, int in_dtype, void* workspace, size_t ws_bytes, void* stream);
 
 /* Number of snapshots of a sequence: floor(seqlen / interval); 0 if interval <= 0 or seqlen < 0. */
 int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);

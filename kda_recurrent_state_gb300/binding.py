@@ -21,7 +21,7 @@ KDA_BF16, KDA_F32 = 0, 1
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_MISALIGNED = 0, 1, 2, 3
 KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_WORKSPACE, KDA_STATUS_GATE_RANGE = 4, 5, 6, 7
 KDA_STATUS_SLOT_RANGE = 8
-KDA_OP_CHUNK, KDA_OP_VARLEN, KDA_OP_DECODE = 0, 1, 2
+KDA_OP_CHUNK, KDA_OP_VARLEN, KDA_OP_DECODE, KDA_OP_BWD = 0, 1, 2, 3
 KDA_GATE_CHANNEL, KDA_GATE_HEAD, KDA_GATE_NONE = 0, 1, 2
 
 _lib = None
@@ -48,6 +48,7 @@ def lib() -> ctypes.CDLL:
         L.kda_gdn_chunk_fwd.argtypes = L.kda_chunk_fwd.argtypes
         L.kda_gdn_varlen_fwd.argtypes = L.kda_varlen_fwd.argtypes
         L.kda_gdn_decode_step.argtypes = L.kda_decode_step.argtypes
+        L.kda_bwd.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P, SZ, P]
         L.kda_varlen_fwd_pool.argtypes = [P, P, P, P, I, P, P, I, I64, I, I, I, I, P, I64, P, I64, P, P, P, P, I, I,
                                           P, SZ, P]
         L.kda_snapshot_count.argtypes = [I64, I64]
@@ -61,7 +62,7 @@ def lib() -> ctypes.CDLL:
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_get_device_status.argtypes = [P]
         for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
-                  L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_varlen_fwd_pool,
+                  L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_varlen_fwd_pool, L.kda_bwd,
                   L.kda_snapshot_offsets,
                   L.kda_get_device_status):
             f.restype = I
@@ -283,3 +284,32 @@ def kda_gdn_decode_step(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=
     """kda_decode_step with log_alpha [B,H] (Gated DeltaNet) or None (DeltaNet); fp32 state."""
     return _decode(lib().kda_gdn_decode_step, "kda_gdn_decode_step", torch.float32, q, k, v, log_alpha, beta, state,
                    out, out_dtype)
+
+
+def kda_bwd(q, k, v, log_alpha, beta, d_out, init_state=None, d_final_state=None, *, gate: int = KDA_GATE_CHANNEL,
+            cu_seqlens=None, return_d_init: bool = True, workspace=None) -> dict:
+    """Gradients of L = sum <d_out, o> + <d_final_state, S_final> through the forward of
+    kda_chunk_fwd (batched q [B,T,H,dk] when cu_seqlens is None, else packed [Ttot,H,dk]).
+    log_alpha's layout follows `gate`.  Returns dict(dq, dk, dv, dlog_alpha, dbeta, d_init)."""
+    if cu_seqlens is None:
+        N, T, H, dk = q.shape
+        t_arg, t_total = T, N * T
+    else:
+        t_total, H, dk = q.shape
+        N = cu_seqlens.numel() - 1
+        t_arg = t_total
+    dv = v.shape[-1]
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = {"dq": torch.empty(q.shape, **f32), "dk": torch.empty(k.shape, **f32), "dv": torch.empty(v.shape, **f32),
+         "dlog_alpha": None if gate == KDA_GATE_NONE else torch.empty(log_alpha.shape, **f32),
+         "dbeta": torch.empty(beta.shape, **f32),
+         "d_init": torch.empty(N, H, dk, dv, **f32) if return_d_init else None}
+    if workspace is None:
+        need = kda_workspace_size(KDA_OP_BWD, N, t_total, H, dk, dv)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = lib().kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), int(gate), _ptr(beta), _ptr(init_state),
+                       _ptr(d_out), _ptr(d_final_state), _ptr(cu_seqlens), N, t_arg, H, dk, dv, _ptr(g["dq"]),
+                       _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlog_alpha"]), _ptr(g["dbeta"]), _ptr(g["d_init"]),
+                       _dt(q), _ptr(workspace), workspace.numel(), _stream(q.device))
+    _check(rc, "kda_bwd")
+    return g

@@ -97,7 +97,8 @@ int64_t kda_snapshot_lookup(const int64_t* offsets_host, int N, int seq, int64_t
 }
 
 size_t kda_workspace_size(int op, int B, int64_t T, int H, int dk, int dv, int chunk) {
-    (void)T; (void)dk; (void)dv;
+    (void)dk; (void)dv;
+    if (op == KDA_OP_BWD) return (B <= 0 || H <= 0 || T < 0) ? 0 : bwd_workspace(B, T, H);
     if (op == KDA_OP_DECODE || B <= 0 || H <= 0 || chunk != 64) return 0;
     return chunk_prefill_workspace(B, H);
 }
@@ -296,6 +297,42 @@ int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const
                               int in_dtype, int out_dtype, void* stream) {
     return decode_common(q, k, v, log_alpha, kGateChannel, beta, state, KDA_BF16, out, B, H, dk, dv, in_dtype,
                          out_dtype, stream);
+}
+
+int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
+            const float* init_states, const float* d_out, const float* d_final_states, const int64_t* cu_seqlens,
+            int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
+            float* dbeta, float* d_init_states, int in_dtype, void* workspace, size_t ws_bytes, void* stream) {
+    if (N < 0 || T < 0 || H < 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(in_dtype)) return KDA_ERR_INVALID_ARG;
+    if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE) return KDA_ERR_INVALID_ARG;
+    if (dk != kD || dv != kD) return KDA_ERR_UNSUPPORTED;
+    if (N == 0 || H == 0) return KDA_OK;
+    const int64_t T_total = cu_seqlens ? T : (int64_t)N * T;
+    const bool gated = gate != KDA_GATE_NONE;
+    if (T_total > 0 && (!q || !k || !v || !beta || !d_out || !dq || !dk_out || !dv_out || !dbeta))
+        return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && gated != (log_alpha != nullptr)) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && gated != (dlog_alpha != nullptr)) return KDA_ERR_INVALID_ARG;
+    const uintptr_t in_al = in_dtype == KDA_BF16 ? 2 : 4;
+    const void* al4[] = {log_alpha, beta, d_out, dq, dk_out, dv_out, dlog_alpha, dbeta};
+    for (const void* p : al4)
+        if (p && !aligned(p, 4)) return KDA_ERR_MISALIGNED;
+    if (!aligned(q, in_al) || !aligned(k, in_al) || !aligned(v, in_al) || (cu_seqlens && !aligned(cu_seqlens, 8)))
+        return KDA_ERR_MISALIGNED;
+    const void* al16[] = {init_states, d_final_states, d_init_states, workspace};
+    for (const void* p : al16)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    const size_t need = kda_workspace_size(KDA_OP_BWD, N, T_total, H, dk, dv, 64);
+    if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
+    BwdProblem p{};
+    p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta; p.init = init_states;
+    p.dout = d_out; p.dfinal = d_final_states;
+    p.dq = dq; p.dk = dk_out; p.dv = dv_out; p.dlog_alpha = dlog_alpha; p.dbeta = dbeta; p.dinit = d_init_states;
+    p.cu_seqlens = cu_seqlens; p.T_uniform = cu_seqlens ? 0 : T; p.T_total = T_total; p.N = N; p.H = H;
+    p.gate = gate == KDA_GATE_CHANNEL ? kGateChannel : gate == KDA_GATE_HEAD ? kGateHead : kGateNone;
+    return launch_bwd(p, in_dtype, workspace, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
+                                                                                              : KDA_ERR_CUDA;
 }
 
 }  // extern "C"

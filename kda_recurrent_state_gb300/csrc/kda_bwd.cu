@@ -1,0 +1,269 @@
+// kda_bwd.cu -- gradients of the KDA recurrence (training), token by token on CUDA cores.
+//
+// The forward step is the "Kimi K3" article's (lshu.cn/news/263999) §四 update with the
+// §二.1 read; the pages give no backward, so it is the reverse mode of that step, one
+// operation at a time.  From S = S_{t-1}:
+//     a = exp(log_alpha_t)    S' = Diag(a) S    p = S'^T k    e = v - p    u = beta e
+//     S_t = S' + k u^T        o_t = S_t^T q
+// and backwards, with dS = dL/dS_t carried from the later tokens:
+//     dS += q do^T                     dq = S_t do
+//     du = dS^T k                      dbeta = du . e        dv = beta du     dp = -beta du
+//     dk = dS u + S' dp                dS' = dS + k dp^T
+//     dlog_alpha_i = a_i sum_j dS'_ij S_ij                   dS_{t-1} = Diag(a) dS'
+// for L = sum_t <do_t, o_t> + <dS_T, S_T>.
+//
+// One CTA of 512 threads walks one (sequence, head).  Thread (c, i) holds row i (key
+// channel) of value columns 32c .. 32c+31 of both S and dS in registers.  Sums over key
+// channels (p, du) are warp reduce-scatters plus a 4-warp pass through shared memory;
+// sums over value columns (dq, dk, dlog_alpha) add the four column blocks in a fixed
+// order, so the result is bit-reproducible.
+//
+// States for the reverse sweep: a forward sweep stores S every 64 tokens (checkpoints,
+// workspace).  Then, segment by segment from the end, the segment is recomputed from its
+// checkpoint keeping S every 8 tokens (per-CTA scratch, small enough to stay in L2), and
+// each 8-token piece is recomputed once more keeping every S_{t-1}, e_t and u_t before
+// its tokens are undone in reverse order.  3 forward steps and 1 backward step per token.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int SEG = 64;         // tokens per checkpoint
+constexpr int SUB = 8;          // tokens per recomputed piece
+constexpr int NT = 512;         // threads: 4 column blocks x 128 rows
+constexpr int BLK = kD * kD;    // floats per state image, laid out [column][row]
+
+__device__ __forceinline__ float ldin(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float ldin(const float* p, size_t i) { return p[i]; }
+
+// Reduce-scatter over a warp: lane l returns the sum over all 32 lanes of x[l].
+__device__ __forceinline__ float warp_reduce_scatter(float (&x)[32], int lane) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const bool up = (lane & d) != 0;  // this lane keeps the upper half of the live values
+#pragma unroll
+        for (int m = 0; m < d; ++m) {
+            const float send = up ? x[m] : x[m + d];
+            const float keep = up ? x[m + d] : x[m];
+            x[m] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+    }
+    return x[0];
+}
+
+struct Shared {
+    float q[SUB][kD], k[SUB][kD], a[SUB][kD], v[SUB][kD], dout[SUB][kD];
+    float e[SUB][kD], u[SUB][kD];
+    float beta[SUB];
+    float red[4][4][32];  // [column block][warp][lane]: per-warp column partials
+    float dp[kD];
+    float rs[4][3][kD];   // [column block][dq, dk, dlog_alpha][row]: per-block row partials
+    float bpart[4];
+    float hpart[4];
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
+    __shared__ Shared sm;
+    const int tid = threadIdx.x;
+    const int c = tid >> 7, i = tid & 127, w = (tid >> 5) & 3, lane = tid & 31;
+    const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
+    int64_t t0, len;
+    if (P.cu_seqlens) {
+        t0 = P.cu_seqlens[s];
+        len = P.cu_seqlens[s + 1] - t0;
+    } else {
+        t0 = (int64_t)s * P.T_uniform;
+        len = P.T_uniform;
+    }
+    const size_t sbase = ((size_t)s * P.H + h) * BLK;  // row-major [D][D] states of this unit
+    const Tin* gq = static_cast<const Tin*>(P.q);
+    const Tin* gk = static_cast<const Tin*>(P.k);
+    const Tin* gv = static_cast<const Tin*>(P.v);
+    // workspace: checkpoints of this head, and this CTA's two 8-slot scratch areas
+    const int64_t slot0 = t0 / SEG + s;  // first checkpoint slot of the sequence (slots never overlap)
+    float* ckpt = P.ckpt + (size_t)h * P.ckpt_slots * BLK;
+    float* sub = P.scratch + (size_t)blockIdx.x * 2 * SUB * BLK;
+    float* st = sub + SUB * BLK;
+    auto img = [&](float* base, int jj) -> float* { return base + (size_t)(c * 32 + jj) * kD + i; };
+
+    float S[32], dS[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) S[jj] = P.init ? P.init[sbase + (size_t)i * kD + c * 32 + jj] : 0.f;
+
+    // inputs of tokens [p0, p0 + n) of the sequence into shared memory
+    auto stage = [&](int64_t p0, int n, bool with_dout) {
+        __syncthreads();
+        for (int idx = tid; idx < SUB * kD; idx += NT) {
+            const int tl = idx >> 7, ch = idx & 127;
+            if (tl < n) {
+                const size_t r = (size_t)(t0 + p0 + tl) * P.H + h;
+                const size_t off = r * kD + ch;
+                sm.q[tl][ch] = ldin(gq, off);
+                sm.k[tl][ch] = ldin(gk, off);
+                sm.v[tl][ch] = ldin(gv, off);
+                sm.a[tl][ch] = P.gate == kGateChannel ? expf(P.log_alpha[off])
+                             : P.gate == kGateHead  ? expf(P.log_alpha[r])
+                                                    : 1.f;
+                if (with_dout) sm.dout[tl][ch] = P.dout[off];
+            }
+        }
+        if (tid < n) sm.beta[tid] = P.beta[(size_t)(t0 + p0 + tid) * P.H + h];
+        __syncthreads();
+    };
+    // one forward step on S (token tl of the staged piece); keeps S_{t-1} in `keep` if set
+    auto fwd_step = [&](int tl, float* keep) {
+        const float ai = sm.a[tl][i], ki = sm.k[tl][i];
+        float x[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            if (keep) *img(keep, jj) = S[jj];
+            S[jj] *= ai;
+            x[jj] = ki * S[jj];
+        }
+        sm.red[c][w][lane] = warp_reduce_scatter(x, lane);
+        __syncthreads();
+        if (w == 0) {
+            const int j = 32 * c + lane;
+            const float p = ((sm.red[c][0][lane] + sm.red[c][1][lane]) + sm.red[c][2][lane]) + sm.red[c][3][lane];
+            const float e = sm.v[tl][j] - p;
+            sm.e[tl][j] = e;
+            sm.u[tl][j] = sm.beta[tl] * e;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) S[jj] += ki * sm.u[tl][32 * c + jj];
+    };
+    // one backward step for token tl of the staged piece (global token t0 + pos)
+    auto bwd_step = [&](int tl, int64_t pos) {
+        const size_t r = (size_t)(t0 + pos) * P.H + h;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) S[jj] = *img(st + (size_t)tl * BLK, jj);  // S_{t-1}
+        const float ai = sm.a[tl][i], ki = sm.k[tl][i], qi = sm.q[tl][i];
+        float dq = 0.f, x[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int j = 32 * c + jj;
+            const float doj = sm.dout[tl][j];
+            dS[jj] += qi * doj;
+            dq += (ai * S[jj] + ki * sm.u[tl][j]) * doj;
+            x[jj] = dS[jj] * ki;
+        }
+        sm.red[c][w][lane] = warp_reduce_scatter(x, lane);
+        __syncthreads();
+        if (w == 0) {
+            const int j = 32 * c + lane;
+            const float du = ((sm.red[c][0][lane] + sm.red[c][1][lane]) + sm.red[c][2][lane]) + sm.red[c][3][lane];
+            const float b = sm.beta[tl];
+            P.dv[r * kD + j] = b * du;
+            sm.dp[j] = -b * du;
+            float bp = du * sm.e[tl][j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) bp += __shfl_xor_sync(0xffffffffu, bp, o);
+            if (lane == 0) sm.bpart[c] = bp;
+        }
+        __syncthreads();
+        float dk = 0.f, da = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int j = 32 * c + jj;
+            const float dpj = sm.dp[j];
+            dk += dS[jj] * sm.u[tl][j] + (ai * S[jj]) * dpj;
+            const float dsp = dS[jj] + ki * dpj;
+            da += dsp * S[jj];
+            dS[jj] = ai * dsp;
+        }
+        sm.rs[c][0][i] = dq;
+        sm.rs[c][1][i] = dk;
+        sm.rs[c][2][i] = ai * da;
+        __syncthreads();
+        if (c == 0) {
+            const size_t o = r * kD + i;
+            P.dq[o] = ((sm.rs[0][0][i] + sm.rs[1][0][i]) + sm.rs[2][0][i]) + sm.rs[3][0][i];
+            P.dk[o] = ((sm.rs[0][1][i] + sm.rs[1][1][i]) + sm.rs[2][1][i]) + sm.rs[3][1][i];
+            const float dla = ((sm.rs[0][2][i] + sm.rs[1][2][i]) + sm.rs[2][2][i]) + sm.rs[3][2][i];
+            if (P.gate == kGateChannel) {
+                P.dlog_alpha[o] = dla;
+            } else if (P.gate == kGateHead) {
+                float hs = dla;
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, o2);
+                if (lane == 0) sm.hpart[w] = hs;
+            }
+        }
+        if (tid == 0) P.dbeta[r] = ((sm.bpart[0] + sm.bpart[1]) + sm.bpart[2]) + sm.bpart[3];
+        if (P.gate == kGateHead) {
+            __syncthreads();
+            if (tid == 0) P.dlog_alpha[r] = ((sm.hpart[0] + sm.hpart[1]) + sm.hpart[2]) + sm.hpart[3];
+        }
+    };
+
+    // forward sweep: checkpoints every SEG tokens
+    for (int64_t t = 0; t < len; t += SUB) {
+        const int n = (int)((len - t) < SUB ? (len - t) : SUB);
+        if (t % SEG == 0) {
+            float* ck = ckpt + (size_t)(slot0 + t / SEG) * BLK;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) *img(ck, jj) = S[jj];
+        }
+        stage(t, n, false);
+        for (int tl = 0; tl < n; ++tl) fwd_step(tl, nullptr);
+    }
+
+    // reverse sweep
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) dS[jj] = P.dfinal ? P.dfinal[sbase + (size_t)i * kD + c * 32 + jj] : 0.f;
+    const int64_t nseg = (len + SEG - 1) / SEG;
+    for (int64_t g = nseg - 1; g >= 0; --g) {
+        const int64_t seg0 = g * SEG;
+        const int seg_len = (int)((len - seg0) < SEG ? (len - seg0) : SEG);
+        const int nsub = (seg_len + SUB - 1) / SUB;
+        const float* ck = ckpt + (size_t)(slot0 + g) * BLK;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) S[jj] = *img(const_cast<float*>(ck), jj);
+        for (int m = 0; m < nsub; ++m) {  // S every SUB tokens of the segment
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) *img(sub + (size_t)m * BLK, jj) = S[jj];
+            if (m + 1 < nsub) {
+                stage(seg0 + m * SUB, SUB, false);
+                for (int tl = 0; tl < SUB; ++tl) fwd_step(tl, nullptr);
+            }
+        }
+        for (int m = nsub - 1; m >= 0; --m) {
+            const int64_t p0 = seg0 + m * SUB;
+            const int n = (int)((seg0 + seg_len - p0) < SUB ? (seg0 + seg_len - p0) : SUB);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) S[jj] = *img(sub + (size_t)m * BLK, jj);
+            stage(p0, n, true);
+            for (int tl = 0; tl < n; ++tl) fwd_step(tl, st + (size_t)tl * BLK);
+            for (int tl = n - 1; tl >= 0; --tl) bwd_step(tl, p0 + tl);
+        }
+    }
+    if (P.dinit) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) P.dinit[sbase + (size_t)i * kD + c * 32 + jj] = dS[jj];
+    }
+}
+
+}  // namespace
+
+size_t bwd_workspace(int N, int64_t T_total, int H) {
+    const size_t slots = (size_t)(T_total / SEG) + (size_t)N + 1;
+    return ((size_t)H * slots + (size_t)N * H * 2 * SUB) * BLK * sizeof(float);
+}
+
+cudaError_t launch_bwd(BwdProblem p, int in_dtype, void* workspace, cudaStream_t st) {
+    const int64_t units = (int64_t)p.N * p.H;
+    if (units == 0) return cudaSuccess;
+    const size_t slots = (size_t)(p.T_total / SEG) + (size_t)p.N + 1;
+    p.ckpt_slots = (int64_t)slots;
+    p.ckpt = static_cast<float*>(workspace);
+    p.scratch = p.ckpt + (size_t)p.H * slots * BLK;
+    if (in_dtype == KDA_BF16)
+        bwd_kernel<__nv_bfloat16><<<(unsigned)units, NT, 0, st>>>(p);
+    else
+        bwd_kernel<float><<<(unsigned)units, NT, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -86,6 +86,36 @@ __host__ __device__ inline void seq_bounds(const SeqProblem& p, int s, int64_t& 
     }
 }
 
+// Gradients of L = sum_t <dout_t, o_t> + <dfinal, S_T> (training).  Sequences as in
+// SeqProblem; gradients in the layouts of their inputs (dlog_alpha per the gate mode).
+struct BwdProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* beta;
+    const float* init;    // [N, H, D, D] or nullptr
+    const float* dout;    // [tokens, H, D]
+    const float* dfinal;  // [N, H, D, D] or nullptr
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dlog_alpha;
+    float* dbeta;
+    float* dinit;         // [N, H, D, D] or nullptr
+    const int64_t* cu_seqlens;
+    int64_t T_uniform;
+    int64_t T_total;
+    int N;
+    int H;
+    int gate;
+    float* ckpt;          // set by launch_bwd from the workspace
+    float* scratch;
+    int64_t ckpt_slots;
+};
+size_t bwd_workspace(int N, int64_t T_total, int H);
+cudaError_t launch_bwd(BwdProblem p, int in_dtype, void* workspace, cudaStream_t st);
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_decode(const DecodeProblem& p, int in_dtype, int out_dtype, int state_dtype, cudaStream_t st);
 // `gate` (a GateMode) travels beside the problem: the chunk kernel takes it as a template

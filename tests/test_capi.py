@@ -155,6 +155,31 @@ def test_pool_validation(L):
     del I64
 
 
+def test_bwd_validation(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    P = ctypes.c_void_p
+
+    def bwd(gate=0, la=16, dla=16, dk=128, ws=None, ws_bytes=0, N=1, T=8, in_dt=0):
+        ptr = P(16)
+        return L.kda_bwd(ptr, ptr, ptr, P(la) if la else None, gate, ptr, None, ptr, None, None, N, T, 1, dk, 128,
+                         ptr, ptr, ptr, P(dla) if dla else None, ptr, None, in_dt, P(ws) if ws else None, ws_bytes,
+                         None)
+
+    need = b.kda_workspace_size(b.KDA_OP_BWD, 1, 8, 1)
+    assert need > 0
+    assert bwd(gate=4, ws=0x10000, ws_bytes=need) == b.KDA_ERR_INVALID_ARG
+    assert bwd(dk=64, ws=0x10000, ws_bytes=need) == b.KDA_ERR_UNSUPPORTED
+    assert bwd(dla=0, ws=0x10000, ws_bytes=need) == b.KDA_ERR_INVALID_ARG               # gated: dlog_alpha needed
+    assert bwd(gate=b.KDA_GATE_NONE, ws=0x10000, ws_bytes=need) == b.KDA_ERR_INVALID_ARG  # DeltaNet: no gates
+    assert bwd(ws=None) == b.KDA_ERR_WORKSPACE
+    assert bwd(ws=0x10000, ws_bytes=need - 1) == b.KDA_ERR_WORKSPACE
+    assert bwd(ws=0x10008, ws_bytes=need) == b.KDA_ERR_MISALIGNED
+    assert bwd(N=0) == b.KDA_OK
+    # workspace: a 64 KB state per 64 tokens (and per sequence) of every head, plus per-(sequence, head) scratch
+    assert b.kda_workspace_size(b.KDA_OP_BWD, 4, 4 * 8192, 32) == (32 * (4 * 8192 // 64 + 4 + 1) + 4 * 32 * 16) * 65536
+
+
 def test_workspace_size(L):
     from kda_recurrent_state_gb300 import binding as b
 
