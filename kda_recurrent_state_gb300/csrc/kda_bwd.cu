@@ -14,9 +14,10 @@
 //
 // One CTA of 512 threads walks one (sequence, head).  Thread (c, i) holds row i (key
 // channel) of value columns 32c .. 32c+31 of both S and dS in registers.  Sums over key
-// channels (p, du) are warp reduce-scatters plus a 4-warp pass through shared memory;
-// sums over value columns (dq, dk, dlog_alpha) add the four column blocks in a fixed
-// order, so the result is bit-reproducible.
+// channels (p, du) stay inside one column block: a warp reduce-scatter and a 4-warp pass
+// through shared memory behind a 128-thread barrier, so the four blocks run on their own.
+// Sums over value columns (dq, dk, dlog_alpha, dbeta) add the four column blocks in a
+// fixed order once per 8-token piece, so the result is bit-reproducible.
 //
 // States for the reverse sweep: a forward sweep stores S every 64 tokens (checkpoints,
 // workspace).  Then, segment by segment from the end, the segment is recomputed from its
@@ -55,16 +56,18 @@ struct Shared {
     float q[SUB][kD], k[SUB][kD], a[SUB][kD], v[SUB][kD], dout[SUB][kD];
     float e[SUB][kD], u[SUB][kD];
     float beta[SUB];
-    float red[4][4][32];  // [column block][warp][lane]: per-warp column partials
-    float dp[kD];
-    float rs[4][3][kD];   // [column block][dq, dk, dlog_alpha][row]: per-block row partials
-    float bpart[4];
-    float hpart[4];
+    float red[2][4][4][32];    // [parity][column block][warp][lane]: per-warp column partials
+    float rs[SUB][4][3][kD];   // [token][column block][dq, dk, dlog_alpha][row]: row partials
+    float bpart[SUB][4];       // [token][column block]: dbeta partials
 };
+
+// Barrier of the 128 threads (4 warps) of column block c; the column sums need no more.
+__device__ __forceinline__ void wg_sync(int c) { asm volatile("bar.sync %0, 128;" ::"r"(c + 1) : "memory"); }
 
 template <typename Tin>
 __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
-    __shared__ Shared sm;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Shared& sm = *reinterpret_cast<Shared*>(smem_raw);
     const int tid = threadIdx.x;
     const int c = tid >> 7, i = tid & 127, w = (tid >> 5) & 3, lane = tid & 31;
     const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
@@ -86,6 +89,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
     float* sub = P.scratch + (size_t)blockIdx.x * 2 * SUB * BLK;
     float* st = sub + SUB * BLK;
     auto img = [&](float* base, int jj) -> float* { return base + (size_t)(c * 32 + jj) * kD + i; };
+    int par = 0;  // parity of the column-partial buffer (the same sequence of steps in every warp)
 
     float S[32], dS[32];
 #pragma unroll
@@ -111,7 +115,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
         if (tid < n) sm.beta[tid] = P.beta[(size_t)(t0 + p0 + tid) * P.H + h];
         __syncthreads();
     };
-    // one forward step on S (token tl of the staged piece); keeps S_{t-1} in `keep` if set
+    // column sum over this block's 128 rows of x[jj] (column 32c + jj): every lane gets
+    // the total of its own column `32c + lane`
+    auto col_sum = [&](float (&x)[32]) -> float {
+        sm.red[par][c][w][lane] = warp_reduce_scatter(x, lane);
+        wg_sync(c);
+        const float t = ((sm.red[par][c][0][lane] + sm.red[par][c][1][lane]) + sm.red[par][c][2][lane]) +
+                        sm.red[par][c][3][lane];
+        par ^= 1;
+        return t;
+    };
+    // one forward step on S (token tl of the staged piece); with `keep`, also S_{t-1}
+    // into the scratch and e, u into shared memory for the backward steps
     auto fwd_step = [&](int tl, float* keep) {
         const float ai = sm.a[tl][i], ki = sm.k[tl][i];
         float x[32];
@@ -121,20 +136,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
             S[jj] *= ai;
             x[jj] = ki * S[jj];
         }
-        sm.red[c][w][lane] = warp_reduce_scatter(x, lane);
-        __syncthreads();
-        if (w == 0) {
-            const int j = 32 * c + lane;
-            const float p = ((sm.red[c][0][lane] + sm.red[c][1][lane]) + sm.red[c][2][lane]) + sm.red[c][3][lane];
-            const float e = sm.v[tl][j] - p;
+        const int j = 32 * c + lane;
+        const float e = sm.v[tl][j] - col_sum(x);
+        const float u = sm.beta[tl] * e;
+        if (keep && w == 0) {
             sm.e[tl][j] = e;
-            sm.u[tl][j] = sm.beta[tl] * e;
+            sm.u[tl][j] = u;
         }
-        __syncthreads();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] += ki * sm.u[tl][32 * c + jj];
+        for (int jj = 0; jj < 32; ++jj) S[jj] += ki * __shfl_sync(0xffffffffu, u, jj);
     };
-    // one backward step for token tl of the staged piece (global token t0 + pos)
+    // one backward step for token tl of the staged piece (token `pos` of the sequence);
+    // row partials go to sm.rs / sm.bpart and are combined once per piece
     auto bwd_step = [&](int tl, int64_t pos) {
         const size_t r = (size_t)(t0 + pos) * P.H + h;
 #pragma unroll
@@ -149,53 +162,60 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
             dq += (ai * S[jj] + ki * sm.u[tl][j]) * doj;
             x[jj] = dS[jj] * ki;
         }
-        sm.red[c][w][lane] = warp_reduce_scatter(x, lane);
-        __syncthreads();
+        const int j = 32 * c + lane;
+        const float du = col_sum(x);
+        const float b = sm.beta[tl];
+        const float dp = -b * du;
         if (w == 0) {
-            const int j = 32 * c + lane;
-            const float du = ((sm.red[c][0][lane] + sm.red[c][1][lane]) + sm.red[c][2][lane]) + sm.red[c][3][lane];
-            const float b = sm.beta[tl];
             P.dv[r * kD + j] = b * du;
-            sm.dp[j] = -b * du;
             float bp = du * sm.e[tl][j];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) bp += __shfl_xor_sync(0xffffffffu, bp, o);
-            if (lane == 0) sm.bpart[c] = bp;
+            if (lane == 0) sm.bpart[tl][c] = bp;
         }
-        __syncthreads();
         float dk = 0.f, da = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
-            const int j = 32 * c + jj;
-            const float dpj = sm.dp[j];
-            dk += dS[jj] * sm.u[tl][j] + (ai * S[jj]) * dpj;
+            const float dpj = __shfl_sync(0xffffffffu, dp, jj);
+            dk += dS[jj] * sm.u[tl][32 * c + jj] + (ai * S[jj]) * dpj;
             const float dsp = dS[jj] + ki * dpj;
             da += dsp * S[jj];
             dS[jj] = ai * dsp;
         }
-        sm.rs[c][0][i] = dq;
-        sm.rs[c][1][i] = dk;
-        sm.rs[c][2][i] = ai * da;
+        sm.rs[tl][c][0][i] = dq;
+        sm.rs[tl][c][1][i] = dk;
+        sm.rs[tl][c][2][i] = ai * da;
+    };
+    // sums over the four column blocks, in a fixed order, for tokens [p0, p0 + n)
+    auto combine = [&](int64_t p0, int n) {
         __syncthreads();
-        if (c == 0) {
-            const size_t o = r * kD + i;
-            P.dq[o] = ((sm.rs[0][0][i] + sm.rs[1][0][i]) + sm.rs[2][0][i]) + sm.rs[3][0][i];
-            P.dk[o] = ((sm.rs[0][1][i] + sm.rs[1][1][i]) + sm.rs[2][1][i]) + sm.rs[3][1][i];
-            const float dla = ((sm.rs[0][2][i] + sm.rs[1][2][i]) + sm.rs[2][2][i]) + sm.rs[3][2][i];
-            if (P.gate == kGateChannel) {
-                P.dlog_alpha[o] = dla;
-            } else if (P.gate == kGateHead) {
-                float hs = dla;
+        for (int idx = tid; idx < n * 3 * kD; idx += NT) {
+            const int tl = idx / (3 * kD), kind = (idx >> 7) % 3, row = idx & 127;
+            const float val = ((sm.rs[tl][0][kind][row] + sm.rs[tl][1][kind][row]) + sm.rs[tl][2][kind][row]) +
+                              sm.rs[tl][3][kind][row];
+            const size_t o = ((size_t)(t0 + p0 + tl) * P.H + h) * kD + row;
+            if (kind == 0)
+                P.dq[o] = val;
+            else if (kind == 1)
+                P.dk[o] = val;
+            else if (P.gate == kGateChannel)
+                P.dlog_alpha[o] = val;
+        }
+        if (P.gate == kGateHead && (tid >> 5) < n) {  // warp tl: the head's gate gradient of token tl
+            const int tl = tid >> 5;
+            float hs = 0.f;
 #pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, o2);
-                if (lane == 0) sm.hpart[w] = hs;
+            for (int m = 0; m < 4; ++m) {
+                const int row = lane + 32 * m;
+                hs += ((sm.rs[tl][0][2][row] + sm.rs[tl][1][2][row]) + sm.rs[tl][2][2][row]) + sm.rs[tl][3][2][row];
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, o);
+            if (lane == 0) P.dlog_alpha[(size_t)(t0 + p0 + tl) * P.H + h] = hs;
         }
-        if (tid == 0) P.dbeta[r] = ((sm.bpart[0] + sm.bpart[1]) + sm.bpart[2]) + sm.bpart[3];
-        if (P.gate == kGateHead) {
-            __syncthreads();
-            if (tid == 0) P.dlog_alpha[r] = ((sm.hpart[0] + sm.hpart[1]) + sm.hpart[2]) + sm.hpart[3];
-        }
+        if (tid < n)
+            P.dbeta[(size_t)(t0 + p0 + tid) * P.H + h] =
+                ((sm.bpart[tid][0] + sm.bpart[tid][1]) + sm.bpart[tid][2]) + sm.bpart[tid][3];
     };
 
     // forward sweep: checkpoints every SEG tokens
@@ -236,7 +256,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
             for (int jj = 0; jj < 32; ++jj) S[jj] = *img(sub + (size_t)m * BLK, jj);
             stage(p0, n, true);
             for (int tl = 0; tl < n; ++tl) fwd_step(tl, st + (size_t)tl * BLK);
+            wg_sync(c);  // e, u of the piece (written by warp 0 of the block) before they are read
             for (int tl = n - 1; tl >= 0; --tl) bwd_step(tl, p0 + tl);
+            combine(p0, n);
         }
     }
     if (P.dinit) {
@@ -259,10 +281,11 @@ cudaError_t launch_bwd(BwdProblem p, int in_dtype, void* workspace, cudaStream_t
     p.ckpt_slots = (int64_t)slots;
     p.ckpt = static_cast<float*>(workspace);
     p.scratch = p.ckpt + (size_t)p.H * slots * BLK;
-    if (in_dtype == KDA_BF16)
-        bwd_kernel<__nv_bfloat16><<<(unsigned)units, NT, 0, st>>>(p);
-    else
-        bwd_kernel<float><<<(unsigned)units, NT, 0, st>>>(p);
+    const int smem = (int)sizeof(Shared);
+    auto kern = in_dtype == KDA_BF16 ? bwd_kernel<__nv_bfloat16> : bwd_kernel<float>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)units, NT, smem, st>>>(p);
     return cudaGetLastError();
 }
 
