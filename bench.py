@@ -41,6 +41,9 @@ PREFILL_FLOP = 6 * D * D + CHUNK * (3 * D + 2 * D)
 # decode: fp32 state read + written (2 x 65,536 B; half that for a bf16 state) + q,k,v bf16,
 # log_alpha, beta, out fp32 per session-head
 DEC_BYTES = 2 * D * D * 4 + 3 * 256 + 512 + 4 + 512
+# backward: the forward step (7 dk dv) and its reverse mode (15 dk dv) per token-head
+BWD_FLOP = 22 * D * D
+FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # CUDA-core fp32 peak from unit counts and the max SM clock
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -339,6 +342,32 @@ def run_ours(args):
                                   f"fp32 out"}
     line["gpu_launches"] += 8
     del xv, vout, vfin, vsnaps
+
+    # ---- backward (training) at B=4, H=32, T=8192: token-serial reverse mode on CUDA cores,
+    # reported against the fp32 CUDA-core peak (ALU-bound, not a tensor-core path)
+    xb = synth.prefill_inputs(4, 8192, 32, seed=synth.SEED_BASE + 1, device=dev, init="normal")
+    do = torch.randn(4, 8192, 32, D, generator=torch.Generator(device=dev).manual_seed(7), device=dev)
+    ws_b = torch.empty(binding.kda_workspace_size(binding.KDA_OP_BWD, 4, 4 * 8192, 32), dtype=torch.uint8, device=dev)
+    bwd = lambda: kda.kda_bwd(xb["q"], xb["k"], xb["v"], xb["log_alpha"], xb["beta"], do, xb["init_state"],
+                              workspace=ws_b)
+    bwd()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(2):
+        bwd()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bt = e0.elapsed_time(e1) / 1e3 / 2
+    btf = 4 * 8192 * 32 * BWD_FLOP / bt / 1e12
+    line["bwd"] = {"tokens_per_s": 4 * 8192 / bt, "ms_per_call": bt * 1e3,
+                   "roofline": {"bound": "alu", "achieved": btf, "peak": FP32_TFLOPS, "unit": "TFLOP/s",
+                                "frac": btf / FP32_TFLOPS,
+                                "peak_source": "152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz (nominal)"},
+                   "workload": "kda_bwd B=4 H=32 T=8192, bf16 q/k/v, fp32 gates/state/cotangents, "
+                               "S0 ~ N(0,0.02); flops = 22 dk dv per token-head"}
+    line["gpu_launches"] += 3
+    assert kda.kda_get_device_status() == 0, "device status raised by the backward"
+    del xb, do, ws_b
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:

@@ -167,3 +167,38 @@ def test_decode_bf16state_rejects_fp32_state():
     with pytest.raises(TypeError):
         kda.kda_decode_step_bf16state(z, z, z, z, torch.zeros(1, 1, device="cuda"), torch.zeros(1, 1, 128, 128,
                                                                                                   device="cuda"))
+
+
+@pytest.mark.parametrize("bf16state", [False, True], ids=["fp32_state", "bf16_state"])
+def test_decode_continues_prefill(bf16state):
+    """A prefill of 300 tokens followed by 20 decode steps on its final state equals the
+    per-token recurrence over all 320 tokens (outputs of the decoded tokens and the final
+    state).  With a bf16-stored state the prefill's state is rounded once before decoding
+    and every decode step rounds again, which the oracle reproduces."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    T0, n, H = 300, 20, 3
+    x = synth.prefill_inputs(2, T0 + n, H, seed=707, device="cuda", init="normal")
+    pre = lambda t: t[:, :T0].contiguous()
+    _, fin = kda.kda_chunk_fwd(pre(x["q"]), pre(x["k"]), pre(x["v"]), pre(x["log_alpha"]), pre(x["beta"]),
+                               x["init_state"])
+    state = fin.to(torch.bfloat16) if bf16state else fin.clone()
+    step = kda.kda_decode_step_bf16state if bf16state else kda.kda_decode_step
+    outs = [step(x["q"][:, t].contiguous(), x["k"][:, t].contiguous(), x["v"][:, t].contiguous(),
+                 x["log_alpha"][:, t].contiguous(), x["beta"][:, t].contiguous(), state) for t in range(T0, T0 + n)]
+    torch.cuda.synchronize()
+    pairs = [(b, h) for b in range(2) for h in range(H)]
+    col = lambda t, b, h: np64(t[b, :, h])
+    S0 = np.stack([np64(x["init_state"][b, h]) for b, h in pairs])
+    args = [np.stack([col(x[nm], b, h) for b, h in pairs]) for nm in ("q", "k", "v", "log_alpha", "beta")]
+    if bf16state:  # fp64 prefill, state rounded once, then the rounding decode steps
+        _, s_mid = oracle.recurrent(*[a[:, :T0] for a in args], S0)
+        ro, rs = oracle.recurrent_bf16state(*[a[:, T0:] for a in args], oracle.round_bf16(s_mid))
+    else:
+        ro_all, rs = oracle.recurrent(*args, S0)
+        ro = ro_all[:, T0:]
+    got = np.stack([np.stack([np64(outs[t][b, h]) for t in range(n)]) for b, h in pairs])
+    assert_close(got, ro, "decoded outputs")
+    assert_close(np.stack([np64(state[b, h]) for b, h in pairs]), rs, "state after decoding")
+    assert kda.kda_get_device_status() == 0

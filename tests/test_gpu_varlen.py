@@ -123,3 +123,28 @@ def test_resume_from_snapshot(prefix):
     assert torch.equal(f2[0], fin[0])
     assert kda.kda_snapshot_lookup(off, 2, 128, 100) == (-1, 0)
 
+
+
+def test_many_sequences_beyond_longest_first_ranking():
+    """300 packed sequences (more than the kernel ranks for its longest-first order, so CTAs
+    take sequences in order), lengths 0..130 with snapshots every 64 tokens: sampled
+    sequences against the oracle, and every sequence bit for bit against its own run."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    g = torch.Generator().manual_seed(606)
+    lengths = torch.randint(0, 131, (300,), generator=g).tolist()
+    x = synth.varlen_inputs(lengths, 1, seed=607, device="cuda", resume_every=3)
+    out, fin, snaps = _run(x, 64, 64)
+    torch.cuda.synchronize()
+    off = kda.kda_snapshot_offsets(x["cu_seqlens"].cpu(), 64)
+    for s in (0, 1, 77, 150, 299):
+        _check_seq(x, s, [0], out, fin, snaps, off, 64, "many")
+    cu = x["cu_seqlens"].tolist()
+    for s in range(0, 300, 7):
+        a, b = cu[s], cu[s + 1]
+        sl = lambda t: t[a:b].unsqueeze(0).contiguous()
+        o1, f1 = kda.kda_chunk_fwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["log_alpha"]), sl(x["beta"]),
+                                   x["init_states"][s:s + 1].contiguous())
+        assert torch.equal(out[a:b], o1[0]) and torch.equal(fin[s], f1[0]), f"sequence {s}"
+    assert kda.kda_get_device_status() == 0
