@@ -73,7 +73,8 @@ typedef enum {
     KDA_ERR_TIMEOUT = 5,     /* device status: a bounded wait inside a kernel expired */
     KDA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than kda_workspace_size() */
     KDA_STATUS_GATE_RANGE = 7, /* device status: a half-chunk's summed log-decay was below -15 ln 2 */
-    KDA_STATUS_SLOT_RANGE = 8  /* device status: a state-pool slot index outside [-1, pool_slots) was skipped */
+    KDA_STATUS_SLOT_RANGE = 8, /* device status: a state-pool slot index outside [-1, pool_slots) was skipped */
+    KDA_ERR_SCRATCH_TOO_SMALL = 9 /* the problem needs more than the library's static scratch (kda_bwd_noalloc) */
 } kda_status;
 
 /* Operation selector of kda_workspace_size(). */
@@ -245,6 +246,22 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
             const float* init_states, const float* d_out, const float* d_final_states, const int64_t* cu_seqlens,
             int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
             float* dbeta, float* d_init_states, int in_dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * kda_bwd without a caller workspace: the scratch is a static device array inside the
+ * library, KDA_NOALLOC_SCRATCH_BYTES bytes per device, reserved when this entry point is
+ * first used on a device (its address is looked up once per device).  Nothing is
+ * allocated per call.  Arguments as for kda_bwd minus workspace and ws_bytes.  Returns
+ * KDA_ERR_SCRATCH_TOO_SMALL, without launching anything, when
+ * kda_workspace_size(KDA_OP_BWD, N, T_total, H, dk, dv, 64) exceeds the static scratch.
+ * Calls on one device share that scratch: at most one may be in flight per device
+ * (issue them on one stream, or synchronise between them).
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
+int kda_bwd_noalloc(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
+                    const float* init_states, const float* d_out, const float* d_final_states,
+                    const int64_t* cu_seqlens, int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out,
+                    float* dv_out, float* dlog_alpha, float* dbeta, float* d_init_states, int in_dtype, void* stream);
 
 /* Number of snapshots of a sequence: floor(seqlen / interval); 0 if interval <= 0 or seqlen < 0. */
 int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);

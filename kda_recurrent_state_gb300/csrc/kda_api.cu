@@ -65,6 +65,8 @@ const char* kda_status_string(int status) {
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
         case KDA_STATUS_GATE_RANGE: return "KDA_STATUS_GATE_RANGE: a half-chunk's summed log-decay is below -15 ln 2";
         case KDA_STATUS_SLOT_RANGE: return "KDA_STATUS_SLOT_RANGE: a state-pool slot index was out of range and skipped";
+        case KDA_ERR_SCRATCH_TOO_SMALL:
+            return "KDA_ERR_SCRATCH_TOO_SMALL: the problem needs more scratch than the library's static 128 MiB";
         default: return "unknown kda status";
     }
 }

@@ -62,7 +62,7 @@ def test_snapshot_lookup(L):
 def test_status_strings(L):
     from kda_recurrent_state_gb300 import binding as b
 
-    for code in range(9):
+    for code in range(10):
         assert b.kda_status_string(code).startswith("KDA_")
     assert "unknown" in b.kda_status_string(99)
 
@@ -178,6 +178,19 @@ def test_bwd_validation(L):
     assert bwd(N=0) == b.KDA_OK
     # workspace: a 64 KB state per 64 tokens (and per sequence) of every head, plus per-(sequence, head) scratch
     assert b.kda_workspace_size(b.KDA_OP_BWD, 4, 4 * 8192, 32) == (32 * (4 * 8192 // 64 + 4 + 1) + 4 * 32 * 16) * 65536
+
+
+def test_bwd_noalloc_rejects_oversize(L):
+    """A problem whose backward scratch exceeds the static 128 MiB is refused before any CUDA call."""
+    from kda_recurrent_state_gb300 import binding as b
+
+    P = ctypes.c_void_p
+    assert b.kda_workspace_size(b.KDA_OP_BWD, 4, 4 * 8192, 32) > b.KDA_NOALLOC_SCRATCH_BYTES
+    ptr = P(16)
+    rc = L.kda_bwd_noalloc(ptr, ptr, ptr, ptr, 0, ptr, None, ptr, None, None, 4, 8192, 32, 128, 128, ptr, ptr, ptr,
+                           ptr, ptr, None, 0, None)
+    assert rc == b.KDA_ERR_SCRATCH_TOO_SMALL
+    assert "static" in b.kda_status_string(rc)
 
 
 def test_workspace_size(L):
