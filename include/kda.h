@@ -198,8 +198,12 @@ int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float
  * instead of recomputing it, with the snapshot block size decoupled from the
  * granularity of prefix matching).  Arguments as for kda_varlen_fwd, except:
  *   gate        kda_gate: the layout of log_alpha ([T_total, H, dk], [T_total, H] or NULL).
- *   pool        float32 [pool_slots, H, dk, dv], 16-byte aligned; slot i holds the states
- *               of all H heads at one position of one sequence.
+ *   pool        [pool_slots, H, dk, dv] of pool_dtype, 16-byte aligned; slot i holds the
+ *               states of all H heads at one position of one sequence.
+ *   pool_dtype  KDA_F32, or KDA_BF16 for a pool that stores states in bf16 ([hubwiz] §3
+ *               sizes the state in bf16): initial states are widened exactly to fp32 and
+ *               snapshots are the fp32 states rounded to nearest-even bf16, which halves
+ *               the pool's memory; the arithmetic stays fp32.
  *   init_slots  device int64 [N] or NULL: sequence s starts from slot init_slots[s]
  *               (-1: zero state).  NULL: every sequence starts from zeros.
  *   snap_slots  device int64 [snap_offsets[N]], required when snapshot_interval > 0:
@@ -211,12 +215,13 @@ int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float
  * same call.  A slot index outside [-1, pool_slots) is not dereferenced: the state is
  * taken as zero, or the snapshot is dropped, and KDA_STATUS_SLOT_RANGE is raised in the
  * device status word.  Results are bit-identical to kda_varlen_fwd (or
- * kda_gdn_varlen_fwd) with the same states gathered into packed arrays; with
+ * kda_gdn_varlen_fwd) with the same states gathered into packed fp32 arrays (a bf16
+ * pool: the widened states in, the snapshots rounded out); with
  * kda_snapshot_lookup, a resumed sequence reproduces the unsplit run bit for bit.
  */
 int kda_varlen_fwd_pool(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
                         const float* beta, const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
-                        int chunk, float* pool, int64_t pool_slots, const int64_t* init_slots,
+                        int chunk, void* pool, int64_t pool_slots, int pool_dtype, const int64_t* init_slots,
                         int64_t snapshot_interval, const int64_t* snap_offsets, const int64_t* snap_slots,
                         float* final_states, void* out, int in_dtype, int out_dtype, void* workspace,
                         size_t ws_bytes, void* stream);

@@ -51,8 +51,8 @@ def lib() -> ctypes.CDLL:
         L.kda_gdn_decode_step.argtypes = L.kda_decode_step.argtypes
         L.kda_bwd.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P, SZ, P]
         L.kda_bwd_noalloc.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P]
-        L.kda_varlen_fwd_pool.argtypes = [P, P, P, P, I, P, P, I, I64, I, I, I, I, P, I64, P, I64, P, P, P, P, I, I,
-                                          P, SZ, P]
+        L.kda_varlen_fwd_pool.argtypes = [P, P, P, P, I, P, P, I, I64, I, I, I, I, P, I64, I, P, I64, P, P, P, P, I,
+                                          I, P, SZ, P]
         L.kda_snapshot_count.argtypes = [I64, I64]
         L.kda_snapshot_count.restype = I64
         L.kda_snapshot_offsets.argtypes = [P, I, I64, P]
@@ -218,7 +218,8 @@ def kda_varlen_fwd(q, k, v, log_alpha, beta, cu_seqlens, init_states=None, *, ch
 def kda_varlen_fwd_pool(q, k, v, log_alpha, beta, cu_seqlens, pool, init_slots=None, snap_slots=None, *,
                         gate: int = KDA_GATE_CHANNEL, chunk: int = 64, snapshot_interval: int = 0,
                         cu_seqlens_host=None, out=None, final_states=None, out_dtype=torch.float32, workspace=None):
-    """Packed sequences over a state pool [pool_slots,H,dk,dv] fp32: sequence s starts from slot
+    """Packed sequences over a state pool [pool_slots,H,dk,dv] (fp32, or bf16 storage with fp32
+    arithmetic): sequence s starts from slot
     init_slots[s] (-1: zeros; None: all zeros) and snapshot m of sequence s goes to slot
     snap_slots[offsets[s] + m - 1] (-1: not stored).  log_alpha's layout is given by `gate`.
     Returns (out, final_states); the snapshots are in the pool."""
@@ -229,8 +230,8 @@ def kda_varlen_fwd_pool(q, k, v, log_alpha, beta, cu_seqlens, pool, init_slots=N
         out = torch.empty(Ttot, H, dv, dtype=out_dtype, device=q.device)
     if final_states is None:
         final_states = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
-    if pool.dtype != torch.float32 or tuple(pool.shape[1:]) != (H, dk, dv):
-        raise ValueError(f"pool must be float32 [slots, {H}, {dk}, {dv}]")
+    if pool.dtype not in (torch.float32, torch.bfloat16) or tuple(pool.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"pool must be float32 or bfloat16 [slots, {H}, {dk}, {dv}]")
     snap_off = None
     if snapshot_interval:
         cu_h = cu_seqlens.cpu() if cu_seqlens_host is None else torch.as_tensor(cu_seqlens_host)
@@ -241,7 +242,7 @@ def kda_varlen_fwd_pool(q, k, v, log_alpha, beta, cu_seqlens, pool, init_slots=N
     ws, ws_bytes = _workspace(KDA_OP_VARLEN, N, Ttot, H, dk, dv, chunk, q.device, workspace)
     rc = lib().kda_varlen_fwd_pool(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), int(gate), _ptr(beta),
                                    _ptr(cu_seqlens), N, Ttot, H, dk, dv, int(chunk), _ptr(pool), pool.shape[0],
-                                   _ptr(init_slots), int(snapshot_interval), _ptr(snap_off), _ptr(snap_slots),
+                                   _dt(pool), _ptr(init_slots), int(snapshot_interval), _ptr(snap_off), _ptr(snap_slots),
                                    _ptr(final_states), _ptr(out), _dt(q), _dt(out), _ptr(ws), ws_bytes,
                                    _stream(q.device))
     _check(rc, "kda_varlen_fwd_pool")

@@ -40,10 +40,10 @@ int check_common(int dk, int dv, int chunk, int in_dtype, int out_dtype) {
     return KDA_OK;
 }
 
-int run_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int chunk, int in_dtype, int out_dtype,
-                void* ws, size_t ws_bytes, cudaStream_t st) {
-    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, pool, gate, in_dtype, out_dtype, st)
-                                 : launch_chunk_prefill(p, pool, gate, in_dtype, out_dtype, ws, ws_bytes, st);
+int run_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int chunk, int in_dtype,
+                int out_dtype, void* ws, size_t ws_bytes, cudaStream_t st) {
+    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, pool, pool_bf16, gate, in_dtype, out_dtype, st)
+                                 : launch_chunk_prefill(p, pool, pool_bf16, gate, in_dtype, out_dtype, ws, ws_bytes, st);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -162,7 +162,8 @@ static int chunk_common(const void* q, const void* k, const void* v, const float
     p.snap_interval = 0; p.snap_offsets = nullptr; p.snapshots = nullptr;
     p.status = status_ptr();
     if (!p.status) return KDA_ERR_CUDA;
-    return run_prefill(p, PoolSlots{nullptr, nullptr, 0}, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes, st);
+    return run_prefill(p, PoolSlots{nullptr, nullptr, 0}, false, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes,
+                       st);
 }
 
 int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
@@ -188,7 +189,7 @@ static int varlen_common(const void* q, const void* k, const void* v, const floa
                          int dv, int chunk, const float* init_states, float* final_states,
                          int64_t snapshot_interval, const int64_t* snap_offsets, float* snapshots, void* out,
                          int in_dtype, int out_dtype, void* workspace, size_t ws_bytes, void* stream,
-                         const PoolSlots& pool) {
+                         const PoolSlots& pool, bool pool_bf16) {
     if (N < 0 || T_total < 0 || H < 0 || snapshot_interval < 0) return KDA_ERR_INVALID_ARG;
     int rc = check_common(dk, dv, chunk, in_dtype, out_dtype);
     if (rc != KDA_OK) return rc;
@@ -219,7 +220,7 @@ static int varlen_common(const void* q, const void* k, const void* v, const floa
     p.snap_interval = snapshot_interval; p.snap_offsets = snap_offsets; p.snapshots = snapshots;
     p.status = status_ptr();
     if (!p.status) return KDA_ERR_CUDA;
-    return run_prefill(p, pool, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes,
+    return run_prefill(p, pool, pool_bf16, gate, chunk, in_dtype, out_dtype, workspace, ws_bytes,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -230,7 +231,7 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log
                    void* workspace, size_t ws_bytes, void* stream) {
     return varlen_common(q, k, v, log_alpha, kGateChannel, beta, cu_seqlens, N, T_total, H, dk, dv, chunk,
                          init_states, final_states, snapshot_interval, snap_offsets, snapshots, out, in_dtype,
-                         out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0});
+                         out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0}, false);
 }
 
 int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
@@ -240,25 +241,27 @@ int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float*
                        void* workspace, size_t ws_bytes, void* stream) {
     return varlen_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, cu_seqlens, N, T_total, H,
                          dk, dv, chunk, init_states, final_states, snapshot_interval, snap_offsets, snapshots, out,
-                         in_dtype, out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0});
+                         in_dtype, out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0}, false);
 }
 
 int kda_varlen_fwd_pool(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
                         const float* beta, const int64_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
-                        int chunk, float* pool, int64_t pool_slots, const int64_t* init_slots,
+                        int chunk, void* pool, int64_t pool_slots, int pool_dtype, const int64_t* init_slots,
                         int64_t snapshot_interval, const int64_t* snap_offsets, const int64_t* snap_slots,
                         float* final_states, void* out, int in_dtype, int out_dtype, void* workspace,
                         size_t ws_bytes, void* stream) {
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE) return KDA_ERR_INVALID_ARG;
-    if (pool_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (pool_slots < 0 || !dtype_ok(pool_dtype)) return KDA_ERR_INVALID_ARG;
     if (snapshot_interval > 0 && !snap_slots) return KDA_ERR_INVALID_ARG;
     if ((init_slots || snapshot_interval > 0) && !pool) return KDA_ERR_INVALID_ARG;
     if (gate == KDA_GATE_HEAD && !log_alpha && T_total > 0) return KDA_ERR_INVALID_ARG;
     const int g = gate == KDA_GATE_CHANNEL ? kGateChannel : gate == KDA_GATE_HEAD ? kGateHead : kGateNone;
+    float* pool_f = static_cast<float*>(pool);  // element type per pool_dtype; the kernels cast back
     return varlen_common(q, k, v, log_alpha, g, beta, cu_seqlens, N, T_total, H, dk, dv, chunk,
-                         init_slots ? pool : nullptr, final_states, snapshot_interval, snap_offsets,
-                         snapshot_interval > 0 ? pool : nullptr, out, in_dtype, out_dtype, workspace, ws_bytes, stream,
-                         PoolSlots{init_slots, snapshot_interval > 0 ? snap_slots : nullptr, pool_slots});
+                         init_slots ? pool_f : nullptr, final_states, snapshot_interval, snap_offsets,
+                         snapshot_interval > 0 ? pool_f : nullptr, out, in_dtype, out_dtype, workspace, ws_bytes,
+                         stream, PoolSlots{init_slots, snapshot_interval > 0 ? snap_slots : nullptr, pool_slots},
+                         pool_dtype == KDA_BF16);
 }
 
 static int decode_common(const void* q, const void* k, const void* v, const float* log_alpha, int gate,

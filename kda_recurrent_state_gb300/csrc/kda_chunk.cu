@@ -288,10 +288,28 @@ __device__ __forceinline__ void tri_column(uint32_t a16, uint32_t dg16, uint8_t*
     }
 }
 
+// The true state Diag(b) D of column j (TMEM lane) rounded to bf16 into a bf16 pool slot.
+// Out of line: rare (snapshots only) and kept out of the kernel's hot code.
+__device__ __noinline__ void store_state_bf16(__nv_bfloat16* dst, uint32_t taddr, const float* bv, int j) {
+#pragma unroll 1
+    for (int piece = 0; piece < 4; ++piece) {
+        uint32_t d[32];
+        tmem_ld32(taddr + piece * 32, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int cc = piece * 32 + e;
+            dst[(size_t)cc * kD + j] = __float2bfloat16_rn(__uint_as_float(d[e]) * bv[cc]);
+        }
+    }
+}
+
 // SG: one log-decay per (token, head) (the scalar gate of Gated DeltaNet), or none at
 // all (DeltaNet, alpha = 1) when P.log_alpha is null.  The gates then come in with beta
 // through the beta loader, and the TMA ring carries q, k and v only.
-template <typename Tin, typename Tout, bool SG>
+// PB: the state pool holds bf16 states (a separate instantiation, so that the common
+// kernels' code is not touched by it).
+template <typename Tin, typename Tout, bool SG, bool PB>
 __global__ void __launch_bounds__(NTHREADS, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
@@ -340,17 +358,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     seq_bounds(P, s, t0, len);
     const int nch = (int)((len + C - 1) / C);
     const size_t sbase = ((size_t)s * P.H + h) * kD * kD;
-    // this unit's initial state (null: zeros), looked up where it is read
+    // this unit's initial state (null: zeros), looked up where it is read; with a bf16 pool
+    // the pointer addresses bf16 entries, which init_at widens
     auto init_state = [&]() -> const float* {
         if (!pool.init_slots) return P.init ? P.init + sbase : nullptr;
         const int64_t slot = checked_slot(pool.init_slots[s], pool.n_slots, P.status);
-        return slot >= 0 ? P.init + ((size_t)slot * P.H + h) * kD * kD : nullptr;
+        if constexpr (PB)
+            return slot >= 0 ? reinterpret_cast<const float*>(reinterpret_cast<const __nv_bfloat16*>(P.init) +
+                                                              ((size_t)slot * P.H + h) * kD * kD)
+                             : nullptr;
+        else
+            return slot >= 0 ? P.init + ((size_t)slot * P.H + h) * kD * kD : nullptr;
+    };
+    auto init_at = [&](const float* S0, size_t i) -> float {
+        if constexpr (PB)
+            return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(S0)[i]);
+        else
+            return S0[i];
     };
 
     if (nch == 0) {  // empty sequence: the final state is the initial state
         if (P.final_state) {
             const float* S0 = init_state();
-            for (int i = tid; i < kD * kD; i += NTHREADS) P.final_state[sbase + i] = S0 ? S0[i] : 0.f;
+            for (int i = tid; i < kD * kD; i += NTHREADS) P.final_state[sbase + i] = S0 ? init_at(S0, i) : 0.f;
         }
         return;
     }
@@ -641,7 +671,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int cc = piece * 32 + e;
-                    const float s0 = S0 ? S0[(size_t)cc * kD + j] : 0.f;
+                    const float s0 = S0 ? init_at(S0, (size_t)cc * kD + j) : 0.f;
                     xs[e] = __float_as_uint(s0 * vec_a[cc]);
                 }
 #pragma unroll
@@ -711,13 +741,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             {
                 const int64_t end_pos = (int64_t)C * n + valid;  // tokens of the sequence consumed so far
                 float* snap = nullptr;
+                __nv_bfloat16* snap16 = nullptr;  // snapshot into a bf16 pool
                 if (P.snap_interval > 0 && valid == C && end_pos % P.snap_interval == 0) {
                     int64_t slot = P.snap_offsets[s] + end_pos / P.snap_interval - 1;
                     if (pool.snap_slots) slot = checked_slot(pool.snap_slots[slot], pool.n_slots, P.status);
-                    if (slot >= 0 && P.snapshots) snap = P.snapshots + ((size_t)slot * P.H + h) * kD * kD;
+                    if constexpr (PB) {
+                        if (slot >= 0 && P.snapshots)
+                            snap16 = reinterpret_cast<__nv_bfloat16*>(P.snapshots) + ((size_t)slot * P.H + h) * kD * kD;
+                    } else {
+                        if (slot >= 0 && P.snapshots) snap = P.snapshots + ((size_t)slot * P.H + h) * kD * kD;
+                    }
                 }
                 float* fin = (last && P.final_state) ? P.final_state + sbase : nullptr;
                 const float* bv = vec_b + (n % 3) * 128;
+                if constexpr (PB)
+                    if (snap16) store_state_bf16(snap16, tmem + lane_base + TM_S, bv, j);
                 if (snap || fin) {  // true state S = Diag(b_n) D, at snapshot positions and the end
 #pragma unroll 1
                     for (int piece = 0; piece < 4; ++piece) {
@@ -1040,7 +1078,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tin, typename Tout, bool SG>
+template <typename Tin, typename Tout, bool SG, bool PB>
 cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, cudaStream_t st) {
     CUtensorMap mq, mk, mv, ml, mo;
     const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -1053,7 +1091,7 @@ cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, cudaStream_t st
                   sizeof(Tout), Tt, p.H))
         return cudaErrorInvalidValue;
     if (SG) ml = mq;  // not read
-    auto kern = chunk_kernel<Tin, Tout, SG>;
+    auto kern = chunk_kernel<Tin, Tout, SG, PB>;
     const int smem = (int)Cfg<Tin>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -1077,21 +1115,25 @@ size_t chunk_prefill_workspace(int N, int H) {
     return 0;
 }
 
-cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
-                                 void* workspace, size_t ws_bytes, cudaStream_t st) {
+template <typename Tin, typename Tout>
+cudaError_t launch_gate(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, cudaStream_t st) {
+    if (pool_bf16)
+        return gate != kGateChannel ? launch_t<Tin, Tout, true, true>(p, pool, st)
+                                    : launch_t<Tin, Tout, false, true>(p, pool, st);
+    return gate != kGateChannel ? launch_t<Tin, Tout, true, false>(p, pool, st)
+                                : launch_t<Tin, Tout, false, false>(p, pool, st);
+}
+
+cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int in_dtype,
+                                 int out_dtype, void* workspace, size_t ws_bytes, cudaStream_t st) {
     (void)workspace;
     (void)ws_bytes;
     if ((int64_t)p.N * p.H == 0) return cudaSuccess;
-    if (gate != kGateChannel) {
-        if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, true>(p, pool, st);
-        if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, true>(p, pool, st);
-        if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, true>(p, pool, st);
-        return launch_t<float, float, true>(p, pool, st);
-    }
-    if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16) return launch_t<__nv_bfloat16, __nv_bfloat16, false>(p, pool, st);
-    if (in_dtype == KDA_BF16) return launch_t<__nv_bfloat16, float, false>(p, pool, st);
-    if (out_dtype == KDA_BF16) return launch_t<float, __nv_bfloat16, false>(p, pool, st);
-    return launch_t<float, float, false>(p, pool, st);
+    if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16)
+        return launch_gate<__nv_bfloat16, __nv_bfloat16>(p, pool, pool_bf16, gate, st);
+    if (in_dtype == KDA_BF16) return launch_gate<__nv_bfloat16, float>(p, pool, pool_bf16, gate, st);
+    if (out_dtype == KDA_BF16) return launch_gate<float, __nv_bfloat16>(p, pool, pool_bf16, gate, st);
+    return launch_gate<float, float>(p, pool, pool_bf16, gate, st);
 }
 
 }  // namespace kda

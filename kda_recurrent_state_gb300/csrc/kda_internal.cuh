@@ -46,6 +46,8 @@ struct SeqProblem {
 // goes to slot snap_slots[k] of SeqProblem::snapshots (-1: not stored).  A slot is [H, D, D].
 // Kept out of SeqProblem so that the chunk kernel's parameter block keeps its size.
 // A slot index outside [-1, n_slots) is skipped and raises KDA_STATUS_SLOT_RANGE.
+// A bf16 pool (the launchers' pool_bf16) holds bf16 states: read widened exactly, snapshots
+// stored rounded to nearest (the arithmetic stays fp32).
 struct PoolSlots {
     const int64_t* init_slots;
     const int64_t* snap_slots;
@@ -120,10 +122,10 @@ cudaError_t launch_bwd(BwdProblem p, int in_dtype, void* workspace, cudaStream_t
 cudaError_t launch_decode(const DecodeProblem& p, int in_dtype, int out_dtype, int state_dtype, cudaStream_t st);
 // `gate` (a GateMode) travels beside the problem: the chunk kernel takes it as a template
 // argument, so it is not part of the kernel's parameter block.
-cudaError_t launch_serial_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
-                                  cudaStream_t st);
-cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
-                                 void* workspace, size_t ws_bytes, cudaStream_t st);
+cudaError_t launch_serial_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int in_dtype,
+                                  int out_dtype, cudaStream_t st);
+cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int in_dtype,
+                                 int out_dtype, void* workspace, size_t ws_bytes, cudaStream_t st);
 size_t chunk_prefill_workspace(int N, int H);
 
 }  // namespace kda

@@ -25,7 +25,7 @@ __device__ __forceinline__ void stout(__nv_bfloat16* p, size_t i, float x) { p[i
 __device__ __forceinline__ void stout(float* p, size_t i, float x) { p[i] = x; }
 
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, PoolSlots pool, int gate) {
+__global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, PoolSlots pool, int pool_bf16, int gate) {
     const int nblk = kD / NJ;
     const int jb = blockIdx.x % nblk;
     const int h = (blockIdx.x / nblk) % p.H;
@@ -39,14 +39,19 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, PoolSlots poo
     __shared__ float red[2][8][NJ];
 
     const size_t sbase = ((size_t)s * p.H + h) * kD * kD;
-    const float* S0 = p.init ? p.init + sbase : nullptr;
+    int64_t S0 = p.init ? (int64_t)sbase : -1;  // element offset of the initial state (-1: zeros)
     if (pool.init_slots) {
         const int64_t slot = checked_slot(pool.init_slots[s], pool.n_slots, p.status);
-        S0 = slot >= 0 ? p.init + ((size_t)slot * p.H + h) * kD * kD : nullptr;
+        S0 = slot >= 0 ? (slot * p.H + h) * kD * kD : -1;
     }
     float S[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) S[i] = S0 ? S0[(size_t)(w * 16 + i) * kD + j] : 0.f;
+    for (int i = 0; i < 16; ++i) {
+        const size_t e = (size_t)S0 + (size_t)(w * 16 + i) * kD + j;
+        S[i] = S0 < 0 ? 0.f
+             : pool_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.init)[e])
+                         : p.init[e];
+    }
 
     const Tin* q = static_cast<const Tin*>(p.q);
     const Tin* k = static_cast<const Tin*>(p.k);
@@ -108,9 +113,15 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, PoolSlots poo
                 int64_t slot = p.snap_offsets[s] + (t + 1) / p.snap_interval - 1;
                 if (pool.snap_slots) slot = checked_slot(pool.snap_slots[slot], pool.n_slots, p.status);
                 if (slot >= 0 && p.snapshots) {
-                    float* dst = p.snapshots + ((size_t)slot * p.H + h) * kD * kD;
+                    const size_t off = ((size_t)slot * p.H + h) * kD * kD;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[(size_t)(w * 16 + i) * kD + j] = S[i];
+                    for (int i = 0; i < 16; ++i) {
+                        const size_t e = off + (size_t)(w * 16 + i) * kD + j;
+                        if (pool_bf16)
+                            reinterpret_cast<__nv_bfloat16*>(p.snapshots)[e] = __float2bfloat16_rn(S[i]);
+                        else
+                            p.snapshots[e] = S[i];
+                    }
                 }
             }
         }
@@ -123,19 +134,19 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, PoolSlots poo
 
 }  // namespace
 
-cudaError_t launch_serial_prefill(const SeqProblem& p, const PoolSlots& pool, int gate, int in_dtype, int out_dtype,
-                                  cudaStream_t st) {
+cudaError_t launch_serial_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int in_dtype,
+                                  int out_dtype, cudaStream_t st) {
     const int64_t units = (int64_t)p.N * p.H * (kD / NJ);
     if (units == 0) return cudaSuccess;
     const unsigned grid = (unsigned)units;
     if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16)
-        serial_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(p, pool, gate);
+        serial_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(p, pool, pool_bf16 ? 1 : 0, gate);
     else if (in_dtype == KDA_BF16)
-        serial_kernel<__nv_bfloat16, float><<<grid, 256, 0, st>>>(p, pool, gate);
+        serial_kernel<__nv_bfloat16, float><<<grid, 256, 0, st>>>(p, pool, pool_bf16 ? 1 : 0, gate);
     else if (out_dtype == KDA_BF16)
-        serial_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(p, pool, gate);
+        serial_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(p, pool, pool_bf16 ? 1 : 0, gate);
     else
-        serial_kernel<float, float><<<grid, 256, 0, st>>>(p, pool, gate);
+        serial_kernel<float, float><<<grid, 256, 0, st>>>(p, pool, pool_bf16 ? 1 : 0, gate);
     return cudaGetLastError();
 }
 

@@ -137,14 +137,16 @@ def test_pool_validation(L):
 
     P, I64 = ctypes.c_void_p, ctypes.c_int64
 
-    def pool(gate=0, la=16, pool_ptr=16, slots=4, init=None, interval=0, snap_off=None, snap_slots=None):
+    def pool(gate=0, la=16, pool_ptr=16, slots=4, init=None, interval=0, snap_off=None, snap_slots=None, pool_dt=1):
         return L.kda_varlen_fwd_pool(P(16), P(16), P(16), P(la) if la else None, gate, P(16), P(16), 2, 100, 1, 128,
-                                     128, 64, P(pool_ptr) if pool_ptr else None, slots, P(init) if init else None,
+                                     128, 64, P(pool_ptr) if pool_ptr else None, slots, pool_dt,
+                                     P(init) if init else None,
                                      interval, P(snap_off) if snap_off else None,
                                      P(snap_slots) if snap_slots else None, P(16), P(16), 0, 1, None, 0, None)
 
     assert pool(gate=5) == b.KDA_ERR_INVALID_ARG
     assert pool(slots=-1) == b.KDA_ERR_INVALID_ARG
+    assert pool(pool_dt=7) == b.KDA_ERR_INVALID_ARG                       # fp32 or bf16 pools only
     assert pool(interval=64, snap_off=16) == b.KDA_ERR_INVALID_ARG        # snap_slots required
     assert pool(pool_ptr=0, init=16) == b.KDA_ERR_INVALID_ARG             # a pool to read from
     assert pool(gate=b.KDA_GATE_HEAD, la=0) == b.KDA_ERR_INVALID_ARG      # scalar gates required

@@ -143,3 +143,51 @@ def test_out_of_range_slots_are_skipped():
     torch.cuda.synchronize()
     assert torch.equal(o, o_p) and torch.equal(f, f_p)
     assert torch.equal(pool[1], snaps[0])
+
+
+@pytest.mark.parametrize("chunk", [64, 1])
+def test_bf16_pool(chunk):
+    """A bf16 pool: snapshots are the fp32 snapshots rounded to nearest bf16 (bit for bit),
+    initial states are widened exactly, and a request resumed from a bf16 snapshot equals a
+    run started from that snapshot widened to fp32, bit for bit; sampled against the oracle."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    xv = synth.varlen_inputs(LENGTHS, H, seed=818, device="cuda")
+    N = len(LENGTHS)
+    off = kda.kda_snapshot_offsets(xv["cu_seqlens"].cpu(), INTERVAL)
+    n_snap = int(off[-1])
+    init_slots = torch.arange(N, dtype=torch.int64)  # slots 0..N-1: initial states
+    snap_slots = torch.arange(N, N + n_snap, dtype=torch.int64)
+    pool = torch.zeros(N + n_snap, H, 128, 128, dtype=torch.bfloat16, device="cuda")
+    pool[:N] = xv["init_states"].to(torch.bfloat16)
+    o, f = kda.kda_varlen_fwd_pool(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], xv["cu_seqlens"], pool,
+                                   init_slots.cuda(), snap_slots.cuda(), chunk=chunk, snapshot_interval=INTERVAL)
+    o_p, f_p, snaps = kda.kda_varlen_fwd(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], xv["cu_seqlens"],
+                                         pool[:N].float(), chunk=chunk, snapshot_interval=INTERVAL)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    assert torch.equal(o, o_p) and torch.equal(f, f_p)
+    assert torch.equal(pool[N:], snaps.to(torch.bfloat16))
+    assert torch.equal(pool[:N], xv["init_states"].to(torch.bfloat16))  # initial-state slots untouched
+
+    # resume sequence 3 (1500 tokens) from its snapshot after 1024 tokens
+    s, covered = 3, 1024
+    idx, cov = kda.kda_snapshot_lookup(off, s, INTERVAL, covered + 100)
+    assert cov == covered
+    a, b = xv["cu_seqlens"][s].item() + covered, xv["cu_seqlens"][s + 1].item()
+    rest = lambda t: t[a:b].contiguous()
+    cu_r = torch.tensor([0, b - a], dtype=torch.int64, device="cuda")
+    o_r, f_r = kda.kda_varlen_fwd_pool(rest(xv["q"]), rest(xv["k"]), rest(xv["v"]), rest(xv["log_alpha"]),
+                                       rest(xv["beta"]), cu_r, pool, torch.tensor([N + idx], device="cuda"),
+                                       chunk=chunk)
+    o_w, f_w, _ = kda.kda_varlen_fwd(rest(xv["q"]), rest(xv["k"]), rest(xv["v"]), rest(xv["log_alpha"]),
+                                     rest(xv["beta"]), cu_r, pool[N + idx:N + idx + 1].float(), chunk=chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(o_r, o_w) and torch.equal(f_r, f_w)
+    heads = [0, 1]
+    ro, rs = oracle.recurrent(packed_heads(xv["q"], a, b, heads), packed_heads(xv["k"], a, b, heads),
+                              packed_heads(xv["v"], a, b, heads), packed_heads(xv["log_alpha"], a, b, heads),
+                              packed_heads(xv["beta"], a, b, heads), np64(pool[N + idx]))
+    assert_close(packed_heads(o_r, 0, b - a, heads), ro, "resumed from bf16 snapshot: out")
+    assert_close(np64(f_r[0]), rs, "resumed from bf16 snapshot: state")
