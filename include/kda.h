@@ -300,6 +300,15 @@ int64_t kda_snapshot_lookup(const int64_t* offsets_host, int N, int seq, int64_t
  */
 size_t kda_workspace_size(int op, int B, int64_t T, int H, int dk, int dv, int chunk);
 
+/*
+ * Diagnostic of the failure detection every kernel relies on: launches one CTA that waits,
+ * with the library's bounded mbarrier wait, on a barrier nothing arrives at.  After the
+ * wait's deadline (about 2 s) the kernel records KDA_ERR_TIMEOUT in the device status word
+ * and returns; no trap, and the context stays usable.  Read the result with
+ * kda_get_device_status().  Returns KDA_OK once the kernel is enqueued.
+ */
+int kda_selftest_bounded_wait(void* stream);
+
 /* Static, human-readable name of a kda_status value. */
 const char* kda_status_string(int status);
 

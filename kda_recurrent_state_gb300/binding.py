@@ -63,9 +63,10 @@ def lib() -> ctypes.CDLL:
         L.kda_status_string.argtypes = [I]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_get_device_status.argtypes = [P]
+        L.kda_selftest_bounded_wait.argtypes = [P]
         for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
                   L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_varlen_fwd_pool, L.kda_bwd,
-                  L.kda_bwd_noalloc,
+                  L.kda_bwd_noalloc, L.kda_selftest_bounded_wait,
                   L.kda_snapshot_offsets,
                   L.kda_get_device_status):
             f.restype = I
@@ -133,6 +134,13 @@ def kda_snapshot_lookup(offsets_host, seq: int, interval: int, prefix_len: int):
 
 def kda_workspace_size(op: int, B: int, T: int, H: int, dk: int = 128, dv: int = 128, chunk: int = 64) -> int:
     return int(lib().kda_workspace_size(int(op), int(B), int(T), int(H), int(dk), int(dv), int(chunk)))
+
+
+def kda_selftest_bounded_wait(stream=None) -> None:
+    """Launch the bounded-wait diagnostic (about 2 s; afterwards the device status reads
+    KDA_ERR_TIMEOUT)."""
+    st = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(None)
+    _check(lib().kda_selftest_bounded_wait(st), "kda_selftest_bounded_wait")
 
 
 def kda_get_device_status(stream=None) -> int:

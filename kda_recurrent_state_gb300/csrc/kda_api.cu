@@ -1,6 +1,8 @@
 // kda_api.cu -- the C ABI of libkda: host-side validation, the device status
 // word and dispatch to the kernels.  Declarations and the contract of every
 // entry point are in include/kda.h.
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -27,6 +29,14 @@ int* status_ptr() {
     }
     return g_status_addr[dev];
 }
+
+// An NVTX range over one entry point, so that a profiler's timeline shows the library's calls.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -170,6 +180,7 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
                   const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
                   int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
                   void* stream) {
+    NvtxRange nvtx_range("kda_chunk_fwd");
     return chunk_common(q, k, v, log_alpha, kGateChannel, beta, init_state, out, final_state, B, T, H, dk, dv,
                         chunk, in_dtype, out_dtype, workspace, ws_bytes, stream);
 }
@@ -178,6 +189,7 @@ int kda_gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* 
                       const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
                       int dv, int chunk, int in_dtype, int out_dtype, void* workspace, size_t ws_bytes,
                       void* stream) {
+    NvtxRange nvtx_range("kda_gdn_chunk_fwd");
     return chunk_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, init_state, out, final_state,
                         B, T, H, dk, dv, chunk, in_dtype, out_dtype, workspace, ws_bytes, stream);
 }
@@ -229,6 +241,7 @@ int kda_varlen_fwd(const void* q, const void* k, const void* v, const float* log
                    const float* init_states, float* final_states, int64_t snapshot_interval,
                    const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
                    void* workspace, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("kda_varlen_fwd");
     return varlen_common(q, k, v, log_alpha, kGateChannel, beta, cu_seqlens, N, T_total, H, dk, dv, chunk,
                          init_states, final_states, snapshot_interval, snap_offsets, snapshots, out, in_dtype,
                          out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0}, false);
@@ -239,6 +252,7 @@ int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float*
                        const float* init_states, float* final_states, int64_t snapshot_interval,
                        const int64_t* snap_offsets, float* snapshots, void* out, int in_dtype, int out_dtype,
                        void* workspace, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("kda_gdn_varlen_fwd");
     return varlen_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, cu_seqlens, N, T_total, H,
                          dk, dv, chunk, init_states, final_states, snapshot_interval, snap_offsets, snapshots, out,
                          in_dtype, out_dtype, workspace, ws_bytes, stream, PoolSlots{nullptr, nullptr, 0}, false);
@@ -250,6 +264,7 @@ int kda_varlen_fwd_pool(const void* q, const void* k, const void* v, const float
                         int64_t snapshot_interval, const int64_t* snap_offsets, const int64_t* snap_slots,
                         float* final_states, void* out, int in_dtype, int out_dtype, void* workspace,
                         size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("kda_varlen_fwd_pool");
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE) return KDA_ERR_INVALID_ARG;
     if (pool_slots < 0 || !dtype_ok(pool_dtype)) return KDA_ERR_INVALID_ARG;
     if (snapshot_interval > 0 && !snap_slots) return KDA_ERR_INVALID_ARG;
@@ -286,6 +301,7 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
 int kda_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
                     float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
                     void* stream) {
+    NvtxRange nvtx_range("kda_decode_step");
     return decode_common(q, k, v, log_alpha, kGateChannel, beta, state, KDA_F32, out, B, H, dk, dv, in_dtype,
                          out_dtype, stream);
 }
@@ -293,6 +309,7 @@ int kda_decode_step(const void* q, const void* k, const void* v, const float* lo
 int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
                         float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
                         void* stream) {
+    NvtxRange nvtx_range("kda_gdn_decode_step");
     return decode_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, state, KDA_F32, out, B, H,
                          dk, dv, in_dtype, out_dtype, stream);
 }
@@ -300,6 +317,7 @@ int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float
 int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const float* log_alpha,
                               const float* beta, void* state, void* out, int B, int H, int dk, int dv,
                               int in_dtype, int out_dtype, void* stream) {
+    NvtxRange nvtx_range("kda_decode_step_bf16state");
     return decode_common(q, k, v, log_alpha, kGateChannel, beta, state, KDA_BF16, out, B, H, dk, dv, in_dtype,
                          out_dtype, stream);
 }
@@ -308,6 +326,7 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
             const float* init_states, const float* d_out, const float* d_final_states, const int64_t* cu_seqlens,
             int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
             float* dbeta, float* d_init_states, int in_dtype, void* workspace, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("kda_bwd");
     if (N < 0 || T < 0 || H < 0) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype)) return KDA_ERR_INVALID_ARG;
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE) return KDA_ERR_INVALID_ARG;
@@ -338,6 +357,13 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     p.gate = gate == KDA_GATE_CHANNEL ? kGateChannel : gate == KDA_GATE_HEAD ? kGateHead : kGateNone;
     return launch_bwd(p, in_dtype, workspace, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
                                                                                               : KDA_ERR_CUDA;
+}
+
+int kda_selftest_bounded_wait(void* stream) {
+    NvtxRange nvtx_range("kda_selftest_bounded_wait");
+    int* st = status_ptr();
+    if (!st) return KDA_ERR_CUDA;
+    return launch_bounded_wait_selftest(st, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 }  // extern "C"

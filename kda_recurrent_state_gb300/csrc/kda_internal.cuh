@@ -127,5 +127,6 @@ cudaError_t launch_serial_prefill(const SeqProblem& p, const PoolSlots& pool, bo
 cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int in_dtype,
                                  int out_dtype, void* workspace, size_t ws_bytes, cudaStream_t st);
 size_t chunk_prefill_workspace(int N, int H);
+cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st);
 
 }  // namespace kda
