@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 constexpr bool FULL = decltype(full_chunk)::value, REV = decltype(reverse)::value;
                 const int q = REV ? 1 - i : i;
                 const uint8_t* sl = sm + L::OFF_RING + ((4 * n + i) % L::NSLOT) * L::SLOT_BYTES;
-                const float* sla = reinterpret_cast<const float*>(sl + L::SLOT_LA);
+                [[maybe_unused]] const float* sla = reinterpret_cast<const float*>(sl + L::SLOT_LA);  // !SG only
                 const Tin* sk = reinterpret_cast<const Tin*>(sl + L::SLOT_K);
                 const Tin* sq = reinterpret_cast<const Tin*>(sl + L::SLOT_Q);
                 const Tin* sv = reinterpret_cast<const Tin*>(sl + L::SLOT_V);
