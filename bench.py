@@ -151,19 +151,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle (CPU) timing
-def time_oracle_sample(n_heads: int, T_s: int, threads: int, seed: int = 1):
-    """Run the fp64 oracle on n_heads x T_s token-heads of workload-shaped synthetic input."""
+def time_oracle_sample(n_heads: int, T_s: int, threads: int, seed: int = 1, x=None):
+    """Run the fp64 oracle on n_heads x T_s token-heads: the first heads of the given inputs x
+    (B=1 token-major tensors, any device), or of workload-shaped synthetic input.  Returns
+    (seconds, (out [n,T,dv], S_final [n,dk,dv]))."""
     import torch
 
     from kda_recurrent_state_gb300 import synth
     from oracle import oracle
 
-    x = synth.prefill_inputs(1, T_s, n_heads, seed=synth.SEED_BASE + 2 + seed, device="cpu")
-    hm = lambda t: t[0].transpose(0, 1).to(torch.float64).contiguous().numpy()
-    args = (hm(x["q"]), hm(x["k"]), hm(x["v"]), hm(x["log_alpha"]), x["beta"][0].t().to(torch.float64).numpy())
+    if x is None:
+        x = synth.prefill_inputs(1, T_s, n_heads, seed=synth.SEED_BASE + 2 + seed, device="cpu")
+    hm = lambda t: t[0, :T_s, :n_heads].transpose(0, 1).to("cpu", torch.float64).contiguous().numpy()
+    args = (hm(x["q"]), hm(x["k"]), hm(x["v"]), hm(x["log_alpha"]),
+            x["beta"][0, :T_s, :n_heads].t().to("cpu", torch.float64).contiguous().numpy())
     t0 = time.perf_counter()
-    oracle.recurrent(*args, threads=threads)
-    return time.perf_counter() - t0
+    res = oracle.recurrent(*args, threads=threads)
+    return time.perf_counter() - t0, res
 
 
 def cpu_cores():
@@ -173,14 +177,28 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def oracle_baseline(sample_heads=48, sample_T=131072):
+def oracle_baseline(x, out, fin, sample_heads=48, sample_T=131072):
+    """The oracle timed on the first sample_heads heads of the bench's own inputs, and the GPU
+    result of the same heads (out, fin of one prefill launch) compared with it."""
+    import numpy as np
+    import torch
+
     threads = cpu_cores()
-    dt = time_oracle_sample(sample_heads, sample_T, threads)
+    dt, (ro, rs) = time_oracle_sample(sample_heads, sample_T, threads, x=x)
     th_per_s = sample_heads * sample_T / dt
-    return {"value": th_per_s / H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"fp64 per-token recurrence on {sample_heads} heads x {sample_T} tokens of the B=1,H=96,"
-                      f"T=131072 workload ({sample_heads * sample_T} token-heads, {dt:.1f} s); tokens/s = "
+    go = out[0, :sample_T, :sample_heads].transpose(0, 1).to("cpu", torch.float64).numpy()
+    gs = fin[0, :sample_heads].to("cpu", torch.float64).numpy()
+    err = lambda g, r: (float(np.linalg.norm(g - r) / np.linalg.norm(r)), float(np.abs(g - r).max()))
+    (ro_rel, ro_max), (rs_rel, rs_max) = err(go, ro), err(gs, rs)
+    base = {"value": th_per_s / H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 per-token recurrence on heads 0..{sample_heads - 1} x {sample_T} tokens of the bench's "
+                      f"B=1,H=96,T=131072 inputs ({sample_heads * sample_T} token-heads, {dt:.1f} s); tokens/s = "
                       f"token-heads/s / 96 heads"}
+    parity = {"against": "fp64 oracle", "heads": sample_heads, "tokens": sample_T,
+              "out": {"rel_l2": ro_rel, "max_abs": ro_max}, "final_state": {"rel_l2": rs_rel, "max_abs": rs_max},
+              "bar": {"rel_l2": 2e-3, "max_abs": 1e-2},
+              "pass": bool(max(ro_rel, rs_rel) <= 2e-3 and max(ro_max, rs_max) <= 1e-2)}
+    return base, parity
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -375,7 +393,12 @@ def run_ours(args):
         line["gpu_launches"] += args.e2e_steps
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_baseline()
+        # the oracle on heads of this very workload, and the GPU result for them (one more
+        # prefill launch outside any timed region: the buffers were reused above)
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, out, fin, chunk=args.chunk,
+                          workspace=ws)
+        torch.cuda.synchronize()
+        line["cpu_baseline"], line["parity"] = oracle_baseline(x, out, fin)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -431,7 +454,7 @@ def run_reference(args):
     sample_heads, sample_T = 8, 32768
     for _ in range(args.warmup):
         time_oracle_sample(1, 1024, threads)
-    dts = [time_oracle_sample(sample_heads, sample_T, threads, seed=i) for i in range(args.steps)]
+    dts = [time_oracle_sample(sample_heads, sample_T, threads, seed=i)[0] for i in range(args.steps)]
     th = sample_heads * sample_T
     value = th / (sum(dts) / len(dts)) / H
     sample = (f"fp64 per-token recurrence, {sample_heads} heads x {sample_T} tokens of the B=1,H=96,T=131072 "
