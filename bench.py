@@ -194,6 +194,9 @@ def oracle_baseline(x, out, fin, sample_heads=48, sample_T=131072):
             "sample": f"fp64 per-token recurrence on heads 0..{sample_heads - 1} x {sample_T} tokens of the bench's "
                       f"B=1,H=96,T=131072 inputs ({sample_heads * sample_T} token-heads, {dt:.1f} s); tokens/s = "
                       f"token-heads/s / 96 heads"}
+    dt1, _ = time_oracle_sample(1, 8192, 1, x=x)  # one thread on a 1-head slice
+    base["single_core"] = {"value": 8192 / dt1 / H, "unit": "tokens/s", "cores": 1,
+                           "sample": f"head 0 x 8192 tokens on one thread ({dt1:.2f} s), extrapolated to 96 heads"}
     parity = {"against": "fp64 oracle", "heads": sample_heads, "tokens": sample_T,
               "out": {"rel_l2": ro_rel, "max_abs": ro_max}, "final_state": {"rel_l2": rs_rel, "max_abs": rs_max},
               "bar": {"rel_l2": 2e-3, "max_abs": 1e-2},
