@@ -190,6 +190,10 @@ int kda_gdn_varlen_fwd(const void* q, const void* k, const void* v, const float*
 int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
                         float* state, void* out, int B, int H, int dk, int dv, int in_dtype, int out_dtype,
                         void* stream);
+/* kda_gdn_decode_step with the state stored in bf16, as in kda_decode_step_bf16state. */
+int kda_gdn_decode_step_bf16state(const void* q, const void* k, const void* v, const float* log_alpha,
+                                  const float* beta, void* state, void* out, int B, int H, int dk, int dv,
+                                  int in_dtype, int out_dtype, void* stream);
 
 /*
  * Packed variable-length prefill over a caller-owned STATE POOL, for prefix reuse in

@@ -49,6 +49,7 @@ def lib() -> ctypes.CDLL:
         L.kda_gdn_chunk_fwd.argtypes = L.kda_chunk_fwd.argtypes
         L.kda_gdn_varlen_fwd.argtypes = L.kda_varlen_fwd.argtypes
         L.kda_gdn_decode_step.argtypes = L.kda_decode_step.argtypes
+        L.kda_gdn_decode_step_bf16state.argtypes = L.kda_decode_step.argtypes
         L.kda_bwd.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P, SZ, P]
         L.kda_bwd_noalloc.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P]
         L.kda_varlen_fwd_pool.argtypes = [P, P, P, P, I, P, P, I, I64, I, I, I, I, P, I64, I, P, I64, P, P, P, P, I,
@@ -66,7 +67,7 @@ def lib() -> ctypes.CDLL:
         L.kda_selftest_bounded_wait.argtypes = [P]
         for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
                   L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_varlen_fwd_pool, L.kda_bwd,
-                  L.kda_bwd_noalloc, L.kda_selftest_bounded_wait,
+                  L.kda_bwd_noalloc, L.kda_selftest_bounded_wait, L.kda_gdn_decode_step_bf16state,
                   L.kda_snapshot_offsets,
                   L.kda_get_device_status):
             f.restype = I
@@ -290,6 +291,12 @@ def kda_decode_step_bf16state(q, k, v, log_alpha, beta, state, out=None, *, out_
     itself runs in fp32 and the output is read before the state is rounded)."""
     return _decode(lib().kda_decode_step_bf16state, "kda_decode_step_bf16state", torch.bfloat16, q, k, v, log_alpha,
                    beta, state, out, out_dtype)
+
+
+def kda_gdn_decode_step_bf16state(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=torch.float32):
+    """kda_gdn_decode_step with a bf16-stored state (fp32 arithmetic)."""
+    return _decode(lib().kda_gdn_decode_step_bf16state, "kda_gdn_decode_step_bf16state", torch.bfloat16, q, k, v,
+                   log_alpha, beta, state, out, out_dtype)
 
 
 def kda_gdn_decode_step(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=torch.float32):

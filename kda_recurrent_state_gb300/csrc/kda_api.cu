@@ -314,6 +314,14 @@ int kda_gdn_decode_step(const void* q, const void* k, const void* v, const float
                          dk, dv, in_dtype, out_dtype, stream);
 }
 
+int kda_gdn_decode_step_bf16state(const void* q, const void* k, const void* v, const float* log_alpha,
+                                  const float* beta, void* state, void* out, int B, int H, int dk, int dv,
+                                  int in_dtype, int out_dtype, void* stream) {
+    NvtxRange nvtx_range("kda_gdn_decode_step_bf16state");
+    return decode_common(q, k, v, log_alpha, log_alpha ? kGateHead : kGateNone, beta, state, KDA_BF16, out, B, H,
+                         dk, dv, in_dtype, out_dtype, stream);
+}
+
 int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const float* log_alpha,
                               const float* beta, void* state, void* out, int B, int H, int dk, int dv,
                               int in_dtype, int out_dtype, void* stream) {

@@ -178,3 +178,39 @@ def test_full_size_sampled():
     assert_close(batch_heads(out[:, -t_s:], [(0, 17)]), ro_all[:, -t_s:], "tail out")
     assert_close(np64(fin[0, 17])[None], rs_all, "final state")
     assert kda.kda_get_device_status() == 0
+
+
+@pytest.mark.parametrize("deltanet", [False, True], ids=["gdn", "deltanet"])
+def test_decode_bf16state(deltanet):
+    """Scalar-gate decode on a bf16-stored state: bit for bit the per-channel bf16-state decode
+    fed the broadcast gate, and against the rounding oracle."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    B, H, steps = 4, 3, 5
+    d = synth.decode_inputs(B, H, seed=631, steps=steps, device="cuda")
+    la_h = None if deltanet else synth.head_gates((steps, B), H, seed=632, device="cuda")
+    s1 = d["state"].to(torch.bfloat16)
+    s0, s2 = s1.clone(), s1.clone()
+    outs = []
+    for s in range(steps):
+        g = None if deltanet else la_h[s]
+        gc = torch.zeros_like(d["log_alpha"][s]) if deltanet else _bcast(la_h[s])
+        o1 = kda.kda_gdn_decode_step_bf16state(d["q"][s], d["k"][s], d["v"][s], g, d["beta"][s], s1)
+        o2 = kda.kda_decode_step_bf16state(d["q"][s], d["k"][s], d["v"][s], gc, d["beta"][s], s2)
+        outs.append(o1)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2)
+    assert torch.equal(s1, s2)
+    pairs = [(b, h) for b in range(B) for h in range(H)]
+    la = torch.zeros(steps, B, H, 128, device="cuda") if deltanet else _bcast(la_h)
+    col = lambda t, b, h: np64(t[:steps, b, h])
+    ro, rs = oracle.recurrent_bf16state(np.stack([col(d["q"], b, h) for b, h in pairs]),
+                                        np.stack([col(d["k"], b, h) for b, h in pairs]),
+                                        np.stack([col(d["v"], b, h) for b, h in pairs]),
+                                        np.stack([col(la, b, h) for b, h in pairs]),
+                                        np.stack([col(d["beta"], b, h) for b, h in pairs]),
+                                        np.stack([np64(s0[b, h]) for b, h in pairs]))
+    got = np.stack([np.stack([np64(outs[s][b, h]) for s in range(steps)]) for b, h in pairs])
+    assert_close(got, ro, "decode out")
+    assert_close(np.stack([np64(s1[b, h]) for b, h in pairs]), rs, "decode state")
