@@ -91,9 +91,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
     auto img = [&](float* base, int jj) -> float* { return base + (size_t)(c * 32 + jj) * kD + i; };
     int par = 0;  // parity of the column-partial buffer (the same sequence of steps in every warp)
 
-    float S[32], dS[32];
+    // S and dS of this thread's row, value columns in pairs (2p, 2p+1): the element-wise
+    // work runs on packed fp32 pairs
+    float2 S[16], dS[16];
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) S[jj] = P.init ? P.init[sbase + (size_t)i * kD + c * 32 + jj] : 0.f;
+    for (int p = 0; p < 16; ++p)
+        S[p] = P.init ? *reinterpret_cast<const float2*>(P.init + sbase + (size_t)i * kD + c * 32 + 2 * p)
+                      : make_float2(0.f, 0.f);
 
     // inputs of tokens [p0, p0 + n) of the sequence into shared memory
     auto stage = [&](int64_t p0, int n, bool with_dout) {
@@ -128,13 +132,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
     // one forward step on S (token tl of the staged piece); with `keep`, also S_{t-1}
     // into the scratch and e, u into shared memory for the backward steps
     auto fwd_step = [&](int tl, float* keep) {
-        const float ai = sm.a[tl][i], ki = sm.k[tl][i];
+        const float2 a2 = make_float2(sm.a[tl][i], sm.a[tl][i]), k2 = make_float2(sm.k[tl][i], sm.k[tl][i]);
         float x[32];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            if (keep) *img(keep, jj) = S[jj];
-            S[jj] *= ai;
-            x[jj] = ki * S[jj];
+        for (int p = 0; p < 16; ++p) {
+            if (keep) {
+                *img(keep, 2 * p) = S[p].x;
+                *img(keep, 2 * p + 1) = S[p].y;
+            }
+            S[p] = __fmul2_rn(S[p], a2);
+            const float2 kx = __fmul2_rn(S[p], k2);
+            x[2 * p] = kx.x;
+            x[2 * p + 1] = kx.y;
         }
         const int j = 32 * c + lane;
         const float e = sm.v[tl][j] - col_sum(x);
@@ -144,24 +153,34 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
             sm.u[tl][j] = u;
         }
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] += ki * __shfl_sync(0xffffffffu, u, jj);
+        for (int p = 0; p < 16; ++p) {
+            const float2 u2 = make_float2(__shfl_sync(0xffffffffu, u, 2 * p), __shfl_sync(0xffffffffu, u, 2 * p + 1));
+            S[p] = __ffma2_rn(k2, u2, S[p]);
+        }
     };
     // one backward step for token tl of the staged piece (token `pos` of the sequence);
     // row partials go to sm.rs / sm.bpart and are combined once per piece
     auto bwd_step = [&](int tl, int64_t pos) {
         const size_t r = (size_t)(t0 + pos) * P.H + h;
+        float* stt = st + (size_t)tl * BLK;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] = *img(st + (size_t)tl * BLK, jj);  // S_{t-1}
+        for (int p = 0; p < 16; ++p) S[p] = make_float2(*img(stt, 2 * p), *img(stt, 2 * p + 1));  // S_{t-1}
         const float ai = sm.a[tl][i], ki = sm.k[tl][i], qi = sm.q[tl][i];
-        float dq = 0.f, x[32];
+        const float2 a2 = make_float2(ai, ai), k2 = make_float2(ki, ki), q2 = make_float2(qi, qi);
+        const float2* dout2 = reinterpret_cast<const float2*>(&sm.dout[tl][32 * c]);
+        const float2* u2s = reinterpret_cast<const float2*>(&sm.u[tl][32 * c]);
+        float2 dq2 = make_float2(0.f, 0.f);
+        float x[32];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int j = 32 * c + jj;
-            const float doj = sm.dout[tl][j];
-            dS[jj] += qi * doj;
-            dq += (ai * S[jj] + ki * sm.u[tl][j]) * doj;
-            x[jj] = dS[jj] * ki;
+        for (int p = 0; p < 16; ++p) {
+            const float2 do2 = dout2[p];
+            dS[p] = __ffma2_rn(q2, do2, dS[p]);
+            dq2 = __ffma2_rn(__ffma2_rn(k2, u2s[p], __fmul2_rn(a2, S[p])), do2, dq2);  // S_t do
+            const float2 kx = __fmul2_rn(dS[p], k2);
+            x[2 * p] = kx.x;
+            x[2 * p + 1] = kx.y;
         }
+        const float dq = dq2.x + dq2.y;
         const int j = 32 * c + lane;
         const float du = col_sum(x);
         const float b = sm.beta[tl];
@@ -173,15 +192,17 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
             for (int o = 16; o > 0; o >>= 1) bp += __shfl_xor_sync(0xffffffffu, bp, o);
             if (lane == 0) sm.bpart[tl][c] = bp;
         }
-        float dk = 0.f, da = 0.f;
+        float2 dk2 = make_float2(0.f, 0.f), da2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const float dpj = __shfl_sync(0xffffffffu, dp, jj);
-            dk += dS[jj] * sm.u[tl][32 * c + jj] + (ai * S[jj]) * dpj;
-            const float dsp = dS[jj] + ki * dpj;
-            da += dsp * S[jj];
-            dS[jj] = ai * dsp;
+        for (int p = 0; p < 16; ++p) {
+            const float2 dp2 = make_float2(__shfl_sync(0xffffffffu, dp, 2 * p), __shfl_sync(0xffffffffu, dp, 2 * p + 1));
+            dk2 = __ffma2_rn(dS[p], u2s[p], dk2);
+            dk2 = __ffma2_rn(__fmul2_rn(a2, S[p]), dp2, dk2);
+            const float2 dsp = __ffma2_rn(k2, dp2, dS[p]);
+            da2 = __ffma2_rn(dsp, S[p], da2);
+            dS[p] = __fmul2_rn(a2, dsp);
         }
+        const float dk = dk2.x + dk2.y, da = da2.x + da2.y;
         sm.rs[tl][c][0][i] = dq;
         sm.rs[tl][c][1][i] = dk;
         sm.rs[tl][c][2][i] = ai * da;
@@ -224,7 +245,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
         if (t % SEG == 0) {
             float* ck = ckpt + (size_t)(slot0 + t / SEG) * BLK;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) *img(ck, jj) = S[jj];
+            for (int p = 0; p < 16; ++p) {
+                *img(ck, 2 * p) = S[p].x;
+                *img(ck, 2 * p + 1) = S[p].y;
+            }
         }
         stage(t, n, false);
         for (int tl = 0; tl < n; ++tl) fwd_step(tl, nullptr);
@@ -232,18 +256,23 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
 
     // reverse sweep
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) dS[jj] = P.dfinal ? P.dfinal[sbase + (size_t)i * kD + c * 32 + jj] : 0.f;
+    for (int p = 0; p < 16; ++p)
+        dS[p] = P.dfinal ? *reinterpret_cast<const float2*>(P.dfinal + sbase + (size_t)i * kD + c * 32 + 2 * p)
+                         : make_float2(0.f, 0.f);
     const int64_t nseg = (len + SEG - 1) / SEG;
     for (int64_t g = nseg - 1; g >= 0; --g) {
         const int64_t seg0 = g * SEG;
         const int seg_len = (int)((len - seg0) < SEG ? (len - seg0) : SEG);
         const int nsub = (seg_len + SUB - 1) / SUB;
-        const float* ck = ckpt + (size_t)(slot0 + g) * BLK;
+        float* ck = ckpt + (size_t)(slot0 + g) * BLK;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) S[jj] = *img(const_cast<float*>(ck), jj);
+        for (int p = 0; p < 16; ++p) S[p] = make_float2(*img(ck, 2 * p), *img(ck, 2 * p + 1));
         for (int m = 0; m < nsub; ++m) {  // S every SUB tokens of the segment
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) *img(sub + (size_t)m * BLK, jj) = S[jj];
+            for (int p = 0; p < 16; ++p) {
+                *img(sub + (size_t)m * BLK, 2 * p) = S[p].x;
+                *img(sub + (size_t)m * BLK, 2 * p + 1) = S[p].y;
+            }
             if (m + 1 < nsub) {
                 stage(seg0 + m * SUB, SUB, false);
                 for (int tl = 0; tl < SUB; ++tl) fwd_step(tl, nullptr);
@@ -252,8 +281,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
         for (int m = nsub - 1; m >= 0; --m) {
             const int64_t p0 = seg0 + m * SUB;
             const int n = (int)((seg0 + seg_len - p0) < SUB ? (seg0 + seg_len - p0) : SUB);
+            float* sm_ = sub + (size_t)m * BLK;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] = *img(sub + (size_t)m * BLK, jj);
+            for (int p = 0; p < 16; ++p) S[p] = make_float2(*img(sm_, 2 * p), *img(sm_, 2 * p + 1));
             stage(p0, n, true);
             for (int tl = 0; tl < n; ++tl) fwd_step(tl, st + (size_t)tl * BLK);
             wg_sync(c);  // e, u of the piece (written by warp 0 of the block) before they are read
@@ -263,7 +293,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
     }
     if (P.dinit) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) P.dinit[sbase + (size_t)i * kD + c * 32 + jj] = dS[jj];
+        for (int p = 0; p < 16; ++p) *reinterpret_cast<float2*>(P.dinit + sbase + (size_t)i * kD + c * 32 + 2 * p) = dS[p];
     }
 }
 
