@@ -272,6 +272,30 @@ int kda_bwd_noalloc(const void* q, const void* k, const void* v, const float* lo
                     const int64_t* cu_seqlens, int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out,
                     float* dv_out, float* dlog_alpha, float* dbeta, float* d_init_states, int in_dtype, void* stream);
 
+/*
+ * kda_chunk_fwd (chunk = 64) on HOST buffers, streamed: the sequence is cut into segments
+ * of segment_tokens tokens (a multiple of 64; 0 selects 4096), and each segment's
+ * host-to-device copy, kernel and device-to-host copy run on three streams (two created
+ * for the call, plus `stream` for the kernels), so that the copies of one segment overlap
+ * the work on its neighbours.  Segments start at chunk boundaries, where a resumed run
+ * reproduces the unsplit one bit for bit: the results equal kda_chunk_fwd's.
+ *   q, k, v, log_alpha, beta, out: HOST pointers in kda_chunk_fwd's [B, T, H, ..] layouts;
+ *               page-locked memory is needed for the copies to overlap (pageable memory
+ *               works, serialised).  Must stay valid and unmodified until `stream` has
+ *               passed the call.
+ *   init_state  DEVICE [B, H, dk, dv] float32 or NULL (zeros), 16-byte aligned.
+ *   final_state HOST [B, H, dk, dv] float32 or NULL.
+ *   workspace   DEVICE, at least kda_host_fwd_workspace_size(...) bytes, 16-byte aligned:
+ *               two segments of staging and two states.
+ * The call returns once everything is enqueued; it is complete when `stream` reaches it.
+ */
+int kda_chunk_fwd_host(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                       const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
+                       int dv, int in_dtype, int out_dtype, int64_t segment_tokens, void* workspace, size_t ws_bytes,
+                       void* stream);
+size_t kda_host_fwd_workspace_size(int B, int H, int dk, int dv, int64_t segment_tokens, int in_dtype,
+                                   int out_dtype);
+
 /* Number of snapshots of a sequence: floor(seqlen / interval); 0 if interval <= 0 or seqlen < 0. */
 int64_t kda_snapshot_count(int64_t seqlen, int64_t interval);
 

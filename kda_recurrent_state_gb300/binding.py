@@ -50,6 +50,9 @@ def lib() -> ctypes.CDLL:
         L.kda_gdn_varlen_fwd.argtypes = L.kda_varlen_fwd.argtypes
         L.kda_gdn_decode_step.argtypes = L.kda_decode_step.argtypes
         L.kda_gdn_decode_step_bf16state.argtypes = L.kda_decode_step.argtypes
+        L.kda_chunk_fwd_host.argtypes = [P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I64, P, SZ, P]
+        L.kda_host_fwd_workspace_size.argtypes = [I, I, I, I, I64, I, I]
+        L.kda_host_fwd_workspace_size.restype = SZ
         L.kda_bwd.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P, SZ, P]
         L.kda_bwd_noalloc.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P]
         L.kda_varlen_fwd_pool.argtypes = [P, P, P, P, I, P, P, I, I64, I, I, I, I, P, I64, I, P, I64, P, P, P, P, I,
@@ -68,6 +71,7 @@ def lib() -> ctypes.CDLL:
         for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
                   L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_varlen_fwd_pool, L.kda_bwd,
                   L.kda_bwd_noalloc, L.kda_selftest_bounded_wait, L.kda_gdn_decode_step_bf16state,
+                  L.kda_chunk_fwd_host,
                   L.kda_snapshot_offsets,
                   L.kda_get_device_status):
             f.restype = I
@@ -178,6 +182,32 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, out=None, final_sta
     beta [B,T,H] fp32, init_state [B,H,dk,dv] fp32 or None.  Returns (out, final_state)."""
     return _chunk("kda_chunk_fwd", q, k, v, log_alpha, beta, init_state, out, final_state, chunk, out_dtype,
                   return_final_state, workspace)
+
+
+def kda_chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, out=None, final_state=None, *,
+                       out_dtype=torch.float32, segment_tokens: int = 0, workspace=None, device=None):
+    """kda_chunk_fwd on HOST tensors (CPU; page-locked for overlap), streamed through the GPU
+    in segments.  init_state is a device tensor or None; out and final_state are host tensors
+    (allocated pinned if None).  Returns (out, final_state) once the call is enqueued on the
+    current stream of `device` (cuda:0 by default); synchronise before reading them."""
+    for t in (q, k, v, log_alpha, beta):
+        if t.is_cuda:
+            raise ValueError("kda_chunk_fwd_host takes host tensors")
+    dev = torch.device(device or "cuda")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, T, H, dv, dtype=out_dtype, pin_memory=True)
+    if final_state is None:
+        final_state = torch.empty(B, H, dk, dv, dtype=torch.float32, pin_memory=True)
+    if workspace is None:
+        need = lib().kda_host_fwd_workspace_size(B, H, dk, dv, int(segment_tokens), _dt(q), _dt(out))
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
+    rc = lib().kda_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state), _ptr(out),
+                                  _ptr(final_state), B, T, H, dk, dv, _dt(q), _dt(out), int(segment_tokens),
+                                  _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(rc, "kda_chunk_fwd_host")
+    return out, final_state
 
 
 def kda_gdn_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, out=None, final_state=None, *, chunk: int = 64,

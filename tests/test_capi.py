@@ -195,6 +195,25 @@ def test_bwd_noalloc_rejects_oversize(L):
     assert "static" in b.kda_status_string(rc)
 
 
+def test_host_fwd_validation(L):
+    from kda_recurrent_state_gb300 import binding as b
+
+    P = ctypes.c_void_p
+    need = L.kda_host_fwd_workspace_size(1, 2, 128, 128, 256, 0, 1)
+    # two segments of staging (bf16 q, k, v; fp32 gates, beta, out) and two fp32 states
+    assert need == 2 * (256 * 2 * (3 * 256 + 512 + 4 + 512)) + 2 * 2 * 65536
+    ptr = P(16)
+
+    def call(seg=256, ws=0x10000, ws_bytes=need, T=100):
+        return L.kda_chunk_fwd_host(ptr, ptr, ptr, ptr, ptr, None, ptr, None, 1, T, 2, 128, 128, 0, 1, seg,
+                                    P(ws) if ws else None, ws_bytes, None)
+
+    assert call(seg=100) == b.KDA_ERR_INVALID_ARG       # not a multiple of the chunk
+    assert call(ws=None) == b.KDA_ERR_WORKSPACE
+    assert call(ws_bytes=need - 1) == b.KDA_ERR_WORKSPACE
+    assert call(ws=0x10008) == b.KDA_ERR_MISALIGNED
+
+
 def test_workspace_size(L):
     from kda_recurrent_state_gb300 import binding as b
 
