@@ -300,7 +300,7 @@ def run_ours(args):
                      "frac_of_hbm": gbytes / gt / 1e9 / peaks["hbm_gbs"],
                      "workload": f"B={B} H={H} T={T}, bf16 q/k/v, "
                                  + ("one fp32 log-decay per token-head" if gate_b else "no decay") + f", {args.out_dtype} out"}
-        line["gpu_launches"] += 7
+        line["gpu_launches"] += 5  # timed launches only (warm-ups excluded)
     assert kda.kda_get_device_status() == 0, "device status raised by the scalar-gate prefill"
     del la_h
 
@@ -327,7 +327,7 @@ def run_ours(args):
                                   "frac": dgbs / peaks["hbm_gbs"]},
                      "workload": f"256 sessions x 96 heads, {'fp32' if state_bytes == 4 else 'bf16'} state in "
                                  f"place, 64 steps, bf16 q/k/v, fp32 out"}
-        line["gpu_launches"] += DEC_STEPS + 3
+        line["gpu_launches"] += DEC_STEPS
         del st
     del d, dout
 
@@ -361,7 +361,7 @@ def run_ours(args):
                       "workload": f"16 packed sequences ({ttot} tokens, log-uniform 1024..65536), H=64, chunk 64, "
                                   f"8 resumed from a state, {int(vsnaps.shape[0])} snapshots every 16384 tokens, "
                                   f"fp32 out"}
-    line["gpu_launches"] += 8
+    line["gpu_launches"] += 5
     del xv, vout, vfin, vsnaps
 
     # ---- backward (training) at B=4, H=32, T=8192: token-serial reverse mode on CUDA cores,
@@ -386,7 +386,7 @@ def run_ours(args):
                                 "peak_source": "152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz (nominal)"},
                    "workload": "kda_bwd B=4 H=32 T=8192, bf16 q/k/v, fp32 gates/state/cotangents, "
                                "S0 ~ N(0,0.02); flops = 22 dk dv per token-head"}
-    line["gpu_launches"] += 3
+    line["gpu_launches"] += 2
     assert kda.kda_get_device_status() == 0, "device status raised by the backward"
     del xb, do, ws_b
 
