@@ -299,7 +299,8 @@ def run_ours(args):
         line[key] = {"tokens_per_s": B * T / gt, "ms_per_call": gt * 1e3, "GB_per_s": gbytes / gt / 1e9,
                      "frac_of_hbm": gbytes / gt / 1e9 / peaks["hbm_gbs"],
                      "workload": f"B={B} H={H} T={T}, bf16 q/k/v, "
-                                 + ("one fp32 log-decay per token-head" if gate_b else "no decay") + f", {args.out_dtype} out"}
+                                 + ("one fp32 log-decay per token-head" if gate_b else "no decay")
+                                 + f", {args.out_dtype} out"}
         line["gpu_launches"] += 5  # timed launches only (warm-ups excluded)
     assert kda.kda_get_device_status() == 0, "device status raised by the scalar-gate prefill"
     del la_h

@@ -281,7 +281,8 @@ def kda_varlen_fwd_pool(q, k, v, log_alpha, beta, cu_seqlens, pool, init_slots=N
     ws, ws_bytes = _workspace(KDA_OP_VARLEN, N, Ttot, H, dk, dv, chunk, q.device, workspace)
     rc = lib().kda_varlen_fwd_pool(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), int(gate), _ptr(beta),
                                    _ptr(cu_seqlens), N, Ttot, H, dk, dv, int(chunk), _ptr(pool), pool.shape[0],
-                                   _dt(pool), _ptr(init_slots), int(snapshot_interval), _ptr(snap_off), _ptr(snap_slots),
+                                   _dt(pool), _ptr(init_slots), int(snapshot_interval), _ptr(snap_off),
+                                   _ptr(snap_slots),
                                    _ptr(final_states), _ptr(out), _dt(q), _dt(out), _ptr(ws), ws_bytes,
                                    _stream(q.device))
     _check(rc, "kda_varlen_fwd_pool")

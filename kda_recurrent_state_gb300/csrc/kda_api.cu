@@ -52,8 +52,9 @@ int check_common(int dk, int dv, int chunk, int in_dtype, int out_dtype) {
 
 int run_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int chunk, int in_dtype,
                 int out_dtype, void* ws, size_t ws_bytes, cudaStream_t st) {
-    cudaError_t e = (chunk == 1) ? launch_serial_prefill(p, pool, pool_bf16, gate, in_dtype, out_dtype, st)
-                                 : launch_chunk_prefill(p, pool, pool_bf16, gate, in_dtype, out_dtype, ws, ws_bytes, st);
+    cudaError_t e = chunk == 1
+                        ? launch_serial_prefill(p, pool, pool_bf16, gate, in_dtype, out_dtype, st)
+                        : launch_chunk_prefill(p, pool, pool_bf16, gate, in_dtype, out_dtype, ws, ws_bytes, st);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -74,7 +75,8 @@ const char* kda_status_string(int status) {
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel expired";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
         case KDA_STATUS_GATE_RANGE: return "KDA_STATUS_GATE_RANGE: a half-chunk's summed log-decay is below -15 ln 2";
-        case KDA_STATUS_SLOT_RANGE: return "KDA_STATUS_SLOT_RANGE: a state-pool slot index was out of range and skipped";
+        case KDA_STATUS_SLOT_RANGE:
+            return "KDA_STATUS_SLOT_RANGE: a state-pool slot index was out of range and skipped";
         case KDA_ERR_SCRATCH_TOO_SMALL:
             return "KDA_ERR_SCRATCH_TOO_SMALL: the problem needs more scratch than the library's static 128 MiB";
         default: return "unknown kda status";

@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
         float2 dk2 = make_float2(0.f, 0.f), da2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int p = 0; p < 16; ++p) {
-            const float2 dp2 = make_float2(__shfl_sync(0xffffffffu, dp, 2 * p), __shfl_sync(0xffffffffu, dp, 2 * p + 1));
+            const float2 dp2 =
+                make_float2(__shfl_sync(0xffffffffu, dp, 2 * p), __shfl_sync(0xffffffffu, dp, 2 * p + 1));
             dk2 = __ffma2_rn(dS[p], u2s[p], dk2);
             dk2 = __ffma2_rn(__fmul2_rn(a2, S[p]), dp2, dk2);
             const float2 dsp = __ffma2_rn(k2, dp2, dS[p]);
@@ -293,7 +294,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
     }
     if (P.dinit) {
 #pragma unroll
-        for (int p = 0; p < 16; ++p) *reinterpret_cast<float2*>(P.dinit + sbase + (size_t)i * kD + c * 32 + 2 * p) = dS[p];
+        for (int p = 0; p < 16; ++p)
+            *reinterpret_cast<float2*>(P.dinit + sbase + (size_t)i * kD + c * 32 + 2 * p) = dS[p];
     }
 }
 

@@ -62,8 +62,8 @@ extern "C" int kda_chunk_fwd_host(const void* q, const void* k, const void* v, c
     if (T > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
     const size_t need = kda_host_fwd_workspace_size(B, H, dk, dv, L, in_dtype, out_dtype);
     if (!workspace || ws_bytes < need) return KDA_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) || (init_state && (reinterpret_cast<uintptr_t>(init_state) & 15u)))
-        return KDA_ERR_MISALIGNED;
+    const bool ws_misaligned = (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0;
+    if (ws_misaligned || (init_state && (reinterpret_cast<uintptr_t>(init_state) & 15u))) return KDA_ERR_MISALIGNED;
 
     const int es = in_dtype == KDA_BF16 ? 2 : 4, oes = out_dtype == KDA_BF16 ? 2 : 4;
     const SegLayout lay = seg_layout(B, H, L, es, oes);
@@ -103,20 +103,21 @@ extern "C" int kda_chunk_fwd_host(const void* q, const void* k, const void* v, c
         uint8_t* buf = ws + b * lay.bytes;
         // host -> device: one 2-D copy per tensor (rows = batch entries of the segment)
         auto h2d = [&](size_t off, const void* src, size_t row) {
-            return chk(cudaMemcpy2DAsync(buf + off, (size_t)Ls * row, static_cast<const uint8_t*>(src) + (size_t)s0 * row,
-                                         (size_t)T * row, (size_t)Ls * row, (size_t)B, cudaMemcpyHostToDevice, hs));
+            const uint8_t* from = static_cast<const uint8_t*>(src) + (size_t)s0 * row;
+            return chk(cudaMemcpy2DAsync(buf + off, (size_t)Ls * row, from, (size_t)T * row, (size_t)Ls * row, (size_t)B,
+                                         cudaMemcpyHostToDevice, hs));
         };
         if (s >= 2 && !chk(cudaStreamWaitEvent(hs, comp_done[b], 0))) break;
-        if (!(h2d(lay.q, q, row_in) && h2d(lay.k, k, row_in) && h2d(lay.v, v, row_in) && h2d(lay.la, log_alpha, row_la) &&
-              h2d(lay.beta, beta, row_b) && chk(cudaEventRecord(in_ready[b], hs))))
+        if (!(h2d(lay.q, q, row_in) && h2d(lay.k, k, row_in) && h2d(lay.v, v, row_in) &&
+              h2d(lay.la, log_alpha, row_la) && h2d(lay.beta, beta, row_b) && chk(cudaEventRecord(in_ready[b], hs))))
             break;
         // the kernel, on the caller's stream
         if (!chk(cudaStreamWaitEvent(cs, in_ready[b], 0))) break;
         if (s >= 2 && !chk(cudaStreamWaitEvent(cs, out_done[b], 0))) break;
+        const float* s_in = s == 0 ? init_state : states[(s - 1) & 1];
         const int r = kda_chunk_fwd(buf + lay.q, buf + lay.k, buf + lay.v, reinterpret_cast<const float*>(buf + lay.la),
-                                    reinterpret_cast<const float*>(buf + lay.beta), s == 0 ? init_state : states[(s - 1) & 1],
-                                    buf + lay.out, states[s & 1], B, Ls, H, dk, dv, 64, in_dtype, out_dtype, nullptr, 0,
-                                    stream);
+                                    reinterpret_cast<const float*>(buf + lay.beta), s_in, buf + lay.out, states[s & 1],
+                                    B, Ls, H, dk, dv, 64, in_dtype, out_dtype, nullptr, 0, stream);
         if (r != KDA_OK) {
             rc = r;
             break;

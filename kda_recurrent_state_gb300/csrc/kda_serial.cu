@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(256) serial_kernel(SeqProblem p, PoolSlots poo
             const int r = idx / NJ, c = idx % NJ;
             if (r < nt) sv[r][c] = ldin(v, ((size_t)(t0 + tb + r) * p.H + h) * kD + jb * NJ + c);
         }
-        if (threadIdx.x < TB && (int)threadIdx.x < nt) sb[threadIdx.x] = p.beta[(size_t)(t0 + tb + threadIdx.x) * p.H + h];
+        if (threadIdx.x < TB && (int)threadIdx.x < nt)
+            sb[threadIdx.x] = p.beta[(size_t)(t0 + tb + threadIdx.x) * p.H + h];
         __syncthreads();
 
         for (int r = 0; r < nt; ++r) {
