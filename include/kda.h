@@ -210,10 +210,10 @@ int kda_gdn_decode_step_bf16state(const void* q, const void* k, const void* v, c
  *               the pool's memory; the arithmetic stays fp32.
  *   init_slots  device int64 [N] or NULL: sequence s starts from slot init_slots[s]
  *               (-1: zero state).  NULL: every sequence starts from zeros.
- *   snap_slots  device int64 [snap_offsets[N]], required when snapshot_interval > 0:
- *               snapshot m of sequence s (as in kda_varlen_fwd) is stored into slot
- *               snap_slots[snap_offsets[s] + m - 1]; -1 means "not stored" (for example
- *               because that prefix is already in the pool).
+ *   snap_slots  device int64 [snap_offsets[N]]: snapshot m of sequence s (as in
+ *               kda_varlen_fwd) is stored into slot snap_slots[snap_offsets[s] + m - 1];
+ *               -1 means "not stored" (for example because that prefix is already in
+ *               the pool).  NULL stores no snapshot (as when there are none to store).
  * final_states stays a dense [N, H, dk, dv] array.  Snapshot slots written by one call
  * must be distinct, and no slot written by a call may be an initial-state slot of the
  * same call.  A slot index outside [-1, pool_slots) is not dereferenced: the state is

@@ -269,7 +269,7 @@ int kda_varlen_fwd_pool(const void* q, const void* k, const void* v, const float
     NvtxRange nvtx_range("kda_varlen_fwd_pool");
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE) return KDA_ERR_INVALID_ARG;
     if (pool_slots < 0 || !dtype_ok(pool_dtype)) return KDA_ERR_INVALID_ARG;
-    if (snapshot_interval > 0 && !snap_slots) return KDA_ERR_INVALID_ARG;
+    if (snapshot_interval > 0 && !snap_slots) snapshot_interval = 0;  // no slot table: nothing is stored
     if ((init_slots || snapshot_interval > 0) && !pool) return KDA_ERR_INVALID_ARG;
     if (gate == KDA_GATE_HEAD && !log_alpha && T_total > 0) return KDA_ERR_INVALID_ARG;
     const int g = gate == KDA_GATE_CHANNEL ? kGateChannel : gate == KDA_GATE_HEAD ? kGateHead : kGateNone;

@@ -147,7 +147,6 @@ def test_pool_validation(L):
     assert pool(gate=5) == b.KDA_ERR_INVALID_ARG
     assert pool(slots=-1) == b.KDA_ERR_INVALID_ARG
     assert pool(pool_dt=7) == b.KDA_ERR_INVALID_ARG                       # fp32 or bf16 pools only
-    assert pool(interval=64, snap_off=16) == b.KDA_ERR_INVALID_ARG        # snap_slots required
     assert pool(pool_ptr=0, init=16) == b.KDA_ERR_INVALID_ARG             # a pool to read from
     assert pool(gate=b.KDA_GATE_HEAD, la=0) == b.KDA_ERR_INVALID_ARG      # scalar gates required
     assert pool(gate=b.KDA_GATE_NONE, la=16) == b.KDA_ERR_INVALID_ARG     # DeltaNet takes no gates

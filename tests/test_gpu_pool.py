@@ -191,3 +191,24 @@ def test_bf16_pool(chunk):
                               packed_heads(xv["beta"], a, b, heads), np64(pool[N + idx]))
     assert_close(packed_heads(o_r, 0, b - a, heads), ro, "resumed from bf16 snapshot: out")
     assert_close(np64(f_r[0]), rs, "resumed from bf16 snapshot: state")
+
+
+def test_no_snapshot_table_stores_nothing():
+    """snapshot_interval > 0 with no slot table (or an empty one, as when no sequence reaches
+    the interval) stores no snapshot and leaves the pool untouched."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    xv = synth.varlen_inputs([100, 30], H, seed=4321, device="cuda")
+    pool = torch.full((3, H, 128, 128), 7.0, device="cuda")
+    pool[0] = xv["init_states"][0]
+    before = pool.clone()
+    o, f = kda.kda_varlen_fwd_pool(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], xv["cu_seqlens"], pool,
+                                   torch.tensor([0, -1], device="cuda"), None, snapshot_interval=128)
+    o2, f2 = kda.kda_varlen_fwd_pool(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], xv["cu_seqlens"], pool,
+                                     torch.tensor([0, -1], device="cuda"),
+                                     torch.empty(0, dtype=torch.int64, device="cuda"), snapshot_interval=128)
+    torch.cuda.synchronize()
+    assert torch.equal(pool, before)
+    assert torch.equal(o, o2) and torch.equal(f, f2)
+    assert kda.kda_get_device_status() == 0
