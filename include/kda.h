@@ -78,7 +78,7 @@ typedef enum {
 } kda_status;
 
 /* Operation selector of kda_workspace_size(). */
-typedef enum { KDA_OP_CHUNK = 0, KDA_OP_VARLEN = 1, KDA_OP_DECODE = 2, KDA_OP_BWD = 3 } kda_op;
+typedef enum { KDA_OP_CHUNK = 0, KDA_OP_VARLEN = 1, KDA_OP_DECODE = 2, KDA_OP_BWD = 3, KDA_OP_CHUNK_BWD = 4 } kda_op;
 
 /* Layout of log_alpha for kda_varlen_fwd_pool: one value per key channel (KDA), one per head
    (Gated DeltaNet), or none (DeltaNet, log_alpha NULL).  See kda_gdn_chunk_fwd. */
@@ -255,6 +255,30 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
             const float* init_states, const float* d_out, const float* d_final_states, const int64_t* cu_seqlens,
             int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
             float* dbeta, float* d_init_states, int in_dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * kda_bwd evaluated in chunks.  Same arguments, loss and results as kda_bwd, plus `chunk`:
+ *   chunk = 64  the chunked reverse mode of the §六.2 WY form ("Kimi K3" article,
+ *               lshu.cn/news/263999): the chunk-local products and all input gradients
+ *               run chunk-parallel as fp32 GEMMs on shared-memory tiles; only the
+ *               chunk-to-chunk state and state-gradient recurrences (two dependent
+ *               products per chunk) are serial per (sequence, head).  fp32 throughout;
+ *               deterministic.  Each chunk factors its decays about its 32nd row, so a
+ *               half-chunk whose summed log-decay is below -80 overflows fp32: the
+ *               kernel then raises KDA_STATUS_GATE_RANGE and the results are not valid
+ *               (use chunk = 1).
+ *   chunk = 1   the token-serial evaluation of kda_bwd (no gate limit).
+ *   workspace   device, kda_workspace_size(KDA_OP_CHUNK_BWD, N, T_total, H, dk, dv, chunk)
+ *               bytes, 16-byte aligned.  For chunk = 64 it holds every chunk's local
+ *               products, state and state gradient: about 4.1 KB per (token, head)
+ *               (about 5.4 GB at N=4, T=8192, H=32).
+ * Returns KDA_ERR_UNSUPPORTED for any other chunk.
+ */
+int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
+                  const float* init_states, const float* d_out, const float* d_final_states,
+                  const int64_t* cu_seqlens, int N, int64_t T, int H, int dk, int dv, int chunk, float* dq,
+                  float* dk_out, float* dv_out, float* dlog_alpha, float* dbeta, float* d_init_states, int in_dtype,
+                  void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * kda_bwd without a caller workspace: the scratch is a static device array inside the

@@ -22,7 +22,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_MISALIGNED = 0, 1, 2, 
 KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_WORKSPACE, KDA_STATUS_GATE_RANGE = 4, 5, 6, 7
 KDA_STATUS_SLOT_RANGE, KDA_ERR_SCRATCH_TOO_SMALL = 8, 9
 KDA_NOALLOC_SCRATCH_BYTES = 128 << 20
-KDA_OP_CHUNK, KDA_OP_VARLEN, KDA_OP_DECODE, KDA_OP_BWD = 0, 1, 2, 3
+KDA_OP_CHUNK, KDA_OP_VARLEN, KDA_OP_DECODE, KDA_OP_BWD, KDA_OP_CHUNK_BWD = 0, 1, 2, 3, 4
 KDA_GATE_CHANNEL, KDA_GATE_HEAD, KDA_GATE_NONE = 0, 1, 2
 
 _lib = None
@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.kda_host_fwd_workspace_size.restype = SZ
         L.kda_bwd.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P, SZ, P]
         L.kda_bwd_noalloc.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, P, P, P, P, P, P, I, P]
+        L.kda_chunk_bwd.argtypes = [P, P, P, P, I, P, P, P, P, P, I, I64, I, I, I, I, P, P, P, P, P, P, I, P, SZ,
+                                    P]
         L.kda_varlen_fwd_pool.argtypes = [P, P, P, P, I, P, P, I, I64, I, I, I, I, P, I64, I, P, I64, P, P, P, P, I,
                                           I, P, SZ, P]
         L.kda_snapshot_count.argtypes = [I64, I64]
@@ -70,7 +72,7 @@ def lib() -> ctypes.CDLL:
         L.kda_selftest_bounded_wait.argtypes = [P]
         for f in (L.kda_chunk_fwd, L.kda_varlen_fwd, L.kda_decode_step, L.kda_decode_step_bf16state,
                   L.kda_gdn_chunk_fwd, L.kda_gdn_varlen_fwd, L.kda_gdn_decode_step, L.kda_varlen_fwd_pool, L.kda_bwd,
-                  L.kda_bwd_noalloc, L.kda_selftest_bounded_wait, L.kda_gdn_decode_step_bf16state,
+                  L.kda_bwd_noalloc, L.kda_chunk_bwd, L.kda_selftest_bounded_wait, L.kda_gdn_decode_step_bf16state,
                   L.kda_chunk_fwd_host,
                   L.kda_snapshot_offsets,
                   L.kda_get_device_status):
@@ -337,11 +339,13 @@ def kda_gdn_decode_step(q, k, v, log_alpha, beta, state, out=None, *, out_dtype=
 
 
 def kda_bwd(q, k, v, log_alpha, beta, d_out, init_state=None, d_final_state=None, *, gate: int = KDA_GATE_CHANNEL,
-            cu_seqlens=None, return_d_init: bool = True, workspace=None, no_alloc: bool = False) -> dict:
+            cu_seqlens=None, return_d_init: bool = True, chunk: int = 64, workspace=None,
+            no_alloc: bool = False) -> dict:
     """Gradients of L = sum <d_out, o> + <d_final_state, S_final> through the forward of
     kda_chunk_fwd (batched q [B,T,H,dk] when cu_seqlens is None, else packed [Ttot,H,dk]).
     log_alpha's layout follows `gate`.  Returns dict(dq, dk, dv, dlog_alpha, dbeta, d_init).
-    no_alloc=True calls kda_bwd_noalloc (the library's static scratch, no workspace)."""
+    chunk=64 calls kda_chunk_bwd (chunked), chunk=1 the token-serial kda_bwd; no_alloc=True
+    calls kda_bwd_noalloc (token-serial, the library's static scratch, no workspace)."""
     if cu_seqlens is None:
         N, T, H, dk = q.shape
         t_arg, t_total = T, N * T
@@ -355,18 +359,20 @@ def kda_bwd(q, k, v, log_alpha, beta, d_out, init_state=None, d_final_state=None
          "dlog_alpha": None if gate == KDA_GATE_NONE else torch.empty(log_alpha.shape, **f32),
          "dbeta": torch.empty(beta.shape, **f32),
          "d_init": torch.empty(N, H, dk, dv, **f32) if return_d_init else None}
-    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), int(gate), _ptr(beta), _ptr(init_state), _ptr(d_out),
-            _ptr(d_final_state), _ptr(cu_seqlens), N, t_arg, H, dk, dv, _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
-            _ptr(g["dlog_alpha"]), _ptr(g["dbeta"]), _ptr(g["d_init"]), _dt(q))
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), int(gate), _ptr(beta), _ptr(init_state), _ptr(d_out),
+            _ptr(d_final_state), _ptr(cu_seqlens), N, t_arg, H, dk, dv)
+    grads = (_ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlog_alpha"]), _ptr(g["dbeta"]),
+             _ptr(g["d_init"]), _dt(q))
     if no_alloc:
-        _check(lib().kda_bwd_noalloc(*args, _stream(q.device)), "kda_bwd_noalloc")
+        _check(lib().kda_bwd_noalloc(*head, *grads, _stream(q.device)), "kda_bwd_noalloc")
         return g
     if workspace is None:
-        need = kda_workspace_size(KDA_OP_BWD, N, t_total, H, dk, dv)
+        need = kda_workspace_size(KDA_OP_CHUNK_BWD, N, t_total, H, dk, dv, chunk)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    rc = lib().kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), int(gate), _ptr(beta), _ptr(init_state),
-                       _ptr(d_out), _ptr(d_final_state), _ptr(cu_seqlens), N, t_arg, H, dk, dv, _ptr(g["dq"]),
-                       _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlog_alpha"]), _ptr(g["dbeta"]), _ptr(g["d_init"]),
-                       _dt(q), _ptr(workspace), workspace.numel(), _stream(q.device))
-    _check(rc, "kda_bwd")
+    if chunk == 1:
+        rc, name = lib().kda_bwd(*head, *grads, _ptr(workspace), workspace.numel(), _stream(q.device)), "kda_bwd"
+    else:
+        rc = lib().kda_chunk_bwd(*head, int(chunk), *grads, _ptr(workspace), workspace.numel(), _stream(q.device))
+        name = "kda_chunk_bwd"
+    _check(rc, name)
     return g

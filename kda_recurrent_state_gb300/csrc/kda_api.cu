@@ -113,6 +113,10 @@ int64_t kda_snapshot_lookup(const int64_t* offsets_host, int N, int seq, int64_t
 size_t kda_workspace_size(int op, int B, int64_t T, int H, int dk, int dv, int chunk) {
     (void)dk; (void)dv;
     if (op == KDA_OP_BWD) return (B <= 0 || H <= 0 || T < 0) ? 0 : bwd_workspace(B, T, H);
+    if (op == KDA_OP_CHUNK_BWD) {
+        if (B <= 0 || H <= 0 || T < 0) return 0;
+        return chunk == 64 ? chunk_bwd_workspace(B, T, H, true) : chunk == 1 ? bwd_workspace(B, T, H) : 0;
+    }
     if (op == KDA_OP_DECODE || B <= 0 || H <= 0 || chunk != 64) return 0;
     return chunk_prefill_workspace(B, H);
 }
@@ -332,15 +336,15 @@ int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const
                          out_dtype, stream);
 }
 
-int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
-            const float* init_states, const float* d_out, const float* d_final_states, const int64_t* cu_seqlens,
-            int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
-            float* dbeta, float* d_init_states, int in_dtype, void* workspace, size_t ws_bytes, void* stream) {
-    NvtxRange nvtx_range("kda_bwd");
+static int bwd_common(const void* q, const void* k, const void* v, const float* log_alpha, int gate,
+                      const float* beta, const float* init_states, const float* d_out, const float* d_final_states,
+                      const int64_t* cu_seqlens, int N, int64_t T, int H, int dk, int dv, int chunk, float* dq,
+                      float* dk_out, float* dv_out, float* dlog_alpha, float* dbeta, float* d_init_states,
+                      int in_dtype, void* workspace, size_t ws_bytes, void* stream) {
     if (N < 0 || T < 0 || H < 0) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(in_dtype)) return KDA_ERR_INVALID_ARG;
     if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_HEAD && gate != KDA_GATE_NONE) return KDA_ERR_INVALID_ARG;
-    if (dk != kD || dv != kD) return KDA_ERR_UNSUPPORTED;
+    if (dk != kD || dv != kD || (chunk != 1 && chunk != 64)) return KDA_ERR_UNSUPPORTED;
     if (N == 0 || H == 0) return KDA_OK;
     const int64_t T_total = cu_seqlens ? T : (int64_t)N * T;
     const bool gated = gate != KDA_GATE_NONE;
@@ -357,7 +361,7 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     const void* al16[] = {init_states, d_final_states, d_init_states, workspace};
     for (const void* p : al16)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
-    const size_t need = kda_workspace_size(KDA_OP_BWD, N, T_total, H, dk, dv, 64);
+    const size_t need = kda_workspace_size(KDA_OP_CHUNK_BWD, N, T_total, H, dk, dv, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
     BwdProblem p{};
     p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta; p.init = init_states;
@@ -365,8 +369,32 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
     p.dq = dq; p.dk = dk_out; p.dv = dv_out; p.dlog_alpha = dlog_alpha; p.dbeta = dbeta; p.dinit = d_init_states;
     p.cu_seqlens = cu_seqlens; p.T_uniform = cu_seqlens ? 0 : T; p.T_total = T_total; p.N = N; p.H = H;
     p.gate = gate == KDA_GATE_CHANNEL ? kGateChannel : gate == KDA_GATE_HEAD ? kGateHead : kGateNone;
-    return launch_bwd(p, in_dtype, workspace, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
-                                                                                              : KDA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (chunk == 1) return launch_bwd(p, in_dtype, workspace, st) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    int* status = status_ptr();
+    if (!status) return KDA_ERR_CUDA;
+    return launch_chunk_bwd(p, in_dtype, workspace, status, st) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
+            const float* init_states, const float* d_out, const float* d_final_states, const int64_t* cu_seqlens,
+            int N, int64_t T, int H, int dk, int dv, float* dq, float* dk_out, float* dv_out, float* dlog_alpha,
+            float* dbeta, float* d_init_states, int in_dtype, void* workspace, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("kda_bwd");
+    return bwd_common(q, k, v, log_alpha, gate, beta, init_states, d_out, d_final_states, cu_seqlens, N, T, H, dk,
+                      dv, 1, dq, dk_out, dv_out, dlog_alpha, dbeta, d_init_states, in_dtype, workspace, ws_bytes,
+                      stream);
+}
+
+int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
+                  const float* init_states, const float* d_out, const float* d_final_states,
+                  const int64_t* cu_seqlens, int N, int64_t T, int H, int dk, int dv, int chunk, float* dq,
+                  float* dk_out, float* dv_out, float* dlog_alpha, float* dbeta, float* d_init_states, int in_dtype,
+                  void* workspace, size_t ws_bytes, void* stream) {
+    NvtxRange nvtx_range("kda_chunk_bwd");
+    return bwd_common(q, k, v, log_alpha, gate, beta, init_states, d_out, d_final_states, cu_seqlens, N, T, H, dk,
+                      dv, chunk, dq, dk_out, dv_out, dlog_alpha, dbeta, d_init_states, in_dtype, workspace,
+                      ws_bytes, stream);
 }
 
 int kda_selftest_bounded_wait(void* stream) {

@@ -1,0 +1,818 @@
+// kda_bwd_chunk.cu -- gradients of the KDA recurrence in chunked form (C = 64), fp32 on CUDA cores.
+//
+// The forward is the "Kimi K3" article's (lshu.cn/news/263999) §四 update with the §二.1 read,
+// rewritten per chunk in the WY form of §六.2.  With the chunk's start state S_0, the in-chunk
+// cumulative log-decay g_r (per key channel) and the reference ref = g_31:
+//     Q~ = q e^{g-ref}   K~ = k e^{g-ref}   K^ = k e^{ref-g}      (row r of each)
+//     T  = (I + strict_lower(diag(beta) K~ K^^T))^-1
+//     U' = T diag(beta) V          W~ = T diag(beta) K~          P = lower_incl(Q~ K^^T)
+//     X  = Diag(e^ref) S_0         U  = U' - W~ X
+//     O  = Q~ X + P U              S_C = Diag(e^{g_C - ref}) (X + K^^T U)
+// The pages give no backward; this is the reverse mode of those products, one at a time.  The
+// output does not depend on ref, so its adjoint is zero and is not formed.  Four passes:
+//   local   (chunk-parallel)  g, Q~, K~, K^, T, W~, U', P, and the chunk's output-gradient term
+//                             E = Q~^T dO - W~^T (P^T dO) of the state gradient
+//   states  (serial per head) S_{n+1} = Diag(e^{g_C-ref}) (X + K^^T (U' - W~ X)), every S_n kept
+//   dstates (serial per head) dS_n = Diag(e^ref) (dD - W~^T (K^ dD) + E), dD = Diag(e^{g_C-ref}) dS_{n+1}
+//   grads   (chunk-parallel, two kernels) every input gradient of the chunk from S_n and dS_{n+1}
+// Every product is a small dense GEMM over shared-memory tiles, so the work runs at CUDA-core
+// throughput instead of the token-serial path's per-token reduction latency.  All arithmetic is
+// fp32; sums are in a fixed order, so the result is bit-reproducible.  e^{g-ref} must stay in fp32
+// range: a chunk whose half-chunk log-decay sum is below -80 raises KDA_STATUS_GATE_RANGE (the
+// token-serial backward has no such limit).
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int C = 64;          // chunk
+constexpr int NT = 512;        // 16 warps
+constexpr int LD = kD + 1;     // row stride of C x D and D x D tiles (odd: column reads hit distinct banks)
+constexpr int LC = C + 1;      // row stride of C x C tiles
+constexpr int TILE_CD = C * LD;
+constexpr int TILE_DD = kD * LD;
+constexpr int TILE_CC = C * LC;
+constexpr float kExpLimit = 80.f;  // |g - ref| beyond this leaves fp32 range in e^{+-(g-ref)}
+
+// Per chunk-head workspace records (floats) and the state arrays.
+constexpr size_t REC_CD = (size_t)C * kD, REC_DD = (size_t)kD * kD, REC_CC = (size_t)C * C;
+
+struct CBwd {
+    BwdProblem p;
+    int* status;
+    const int64_t* co;  // [N+1] first chunk index of each sequence
+    int64_t* co_w;
+    // per chunk-head (index (cg * H + h)):
+    float* Wt;  // W~ [C][D]; after the first gradient kernel: dW~
+    float* Up;  // U' [C][D]; then dU
+    float* Kh;  // K^ [C][D]
+    float* Ej;  // E [D][D]; then dQ~ (first half) and dK^ (second half), partial
+    float* Tm;  // T [C][C]
+    float* Pq;  // P [C][C]; then dP
+    float* sc;  // [3][D]: e^ref, e^{g_C - ref}, and the final-decay gradient sum_j S_C dS_C
+    float* dS;  // [D][D] gradient w.r.t. the chunk's end state
+    float* S;   // per (sequence, n) for n = 0..chunks: S_n at slot (co[s] + s + n) * H + h
+};
+
+// Register fragment of an M x N product spread over the 16 warps: warp w holds rows
+// w*MR .. w*MR+MR-1, lane l holds columns l + 32 j.
+template <int M, int N>
+struct Frag {
+    static constexpr int MR = M / 16, NJ = N / 32;
+    float v[MR][NJ];
+    __device__ __forceinline__ static int row(int i) { return (int)(threadIdx.x >> 5) * MR + i; }
+    __device__ __forceinline__ static int col(int j) { return (int)(threadIdx.x & 31) + 32 * j; }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < MR; ++i)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) v[i][j] = 0.f;
+    }
+};
+
+// f (+/-)= A B, A(m, k) = A[m * ARS + k * ACS], B(k, n) = B[k * BRS + n * BCS], k in [0, K).
+// A is read by all lanes of a warp at once (a broadcast); B's columns go to distinct lanes.
+template <bool NEG, int K, int ARS, int ACS, int BRS, int BCS, int M, int N>
+__device__ __forceinline__ void gemm(Frag<M, N>& f, const float* A, const float* B) {
+    constexpr int MR = M / 16, NJ = N / 32;
+    const float* a0 = A + (threadIdx.x >> 5) * MR * ARS;
+    const float* b0 = B + (threadIdx.x & 31) * BCS;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[MR], b[NJ];
+#pragma unroll
+        for (int i = 0; i < MR; ++i) a[i] = a0[i * ARS + k * ACS];
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) b[j] = b0[k * BRS + 32 * j * BCS];
+#pragma unroll
+        for (int i = 0; i < MR; ++i)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) f.v[i][j] = fmaf(NEG ? -a[i] : a[i], b[j], f.v[i][j]);
+    }
+}
+
+template <int M, int N>
+__device__ __forceinline__ void to_smem(const Frag<M, N>& f, float* dst, int ld) {
+#pragma unroll
+    for (int i = 0; i < Frag<M, N>::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < Frag<M, N>::NJ; ++j) dst[Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)] = f.v[i][j];
+}
+template <int M, int N>
+__device__ __forceinline__ void to_global(const Frag<M, N>& f, float* dst) {
+#pragma unroll
+    for (int i = 0; i < Frag<M, N>::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < Frag<M, N>::NJ; ++j) dst[Frag<M, N>::row(i) * N + Frag<M, N>::col(j)] = f.v[i][j];
+}
+template <int M, int N>
+__device__ __forceinline__ void from_global(Frag<M, N>& f, const float* src) {
+#pragma unroll
+    for (int i = 0; i < Frag<M, N>::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < Frag<M, N>::NJ; ++j) f.v[i][j] = src[Frag<M, N>::row(i) * N + Frag<M, N>::col(j)];
+}
+
+// Dense [rows][D] record in global memory -> shared tile with row stride LD, optionally scaled per row.
+__device__ __forceinline__ void load_tile(float* dst, const float* src, int rows, const float* row_scale = nullptr) {
+    for (int idx = threadIdx.x; idx < rows * kD; idx += NT) {
+        const int r = idx >> 7, c = idx & 127;
+        const float x = src[idx];
+        dst[r * LD + c] = row_scale ? row_scale[r] * x : x;
+    }
+}
+__device__ __forceinline__ void load_cc(float* dst, const float* src) {
+    for (int idx = threadIdx.x; idx < C * C; idx += NT) dst[(idx >> 6) * LC + (idx & 63)] = src[idx];
+}
+
+__device__ __forceinline__ float ldin(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float ldin(const float* p, size_t i) { return p[i]; }
+
+__device__ __forceinline__ void seq_of(const BwdProblem& P, int s, int64_t& start, int64_t& len) {
+    if (P.cu_seqlens) {
+        start = P.cu_seqlens[s];
+        len = P.cu_seqlens[s + 1] - start;
+    } else {
+        start = (int64_t)s * P.T_uniform;
+        len = P.T_uniform;
+    }
+}
+
+struct ChunkAt {
+    int s;
+    int64_t n, tok0;
+    int L;  // valid rows
+};
+
+// The chunk with global index cg: the last sequence s with co[s] <= cg (empty sequences own no chunk).
+__device__ __forceinline__ bool locate_chunk(const CBwd& W, int64_t cg, ChunkAt& c) {
+    const int N = W.p.N;
+    if (cg >= W.co[N]) return false;
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (W.co[mid] <= cg) lo = mid; else hi = mid - 1;
+    }
+    int64_t start, len;
+    seq_of(W.p, lo, start, len);
+    c.s = lo;
+    c.n = cg - W.co[lo];
+    c.tok0 = start + c.n * C;
+    const int64_t rem = len - c.n * C;
+    c.L = rem < C ? (int)rem : C;
+    return true;
+}
+
+__global__ void chunk_offsets_kernel(CBwd W) {
+    __shared__ int64_t part[1024];
+    const int N = W.p.N, t = threadIdx.x;
+    const int per = (N + 1023) / 1024;
+    const int s0 = min(N, t * per), s1 = min(N, s0 + per);
+    auto nch = [&](int s) {
+        int64_t start, len;
+        seq_of(W.p, s, start, len);
+        return (len + C - 1) / C;
+    };
+    int64_t sum = 0;
+    for (int s = s0; s < s1; ++s) sum += nch(s);
+    part[t] = sum;
+    __syncthreads();
+    if (t == 0) {
+        int64_t run = 0;
+        for (int i = 0; i < 1024; ++i) {
+            const int64_t x = part[i];
+            part[i] = run;
+            run += x;
+        }
+        W.co_w[N] = run;
+    }
+    __syncthreads();
+    int64_t run = part[t];
+    for (int s = s0; s < s1; ++s) {
+        W.co_w[s] = run;
+        run += nch(s);
+    }
+}
+
+// Cumulative log-decay of the chunk into g (rows >= L: no decay), and beta (rows >= L: 0).
+__device__ __forceinline__ void load_gates(const CBwd& W, const ChunkAt& c, int h, float* g, float* beta) {
+    const BwdProblem& P = W.p;
+    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
+        const int r = idx >> 7, col = idx & 127;
+        float la = 0.f;
+        if (r < c.L) {
+            const size_t row = (size_t)(c.tok0 + r) * P.H + h;
+            la = P.gate == kGateChannel ? P.log_alpha[row * kD + col] : P.gate == kGateHead ? P.log_alpha[row] : 0.f;
+        }
+        g[r * LD + col] = la;
+    }
+    if (beta && threadIdx.x < C)
+        beta[threadIdx.x] = (int)threadIdx.x < c.L ? P.beta[(size_t)(c.tok0 + threadIdx.x) * P.H + h] : 0.f;
+    __syncthreads();
+    if (threadIdx.x < kD) {
+        float run = 0.f;
+        for (int r = 0; r < C; ++r) {
+            run += g[r * LD + threadIdx.x];
+            g[r * LD + threadIdx.x] = run;
+        }
+    }
+    __syncthreads();
+}
+
+// Q~, K~, K^ of the chunk from q, k and the cumulative decay g (rows >= L: zero).
+template <typename Tin>
+__device__ __forceinline__ void scaled_qk(const CBwd& W, const ChunkAt& c, int h, const float* g, float* sQ,
+                                          float* sK, float* sH, float* Kh_out) {
+    const Tin* q = static_cast<const Tin*>(W.p.q);
+    const Tin* k = static_cast<const Tin*>(W.p.k);
+    bool bad = false;
+    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
+        const int r = idx >> 7, col = idx & 127;
+        const float x = g[r * LD + col] - g[31 * LD + col];
+        bad |= fabsf(x) > kExpLimit;
+        const float e = expf(x), f = expf(-x);
+        float qv = 0.f, kv = 0.f;
+        if (r < c.L) {
+            const size_t off = ((size_t)(c.tok0 + r) * W.p.H + h) * kD + col;
+            qv = ldin(q, off);
+            kv = ldin(k, off);
+        }
+        sQ[r * LD + col] = qv * e;
+        sK[r * LD + col] = kv * e;
+        sH[r * LD + col] = kv * f;
+        if (Kh_out) Kh_out[idx] = kv * f;
+    }
+    if (bad) atomicCAS(W.status, 0, (int)KDA_STATUS_GATE_RANGE);
+}
+
+// In place: the strictly lower C x C matrix A (stride LC) becomes T = (I + A)^-1, by 16 x 16 blocks:
+// diagonal blocks by substitution, then T_ab = -Dg_a sum_{k=b}^{a-1} A_ak T_kb block row by block row.
+// `y` is scratch for 3 blocks.
+__device__ void invert_unit_lower(float* A, float* y) {
+    const int t = threadIdx.x;
+    float x[16];
+    if (t < 64) {  // column j of diagonal block a
+        const int a = t >> 4, j = t & 15;
+        const float* Ab = A + (a * 16) * LC + a * 16;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float s = r == j ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) s = fmaf(-Ab[r * LC + i], x[i], s);
+            x[r] = s;
+        }
+    }
+    __syncthreads();
+    if (t < 64) {
+        const int a = t >> 4, j = t & 15;
+        float* Ab = A + (a * 16) * LC + a * 16;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Ab[r * LC + j] = x[r];
+    }
+    __syncthreads();
+    for (int a = 1; a < 4; ++a) {
+        for (int idx = t; idx < a * 256; idx += NT) {  // Y_ab = sum_{k=b}^{a-1} A_ak T_kb
+            const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+            float s = 0.f;
+            for (int k = b; k < a; ++k) {
+                const float* Ar = A + (a * 16 + r) * LC + k * 16;
+                const float* Tk = A + (k * 16) * LC + b * 16 + cc;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) s = fmaf(Ar[m], Tk[m * LC], s);
+            }
+            y[idx] = s;
+        }
+        __syncthreads();
+        for (int idx = t; idx < a * 256; idx += NT) {  // T_ab = -Dg_a Y_ab
+            const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+            const float* Dr = A + (a * 16 + r) * LC + a * 16;
+            const float* Yb = y + b * 256 + cc;
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) s = fmaf(Dr[m], Yb[m * 16], s);
+            A[(a * 16 + r) * LC + b * 16 + cc] = -s;
+        }
+        __syncthreads();
+    }
+}
+
+// ---- pass 1: the chunk's local terms ------------------------------------------------------
+constexpr int SMEM_LOCAL = (5 * TILE_CD + 2 * TILE_CC + 3 * 256 + C) * 4;
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
+    extern __shared__ __align__(16) float sm[];
+    float* sA = sm;              // g, then beta V, then W~
+    float* sQ = sA + TILE_CD;    // Q~
+    float* sK = sQ + TILE_CD;    // K~, then beta K~, then P^T dO
+    float* sH = sK + TILE_CD;    // K^
+    float* sO = sH + TILE_CD;    // dO
+    float* sP = sO + TILE_CD;    // P
+    float* sT = sP + TILE_CC;    // strict_lower(beta K~ K^^T), then T
+    float* sY = sT + TILE_CC;    // inverse scratch
+    float* sB = sY + 3 * 256;    // beta
+    const BwdProblem& P = W.p;
+    const int h = blockIdx.x % P.H;
+    const int64_t cg = blockIdx.x / P.H;
+    ChunkAt c;
+    if (!locate_chunk(W, cg, c)) return;
+    const size_t ch = (size_t)cg * P.H + h;
+
+    load_gates(W, c, h, sA, sB);
+    scaled_qk<Tin>(W, c, h, sA, sQ, sK, sH, W.Kh + ch * REC_CD);
+    if (threadIdx.x < kD) {
+        const float ref = sA[31 * LD + threadIdx.x];
+        W.sc[ch * 3 * kD + threadIdx.x] = expf(ref);
+        W.sc[ch * 3 * kD + kD + threadIdx.x] = expf(sA[63 * LD + threadIdx.x] - ref);
+    }
+    __syncthreads();
+    const Tin* v = static_cast<const Tin*>(P.v);
+    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
+        const int r = idx >> 7, col = idx & 127;
+        float vv = 0.f, dov = 0.f;
+        if (r < c.L) {
+            const size_t off = ((size_t)(c.tok0 + r) * P.H + h) * kD + col;
+            vv = ldin(v, off);
+            dov = P.dout[off];
+        }
+        sA[r * LD + col] = sB[r] * vv;
+        sO[r * LD + col] = dov;
+    }
+    {
+        Frag<C, C> gk, pq;
+        gk.zero();
+        pq.zero();
+        gemm<false, kD, LD, 1, 1, LD>(gk, sK, sH);  // K~ K^^T
+        gemm<false, kD, LD, 1, 1, LD>(pq, sQ, sH);  // Q~ K^^T
+#pragma unroll
+        for (int i = 0; i < Frag<C, C>::MR; ++i)
+#pragma unroll
+            for (int j = 0; j < Frag<C, C>::NJ; ++j) {
+                const int r = Frag<C, C>::row(i), cc = Frag<C, C>::col(j);
+                sT[r * LC + cc] = cc < r ? sB[r] * gk.v[i][j] : 0.f;
+                const float pv = cc <= r ? pq.v[i][j] : 0.f;
+                sP[r * LC + cc] = pv;
+                W.Pq[ch * REC_CC + r * C + cc] = pv;
+            }
+    }
+    __syncthreads();
+    invert_unit_lower(sT, sY);
+    for (int idx = threadIdx.x; idx < C * C; idx += NT) W.Tm[ch * REC_CC + idx] = sT[(idx >> 6) * LC + (idx & 63)];
+    {
+        Frag<C, kD> u;
+        u.zero();
+        gemm<false, C, LC, 1, LD, 1>(u, sT, sA);  // U' = T (beta V)
+        to_global(u, W.Up + ch * REC_CD);
+    }
+    for (int idx = threadIdx.x; idx < C * kD; idx += NT) sK[(idx >> 7) * LD + (idx & 127)] *= sB[idx >> 7];
+    __syncthreads();
+    {
+        Frag<C, kD> w;
+        w.zero();
+        gemm<false, C, LC, 1, LD, 1>(w, sT, sK);  // W~ = T (beta K~)
+        to_smem(w, sA, LD);
+        to_global(w, W.Wt + ch * REC_CD);
+    }
+    __syncthreads();
+    {
+        Frag<C, kD> pd;
+        pd.zero();
+        gemm<false, C, 1, LC, LD, 1>(pd, sP, sO);  // P^T dO
+        to_smem(pd, sK, LD);
+    }
+    __syncthreads();
+    {
+        Frag<kD, kD> e;
+        e.zero();
+        gemm<false, C, 1, LD, LD, 1>(e, sQ, sO);  // Q~^T dO
+        gemm<true, C, 1, LD, LD, 1>(e, sA, sK);   // - W~^T (P^T dO)
+        to_global(e, W.Ej + ch * REC_DD);
+    }
+}
+
+// ---- pass 2: chunk-start states, serial per (sequence, head) -----------------------------------
+constexpr int SMEM_STATES = (TILE_DD + 3 * TILE_CD + 2 * kD) * 4;
+
+__global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
+    extern __shared__ __align__(16) float sm[];
+    float* sX = sm;              // X = Diag(e^ref) S
+    float* sU = sX + TILE_DD;    // U
+    float* sW = sU + TILE_CD;    // W~
+    float* sH = sW + TILE_CD;    // K^
+    float* sE = sH + TILE_CD;    // e^ref, e^{g_C - ref}
+    const BwdProblem& P = W.p;
+    const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
+    int64_t start, len;
+    seq_of(P, s, start, len);
+    const int64_t nc = (len + C - 1) / C, base = W.co[s];
+    using F = Frag<kD, kD>;
+    F S;
+    if (P.init) from_global(S, P.init + ((size_t)s * P.H + h) * REC_DD);
+    else S.zero();
+    for (int64_t n = 0; n <= nc; ++n) {
+        to_global(S, W.S + ((size_t)(base + s + n) * P.H + h) * REC_DD);
+        if (n == nc) break;
+        const size_t ch = (size_t)(base + n) * P.H + h;
+        if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
+        load_tile(sW, W.Wt + ch * REC_CD, C);
+        load_tile(sH, W.Kh + ch * REC_CD, C);
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < F::MR; ++i)
+#pragma unroll
+            for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= sE[F::row(i)];
+        to_smem(S, sX, LD);
+        __syncthreads();
+        Frag<C, kD> u;
+        from_global(u, W.Up + ch * REC_CD);
+        gemm<true, kD, LD, 1, LD, 1>(u, sW, sX);  // U = U' - W~ X
+        to_smem(u, sU, LD);
+        __syncthreads();
+        gemm<false, C, 1, LD, LD, 1>(S, sH, sU);  // X + K^^T U
+#pragma unroll
+        for (int i = 0; i < F::MR; ++i)
+#pragma unroll
+            for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= sE[kD + F::row(i)];
+        __syncthreads();
+    }
+}
+
+// ---- pass 3: state gradients at chunk ends, serial per (sequence, head), last chunk first --------
+constexpr int SMEM_DSTATES = SMEM_STATES;
+
+__global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
+    extern __shared__ __align__(16) float sm[];
+    float* sD = sm;              // dD = Diag(e^{g_C - ref}) dS
+    float* sZ = sD + TILE_DD;    // K^ dD
+    float* sW = sZ + TILE_CD;    // W~
+    float* sH = sW + TILE_CD;    // K^
+    float* sE = sH + TILE_CD;
+    const BwdProblem& P = W.p;
+    const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
+    int64_t start, len;
+    seq_of(P, s, start, len);
+    const int64_t nc = (len + C - 1) / C, base = W.co[s];
+    using F = Frag<kD, kD>;
+    F dS;
+    if (P.dfinal) from_global(dS, P.dfinal + ((size_t)s * P.H + h) * REC_DD);
+    else dS.zero();
+    for (int64_t n = nc - 1; n >= 0; --n) {
+        const size_t ch = (size_t)(base + n) * P.H + h;
+        to_global(dS, W.dS + ch * REC_DD);
+        if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
+        load_tile(sW, W.Wt + ch * REC_CD, C);
+        load_tile(sH, W.Kh + ch * REC_CD, C);
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < F::MR; ++i)
+#pragma unroll
+            for (int j = 0; j < F::NJ; ++j) dS.v[i][j] *= sE[kD + F::row(i)];
+        to_smem(dS, sD, LD);
+        __syncthreads();
+        Frag<C, kD> z;
+        z.zero();
+        gemm<false, kD, LD, 1, LD, 1>(z, sH, sD);  // K^ dD
+        to_smem(z, sZ, LD);
+        __syncthreads();
+        gemm<true, C, 1, LD, LD, 1>(dS, sW, sZ);  // dD - W~^T (K^ dD)
+        const float* E = W.Ej + ch * REC_DD;
+#pragma unroll
+        for (int i = 0; i < F::MR; ++i)
+#pragma unroll
+            for (int j = 0; j < F::NJ; ++j)
+                dS.v[i][j] = (dS.v[i][j] + E[F::row(i) * kD + F::col(j)]) * sE[F::row(i)];
+        __syncthreads();
+    }
+    if (P.dinit) to_global(dS, P.dinit + ((size_t)s * P.H + h) * REC_DD);
+}
+
+// ---- pass 4a: the state-dependent gradient products of each chunk --------------------------------
+constexpr int SMEM_GRAD_A = (TILE_DD + 4 * TILE_CD + TILE_CC + 2 * kD) * 4;
+
+__global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
+    extern __shared__ __align__(16) float sm[];
+    float* sR = sm;              // X, then dD, then X
+    float* s1 = sR + TILE_DD;    // W~, then K^
+    float* s2 = s1 + TILE_CD;    // U
+    float* s3 = s2 + TILE_CD;    // dU
+    float* s4 = s3 + TILE_CD;    // dO
+    float* s5 = s4 + TILE_CD;    // P, then dP
+    float* sE = s5 + TILE_CC;
+    const BwdProblem& P = W.p;
+    const int h = blockIdx.x % P.H;
+    const int64_t cg = blockIdx.x / P.H;
+    ChunkAt c;
+    if (!locate_chunk(W, cg, c)) return;
+    const size_t ch = (size_t)cg * P.H + h;
+    const size_t s_slot = ((size_t)(W.co[c.s] + c.s + c.n) * P.H + h) * REC_DD;
+    const float* S0 = W.S + s_slot;
+    const float* SC = W.S + s_slot + (size_t)P.H * REC_DD;  // the next state of the same sequence
+    const float* dSC = W.dS + ch * REC_DD;
+    if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
+    __syncthreads();
+    load_tile(sR, S0, kD, sE);
+    load_tile(s1, W.Wt + ch * REC_CD, C);
+    __syncthreads();
+    Frag<C, kD> u;
+    from_global(u, W.Up + ch * REC_CD);
+    gemm<true, kD, LD, 1, LD, 1>(u, s1, sR);  // U = U' - W~ X
+    to_smem(u, s2, LD);
+    {  // final-decay gradient: sum_j S_C[c][j] dS_C[c][j], one warp per row
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        for (int r = w; r < kD; r += 16) {
+            float a = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a = fmaf(SC[r * kD + l + 32 * j], dSC[r * kD + l + 32 * j], a);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (l == 0) W.sc[ch * 3 * kD + 2 * kD + r] = a;
+        }
+    }
+    __syncthreads();
+    load_tile(sR, dSC, kD, sE + kD);  // dD
+    load_tile(s1, W.Kh + ch * REC_CD, C);
+    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
+        const int r = idx >> 7, col = idx & 127;
+        s4[r * LD + col] = r < c.L ? P.dout[((size_t)(c.tok0 + r) * P.H + h) * kD + col] : 0.f;
+    }
+    load_cc(s5, W.Pq + ch * REC_CC);
+    __syncthreads();
+    Frag<C, kD> du, acc;
+    du.zero();
+    gemm<false, kD, LD, 1, LD, 1>(du, s1, sR);  // K^ dD
+    gemm<false, C, 1, LC, LD, 1>(du, s5, s4);   // + P^T dO
+    to_smem(du, s3, LD);
+    to_global(du, W.Up + ch * REC_CD);
+    acc.zero();
+    gemm<false, kD, LD, 1, 1, LD>(acc, s2, sR);  // dK^ = U dD^T
+    to_global(acc, W.Ej + ch * REC_DD + REC_CD);
+    Frag<C, C> dp;
+    dp.zero();
+    gemm<false, kD, LD, 1, 1, LD>(dp, s4, s2);  // dP = lower(dO U^T)
+    __syncthreads();
+    load_tile(sR, S0, kD, sE);  // X again
+#pragma unroll
+    for (int i = 0; i < Frag<C, C>::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < Frag<C, C>::NJ; ++j) {
+            const int r = Frag<C, C>::row(i), cc = Frag<C, C>::col(j);
+            const float x = cc <= r ? dp.v[i][j] : 0.f;
+            s5[r * LC + cc] = x;
+            W.Pq[ch * REC_CC + r * C + cc] = x;
+        }
+    __syncthreads();
+    acc.zero();
+    gemm<false, kD, LD, 1, 1, LD>(acc, s4, sR);  // dQ~ = dO X^T
+    gemm<false, C, LC, 1, LD, 1>(acc, s5, s1);   //      + dP K^
+    to_global(acc, W.Ej + ch * REC_DD);
+    acc.zero();
+    gemm<true, kD, LD, 1, 1, LD>(acc, s3, sR);  // dW~ = -dU X^T
+    to_global(acc, W.Wt + ch * REC_CD);
+}
+
+// ---- pass 4b: the chunk's local gradient products and the input gradients ----------------------
+constexpr int SMEM_GRAD_B = (5 * TILE_CD + 3 * TILE_CC + C + kD) * 4;
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
+    extern __shared__ __align__(16) float sm[];
+    float* s0 = sm;              // g, then V, then d(g - ref)
+    float* sQ = s0 + TILE_CD;    // Q~
+    float* sK = sQ + TILE_CD;    // K~
+    float* sH = sK + TILE_CD;    // K^
+    float* sX = sH + TILE_CD;    // dU, then dW~, then g
+    float* sT = sX + TILE_CD;    // T
+    float* sP = sT + TILE_CC;    // dP, then Y = dT T^T
+    float* sM = sP + TILE_CC;    // dT, then dA, then diag(beta) dA
+    float* sB = sM + TILE_CC;    // beta
+    float* sG = sB + C;          // final-decay gradient
+    const BwdProblem& P = W.p;
+    const int h = blockIdx.x % P.H;
+    const int64_t cg = blockIdx.x / P.H;
+    ChunkAt c;
+    if (!locate_chunk(W, cg, c)) return;
+    const size_t ch = (size_t)cg * P.H + h;
+    using F = Frag<C, kD>;
+    using FC = Frag<C, C>;
+
+    load_gates(W, c, h, s0, sB);
+    scaled_qk<Tin>(W, c, h, s0, sQ, sK, sH, nullptr);
+    if (threadIdx.x < kD) sG[threadIdx.x] = W.sc[ch * 3 * kD + 2 * kD + threadIdx.x];
+    load_cc(sT, W.Tm + ch * REC_CC);
+    load_cc(sP, W.Pq + ch * REC_CC);
+    load_tile(sX, W.Up + ch * REC_CD, C);  // dU
+    __syncthreads();
+    const Tin* v = static_cast<const Tin*>(P.v);
+    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
+        const int r = idx >> 7, col = idx & 127;
+        s0[r * LD + col] = r < c.L ? ldin(v, ((size_t)(c.tok0 + r) * P.H + h) * kD + col) : 0.f;
+    }
+    __syncthreads();
+
+    float db[F::MR];  // per-lane partial sums of dbeta for this warp's rows
+#pragma unroll
+    for (int i = 0; i < F::MR; ++i) db[i] = 0.f;
+    F dKh, dKt, t;
+    from_global(dKh, W.Ej + ch * REC_DD + REC_CD);
+    gemm<false, C, 1, LC, LD, 1>(dKh, sP, sQ);  // + dP^T Q~
+    FC dT;
+    dT.zero();
+    gemm<false, kD, LD, 1, 1, LD>(dT, sX, s0);  // dU V^T
+    t.zero();
+    gemm<false, C, 1, LC, LD, 1>(t, sT, sX);  // T^T dU
+#pragma unroll
+    for (int i = 0; i < F::MR; ++i) {
+        const int r = F::row(i);
+#pragma unroll
+        for (int j = 0; j < F::NJ; ++j) {
+            db[i] = fmaf(t.v[i][j], s0[r * LD + F::col(j)], db[i]);
+            if (r < c.L) P.dv[((size_t)(c.tok0 + r) * P.H + h) * kD + F::col(j)] = sB[r] * t.v[i][j];
+        }
+    }
+    __syncthreads();
+    load_tile(sX, W.Wt + ch * REC_CD, C);  // dW~
+    __syncthreads();
+    gemm<false, kD, LD, 1, 1, LD>(dT, sX, sK);  // + dW~ K~^T
+#pragma unroll
+    for (int i = 0; i < FC::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < FC::NJ; ++j) {
+            const int r = FC::row(i), cc = FC::col(j);
+            sM[r * LC + cc] = sB[cc] * dT.v[i][j];
+        }
+    t.zero();
+    gemm<false, C, 1, LC, LD, 1>(t, sT, sX);  // T^T dW~
+#pragma unroll
+    for (int i = 0; i < F::MR; ++i) {
+        const int r = F::row(i);
+#pragma unroll
+        for (int j = 0; j < F::NJ; ++j) {
+            db[i] = fmaf(t.v[i][j], sK[r * LD + F::col(j)], db[i]);
+            dKt.v[i][j] = sB[r] * t.v[i][j];
+        }
+    }
+    __syncthreads();
+    {
+        FC y;
+        y.zero();
+        gemm<false, C, LC, 1, 1, LC>(y, sM, sT);  // Y = dT T^T
+        to_smem(y, sP, LC);
+    }
+    __syncthreads();
+    {
+        FC a;
+        a.zero();
+        gemm<true, C, 1, LC, LC, 1>(a, sT, sP);  // dA = -T^T Y, strictly lower part
+#pragma unroll
+        for (int i = 0; i < FC::MR; ++i)
+#pragma unroll
+            for (int j = 0; j < FC::NJ; ++j) {
+                const int r = FC::row(i), cc = FC::col(j);
+                sM[r * LC + cc] = cc < r ? a.v[i][j] : 0.f;
+            }
+    }
+    __syncthreads();
+    t.zero();
+    gemm<false, C, LC, 1, LD, 1>(t, sM, sH);  // dA K^
+#pragma unroll
+    for (int i = 0; i < F::MR; ++i) {
+        const int r = F::row(i);
+#pragma unroll
+        for (int j = 0; j < F::NJ; ++j) {
+            db[i] = fmaf(t.v[i][j], sK[r * LD + F::col(j)], db[i]);
+            dKt.v[i][j] = fmaf(sB[r], t.v[i][j], dKt.v[i][j]);
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < C * C; idx += NT) sM[(idx >> 6) * LC + (idx & 63)] *= sB[idx >> 6];
+    __syncthreads();
+    gemm<false, C, 1, LC, LD, 1>(dKh, sM, sK);  // + (diag(beta) dA)^T K~
+
+    // beta gradient: this warp's rows are complete across its 32 lanes
+#pragma unroll
+    for (int i = 0; i < F::MR; ++i) {
+        float x = db[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        const int r = F::row(i);
+        if ((threadIdx.x & 31) == 0 && r < c.L) P.dbeta[(size_t)(c.tok0 + r) * P.H + h] = x;
+    }
+    // decay gradient and dq, dk
+    __syncthreads();
+    load_gates(W, c, h, sX, nullptr);  // g again
+    F dQt;
+    from_global(dQt, W.Ej + ch * REC_DD);
+#pragma unroll
+    for (int i = 0; i < F::MR; ++i) {
+        const int r = F::row(i);
+#pragma unroll
+        for (int j = 0; j < F::NJ; ++j) {
+            const int col = F::col(j);
+            const int o = r * LD + col;
+            const float x = sX[o] - sX[31 * LD + col];
+            const float e = expf(x), f = expf(-x);
+            if (r < c.L) {
+                const size_t off = ((size_t)(c.tok0 + r) * P.H + h) * kD + col;
+                P.dq[off] = dQt.v[i][j] * e;
+                P.dk[off] = fmaf(dKt.v[i][j], e, dKh.v[i][j] * f);
+            }
+            float dl = fmaf(dQt.v[i][j], sQ[o], fmaf(dKt.v[i][j], sK[o], -dKh.v[i][j] * sH[o]));
+            if (r == C - 1) dl += sG[col];
+            s0[o] = dl;
+        }
+    }
+    __syncthreads();
+    if (P.gate == kGateNone) return;
+    if (threadIdx.x < kD) {  // reverse cumulative sum over the chunk's rows
+        float run = 0.f;
+        for (int r = C - 1; r >= 0; --r) {
+            run += s0[r * LD + threadIdx.x];
+            s0[r * LD + threadIdx.x] = run;
+        }
+    }
+    __syncthreads();
+    if (P.gate == kGateChannel) {
+        for (int idx = threadIdx.x; idx < c.L * kD; idx += NT) {
+            const int r = idx >> 7, col = idx & 127;
+            P.dlog_alpha[((size_t)(c.tok0 + r) * P.H + h) * kD + col] = s0[r * LD + col];
+        }
+    } else {  // one gate per head: the sum over key channels, one warp per row
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        for (int r = w; r < c.L; r += 16) {
+            float a = ((s0[r * LD + l] + s0[r * LD + l + 32]) + s0[r * LD + l + 64]) + s0[r * LD + l + 96];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (l == 0) P.dlog_alpha[(size_t)(c.tok0 + r) * P.H + h] = a;
+        }
+    }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Upper bound on the number of chunks: sum_s ceil(len_s / C) <= T_total / C + N.
+int64_t chunk_bound(int N, int64_t T_total, bool varlen, int64_t T_uniform) {
+    return varlen ? T_total / C + N : (int64_t)N * ((T_uniform + C - 1) / C);
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace(int N, int64_t T_total, int H, bool varlen) {
+    const int64_t T_uniform = varlen || N == 0 ? 0 : T_total / N;
+    const size_t nch = (size_t)chunk_bound(N, T_total, varlen, T_uniform) * H;
+    const size_t per = 3 * REC_CD + 2 * REC_DD + 2 * REC_CC + 3 * kD;  // Wt Up Kh, Ej dS, Tm Pq, sc
+    const size_t states = ((size_t)chunk_bound(N, T_total, varlen, T_uniform) + N) * H * REC_DD;
+    return align256((size_t)(N + 1) * 8) + align256(nch * per * 4) + align256(states * 4);
+}
+
+cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace, int* status, cudaStream_t st) {
+    if (p.N == 0 || p.H == 0) return cudaSuccess;
+    const bool varlen = p.cu_seqlens != nullptr;
+    const int64_t ncb = chunk_bound(p.N, p.T_total, varlen, p.T_uniform);
+    const size_t nch = (size_t)ncb * p.H;
+    CBwd W{};
+    W.p = p;
+    W.status = status;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    W.co_w = reinterpret_cast<int64_t*>(ws);
+    W.co = W.co_w;
+    float* f = reinterpret_cast<float*>(ws + align256((size_t)(p.N + 1) * 8));
+    W.Wt = f; f += nch * REC_CD;
+    W.Up = f; f += nch * REC_CD;
+    W.Kh = f; f += nch * REC_CD;
+    W.Ej = f; f += nch * REC_DD;
+    W.dS = f; f += nch * REC_DD;
+    W.Tm = f; f += nch * REC_CC;
+    W.Pq = f; f += nch * REC_CC;
+    W.sc = f; f += nch * 3 * kD;
+    W.S = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(W.co_w) + align256((size_t)(p.N + 1) * 8) +
+                                   align256(nch * (3 * REC_CD + 2 * REC_DD + 2 * REC_CC + 3 * kD) * 4));
+    chunk_offsets_kernel<<<1, 1024, 0, st>>>(W);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const bool bf = in_dtype == KDA_BF16;
+    auto local = bf ? cbwd_local<__nv_bfloat16> : cbwd_local<float>;
+    auto grad_local = bf ? cbwd_grad_local<__nv_bfloat16> : cbwd_grad_local<float>;
+    struct K {
+        const void* fn;
+        int smem;
+    };
+    const K ks[] = {{(const void*)local, SMEM_LOCAL},
+                    {(const void*)cbwd_states, SMEM_STATES},
+                    {(const void*)cbwd_dstates, SMEM_DSTATES},
+                    {(const void*)cbwd_grad_state, SMEM_GRAD_A},
+                    {(const void*)grad_local, SMEM_GRAD_B}};
+    for (const K& k : ks)
+        if ((e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem)) != cudaSuccess)
+            return e;
+    const unsigned chunk_ctas = (unsigned)nch, seq_ctas = (unsigned)((int64_t)p.N * p.H);
+    if (chunk_ctas > 0) local<<<chunk_ctas, NT, SMEM_LOCAL, st>>>(W);
+    cbwd_states<<<seq_ctas, NT, SMEM_STATES, st>>>(W);
+    cbwd_dstates<<<seq_ctas, NT, SMEM_DSTATES, st>>>(W);
+    if (chunk_ctas > 0) {
+        cbwd_grad_state<<<chunk_ctas, NT, SMEM_GRAD_A, st>>>(W);
+        grad_local<<<chunk_ctas, NT, SMEM_GRAD_B, st>>>(W);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

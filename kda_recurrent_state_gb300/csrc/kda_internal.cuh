@@ -117,6 +117,10 @@ struct BwdProblem {
 };
 size_t bwd_workspace(int N, int64_t T_total, int H);
 cudaError_t launch_bwd(BwdProblem p, int in_dtype, void* workspace, cudaStream_t st);
+// The chunked backward (C = 64): workspace bytes for N sequences, T_total tokens, H heads
+// (varlen: packed by cu_seqlens), and its launch sequence.
+size_t chunk_bwd_workspace(int N, int64_t T_total, int H, bool varlen);
+cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace, int* status, cudaStream_t st);
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_decode(const DecodeProblem& p, int in_dtype, int out_dtype, int state_dtype, cudaStream_t st);

@@ -1,5 +1,6 @@
-"""GPU parity of kda_bwd (the gradients for training) against the fp64 oracle's reverse
-mode, through the C ABI.
+"""GPU parity of the backward (the gradients for training) against the fp64 oracle's reverse
+mode, through the C ABI: the chunked kda_chunk_bwd (chunk = 64) and the token-serial
+kda_bwd (chunk = 1).
 
 The loss is L = sum_t <do_t, o_t> + <dS_T, S_T> with random cotangents.  Tolerance, per
 gradient: rel-L2 <= 2e-3 (the forward's bar) and max-abs <= 1e-2 of the gradient's own
@@ -32,9 +33,13 @@ def _oracle_grads(x, la_full, do, dSf, pairs):
                                 batch_heads(do, pairs), dsf)
 
 
+CHUNKS = pytest.mark.parametrize("chunk", [64, 1])
+
+
+@CHUNKS
 @pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("T", [1, 7, 64, 65, 200])
-def test_bwd_parity(T, in_dtype):
+def test_bwd_parity(T, in_dtype, chunk):
     import kda_recurrent_state_gb300 as kda
     from kda_recurrent_state_gb300 import synth
 
@@ -43,8 +48,9 @@ def test_bwd_parity(T, in_dtype):
     g = torch.Generator(device="cuda").manual_seed(5200 + T)
     do = torch.randn(B, T, H, 128, generator=g, device="cuda")
     dSf = torch.randn(B, H, 128, 128, generator=g, device="cuda")
-    got = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], dSf)
+    got = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], dSf, chunk=chunk)
     torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
     pairs = [(b, h) for b in range(B) for h in range(H)]
     ref = _oracle_grads(x, x["log_alpha"], do, dSf, pairs)
     for name in ("dq", "dk", "dv", "dlog_alpha", "dbeta"):
@@ -52,8 +58,9 @@ def test_bwd_parity(T, in_dtype):
     _close(np.stack([np64(got["d_init"][b, h]) for b, h in pairs]), ref["dS0"], "d_init")
 
 
+@CHUNKS
 @pytest.mark.parametrize("gate", [1, 2], ids=["head", "none"])
-def test_bwd_scalar_and_no_gate(gate):
+def test_bwd_scalar_and_no_gate(gate, chunk):
     """Gated DeltaNet's per-head gate gets the sum over key channels of the per-channel
     gradient of the broadcast gate; DeltaNet has no gate gradient."""
     import kda_recurrent_state_gb300 as kda
@@ -64,7 +71,7 @@ def test_bwd_scalar_and_no_gate(gate):
     la_h = synth.head_gates((B, T), H, seed=5302, device="cuda") if gate == 1 else None
     g = torch.Generator(device="cuda").manual_seed(5303)
     do = torch.randn(B, T, H, 128, generator=g, device="cuda")
-    got = kda.kda_bwd(x["q"], x["k"], x["v"], la_h, x["beta"], do, x["init_state"], None, gate=gate)
+    got = kda.kda_bwd(x["q"], x["k"], x["v"], la_h, x["beta"], do, x["init_state"], None, gate=gate, chunk=chunk)
     torch.cuda.synchronize()
     pairs = [(0, h) for h in range(H)]
     la_full = _bcast(la_h) if gate == 1 else torch.zeros_like(x["log_alpha"])
@@ -78,7 +85,8 @@ def test_bwd_scalar_and_no_gate(gate):
         assert got["dlog_alpha"] is None
 
 
-def test_bwd_varlen():
+@CHUNKS
+def test_bwd_varlen(chunk):
     """Packed sequences (one empty, ragged tails): each sequence's gradients against the oracle;
     an empty sequence passes its final-state cotangent through to its initial state."""
     import kda_recurrent_state_gb300 as kda
@@ -90,7 +98,7 @@ def test_bwd_varlen():
     do = torch.randn(xv["q"].shape[0], H, 128, generator=g, device="cuda")
     dSf = torch.randn(len(lengths), H, 128, 128, generator=g, device="cuda")
     got = kda.kda_bwd(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], do, xv["init_states"], dSf,
-                      cu_seqlens=xv["cu_seqlens"])
+                      cu_seqlens=xv["cu_seqlens"], chunk=chunk)
     torch.cuda.synchronize()
     cu = xv["cu_seqlens"].tolist()
     heads = [0, 1]
@@ -108,7 +116,8 @@ def test_bwd_varlen():
         _close(np64(got["d_init"][s]), ref["dS0"], f"seq {s} d_init")
 
 
-def test_bwd_slow_gates_long():
+@CHUNKS
+def test_bwd_slow_gates_long(chunk):
     """Slow gates keep gradients flowing back over thousands of tokens and across many
     checkpoint segments: B=1, H=2, T=2048."""
     import kda_recurrent_state_gb300 as kda
@@ -117,7 +126,7 @@ def test_bwd_slow_gates_long():
     x = synth.prefill_inputs(1, 2048, 2, seed=5501, device="cuda", init="normal", gate="slow")
     g = torch.Generator(device="cuda").manual_seed(5502)
     do = torch.randn(1, 2048, 2, 128, generator=g, device="cuda")
-    got = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"])
+    got = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], chunk=chunk)
     torch.cuda.synchronize()
     pairs = [(0, 0), (0, 1)]
     ref = _oracle_grads(x, x["log_alpha"], do, None, pairs)
@@ -126,14 +135,51 @@ def test_bwd_slow_gates_long():
     _close(np.stack([np64(got["d_init"][b, h]) for b, h in pairs]), ref["dS0"], "d_init")
 
 
-def test_bwd_deterministic():
+@CHUNKS
+def test_bwd_deterministic(chunk):
     import kda_recurrent_state_gb300 as kda
     from kda_recurrent_state_gb300 import synth
 
     x = synth.prefill_inputs(2, 333, 3, seed=5601, device="cuda", init="normal")
     do = torch.randn(2, 333, 3, 128, generator=torch.Generator(device="cuda").manual_seed(1), device="cuda")
-    g1 = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"])
-    g2 = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"])
+    g1 = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], chunk=chunk)
+    g2 = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], chunk=chunk)
     torch.cuda.synchronize()
     for name in g1:
         assert torch.equal(g1[name], g2[name]), name
+
+
+def test_chunk_bwd_gate_range_is_reported():
+    """A half-chunk whose summed log-decay is below -80 cannot be factored in fp32: the chunked
+    backward records KDA_STATUS_GATE_RANGE (nothing faults), and chunk = 1 still matches the oracle."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    x = synth.prefill_inputs(1, 64, 1, seed=5701, device="cuda", init="normal")
+    la = x["log_alpha"].clone()
+    la[0, 40:44] = -30.0  # rows 32..63 of the chunk sum to about -120
+    do = torch.randn(1, 64, 1, 128, generator=torch.Generator(device="cuda").manual_seed(5702), device="cuda")
+    kda.kda_get_device_status()
+    kda.kda_bwd(x["q"], x["k"], x["v"], la, x["beta"], do, x["init_state"], chunk=64)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == kda.binding.KDA_STATUS_GATE_RANGE
+    got = kda.kda_bwd(x["q"], x["k"], x["v"], la, x["beta"], do, x["init_state"], chunk=1)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    ref = _oracle_grads(dict(x, log_alpha=la), la, do, None, [(0, 0)])
+    for name in ("dq", "dk", "dv", "dbeta"):
+        _close(batch_heads(got[name], [(0, 0)]), ref[name], name)
+
+
+def test_chunk_bwd_workspace_and_bad_chunk():
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    x = synth.prefill_inputs(1, 100, 1, seed=5801, device="cuda")
+    do = torch.zeros(1, 100, 1, 128, device="cuda")
+    with pytest.raises(kda.KdaError):
+        kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, chunk=16)
+    need = kda.kda_workspace_size(kda.KDA_OP_CHUNK_BWD, 1, 100, 1, chunk=64)
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kda.KdaError):
+        kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, chunk=64, workspace=small)

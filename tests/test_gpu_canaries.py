@@ -92,21 +92,24 @@ def test_pool_and_backward_stay_in_bounds():
 
     x = synth.prefill_inputs(1, 77, 2, seed=1205, device="cuda", init="normal")
     do = torch.randn(1, 77, 2, 128, device="cuda")
-    g = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"])
-    bufs = {}
-    for name, t in g.items():
-        bufs[name] = guarded(tuple(t.shape), torch.float32)
     lib = kda.binding.lib()
     P = kda.binding._ptr
-    need = kda.kda_workspace_size(kda.KDA_OP_BWD, 1, 77, 2)
-    wb, ws = guarded((need // 4,), torch.float32)
-    rc = lib.kda_bwd(P(x["q"]), P(x["k"]), P(x["v"]), P(x["log_alpha"]), 0, P(x["beta"]), P(x["init_state"]), P(do),
-                     None, None, 1, 77, 2, 128, 128, P(bufs["dq"][1]), P(bufs["dk"][1]), P(bufs["dv"][1]),
-                     P(bufs["dlog_alpha"][1]), P(bufs["dbeta"][1]), P(bufs["d_init"][1]), 0, P(ws), need,
-                     kda.binding._stream(None))
-    torch.cuda.synchronize()
-    assert rc == 0
-    for name, (b, v) in bufs.items():
-        assert guards_intact(b), name
-        assert torch.equal(v, g[name]), name
-    assert guards_intact(wb)
+    for chunk in (1, 64):  # token-serial kda_bwd, chunked kda_chunk_bwd
+        g = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], chunk=chunk)
+        bufs = {name: guarded(tuple(t.shape), torch.float32) for name, t in g.items()}
+        need = kda.kda_workspace_size(kda.KDA_OP_CHUNK_BWD, 1, 77, 2, chunk=chunk)
+        wb, ws = guarded((need // 4,), torch.float32)
+        head = (P(x["q"]), P(x["k"]), P(x["v"]), P(x["log_alpha"]), 0, P(x["beta"]), P(x["init_state"]), P(do),
+                None, None, 1, 77, 2, 128, 128)
+        grads = (P(bufs["dq"][1]), P(bufs["dk"][1]), P(bufs["dv"][1]), P(bufs["dlog_alpha"][1]), P(bufs["dbeta"][1]),
+                 P(bufs["d_init"][1]), 0)
+        if chunk == 1:
+            rc = lib.kda_bwd(*head, *grads, P(ws), need, kda.binding._stream(None))
+        else:
+            rc = lib.kda_chunk_bwd(*head, chunk, *grads, P(ws), need, kda.binding._stream(None))
+        torch.cuda.synchronize()
+        assert rc == 0
+        for name, (b, v) in bufs.items():
+            assert guards_intact(b), (chunk, name)
+            assert torch.equal(v, g[name]), (chunk, name)
+        assert guards_intact(wb), chunk

@@ -17,7 +17,7 @@ def test_noalloc_equals_workspace_call():
     x = synth.prefill_inputs(2, 500, 3, seed=9101, device="cuda", init="normal")
     do = torch.randn(2, 500, 3, 128, generator=torch.Generator(device="cuda").manual_seed(9102), device="cuda")
     dSf = torch.randn(2, 3, 128, 128, generator=torch.Generator(device="cuda").manual_seed(9103), device="cuda")
-    ref = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], dSf)
+    ref = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], dSf, chunk=1)
     got = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], dSf, no_alloc=True)
     torch.cuda.synchronize()
     for name in ref:
@@ -26,7 +26,7 @@ def test_noalloc_equals_workspace_call():
     xv = synth.varlen_inputs([300, 0, 129], 2, seed=9104, device="cuda")
     dov = torch.randn(429, 2, 128, generator=torch.Generator(device="cuda").manual_seed(9105), device="cuda")
     refv = kda.kda_bwd(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], dov, xv["init_states"],
-                       cu_seqlens=xv["cu_seqlens"])
+                       cu_seqlens=xv["cu_seqlens"], chunk=1)
     gotv = kda.kda_bwd(xv["q"], xv["k"], xv["v"], xv["log_alpha"], xv["beta"], dov, xv["init_states"],
                        cu_seqlens=xv["cu_seqlens"], no_alloc=True)
     torch.cuda.synchronize()
