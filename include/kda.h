@@ -267,6 +267,7 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
  *               half-chunk whose summed log-decay is below -80 overflows fp32: the
  *               kernel then raises KDA_STATUS_GATE_RANGE and the results are not valid
  *               (use chunk = 1).
+ *               q, k, v and d_out must be 16-byte aligned (KDA_ERR_MISALIGNED otherwise).
  *   chunk = 1   the token-serial evaluation of kda_bwd (no gate limit).
  *   workspace   device, kda_workspace_size(KDA_OP_CHUNK_BWD, N, T_total, H, dk, dv, chunk)
  *               bytes, 16-byte aligned.  For chunk = 64 it holds every chunk's local

@@ -361,6 +361,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const float* 
     const void* al16[] = {init_states, d_final_states, d_init_states, workspace};
     for (const void* p : al16)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if (chunk == 64 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(d_out)))
+        return KDA_ERR_MISALIGNED;  // read as 16-byte (fp32) or 8-byte (bf16) vectors
     const size_t need = kda_workspace_size(KDA_OP_CHUNK_BWD, N, T_total, H, dk, dv, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return KDA_ERR_WORKSPACE;
     BwdProblem p{};

@@ -27,8 +27,10 @@ namespace {
 
 constexpr int C = 64;          // chunk
 constexpr int NT = 512;        // 16 warps
-constexpr int LD = kD + 1;     // row stride of C x D and D x D tiles (odd: column reads hit distinct banks)
-constexpr int LC = C + 1;      // row stride of C x C tiles
+// Row strides of the shared tiles: multiples of 4 floats (16-byte rows for 128-bit loads) and
+// 4 more than a multiple of 32, so 8 consecutive rows start in 8 distinct 16-byte bank groups.
+constexpr int LD = kD + 4;     // C x D and D x D tiles
+constexpr int LC = C + 4;      // C x C tiles
 constexpr int TILE_CD = C * LD;
 constexpr int TILE_DD = kD * LD;
 constexpr int TILE_CC = C * LC;
@@ -71,23 +73,49 @@ struct Frag {
 };
 
 // f (+/-)= A B, A(m, k) = A[m * ARS + k * ACS], B(k, n) = B[k * BRS + n * BCS], k in [0, K).
-// A is read by all lanes of a warp at once (a broadcast); B's columns go to distinct lanes.
+// One of ARS, ACS is 1 (A is stored k-contiguous or m-contiguous) and one of BRS, BCS is 1.
+// Four k at a time: A is read by all lanes of a warp at once (a broadcast) with 128-bit loads
+// along its contiguous dimension; B's columns go to distinct lanes, with 128-bit loads along k
+// when B is stored k-contiguous and 32-bit loads otherwise.  Rows, strides and k steps are
+// multiples of 4 floats, so every 128-bit access is aligned.
 template <bool NEG, int K, int ARS, int ACS, int BRS, int BCS, int M, int N>
 __device__ __forceinline__ void gemm(Frag<M, N>& f, const float* A, const float* B) {
     constexpr int MR = M / 16, NJ = N / 32;
-    const float* a0 = A + (threadIdx.x >> 5) * MR * ARS;
-    const float* b0 = B + (threadIdx.x & 31) * BCS;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float a[MR], b[NJ];
+    constexpr bool A_KC = ACS == 1, B_KC = BRS == 1;
+    static_assert((A_KC || ARS == 1) && (B_KC || BCS == 1) && K % 4 == 0 && MR % 4 == 0, "layout");
+    const int m0 = (threadIdx.x >> 5) * MR, l = threadIdx.x & 31;
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        float a[MR][4], b[NJ][4];
 #pragma unroll
-        for (int i = 0; i < MR; ++i) a[i] = a0[i * ARS + k * ACS];
+        for (int i = 0; i < MR; ++i) {
+            if (A_KC) {
+                const float4 t = *reinterpret_cast<const float4*>(A + (m0 + i) * ARS + k0);
+                a[i][0] = t.x; a[i][1] = t.y; a[i][2] = t.z; a[i][3] = t.w;
+            } else if (i % 4 == 0) {
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) b[j] = b0[k * BRS + 32 * j * BCS];
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float4 t = *reinterpret_cast<const float4*>(A + (k0 + kk) * ACS + m0 + i);
+                    a[i][kk] = t.x; a[i + 1][kk] = t.y; a[i + 2][kk] = t.z; a[i + 3][kk] = t.w;
+                }
+            }
+        }
 #pragma unroll
-        for (int i = 0; i < MR; ++i)
+        for (int j = 0; j < NJ; ++j) {
+            if (B_KC) {
+                const float4 t = *reinterpret_cast<const float4*>(B + (l + 32 * j) * BCS + k0);
+                b[j][0] = t.x; b[j][1] = t.y; b[j][2] = t.z; b[j][3] = t.w;
+            } else {
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) f.v[i][j] = fmaf(NEG ? -a[i] : a[i], b[j], f.v[i][j]);
+                for (int kk = 0; kk < 4; ++kk) b[j][kk] = B[(k0 + kk) * BRS + l + 32 * j];
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int i = 0; i < MR; ++i)
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) f.v[i][j] = fmaf(NEG ? -a[i][kk] : a[i][kk], b[j][kk], f.v[i][j]);
     }
 }
 
@@ -113,20 +141,45 @@ __device__ __forceinline__ void from_global(Frag<M, N>& f, const float* src) {
         for (int j = 0; j < Frag<M, N>::NJ; ++j) f.v[i][j] = src[Frag<M, N>::row(i) * N + Frag<M, N>::col(j)];
 }
 
-// Dense [rows][D] record in global memory -> shared tile with row stride LD, optionally scaled per row.
-__device__ __forceinline__ void load_tile(float* dst, const float* src, int rows, const float* row_scale = nullptr) {
-    for (int idx = threadIdx.x; idx < rows * kD; idx += NT) {
-        const int r = idx >> 7, c = idx & 127;
-        const float x = src[idx];
-        dst[r * LD + c] = row_scale ? row_scale[r] * x : x;
+// Dense [ROWS][D] record in global memory -> shared tile with row stride LD, optionally scaled per
+// row.  Every thread issues all of its 16-byte loads before it stores any.
+template <int ROWS>
+__device__ __forceinline__ void load_tile(float* dst, const float* src, const float* row_scale = nullptr) {
+    constexpr int PER = ROWS * (kD / 4) / NT;  // float4 per thread
+    float4 x[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = reinterpret_cast<const float4*>(src)[threadIdx.x + i * NT];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int g = threadIdx.x + i * NT, r = g >> 5, c4 = (g & 31) * 4;
+        float4 v = x[i];
+        if (row_scale) {
+            const float sc = row_scale[r];
+            v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
+        }
+        *reinterpret_cast<float4*>(dst + r * LD + c4) = v;
     }
 }
 __device__ __forceinline__ void load_cc(float* dst, const float* src) {
-    for (int idx = threadIdx.x; idx < C * C; idx += NT) dst[(idx >> 6) * LC + (idx & 63)] = src[idx];
+    constexpr int PER = C * C / 4 / NT;
+    float4 x[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = reinterpret_cast<const float4*>(src)[threadIdx.x + i * NT];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int g = threadIdx.x + i * NT;
+        *reinterpret_cast<float4*>(dst + (g >> 4) * LC + (g & 15) * 4) = x[i];
+    }
 }
 
-__device__ __forceinline__ float ldin(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
-__device__ __forceinline__ float ldin(const float* p, size_t i) { return p[i]; }
+// Four consecutive elements as fp32 (bf16 widens exactly: it is the high half of an fp32).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ float4 scale4(float4 v, float s) { return make_float4(v.x * s, v.y * s, v.z * s, v.w * s); }
 
 __device__ __forceinline__ void seq_of(const BwdProblem& P, int s, int64_t& start, int64_t& len) {
     if (P.cu_seqlens) {
@@ -143,6 +196,17 @@ struct ChunkAt {
     int64_t n, tok0;
     int L;  // valid rows
 };
+
+// The chunk's rows of a token-major [.., H, D] tensor at head h, in groups of 4 elements (rows >= L:
+// zero).  Group i of thread t is row (t + i NT) / 32, columns 4 ((t + i NT) % 32) .. +3.
+template <typename Tin>
+__device__ __forceinline__ void load_rows(float4 (&x)[4], const Tin* src, const ChunkAt& c, int H, int h) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int g = threadIdx.x + i * NT, r = g >> 5, c4 = (g & 31) * 4;
+        x[i] = r < c.L ? ld4(src + ((size_t)(c.tok0 + r) * H + h) * kD + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
 
 // The chunk with global index cg: the last sequence s with co[s] <= cg (empty sequences own no chunk).
 __device__ __forceinline__ bool locate_chunk(const CBwd& W, int64_t cg, ChunkAt& c) {
@@ -194,28 +258,33 @@ __global__ void chunk_offsets_kernel(CBwd W) {
     }
 }
 
-// Cumulative log-decay of the chunk into g (rows >= L: no decay), and beta (rows >= L: 0).
-__device__ __forceinline__ void load_gates(const CBwd& W, const ChunkAt& c, int h, float* g, float* beta) {
+// Cumulative log-decay of the chunk into g (rows >= L: no decay), and beta (rows >= L: 0).  Thread t
+// scans rows 16 sg .. 16 sg + 15 of channel ch (sg = t / 128, ch = t % 128) in registers; each
+// segment is then offset by the totals of the segments before it (`tot`: 4 x D scratch).
+__device__ __forceinline__ void load_gates(const CBwd& W, const ChunkAt& c, int h, float* g, float* beta, float* tot) {
     const BwdProblem& P = W.p;
-    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
-        const int r = idx >> 7, col = idx & 127;
+    const int ch = threadIdx.x & 127, sg = threadIdx.x >> 7;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = sg * 16 + i;
         float la = 0.f;
         if (r < c.L) {
             const size_t row = (size_t)(c.tok0 + r) * P.H + h;
-            la = P.gate == kGateChannel ? P.log_alpha[row * kD + col] : P.gate == kGateHead ? P.log_alpha[row] : 0.f;
+            la = P.gate == kGateChannel ? P.log_alpha[row * kD + ch] : P.gate == kGateHead ? P.log_alpha[row] : 0.f;
         }
-        g[r * LD + col] = la;
+        x[i] = la;
     }
+#pragma unroll
+    for (int i = 1; i < 16; ++i) x[i] += x[i - 1];
+    tot[sg * kD + ch] = x[15];
     if (beta && threadIdx.x < C)
         beta[threadIdx.x] = (int)threadIdx.x < c.L ? P.beta[(size_t)(c.tok0 + threadIdx.x) * P.H + h] : 0.f;
     __syncthreads();
-    if (threadIdx.x < kD) {
-        float run = 0.f;
-        for (int r = 0; r < C; ++r) {
-            run += g[r * LD + threadIdx.x];
-            g[r * LD + threadIdx.x] = run;
-        }
-    }
+    float off = 0.f;
+    for (int k = 0; k < sg; ++k) off += tot[k * kD + ch];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[(sg * 16 + i) * LD + ch] = x[i] + off;
     __syncthreads();
 }
 
@@ -223,24 +292,31 @@ __device__ __forceinline__ void load_gates(const CBwd& W, const ChunkAt& c, int 
 template <typename Tin>
 __device__ __forceinline__ void scaled_qk(const CBwd& W, const ChunkAt& c, int h, const float* g, float* sQ,
                                           float* sK, float* sH, float* Kh_out) {
-    const Tin* q = static_cast<const Tin*>(W.p.q);
-    const Tin* k = static_cast<const Tin*>(W.p.k);
+    float4 q4[4], k4[4];
+    load_rows(q4, static_cast<const Tin*>(W.p.q), c, W.p.H, h);
+    load_rows(k4, static_cast<const Tin*>(W.p.k), c, W.p.H, h);
     bool bad = false;
-    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
-        const int r = idx >> 7, col = idx & 127;
-        const float x = g[r * LD + col] - g[31 * LD + col];
-        bad |= fabsf(x) > kExpLimit;
-        const float e = expf(x), f = expf(-x);
-        float qv = 0.f, kv = 0.f;
-        if (r < c.L) {
-            const size_t off = ((size_t)(c.tok0 + r) * W.p.H + h) * kD + col;
-            qv = ldin(q, off);
-            kv = ldin(k, off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gi = threadIdx.x + i * NT, r = gi >> 5, c4 = (gi & 31) * 4;
+        const float4 gr = *reinterpret_cast<const float4*>(g + r * LD + c4);
+        const float4 g31 = *reinterpret_cast<const float4*>(g + 31 * LD + c4);
+        const float x[4] = {gr.x - g31.x, gr.y - g31.y, gr.z - g31.z, gr.w - g31.w};
+        const float qa[4] = {q4[i].x, q4[i].y, q4[i].z, q4[i].w}, ka[4] = {k4[i].x, k4[i].y, k4[i].z, k4[i].w};
+        float qo[4], ko[4], ho[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            bad |= fabsf(x[e]) > kExpLimit;
+            const float ee = expf(x[e]), ff = expf(-x[e]);
+            qo[e] = qa[e] * ee;
+            ko[e] = ka[e] * ee;
+            ho[e] = ka[e] * ff;
         }
-        sQ[r * LD + col] = qv * e;
-        sK[r * LD + col] = kv * e;
-        sH[r * LD + col] = kv * f;
-        if (Kh_out) Kh_out[idx] = kv * f;
+        *reinterpret_cast<float4*>(sQ + r * LD + c4) = make_float4(qo[0], qo[1], qo[2], qo[3]);
+        *reinterpret_cast<float4*>(sK + r * LD + c4) = make_float4(ko[0], ko[1], ko[2], ko[3]);
+        const float4 hv = make_float4(ho[0], ho[1], ho[2], ho[3]);
+        *reinterpret_cast<float4*>(sH + r * LD + c4) = hv;
+        if (Kh_out) *reinterpret_cast<float4*>(Kh_out + r * kD + c4) = hv;
     }
     if (bad) atomicCAS(W.status, 0, (int)KDA_STATUS_GATE_RANGE);
 }
@@ -318,7 +394,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
     if (!locate_chunk(W, cg, c)) return;
     const size_t ch = (size_t)cg * P.H + h;
 
-    load_gates(W, c, h, sA, sB);
+    load_gates(W, c, h, sA, sB, sY);
     scaled_qk<Tin>(W, c, h, sA, sQ, sK, sH, W.Kh + ch * REC_CD);
     if (threadIdx.x < kD) {
         const float ref = sA[31 * LD + threadIdx.x];
@@ -326,17 +402,16 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
         W.sc[ch * 3 * kD + kD + threadIdx.x] = expf(sA[63 * LD + threadIdx.x] - ref);
     }
     __syncthreads();
-    const Tin* v = static_cast<const Tin*>(P.v);
-    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
-        const int r = idx >> 7, col = idx & 127;
-        float vv = 0.f, dov = 0.f;
-        if (r < c.L) {
-            const size_t off = ((size_t)(c.tok0 + r) * P.H + h) * kD + col;
-            vv = ldin(v, off);
-            dov = P.dout[off];
+    {
+        float4 v4[4], o4[4];
+        load_rows(v4, static_cast<const Tin*>(P.v), c, P.H, h);
+        load_rows(o4, P.dout, c, P.H, h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gi = threadIdx.x + i * NT, r = gi >> 5, c4 = (gi & 31) * 4;
+            *reinterpret_cast<float4*>(sA + r * LD + c4) = scale4(v4[i], sB[r]);
+            *reinterpret_cast<float4*>(sO + r * LD + c4) = o4[i];
         }
-        sA[r * LD + col] = sB[r] * vv;
-        sO[r * LD + col] = dov;
     }
     {
         Frag<C, C> gk, pq;
@@ -414,8 +489,8 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
         if (n == nc) break;
         const size_t ch = (size_t)(base + n) * P.H + h;
         if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
-        load_tile(sW, W.Wt + ch * REC_CD, C);
-        load_tile(sH, W.Kh + ch * REC_CD, C);
+        load_tile<C>(sW, W.Wt + ch * REC_CD);
+        load_tile<C>(sH, W.Kh + ch * REC_CD);
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
@@ -460,8 +535,8 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
         const size_t ch = (size_t)(base + n) * P.H + h;
         to_global(dS, W.dS + ch * REC_DD);
         if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
-        load_tile(sW, W.Wt + ch * REC_CD, C);
-        load_tile(sH, W.Kh + ch * REC_CD, C);
+        load_tile<C>(sW, W.Wt + ch * REC_CD);
+        load_tile<C>(sH, W.Kh + ch * REC_CD);
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
@@ -510,8 +585,8 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     const float* dSC = W.dS + ch * REC_DD;
     if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
     __syncthreads();
-    load_tile(sR, S0, kD, sE);
-    load_tile(s1, W.Wt + ch * REC_CD, C);
+    load_tile<kD>(sR, S0, sE);
+    load_tile<C>(s1, W.Wt + ch * REC_CD);
     __syncthreads();
     Frag<C, kD> u;
     from_global(u, W.Up + ch * REC_CD);
@@ -529,11 +604,16 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
         }
     }
     __syncthreads();
-    load_tile(sR, dSC, kD, sE + kD);  // dD
-    load_tile(s1, W.Kh + ch * REC_CD, C);
-    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
-        const int r = idx >> 7, col = idx & 127;
-        s4[r * LD + col] = r < c.L ? P.dout[((size_t)(c.tok0 + r) * P.H + h) * kD + col] : 0.f;
+    load_tile<kD>(sR, dSC, sE + kD);  // dD
+    load_tile<C>(s1, W.Kh + ch * REC_CD);
+    {
+        float4 o4[4];
+        load_rows(o4, P.dout, c, P.H, h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gi = threadIdx.x + i * NT;
+            *reinterpret_cast<float4*>(s4 + (gi >> 5) * LD + (gi & 31) * 4) = o4[i];
+        }
     }
     load_cc(s5, W.Pq + ch * REC_CC);
     __syncthreads();
@@ -550,7 +630,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     dp.zero();
     gemm<false, kD, LD, 1, 1, LD>(dp, s4, s2);  // dP = lower(dO U^T)
     __syncthreads();
-    load_tile(sR, S0, kD, sE);  // X again
+    load_tile<kD>(sR, S0, sE);  // X again
 #pragma unroll
     for (int i = 0; i < Frag<C, C>::MR; ++i)
 #pragma unroll
@@ -595,17 +675,21 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     using F = Frag<C, kD>;
     using FC = Frag<C, C>;
 
-    load_gates(W, c, h, s0, sB);
+    load_gates(W, c, h, s0, sB, sM);
     scaled_qk<Tin>(W, c, h, s0, sQ, sK, sH, nullptr);
     if (threadIdx.x < kD) sG[threadIdx.x] = W.sc[ch * 3 * kD + 2 * kD + threadIdx.x];
     load_cc(sT, W.Tm + ch * REC_CC);
     load_cc(sP, W.Pq + ch * REC_CC);
-    load_tile(sX, W.Up + ch * REC_CD, C);  // dU
+    load_tile<C>(sX, W.Up + ch * REC_CD);  // dU
     __syncthreads();
-    const Tin* v = static_cast<const Tin*>(P.v);
-    for (int idx = threadIdx.x; idx < C * kD; idx += NT) {
-        const int r = idx >> 7, col = idx & 127;
-        s0[r * LD + col] = r < c.L ? ldin(v, ((size_t)(c.tok0 + r) * P.H + h) * kD + col) : 0.f;
+    {
+        float4 v4[4];
+        load_rows(v4, static_cast<const Tin*>(P.v), c, P.H, h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gi = threadIdx.x + i * NT;
+            *reinterpret_cast<float4*>(s0 + (gi >> 5) * LD + (gi & 31) * 4) = v4[i];
+        }
     }
     __syncthreads();
 
@@ -630,7 +714,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
         }
     }
     __syncthreads();
-    load_tile(sX, W.Wt + ch * REC_CD, C);  // dW~
+    load_tile<C>(sX, W.Wt + ch * REC_CD);  // dW~
     __syncthreads();
     gemm<false, kD, LD, 1, 1, LD>(dT, sX, sK);  // + dW~ K~^T
 #pragma unroll
@@ -699,7 +783,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     }
     // decay gradient and dq, dk
     __syncthreads();
-    load_gates(W, c, h, sX, nullptr);  // g again
+    load_gates(W, c, h, sX, nullptr, sM);  // g again
     F dQt;
     from_global(dQt, W.Ej + ch * REC_DD);
 #pragma unroll
