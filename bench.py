@@ -41,8 +41,11 @@ PREFILL_FLOP = 6 * D * D + CHUNK * (3 * D + 2 * D)
 # decode: fp32 state read + written (2 x 65,536 B; half that for a bf16 state) + q,k,v bf16,
 # log_alpha, beta, out fp32 per session-head
 DEC_BYTES = 2 * D * D * 4 + 3 * 256 + 512 + 4 + 512
-# backward: the forward step (7 dk dv) and its reverse mode (15 dk dv) per token-head
-BWD_FLOP = 22 * D * D
+# backward, chunked (C = 64): the fp32 GEMMs of one chunk-head, 2 M N K each with the C x C
+# products counted in full as computed: 15 of C x C x D, 11 of C x D x D, 2 of C x C x C, plus the
+# triangular inverse (2 C^3 / 3); per token-head, divided by C
+BWD_CHUNK_FLOP = (15 * 2 * CHUNK * CHUNK * D + 11 * 2 * CHUNK * D * D + 2 * 2 * CHUNK ** 3
+                  + 2 * CHUNK ** 3 // 3) / CHUNK
 FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # CUDA-core fp32 peak from unit counts and the max SM clock
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -365,13 +368,14 @@ def run_ours(args):
     line["gpu_launches"] += 5
     del xv, vout, vfin, vsnaps
 
-    # ---- backward (training) at B=4, H=32, T=8192: token-serial reverse mode on CUDA cores,
-    # reported against the fp32 CUDA-core peak (ALU-bound, not a tensor-core path)
+    # ---- backward (training) at B=4, H=32, T=8192: the chunked reverse mode (fp32 GEMMs on CUDA
+    # cores), reported against the fp32 CUDA-core peak (ALU-bound, not a tensor-core path)
     xb = synth.prefill_inputs(4, 8192, 32, seed=synth.SEED_BASE + 1, device=dev, init="normal")
     do = torch.randn(4, 8192, 32, D, generator=torch.Generator(device=dev).manual_seed(7), device=dev)
-    ws_b = torch.empty(binding.kda_workspace_size(binding.KDA_OP_BWD, 4, 4 * 8192, 32), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(binding.kda_workspace_size(binding.KDA_OP_CHUNK_BWD, 4, 4 * 8192, 32, chunk=CHUNK),
+                       dtype=torch.uint8, device=dev)
     bwd = lambda: kda.kda_bwd(xb["q"], xb["k"], xb["v"], xb["log_alpha"], xb["beta"], do, xb["init_state"],
-                              workspace=ws_b)
+                              chunk=CHUNK, workspace=ws_b)
     bwd()
     torch.cuda.synchronize()
     e0.record(stream)
@@ -380,14 +384,15 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     bt = e0.elapsed_time(e1) / 1e3 / 2
-    btf = 4 * 8192 * 32 * BWD_FLOP / bt / 1e12
+    btf = 4 * 8192 * 32 * BWD_CHUNK_FLOP / bt / 1e12
     line["bwd"] = {"tokens_per_s": 4 * 8192 / bt, "ms_per_call": bt * 1e3,
                    "roofline": {"bound": "alu", "achieved": btf, "peak": FP32_TFLOPS, "unit": "TFLOP/s",
                                 "frac": btf / FP32_TFLOPS,
                                 "peak_source": "152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz (nominal)"},
-                   "workload": "kda_bwd B=4 H=32 T=8192, bf16 q/k/v, fp32 gates/state/cotangents, "
-                               "S0 ~ N(0,0.02); flops = 22 dk dv per token-head"}
-    line["gpu_launches"] += 2
+                   "workload": "kda_chunk_bwd chunk 64, B=4 H=32 T=8192, bf16 q/k/v, fp32 gates/state/"
+                               f"cotangents, S0 ~ N(0,0.02); flops = {BWD_CHUNK_FLOP:.0f} per token-head "
+                               "(the chunked form's fp32 GEMMs)"}
+    line["gpu_launches"] += 12  # 6 launches per call
     assert kda.kda_get_device_status() == 0, "device status raised by the backward"
     del xb, do, ws_b
 
