@@ -12,7 +12,7 @@
 // output does not depend on ref, so its adjoint is zero and is not formed.  Four passes:
 //   local   (chunk-parallel)  g, Q~, K~, K^, T, W~, U', P, and the chunk's output-gradient term
 //                             E = Q~^T dO - W~^T (P^T dO) of the state gradient
-//   states  (serial per head) S_{n+1} = Diag(e^{g_C-ref}) (X + K^^T (U' - W~ X)), every S_n kept
+//   states  (serial per head) S_{n+1} = Diag(e^{g_C-ref}) (X + K^^T (U' - W~ X)), every S_n and U kept
 //   dstates (serial per head) dS_n = Diag(e^ref) (dD - W~^T (K^ dD) + E), dD = Diag(e^{g_C-ref}) dS_{n+1}
 //   grads   (chunk-parallel, two kernels) every input gradient of the chunk from S_n and dS_{n+1}
 // Every product is a small dense GEMM over shared-memory tiles, so the work runs at CUDA-core
@@ -46,7 +46,7 @@ struct CBwd {
     int64_t* co_w;
     // per chunk-head (index (cg * H + h)):
     float* Wt;  // W~ [C][D]; after the first gradient kernel: dW~
-    float* Up;  // U' [C][D]; then dU
+    float* Up;  // U' [C][D]; then U (states pass); then dU
     float* Kh;  // K^ [C][D]
     float* Ej;  // E [D][D]; then dQ~ (first half) and dK^ (second half), partial
     float* Tm;  // T [C][C]
@@ -170,6 +170,26 @@ __device__ __forceinline__ void load_cc(float* dst, const float* src) {
         const int g = threadIdx.x + i * NT;
         *reinterpret_cast<float4*>(dst + (g >> 4) * LC + (g & 15) * 4) = x[i];
     }
+}
+
+// Asynchronous 16-byte global -> shared copies (cp.async), committed and awaited in groups.
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// A dense [C][D] record into a shared tile with row stride LD, and a vector of 2 D scales.
+__device__ __forceinline__ void tile_async(float* dst, const float* src) {
+#pragma unroll
+    for (int i = 0; i < C * kD / 4 / NT; ++i) {
+        const int g = threadIdx.x + i * NT;
+        cp_async16(dst + (g >> 5) * LD + (g & 31) * 4, src + g * 4);
+    }
+}
+__device__ __forceinline__ void scales_async(float* dst, const float* src) {
+    if (threadIdx.x < 2 * kD / 4) cp_async16(dst + 4 * threadIdx.x, src + 4 * threadIdx.x);
 }
 
 // Four consecutive elements as fp32 (bf16 widens exactly: it is the high half of an fp32).
@@ -466,7 +486,9 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
 }
 
 // ---- pass 2: chunk-start states, serial per (sequence, head) -----------------------------------
-constexpr int SMEM_STATES = (TILE_DD + 3 * TILE_CD + 2 * kD) * 4;
+// W~ and the scales of chunk n+1 are copied in while K^^T U of chunk n runs, and K^ of chunk n+1
+// while the next chunk's W~ X runs (cp.async groups; the scales are double-buffered).
+constexpr int SMEM_STATES = (TILE_DD + 3 * TILE_CD + 4 * kD) * 4;
 
 __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
     extern __shared__ __align__(16) float sm[];
@@ -474,7 +496,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
     float* sU = sX + TILE_DD;    // U
     float* sW = sU + TILE_CD;    // W~
     float* sH = sW + TILE_CD;    // K^
-    float* sE = sH + TILE_CD;    // e^ref, e^{g_C - ref}
+    float* sE = sH + TILE_CD;    // [2][e^ref, e^{g_C - ref}]
     const BwdProblem& P = W.p;
     const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
     int64_t start, len;
@@ -484,35 +506,58 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
     F S;
     if (P.init) from_global(S, P.init + ((size_t)s * P.H + h) * REC_DD);
     else S.zero();
+    if (nc > 0) {
+        const size_t ch0 = (size_t)base * P.H + h;
+        tile_async(sW, W.Wt + ch0 * REC_CD);
+        scales_async(sE, W.sc + ch0 * 3 * kD);
+        cp_commit();
+        tile_async(sH, W.Kh + ch0 * REC_CD);
+        cp_commit();
+    }
     for (int64_t n = 0; n <= nc; ++n) {
         to_global(S, W.S + ((size_t)(base + s + n) * P.H + h) * REC_DD);
         if (n == nc) break;
         const size_t ch = (size_t)(base + n) * P.H + h;
-        if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
-        load_tile<C>(sW, W.Wt + ch * REC_CD);
-        load_tile<C>(sH, W.Kh + ch * REC_CD);
+        const float* e = sE + (n & 1) * 2 * kD;
+        Frag<C, kD> u;
+        from_global(u, W.Up + ch * REC_CD);
+        cp_wait<1>();  // W~ and the scales of this chunk
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
-            for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= sE[F::row(i)];
+            for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= e[F::row(i)];
         to_smem(S, sX, LD);
         __syncthreads();
-        Frag<C, kD> u;
-        from_global(u, W.Up + ch * REC_CD);
         gemm<true, kD, LD, 1, LD, 1>(u, sW, sX);  // U = U' - W~ X
         to_smem(u, sU, LD);
+        to_global(u, W.Up + ch * REC_CD);  // U replaces U' (read back by the gradient pass)
+        __syncthreads();
+        if (n + 1 < nc) {
+            tile_async(sW, W.Wt + (ch + P.H) * REC_CD);
+            scales_async(sE + ((n + 1) & 1) * 2 * kD, W.sc + (ch + P.H) * 3 * kD);
+            cp_commit();
+            cp_wait<1>();  // K^ of this chunk
+        } else {
+            cp_wait<0>();
+        }
         __syncthreads();
         gemm<false, C, 1, LD, LD, 1>(S, sH, sU);  // X + K^^T U
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
-            for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= sE[kD + F::row(i)];
+            for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= e[kD + F::row(i)];
         __syncthreads();
+        if (n + 1 < nc) {
+            tile_async(sH, W.Kh + (ch + P.H) * REC_CD);
+            cp_commit();
+        }
     }
 }
 
 // ---- pass 3: state gradients at chunk ends, serial per (sequence, head), last chunk first --------
+// K^ and the scales of chunk n-1 are copied in while W~^T Z of chunk n runs, and W~ of chunk n-1
+// while the next chunk's K^ dD runs.
 constexpr int SMEM_DSTATES = SMEM_STATES;
 
 __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
@@ -521,7 +566,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
     float* sZ = sD + TILE_DD;    // K^ dD
     float* sW = sZ + TILE_CD;    // W~
     float* sH = sW + TILE_CD;    // K^
-    float* sE = sH + TILE_CD;
+    float* sE = sH + TILE_CD;    // [2][e^ref, e^{g_C - ref}]
     const BwdProblem& P = W.p;
     const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
     int64_t start, len;
@@ -531,17 +576,24 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
     F dS;
     if (P.dfinal) from_global(dS, P.dfinal + ((size_t)s * P.H + h) * REC_DD);
     else dS.zero();
+    if (nc > 0) {
+        const size_t chl = (size_t)(base + nc - 1) * P.H + h;
+        tile_async(sH, W.Kh + chl * REC_CD);
+        scales_async(sE + ((nc - 1) & 1) * 2 * kD, W.sc + chl * 3 * kD);
+        cp_commit();
+        tile_async(sW, W.Wt + chl * REC_CD);
+        cp_commit();
+    }
     for (int64_t n = nc - 1; n >= 0; --n) {
         const size_t ch = (size_t)(base + n) * P.H + h;
+        const float* e = sE + (n & 1) * 2 * kD;
         to_global(dS, W.dS + ch * REC_DD);
-        if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
-        load_tile<C>(sW, W.Wt + ch * REC_CD);
-        load_tile<C>(sH, W.Kh + ch * REC_CD);
+        cp_wait<1>();  // K^ and the scales of this chunk
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
-            for (int j = 0; j < F::NJ; ++j) dS.v[i][j] *= sE[kD + F::row(i)];
+            for (int j = 0; j < F::NJ; ++j) dS.v[i][j] *= e[kD + F::row(i)];
         to_smem(dS, sD, LD);
         __syncthreads();
         Frag<C, kD> z;
@@ -549,14 +601,27 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
         gemm<false, kD, LD, 1, LD, 1>(z, sH, sD);  // K^ dD
         to_smem(z, sZ, LD);
         __syncthreads();
+        if (n > 0) {
+            tile_async(sH, W.Kh + (ch - P.H) * REC_CD);
+            scales_async(sE + ((n - 1) & 1) * 2 * kD, W.sc + (ch - P.H) * 3 * kD);
+            cp_commit();
+            cp_wait<1>();  // W~ of this chunk
+        } else {
+            cp_wait<0>();
+        }
+        __syncthreads();
         gemm<true, C, 1, LD, LD, 1>(dS, sW, sZ);  // dD - W~^T (K^ dD)
         const float* E = W.Ej + ch * REC_DD;
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
             for (int j = 0; j < F::NJ; ++j)
-                dS.v[i][j] = (dS.v[i][j] + E[F::row(i) * kD + F::col(j)]) * sE[F::row(i)];
+                dS.v[i][j] = (dS.v[i][j] + E[F::row(i) * kD + F::col(j)]) * e[F::row(i)];
         __syncthreads();
+        if (n > 0) {
+            tile_async(sW, W.Wt + (ch - P.H) * REC_CD);
+            cp_commit();
+        }
     }
     if (P.dinit) to_global(dS, P.dinit + ((size_t)s * P.H + h) * REC_DD);
 }
@@ -566,8 +631,8 @@ constexpr int SMEM_GRAD_A = (TILE_DD + 4 * TILE_CD + TILE_CC + 2 * kD) * 4;
 
 __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     extern __shared__ __align__(16) float sm[];
-    float* sR = sm;              // X, then dD, then X
-    float* s1 = sR + TILE_DD;    // W~, then K^
+    float* sR = sm;              // dD, then X
+    float* s1 = sR + TILE_DD;    // K^
     float* s2 = s1 + TILE_CD;    // U
     float* s3 = s2 + TILE_CD;    // dU
     float* s4 = s3 + TILE_CD;    // dO
@@ -584,14 +649,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     const float* SC = W.S + s_slot + (size_t)P.H * REC_DD;  // the next state of the same sequence
     const float* dSC = W.dS + ch * REC_DD;
     if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
-    __syncthreads();
-    load_tile<kD>(sR, S0, sE);
-    load_tile<C>(s1, W.Wt + ch * REC_CD);
-    __syncthreads();
-    Frag<C, kD> u;
-    from_global(u, W.Up + ch * REC_CD);
-    gemm<true, kD, LD, 1, LD, 1>(u, s1, sR);  // U = U' - W~ X
-    to_smem(u, s2, LD);
+    load_tile<C>(s2, W.Up + ch * REC_CD);  // U, stored by the states pass
     {  // final-decay gradient: sum_j S_C[c][j] dS_C[c][j], one warp per row
         const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
         for (int r = w; r < kD; r += 16) {
