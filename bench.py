@@ -496,6 +496,23 @@ def profile_case():
     print("profile case done")
 
 
+def profile_bwd():
+    """Small backward workload for ncu captures: the chunked backward on B=1, H=32, T=8192
+    (4,096 chunk-heads, 1.4 GB of workspace), two calls."""
+    import torch
+
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    x = synth.prefill_inputs(1, 8192, 32, seed=synth.SEED_BASE + 6, device="cuda", init="normal")
+    do = torch.randn(1, 8192, 32, D, generator=torch.Generator(device="cuda").manual_seed(8), device="cuda")
+    for _ in range(2):
+        kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], chunk=CHUNK)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    print("profile bwd done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -513,10 +530,15 @@ def main():
     ap.add_argument("--profile-case", action="store_true",
                     help="run two launches of the chunked prefill on B=1,H=16,T=32768 (fp32 out) and exit: the "
                          "small case the committed ncu summaries are captured on")
+    ap.add_argument("--profile-bwd", action="store_true",
+                    help="run two chunked backward calls on B=1,H=32,T=8192 and exit: the small case of the "
+                         "committed backward ncu summary")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
     if args.profile_case:
         profile_case()
+    elif args.profile_bwd:
+        profile_bwd()
     elif args.impl == "reference":
         run_reference(args)
     else:
