@@ -181,6 +181,41 @@ def test_bwd_validation(L):
     assert b.kda_workspace_size(b.KDA_OP_BWD, 4, 4 * 8192, 32) == (32 * (4 * 8192 // 64 + 4 + 1) + 4 * 32 * 16) * 65536
 
 
+def test_chunk_bwd_validation(L):
+    """kda_chunk_bwd: chunk 64 (chunked) or 1 (token-serial); 16-byte aligned q, k, v, d_out for
+    chunk 64; its workspace size, written out from the records it holds."""
+    from kda_recurrent_state_gb300 import binding as b
+
+    P = ctypes.c_void_p
+
+    def cbwd(chunk=64, q=16, ws=0x10000, ws_bytes=None, N=1, T=8):
+        ptr = P(16)
+        if ws_bytes is None:
+            ws_bytes = b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, N, N * T, 1, chunk=chunk)
+        return L.kda_chunk_bwd(P(q), ptr, ptr, ptr, 0, ptr, None, ptr, None, None, N, T, 1, 128, 128, chunk, ptr, ptr,
+                               ptr, ptr, ptr, None, 0, P(ws) if ws else None, ws_bytes, None)
+
+    assert cbwd(chunk=16, ws_bytes=1 << 20) == b.KDA_ERR_UNSUPPORTED
+    assert cbwd(chunk=0, ws_bytes=1 << 20) == b.KDA_ERR_UNSUPPORTED
+    assert cbwd(q=0x1008) == b.KDA_ERR_MISALIGNED        # 8-byte aligned: enough for chunk 1 only
+    assert cbwd(chunk=64, ws=None) == b.KDA_ERR_WORKSPACE
+    need = b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, 1, 8, 1, chunk=64)
+    assert cbwd(ws_bytes=need - 1) == b.KDA_ERR_WORKSPACE
+    assert cbwd(N=0) == b.KDA_OK
+    # chunk 1 is kda_bwd, with kda_bwd's workspace
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, 4, 4 * 8192, 32, chunk=1) == \
+        b.kda_workspace_size(b.KDA_OP_BWD, 4, 4 * 8192, 32)
+    # chunk 64: per chunk-head W~, U', K^ (C x D), E and dS (D x D), T and P (C x C) and three D-vectors;
+    # per (chunk + sequence) and head one D x D state; at most T_total / 64 + N chunks
+    C, D, N, Tt, H = 64, 128, 4, 4 * 8192, 32
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    nch = (Tt // C + N) * H
+    per = 3 * C * D + 2 * D * D + 2 * C * C + 3 * D
+    want = al((N + 1) * 8) + al(nch * per * 4) + al((Tt // C + N) * H * D * D * 4 + N * H * D * D * 4)
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, N, Tt, H, chunk=64) == want
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, N, Tt, H, chunk=16) == 0
+
+
 def test_bwd_noalloc_rejects_oversize(L):
     """A problem whose backward scratch exceeds the static 128 MiB is refused before any CUDA call."""
     from kda_recurrent_state_gb300 import binding as b
