@@ -84,7 +84,7 @@ __device__ __forceinline__ void gemm(Frag<M, N>& f, const float* A, const float*
     constexpr bool A_KC = ACS == 1, B_KC = BRS == 1;
     static_assert((A_KC || ARS == 1) && (B_KC || BCS == 1) && K % 4 == 0 && MR % 4 == 0, "layout");
     const int m0 = (threadIdx.x >> 5) * MR, l = threadIdx.x & 31;
-#pragma unroll 2
+#pragma unroll 4
     for (int k0 = 0; k0 < K; k0 += 4) {
         float a[MR][4], b[NJ][4];
 #pragma unroll

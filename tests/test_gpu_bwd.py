@@ -183,3 +183,22 @@ def test_chunk_bwd_workspace_and_bad_chunk():
     small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(kda.KdaError):
         kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, chunk=64, workspace=small)
+
+
+def test_chunk_bwd_full_size_sampled():
+    """The timed backward configuration (B=4, H=32, T=8192, bf16 inputs, S0 ~ N(0,0.02), chunk 64):
+    two sampled (sequence, head) pairs over all 8192 tokens against the oracle."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    B, T, H = 4, 8192, 32
+    x = synth.prefill_inputs(B, T, H, seed=synth.SEED_BASE + 1, device="cuda", init="normal")
+    do = torch.randn(B, T, H, 128, generator=torch.Generator(device="cuda").manual_seed(7), device="cuda")
+    got = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], chunk=64)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    pairs = [(1, 5), (3, 30)]
+    ref = _oracle_grads(x, x["log_alpha"], do, None, pairs)
+    for name in ("dq", "dk", "dv", "dlog_alpha", "dbeta"):
+        _close(batch_heads(got[name], pairs), ref[name], name)
+    _close(np.stack([np64(got["d_init"][b, h]) for b, h in pairs]), ref["dS0"], "d_init")
