@@ -202,3 +202,19 @@ def test_chunk_bwd_full_size_sampled():
     for name in ("dq", "dk", "dv", "dlog_alpha", "dbeta"):
         _close(batch_heads(got[name], pairs), ref[name], name)
     _close(np.stack([np64(got["d_init"][b, h]) for b, h in pairs]), ref["dS0"], "d_init")
+
+
+@CHUNKS
+def test_bwd_no_tokens(chunk):
+    """T = 0: no gradient but the initial state's, which equals the final state's cotangent."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    x = synth.prefill_inputs(2, 0, 3, seed=5901, device="cuda", init="normal")
+    dSf = torch.randn(2, 3, 128, 128, generator=torch.Generator(device="cuda").manual_seed(5902), device="cuda")
+    do = torch.zeros(2, 0, 3, 128, device="cuda")
+    got = kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], dSf, chunk=chunk)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    assert torch.equal(got["d_init"], dSf)
+    assert got["dq"].numel() == 0 and got["dbeta"].numel() == 0
