@@ -8,7 +8,8 @@ largest magnitude).  One reading is added for inputs outside the workloads: on t
 path the operands are fp16, and when an output's reference is nearly cancelled (a single
 token whose q.k is close to 0, so o = beta (q.k) v is small) their rounding gives a large
 relative error at a tiny absolute one.  There the relative bar is replaced by
-max-abs <= 1e-3, ten times tighter than the absolute bar."""
+max-abs <= 1e-3, ten times tighter than the absolute bar.  A gradient that is identically
+zero in the oracle has no relative error at all; there the absolute bar alone applies."""
 import random
 
 import numpy as np
@@ -188,3 +189,57 @@ def test_random_decode():
         ro, rs = fn(seq(d["q"]), seq(d["k"]), seq(d["v"]), seq(d["log_alpha"]), seq(d["beta"]), S0)
         _check("out", np.stack([np64(o[b, h]) for o in outs])[None], ro, c, 1)
         _check("state", np64(state[b, h].float())[None], rs, c, 1)
+
+
+def test_random_bwd_packed():
+    """The chunked backward on random packed batches (empty and one-token sequences, every gate
+    layout, both input dtypes, with and without a final-state cotangent): a sampled (sequence,
+    head) against the oracle, and empty sequences passing d_final through.  A gradient that is
+    identically zero in the oracle (dlog alpha of a one-token sequence from a zero state: the
+    output does not depend on that gate) has no relative error, so there the absolute bar applies."""
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+    from oracle import oracle
+
+    rng = random.Random("bwd-packed")
+    for _ in range(CASES):
+        N, H = rng.randrange(1, 7), rng.choice([1, 2, 3])
+        lengths = [rng.choice([0, 1, 2, 63, 64, 65, 128, rng.randrange(0, 700)]) for _ in range(N)]
+        dt, gl, gate = rng.choice([torch.bfloat16, torch.float32]), rng.choice(["config", "slow"]), rng.choice([0, 0, 1, 2])
+        seed = rng.randrange(10**6)
+        c = dict(lengths=lengths, H=H, dt=dt, gl=gl, gate=gate, seed=seed)
+        xv = synth.varlen_inputs(lengths, H, seed=seed, device="cuda", in_dtype=dt, gate=gl)
+        Tt = xv["q"].shape[0]
+        la = {0: xv["log_alpha"], 1: synth.head_gates((Tt,), H, seed=seed + 1, device="cuda", gate=gl), 2: None}[gate]
+        gen = torch.Generator(device="cuda").manual_seed(seed + 2)
+        do = torch.randn(Tt, H, 128, generator=gen, device="cuda")
+        dSf = torch.randn(N, H, 128, 128, generator=gen, device="cuda") if rng.random() < 0.5 else None
+        g = kda.kda_bwd(xv["q"], xv["k"], xv["v"], la, xv["beta"], do, xv["init_states"], dSf, gate=gate,
+                        cu_seqlens=xv["cu_seqlens"], chunk=64)
+        torch.cuda.synchronize()
+        assert kda.kda_get_device_status() == 0, c
+        cu = xv["cu_seqlens"].tolist()
+        for s in range(N):
+            if cu[s] == cu[s + 1]:
+                want = dSf[s] if dSf is not None else torch.zeros_like(g["d_init"][s])
+                assert torch.equal(g["d_init"][s], want), (c, s)
+        s = rng.choice([i for i in range(N) if cu[i + 1] > cu[i]] or [None])
+        if s is None:
+            continue
+        a, b, h = cu[s], cu[s + 1], rng.randrange(H)
+        la_full = (torch.zeros(Tt, H, 128, device="cuda") if gate == 2
+                   else la.unsqueeze(-1).expand(Tt, H, 128) if gate == 1 else la)
+        ref = oracle.recurrent_bwd(packed_heads(xv["q"], a, b, [h]), packed_heads(xv["k"], a, b, [h]),
+                                   packed_heads(xv["v"], a, b, [h]), packed_heads(la_full, a, b, [h]),
+                                   packed_heads(xv["beta"], a, b, [h]), np64(xv["init_states"][s, h])[None],
+                                   packed_heads(do, a, b, [h]), None if dSf is None else np64(dSf[s, h])[None])
+        pairs = [("dq", ref["dq"]), ("dk", ref["dk"]), ("dv", ref["dv"]), ("dbeta", ref["dbeta"])]
+        if gate != 2:
+            pairs.append(("dlog_alpha", ref["dlog_alpha"] if gate == 0 else ref["dlog_alpha"].sum(-1)))
+        for name, r in pairs:
+            got = packed_heads(g[name], a, b, [h])
+            if not np.any(r):  # identically zero: the absolute bar
+                assert float(np.abs(got).max()) <= MAX_ABS, (name, c, s)
+            else:
+                _check(name, got, r, dict(c, seq=s, head=h), 1, grad=True)
+        _check("d_init", np64(g["d_init"][s, h])[None], ref["dS0"], dict(c, seq=s, head=h), 1, grad=True)
