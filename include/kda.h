@@ -72,7 +72,8 @@ typedef enum {
     KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
     KDA_ERR_TIMEOUT = 5,     /* device status: a bounded wait inside a kernel expired */
     KDA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than kda_workspace_size() */
-    KDA_STATUS_GATE_RANGE = 7, /* device status: a half-chunk's summed log-decay was below -15 ln 2 */
+    KDA_STATUS_GATE_RANGE = 7, /* device status: a half-chunk's summed log-decay was below -15 ln 2
+                                  (chunked forward) or -80 (kda_chunk_bwd) */
     KDA_STATUS_SLOT_RANGE = 8, /* device status: a state-pool slot index outside [-1, pool_slots) was skipped */
     KDA_ERR_SCRATCH_TOO_SMALL = 9 /* the problem needs more than the library's static scratch (kda_bwd_noalloc) */
 } kda_status;

@@ -74,7 +74,9 @@ const char* kda_status_string(int status) {
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel expired";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
-        case KDA_STATUS_GATE_RANGE: return "KDA_STATUS_GATE_RANGE: a half-chunk's summed log-decay is below -15 ln 2";
+        case KDA_STATUS_GATE_RANGE:
+            return "KDA_STATUS_GATE_RANGE: a half-chunk's summed log-decay is below -15 ln 2 (chunked forward) or -80 "
+                   "(kda_chunk_bwd); use chunk = 1";
         case KDA_STATUS_SLOT_RANGE:
             return "KDA_STATUS_SLOT_RANGE: a state-pool slot index was out of range and skipped";
         case KDA_ERR_SCRATCH_TOO_SMALL:
