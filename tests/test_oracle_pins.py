@@ -405,7 +405,21 @@ def pin_bwd_closed_form_no_write(lib):
                                    atol=1e-12)
 
 
-BWD_PINS = [pin_bwd_finite_differences, pin_bwd_closed_form_no_write]
+def pin_bwd_first_gate_from_zero_state(lib):
+    """From a zero initial state the first token's gate multiplies nothing (S_1 = beta_1 k_1 v_1^T),
+    so no output depends on it and its gradient is exactly zero; from a non-zero state it is not.
+    Later tokens' gate gradients are non-zero either way."""
+    rng = np.random.default_rng(33)
+    q, k, v, la, b = _inputs(rng, 1, 5, 6, 4)
+    do, dSf = rng.standard_normal((1, 5, 4)), rng.standard_normal((1, 6, 4))
+    g0 = oracle.recurrent_bwd(q, k, v, la, b, np.zeros((1, 6, 4)), do, dSf, lib=lib)
+    np.testing.assert_array_equal(g0["dlog_alpha"][0, 0], 0.0)
+    assert np.all(np.abs(g0["dlog_alpha"][0, 1:]).max(axis=-1) > 0)
+    g1 = oracle.recurrent_bwd(q, k, v, la, b, rng.standard_normal((1, 6, 4)), do, dSf, lib=lib)
+    assert np.abs(g1["dlog_alpha"][0, 0]).max() > 0
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_closed_form_no_write, pin_bwd_first_gate_from_zero_state]
 
 
 @pytest.mark.parametrize("pin", BWD_PINS, ids=[p.__name__ for p in BWD_PINS])
