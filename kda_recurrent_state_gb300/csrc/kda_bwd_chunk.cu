@@ -12,8 +12,9 @@
 // output does not depend on ref, so its adjoint is zero and is not formed.  Four passes:
 //   local   (chunk-parallel)  g, Q~, K~, K^, T, W~, U', P, and the chunk's output-gradient term
 //                             E = Q~^T dO - W~^T (P^T dO) of the state gradient
-//   states  (serial per head) S_{n+1} = Diag(e^{g_C-ref}) (X + K^^T (U' - W~ X)), every S_n and U kept
-//   dstates (serial per head) dS_n = Diag(e^ref) (dD - W~^T (K^ dD) + E), dD = Diag(e^{g_C-ref}) dS_{n+1}
+//   states  (serial per head, split over value columns when SMs are idle)
+//                             S_{n+1} = Diag(e^{g_C-ref}) (X + K^^T (U' - W~ X)), every S_n and U kept
+//   dstates (the same)        dS_n = Diag(e^ref) (dD - W~^T (K^ dD) + E), dD = Diag(e^{g_C-ref}) dS_{n+1}
 //   grads   (chunk-parallel, two kernels) every input gradient of the chunk from S_n and dS_{n+1}
 // Every product is a small dense GEMM over shared-memory tiles, so the work runs at CUDA-core
 // throughput instead of the token-serial path's per-token reduction latency.  All arithmetic is
@@ -126,19 +127,20 @@ __device__ __forceinline__ void to_smem(const Frag<M, N>& f, float* dst, int ld)
 #pragma unroll
         for (int j = 0; j < Frag<M, N>::NJ; ++j) dst[Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)] = f.v[i][j];
 }
+// Global copies of a fragment: row r of the block at dst + r * ld (a column slice when ld > N).
 template <int M, int N>
-__device__ __forceinline__ void to_global(const Frag<M, N>& f, float* dst) {
+__device__ __forceinline__ void to_global(const Frag<M, N>& f, float* dst, int ld = N) {
 #pragma unroll
     for (int i = 0; i < Frag<M, N>::MR; ++i)
 #pragma unroll
-        for (int j = 0; j < Frag<M, N>::NJ; ++j) dst[Frag<M, N>::row(i) * N + Frag<M, N>::col(j)] = f.v[i][j];
+        for (int j = 0; j < Frag<M, N>::NJ; ++j) dst[(size_t)Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)] = f.v[i][j];
 }
 template <int M, int N>
-__device__ __forceinline__ void from_global(Frag<M, N>& f, const float* src) {
+__device__ __forceinline__ void from_global(Frag<M, N>& f, const float* src, int ld = N) {
 #pragma unroll
     for (int i = 0; i < Frag<M, N>::MR; ++i)
 #pragma unroll
-        for (int j = 0; j < Frag<M, N>::NJ; ++j) f.v[i][j] = src[Frag<M, N>::row(i) * N + Frag<M, N>::col(j)];
+        for (int j = 0; j < Frag<M, N>::NJ; ++j) f.v[i][j] = src[(size_t)Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)];
 }
 
 // Dense [ROWS][D] record in global memory -> shared tile with row stride LD, optionally scaled per
@@ -485,26 +487,38 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
     }
 }
 
-// ---- pass 2: chunk-start states, serial per (sequence, head) -----------------------------------
-// W~ and the scales of chunk n+1 are copied in while K^^T U of chunk n runs, and K^ of chunk n+1
-// while the next chunk's W~ X runs (cp.async groups; the scales are double-buffered).
-constexpr int SMEM_STATES = (TILE_DD + 3 * TILE_CD + 4 * kD) * 4;
+// ---- passes 2 and 3: the serial recurrences ----------------------------------------------------
+// Value columns are independent in both recurrences, so a (sequence, head) unit may be split over
+// kD / NCOL CTAs, each carrying NCOL columns of the state (or its gradient); the launch splits
+// when the units alone would leave SMs idle.  Every output element sums over k in the same order
+// at every NCOL, so the split changes no bit of the result.
+template <int NCOL>
+constexpr int smem_serial() {
+    return (kD * (NCOL + 4) + C * (NCOL + 4) + 2 * TILE_CD + 4 * kD) * 4;
+}
 
+// Pass 2: chunk-start states.  W~ and the scales of chunk n+1 are copied in while K^^T U of
+// chunk n runs, and K^ of chunk n+1 while the next chunk's W~ X runs (cp.async groups; the
+// scales are double-buffered).
+template <int NCOL>
 __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
+    constexpr int LS = NCOL + 4;  // row stride of the column-slice tiles
     extern __shared__ __align__(16) float sm[];
-    float* sX = sm;              // X = Diag(e^ref) S
-    float* sU = sX + TILE_DD;    // U
-    float* sW = sU + TILE_CD;    // W~
+    float* sX = sm;              // X = Diag(e^ref) S, this CTA's columns
+    float* sU = sX + kD * LS;    // U, this CTA's columns
+    float* sW = sU + C * LS;     // W~
     float* sH = sW + TILE_CD;    // K^
     float* sE = sH + TILE_CD;    // [2][e^ref, e^{g_C - ref}]
     const BwdProblem& P = W.p;
-    const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
+    constexpr int PARTS = kD / NCOL;
+    const int unit = blockIdx.x / PARTS, c0 = (blockIdx.x % PARTS) * NCOL;
+    const int h = unit % P.H, s = unit / P.H;
     int64_t start, len;
     seq_of(P, s, start, len);
     const int64_t nc = (len + C - 1) / C, base = W.co[s];
-    using F = Frag<kD, kD>;
+    using F = Frag<kD, NCOL>;
     F S;
-    if (P.init) from_global(S, P.init + ((size_t)s * P.H + h) * REC_DD);
+    if (P.init) from_global(S, P.init + ((size_t)s * P.H + h) * REC_DD + c0, kD);
     else S.zero();
     if (nc > 0) {
         const size_t ch0 = (size_t)base * P.H + h;
@@ -515,23 +529,23 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
         cp_commit();
     }
     for (int64_t n = 0; n <= nc; ++n) {
-        to_global(S, W.S + ((size_t)(base + s + n) * P.H + h) * REC_DD);
+        to_global(S, W.S + ((size_t)(base + s + n) * P.H + h) * REC_DD + c0, kD);
         if (n == nc) break;
         const size_t ch = (size_t)(base + n) * P.H + h;
         const float* e = sE + (n & 1) * 2 * kD;
-        Frag<C, kD> u;
-        from_global(u, W.Up + ch * REC_CD);
+        Frag<C, NCOL> u;
+        from_global(u, W.Up + ch * REC_CD + c0, kD);
         cp_wait<1>();  // W~ and the scales of this chunk
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
             for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= e[F::row(i)];
-        to_smem(S, sX, LD);
+        to_smem(S, sX, LS);
         __syncthreads();
-        gemm<true, kD, LD, 1, LD, 1>(u, sW, sX);  // U = U' - W~ X
-        to_smem(u, sU, LD);
-        to_global(u, W.Up + ch * REC_CD);  // U replaces U' (read back by the gradient pass)
+        gemm<true, kD, LD, 1, LS, 1>(u, sW, sX);  // U = U' - W~ X
+        to_smem(u, sU, LS);
+        to_global(u, W.Up + ch * REC_CD + c0, kD);  // U replaces U' (read back by the gradient pass)
         __syncthreads();
         if (n + 1 < nc) {
             tile_async(sW, W.Wt + (ch + P.H) * REC_CD);
@@ -542,7 +556,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
             cp_wait<0>();
         }
         __syncthreads();
-        gemm<false, C, 1, LD, LD, 1>(S, sH, sU);  // X + K^^T U
+        gemm<false, C, 1, LD, LS, 1>(S, sH, sU);  // X + K^^T U
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
@@ -555,26 +569,27 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
     }
 }
 
-// ---- pass 3: state gradients at chunk ends, serial per (sequence, head), last chunk first --------
-// K^ and the scales of chunk n-1 are copied in while W~^T Z of chunk n runs, and W~ of chunk n-1
-// while the next chunk's K^ dD runs.
-constexpr int SMEM_DSTATES = SMEM_STATES;
-
+// Pass 3: state gradients at chunk ends, last chunk first.  K^ and the scales of chunk n-1 are
+// copied in while W~^T Z of chunk n runs, and W~ of chunk n-1 while the next chunk's K^ dD runs.
+template <int NCOL>
 __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
+    constexpr int LS = NCOL + 4;
     extern __shared__ __align__(16) float sm[];
-    float* sD = sm;              // dD = Diag(e^{g_C - ref}) dS
-    float* sZ = sD + TILE_DD;    // K^ dD
-    float* sW = sZ + TILE_CD;    // W~
+    float* sD = sm;              // dD = Diag(e^{g_C - ref}) dS, this CTA's columns
+    float* sZ = sD + kD * LS;    // K^ dD, this CTA's columns
+    float* sW = sZ + C * LS;     // W~
     float* sH = sW + TILE_CD;    // K^
     float* sE = sH + TILE_CD;    // [2][e^ref, e^{g_C - ref}]
     const BwdProblem& P = W.p;
-    const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
+    constexpr int PARTS = kD / NCOL;
+    const int unit = blockIdx.x / PARTS, c0 = (blockIdx.x % PARTS) * NCOL;
+    const int h = unit % P.H, s = unit / P.H;
     int64_t start, len;
     seq_of(P, s, start, len);
     const int64_t nc = (len + C - 1) / C, base = W.co[s];
-    using F = Frag<kD, kD>;
+    using F = Frag<kD, NCOL>;
     F dS;
-    if (P.dfinal) from_global(dS, P.dfinal + ((size_t)s * P.H + h) * REC_DD);
+    if (P.dfinal) from_global(dS, P.dfinal + ((size_t)s * P.H + h) * REC_DD + c0, kD);
     else dS.zero();
     if (nc > 0) {
         const size_t chl = (size_t)(base + nc - 1) * P.H + h;
@@ -587,19 +602,19 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
     for (int64_t n = nc - 1; n >= 0; --n) {
         const size_t ch = (size_t)(base + n) * P.H + h;
         const float* e = sE + (n & 1) * 2 * kD;
-        to_global(dS, W.dS + ch * REC_DD);
+        to_global(dS, W.dS + ch * REC_DD + c0, kD);
         cp_wait<1>();  // K^ and the scales of this chunk
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
             for (int j = 0; j < F::NJ; ++j) dS.v[i][j] *= e[kD + F::row(i)];
-        to_smem(dS, sD, LD);
+        to_smem(dS, sD, LS);
         __syncthreads();
-        Frag<C, kD> z;
+        Frag<C, NCOL> z;
         z.zero();
-        gemm<false, kD, LD, 1, LD, 1>(z, sH, sD);  // K^ dD
-        to_smem(z, sZ, LD);
+        gemm<false, kD, LD, 1, LS, 1>(z, sH, sD);  // K^ dD
+        to_smem(z, sZ, LS);
         __syncthreads();
         if (n > 0) {
             tile_async(sH, W.Kh + (ch - P.H) * REC_CD);
@@ -610,20 +625,20 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
             cp_wait<0>();
         }
         __syncthreads();
-        gemm<true, C, 1, LD, LD, 1>(dS, sW, sZ);  // dD - W~^T (K^ dD)
-        const float* E = W.Ej + ch * REC_DD;
+        gemm<true, C, 1, LD, LS, 1>(dS, sW, sZ);  // dD - W~^T (K^ dD)
+        const float* E = W.Ej + ch * REC_DD + c0;
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
             for (int j = 0; j < F::NJ; ++j)
-                dS.v[i][j] = (dS.v[i][j] + E[F::row(i) * kD + F::col(j)]) * e[F::row(i)];
+                dS.v[i][j] = (dS.v[i][j] + E[(size_t)F::row(i) * kD + F::col(j)]) * e[F::row(i)];
         __syncthreads();
         if (n > 0) {
             tile_async(sW, W.Wt + (ch - P.H) * REC_CD);
             cp_commit();
         }
     }
-    if (P.dinit) to_global(dS, P.dinit + ((size_t)s * P.H + h) * REC_DD);
+    if (P.dinit) to_global(dS, P.dinit + ((size_t)s * P.H + h) * REC_DD + c0, kD);
 }
 
 // ---- pass 4a: the state-dependent gradient products of each chunk --------------------------------
@@ -938,18 +953,33 @@ cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace,
         const void* fn;
         int smem;
     };
+    // Column split of the serial passes: while twice the units still fit on the SMs, halve the
+    // columns per CTA (128, 64 or 32).
+    int sms = 0, dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const int64_t units = (int64_t)p.N * p.H;
+    int parts = 1;
+    while (parts < 4 && units * parts * 2 <= sms) parts *= 2;
+    const void* states = parts == 1 ? (const void*)cbwd_states<128> : parts == 2 ? (const void*)cbwd_states<64>
+                                                                                : (const void*)cbwd_states<32>;
+    const void* dstates = parts == 1 ? (const void*)cbwd_dstates<128> : parts == 2 ? (const void*)cbwd_dstates<64>
+                                                                                  : (const void*)cbwd_dstates<32>;
+    const int smem_ser = parts == 1 ? smem_serial<128>() : parts == 2 ? smem_serial<64>() : smem_serial<32>();
     const K ks[] = {{(const void*)local, SMEM_LOCAL},
-                    {(const void*)cbwd_states, SMEM_STATES},
-                    {(const void*)cbwd_dstates, SMEM_DSTATES},
+                    {states, smem_ser},
+                    {dstates, smem_ser},
                     {(const void*)cbwd_grad_state, SMEM_GRAD_A},
                     {(const void*)grad_local, SMEM_GRAD_B}};
     for (const K& k : ks)
         if ((e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem)) != cudaSuccess)
             return e;
-    const unsigned chunk_ctas = (unsigned)nch, seq_ctas = (unsigned)((int64_t)p.N * p.H);
+    const unsigned chunk_ctas = (unsigned)nch, seq_ctas = (unsigned)(units * parts);
     if (chunk_ctas > 0) local<<<chunk_ctas, NT, SMEM_LOCAL, st>>>(W);
-    cbwd_states<<<seq_ctas, NT, SMEM_STATES, st>>>(W);
-    cbwd_dstates<<<seq_ctas, NT, SMEM_DSTATES, st>>>(W);
+    void* args[] = {&W};
+    if ((e = cudaLaunchKernel(states, dim3(seq_ctas), dim3(NT), args, (size_t)smem_ser, st)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernel(dstates, dim3(seq_ctas), dim3(NT), args, (size_t)smem_ser, st)) != cudaSuccess) return e;
     if (chunk_ctas > 0) {
         cbwd_grad_state<<<chunk_ctas, NT, SMEM_GRAD_A, st>>>(W);
         grad_local<<<chunk_ctas, NT, SMEM_GRAD_B, st>>>(W);
