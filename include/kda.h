@@ -263,7 +263,9 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
  *               lshu.cn/news/263999): the chunk-local products and all input gradients
  *               run chunk-parallel as fp32 GEMMs on shared-memory tiles; only the
  *               chunk-to-chunk state and state-gradient recurrences (two dependent
- *               products per chunk) are serial per (sequence, head).  fp32 throughout;
+ *               products per chunk) are serial per (sequence, head), split over value
+ *               columns onto 2 or 4 CTAs when the units alone leave SMs idle (the
+ *               results are the same bit for bit).  fp32 throughout;
  *               deterministic.  Each chunk factors its decays about its 32nd row, so a
  *               half-chunk whose summed log-decay is below -80 overflows fp32: the
  *               kernel then raises KDA_STATUS_GATE_RANGE and the results are not valid
