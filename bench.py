@@ -42,9 +42,9 @@ PREFILL_FLOP = 6 * D * D + CHUNK * (3 * D + 2 * D)
 # log_alpha, beta, out fp32 per session-head
 DEC_BYTES = 2 * D * D * 4 + 3 * 256 + 512 + 4 + 512
 # backward, chunked (C = 64): the fp32 GEMMs of one chunk-head, 2 M N K each with the C x C
-# products counted in full as computed: 15 of C x C x D, 11 of C x D x D, 2 of C x C x C, plus the
+# products counted in full as computed: 15 of C x C x D, 10 of C x D x D, 2 of C x C x C, plus the
 # triangular inverse (2 C^3 / 3); per token-head, divided by C
-BWD_CHUNK_FLOP = (15 * 2 * CHUNK * CHUNK * D + 11 * 2 * CHUNK * D * D + 2 * 2 * CHUNK ** 3
+BWD_CHUNK_FLOP = (15 * 2 * CHUNK * CHUNK * D + 10 * 2 * CHUNK * D * D + 2 * 2 * CHUNK ** 3
                   + 2 * CHUNK ** 3 // 3) / CHUNK
 FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # CUDA-core fp32 peak from unit counts and the max SM clock
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
