@@ -20,7 +20,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -50,23 +49,22 @@ FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # CUDA-core fp32 peak from unit cou
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_chunk_prefill_B1_H16_T32768.md")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_chunk_prefill_B1_H16_T32768.json")
 CHUNK_SRC = os.path.join(ROOT, "kda_recurrent_state_gb300", "csrc", "kda_chunk.cu")
 
 
 def measured_traffic_per_token_head():
-    """DRAM bytes per token-head of the chunked prefill from the committed ncu summary, or
-    None when that summary was taken on a different version of the kernel source."""
+    """DRAM bytes per token-head of the chunked prefill from the JSON record written beside the
+    committed ncu summary, or None when that record was taken on a different version of the
+    kernel source (its sha256 is part of the record)."""
     try:
-        text = open(PROFILE_TRAFFIC).read()
+        rec = json.load(open(PROFILE_TRAFFIC))
         sha = hashlib.sha256(open(CHUNK_SRC, "rb").read()).hexdigest()
-    except OSError:
+    except (OSError, ValueError):
         return None
-    m = re.search(r"kernel source sha256: ([0-9a-f]{64})", text)
-    t = re.search(r"dram bytes per token-head: ([0-9.]+)", text)
-    if not m or not t or m.group(1) != sha:
+    if rec.get("kernel_source_sha256") != sha or "dram_bytes_per_token_head" not in rec:
         return None
-    return float(t.group(1))
+    return float(rec["dram_bytes_per_token_head"])
 
 
 def load_peaks():
@@ -442,7 +440,8 @@ def e2e(args, x, out, fin, ws, dev, out_dtype):
         kda.kda_chunk_fwd_host(host["q"], host["k"], host["v"], host["log_alpha"], host["beta"], None, hout, hfin,
                                segment_tokens=seg, workspace=hws, device=dev)
 
-    step()
+    for _ in range(2):  # warm-up: first touch of the pinned buffers and the copy engines
+        step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -513,6 +512,24 @@ def profile_bwd():
     print("profile bwd done")
 
 
+def profile_decode():
+    """Small decode workload for ncu captures: 64 sessions x 96 heads (fp32 state 0.40 GB, bf16
+    state 0.20 GB, both larger than L2), three steps of each kernel, the state updated in place."""
+    import torch
+
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    d = synth.decode_inputs(64, H, seed=synth.SEED_BASE + 7, steps=3, device="cuda")
+    for fn, st in ((kda.kda_decode_step, d["state"].clone()),
+                   (kda.kda_decode_step_bf16state, d["state"].to(torch.bfloat16))):
+        for s in range(3):
+            fn(d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s], d["beta"][s], st)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    print("profile decode done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,7 +538,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk", type=int, default=64, choices=[1, 64])
     ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
@@ -533,9 +550,14 @@ def main():
     ap.add_argument("--profile-bwd", action="store_true",
                     help="run two chunked backward calls on B=1,H=32,T=8192 and exit: the small case of the "
                          "committed backward ncu summary")
+    ap.add_argument("--profile-decode", action="store_true",
+                    help="run three steps each of the fp32-state and bf16-state decode on 64 sessions x 96 heads "
+                         "and exit: the small case of the committed decode ncu summary")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed warm-up steps
-    if args.profile_case:
+    if args.profile_decode:
+        profile_decode()
+    elif args.profile_case:
         profile_case()
     elif args.profile_bwd:
         profile_bwd()
