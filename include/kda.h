@@ -20,7 +20,8 @@
  *   - Layouts are row-major and token-major:
  *       q, k        [.., H, d_k]   (in_dtype: KDA_BF16 or KDA_F32)
  *       v           [.., H, d_v]   (in_dtype)
- *       log_alpha   [.., H, d_k]   float32, finite and <= 0
+ *       log_alpha   [.., H, d_k]   float32, <= 0 (-inf allowed in the forward calls:
+ *                                  alpha = 0; the backward wants finite values)
  *       beta        [.., H]        float32
  *       state       [.., H, d_k, d_v] float32, row i = key channel i
  *       out         [.., H, d_v]   (out_dtype)
@@ -35,20 +36,28 @@
  *     and snap_offsets 8 bytes; the other decode operands their element size.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  A return of KDA_OK means the work was enqueued.
- *     Faults found inside a kernel (a bounded wait that ran out, a gate out of
- *     the supported range) are recorded in a device status word, never by a
+ *     Faults found inside a kernel (a bounded wait that ran out, a state-pool
+ *     slot out of range) are recorded in a device status word, never by a
  *     trap; read them with kda_get_device_status().
  *   - No C++ exception crosses this boundary.  Results are bit-reproducible
  *     from run to run on the same GPU.
  *   - Numerics of the chunk = 64 path: tensor-core products take fp16 operands
- *     with fp32 accumulation; the state and every carry are fp32.  Inputs must
- *     stay inside the fp16 range after gating: decay factors are taken
- *     relative to the log-decay after a chunk's first 32 tokens, so within
- *     every 64-token chunk the summed log_alpha of tokens 1..31 and of
- *     tokens 32..63 must each be >= -15 ln 2 (about -10.4) per key channel
- *     (otherwise KDA_STATUS_GATE_RANGE is raised in the device status word),
- *     and q, k elements are then scaled by at most 2^15, which L2-normalised
- *     rows (|q_c|, |k_c| <= 1) always satisfy.
+ *     with fp32 accumulation; the state and every carry are fp32.  Decay
+ *     factors are taken relative to the log-decay after a chunk's first 32
+ *     tokens, which keeps every fp16 operand within 2^10 of its undecayed
+ *     value while, in every 64-token chunk, the summed log_alpha of tokens
+ *     1..31 and of tokens 32..63 are each >= -10 ln 2 (about -6.9) per key
+ *     channel.  That covers gates down to a mean of about -0.2 per token.  A
+ *     (sequence, head) with any chunk beyond that bound is marked by the kernel
+ *     and recomputed within the same call by a second pass of the same kernel,
+ *     in which each chunk within the bound goes through the same products (bit
+ *     for bit) and each chunk beyond it applies its tokens one at a time in
+ *     fp32 (exact for any alpha).  So every log_alpha <= 0 is supported,
+ *     including -inf (alpha = 0); only the speed of such units differs, and
+ *     since a chunk's path depends on its own gates only, runs resumed at chunk
+ *     boundaries and snapshots stay bit-exact.  The chunked backward recomputes
+ *     units beyond its fp32 bound (-80 per half-chunk) with the token-serial
+ *     backward.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -72,8 +81,8 @@ typedef enum {
     KDA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
     KDA_ERR_TIMEOUT = 5,     /* device status: a bounded wait inside a kernel expired */
     KDA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than kda_workspace_size() */
-    KDA_STATUS_GATE_RANGE = 7, /* device status: a half-chunk's summed log-decay was below -15 ln 2
-                                  (chunked forward) or -80 (kda_chunk_bwd) */
+    KDA_STATUS_GATE_RANGE = 7, /* no longer raised: units whose gates leave the chunked kernels' range are
+                                  recomputed exactly within the same call (the code is kept for the ABI) */
     KDA_STATUS_SLOT_RANGE = 8, /* device status: a state-pool slot index outside [-1, pool_slots) was skipped */
     KDA_ERR_SCRATCH_TOO_SMALL = 9 /* the problem needs more than the library's static scratch (kda_bwd_noalloc) */
 } kda_status;
@@ -97,7 +106,9 @@ typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_HEAD = 1, KDA_GATE_NONE = 2 } kda_
  *   out         [B, T, H, dv]  out_dtype, o_t = S_t^T q_t
  *   final_state [B, H, dk, dv] float32, or NULL if not wanted
  *   workspace   device scratch of at least kda_workspace_size(KDA_OP_CHUNK, ...)
- *               bytes (may be NULL when that size is 0); contents need no
+ *               bytes, 16-byte aligned (chunk = 64: one int per (sequence, head),
+ *               rounded up to 256 bytes, marking the units the exact pass
+ *               recomputes; chunk = 1: 0 bytes, may be NULL); contents need no
  *               initialisation and are not preserved.
  * B, T or H equal to 0 is valid (nothing to compute; with T = 0 the final
  * state is the initial state).  init_state may alias final_state.
@@ -176,8 +187,8 @@ int kda_decode_step_bf16state(const void* q, const void* k, const void* v, const
  *              NULL selects DeltaNet (alpha = 1 everywhere).
  * Every other argument, the layouts, the snapshot rules, the results' bit-exact
  * reproducibility and the error codes are those of kda_chunk_fwd,
- * kda_varlen_fwd and kda_decode_step.  The per-half-chunk gate range of
- * kda_chunk_fwd applies to the scalar gate in the same way.
+ * kda_varlen_fwd and kda_decode_step.  The chunked path's gate bound, and the
+ * exact recomputation of the units beyond it, apply to the scalar gate in the same way.
  */
 int kda_gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
                       const float* init_state, void* out, float* final_state, int B, int64_t T, int H, int dk,
@@ -266,16 +277,18 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
  *               products per chunk) are serial per (sequence, head), split over value
  *               columns onto 2 or 4 CTAs when the units alone leave SMs idle (the
  *               results are the same bit for bit).  fp32 throughout;
- *               deterministic.  Each chunk factors its decays about its 32nd row, so a
- *               half-chunk whose summed log-decay is below -80 overflows fp32: the
- *               kernel then raises KDA_STATUS_GATE_RANGE and the results are not valid
- *               (use chunk = 1).
+ *               deterministic.  Each chunk factors its decays about its 32nd row, which
+ *               stays in fp32 range while every half-chunk's summed log-decay is >= -80;
+ *               a (sequence, head) with a chunk beyond that is recomputed in the same
+ *               call by the token-serial backward (chunk = 1), so every finite gate is
+ *               supported.
  *               q, k, v and d_out must be 16-byte aligned (KDA_ERR_MISALIGNED otherwise).
  *   chunk = 1   the token-serial evaluation of kda_bwd (no gate limit).
  *   workspace   device, kda_workspace_size(KDA_OP_CHUNK_BWD, N, T_total, H, dk, dv, chunk)
  *               bytes, 16-byte aligned.  For chunk = 64 it holds every chunk's local
  *               products, state and state gradient: about 4.1 KB per (token, head)
- *               (about 5.4 GB at N=4, T=8192, H=32).
+ *               (about 5.4 GB at N=4, T=8192, H=32), and at least the token-serial
+ *               backward's workspace, which the recomputation reuses.
  * Returns KDA_ERR_UNSUPPORTED for any other chunk.
  */
 int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* log_alpha, int gate, const float* beta,
@@ -286,9 +299,12 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
 
 /*
  * kda_bwd without a caller workspace: the scratch is a static device array inside the
- * library, KDA_NOALLOC_SCRATCH_BYTES bytes per device, reserved when this entry point is
- * first used on a device (its address is looked up once per device).  Nothing is
- * allocated per call.  Arguments as for kda_bwd minus workspace and ws_bytes.  Returns
+ * library, KDA_NOALLOC_SCRATCH_BYTES bytes per device.  Under lazy module loading
+ * (CUDA_MODULE_LOADING=LAZY, the default) it is reserved on a device when this entry point
+ * is first used there, and that first call should come before any stream capture; with
+ * CUDA_MODULE_LOADING=EAGER every context that loads the library reserves it at creation.
+ * Its address is looked up on every call (so it stays valid across cudaDeviceReset).
+ * Nothing is allocated per call.  Arguments as for kda_bwd minus workspace and ws_bytes.  Returns
  * KDA_ERR_SCRATCH_TOO_SMALL, without launching anything, when
  * kda_workspace_size(KDA_OP_BWD, N, T_total, H, dk, dv, 64) exceeds the static scratch.
  * Calls on one device share that scratch: at most one may be in flight per device
@@ -370,8 +386,8 @@ const char* kda_status_string(int status);
 
 /*
  * Waits for `stream`, then reads and clears the device status word of the
- * current device: KDA_OK, KDA_ERR_TIMEOUT, KDA_STATUS_GATE_RANGE or KDA_STATUS_SLOT_RANGE (the first
- * fault recorded since the last read).  Returns KDA_ERR_CUDA if the read fails.
+ * current device: KDA_OK, KDA_ERR_TIMEOUT or KDA_STATUS_SLOT_RANGE (the first fault
+ * recorded since the last read).  Returns KDA_ERR_CUDA if the read fails.
  */
 int kda_get_device_status(void* stream);
 

@@ -3,8 +3,6 @@
 // entry point are in include/kda.h.
 #include <nvtx3/nvToolsExt.h>
 
-#include <mutex>
-
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -14,20 +12,11 @@ namespace {
 // that ran out, a gate out of range) here instead of trapping.
 __device__ int g_status;
 
-constexpr int kMaxDevices = 64;
-int* g_status_addr[kMaxDevices];
-std::mutex g_status_mu;
-
+// Device address of the status word on the current device, looked up on every call (not
+// cached, so that it stays valid across a cudaDeviceReset, which reloads the module).
 int* status_ptr() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(g_status_mu);
-    if (!g_status_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-        g_status_addr[dev] = static_cast<int*>(p);
-    }
-    return g_status_addr[dev];
+    void* p = nullptr;
+    return cudaGetSymbolAddress(&p, g_status) == cudaSuccess ? static_cast<int*>(p) : nullptr;
 }
 
 // An NVTX range over one entry point, so that a profiler's timeline shows the library's calls.
@@ -75,8 +64,8 @@ const char* kda_status_string(int status) {
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel expired";
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
         case KDA_STATUS_GATE_RANGE:
-            return "KDA_STATUS_GATE_RANGE: a half-chunk's summed log-decay is below -15 ln 2 (chunked forward) or -80 "
-                   "(kda_chunk_bwd); use chunk = 1";
+            return "KDA_STATUS_GATE_RANGE: no longer raised (units whose gates leave the chunked kernels' range are "
+                   "recomputed exactly within the same call)";
         case KDA_STATUS_SLOT_RANGE:
             return "KDA_STATUS_SLOT_RANGE: a state-pool slot index was out of range and skipped";
         case KDA_ERR_SCRATCH_TOO_SMALL:

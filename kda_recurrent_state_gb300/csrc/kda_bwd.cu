@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_kernel(BwdProblem P) {
     const int tid = threadIdx.x;
     const int c = tid >> 7, i = tid & 127, w = (tid >> 5) & 3, lane = tid & 31;
     const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
+    if (P.redo && !P.redo[(size_t)s * P.H + h]) return;  // as the chunked backward's exact second pass
     int64_t t0, len;
     if (P.cu_seqlens) {
         t0 = P.cu_seqlens[s];

@@ -19,8 +19,9 @@
 // Every product is a small dense GEMM over shared-memory tiles, so the work runs at CUDA-core
 // throughput instead of the token-serial path's per-token reduction latency.  All arithmetic is
 // fp32; sums are in a fixed order, so the result is bit-reproducible.  e^{g-ref} must stay in fp32
-// range: a chunk whose half-chunk log-decay sum is below -80 raises KDA_STATUS_GATE_RANGE (the
-// token-serial backward has no such limit).
+// range: a (sequence, head) with a chunk whose half-chunk log-decay sum is below -80 is flagged,
+// and after these passes the token-serial backward (which has no such limit) recomputes exactly
+// those units.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -45,6 +46,7 @@ struct CBwd {
     int* status;
     const int64_t* co;  // [N+1] first chunk index of each sequence
     int64_t* co_w;
+    int* redo;          // [N * H]: 1 where a chunk of the unit left the fp32 range of e^{+-(g-ref)}
     // per chunk-head (index (cg * H + h)):
     float* Wt;  // W~ [C][D]; after the first gradient kernel: dW~
     float* Up;  // U' [C][D]; then U (states pass); then dU
@@ -278,6 +280,7 @@ __global__ void chunk_offsets_kernel(CBwd W) {
         W.co_w[s] = run;
         run += nch(s);
     }
+    for (int64_t u = t; u < (int64_t)N * W.p.H; u += 1024) W.redo[u] = 0;
 }
 
 // Cumulative log-decay of the chunk into g (rows >= L: no decay), and beta (rows >= L: 0).  Thread t
@@ -340,7 +343,7 @@ __device__ __forceinline__ void scaled_qk(const CBwd& W, const ChunkAt& c, int h
         *reinterpret_cast<float4*>(sH + r * LD + c4) = hv;
         if (Kh_out) *reinterpret_cast<float4*>(Kh_out + r * kD + c4) = hv;
     }
-    if (bad) atomicCAS(W.status, 0, (int)KDA_STATUS_GATE_RANGE);
+    if (bad) W.redo[(size_t)c.s * W.p.H + h] = 1;
 }
 
 // In place: the strictly lower C x C matrix A (stride LC) becomes T = (I + A)^-1, by 16 x 16 blocks:
@@ -913,12 +916,18 @@ int64_t chunk_bound(int N, int64_t T_total, bool varlen, int64_t T_uniform) {
 
 }  // namespace
 
+// Layout: chunk offsets [N+1] | redo flags [N*H] | records | states.  The token-serial backward
+// that recomputes flagged units runs after the chunked passes and reuses everything from the
+// records on, so that part is at least bwd_workspace() long.
 size_t chunk_bwd_workspace(int N, int64_t T_total, int H, bool varlen) {
     const int64_t T_uniform = varlen || N == 0 ? 0 : T_total / N;
     const size_t nch = (size_t)chunk_bound(N, T_total, varlen, T_uniform) * H;
     const size_t per = 3 * REC_CD + 2 * REC_DD + 2 * REC_CC + 3 * kD;  // Wt Up Kh, Ej dS, Tm Pq, sc
     const size_t states = ((size_t)chunk_bound(N, T_total, varlen, T_uniform) + N) * H * REC_DD;
-    return align256((size_t)(N + 1) * 8) + align256(nch * per * 4) + align256(states * 4);
+    size_t tail = align256(nch * per * 4) + align256(states * 4);
+    const size_t serial = bwd_workspace(N, T_total, H);
+    if (tail < serial) tail = align256(serial);
+    return align256((size_t)(N + 1) * 8) + align256((size_t)N * H * 4) + tail;
 }
 
 cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace, int* status, cudaStream_t st) {
@@ -932,7 +941,9 @@ cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace,
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     W.co_w = reinterpret_cast<int64_t*>(ws);
     W.co = W.co_w;
-    float* f = reinterpret_cast<float*>(ws + align256((size_t)(p.N + 1) * 8));
+    W.redo = reinterpret_cast<int*>(ws + align256((size_t)(p.N + 1) * 8));
+    uint8_t* tail = ws + align256((size_t)(p.N + 1) * 8) + align256((size_t)p.N * p.H * 4);
+    float* f = reinterpret_cast<float*>(tail);
     W.Wt = f; f += nch * REC_CD;
     W.Up = f; f += nch * REC_CD;
     W.Kh = f; f += nch * REC_CD;
@@ -941,8 +952,7 @@ cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace,
     W.Tm = f; f += nch * REC_CC;
     W.Pq = f; f += nch * REC_CC;
     W.sc = f; f += nch * 3 * kD;
-    W.S = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(W.co_w) + align256((size_t)(p.N + 1) * 8) +
-                                   align256(nch * (3 * REC_CD + 2 * REC_DD + 2 * REC_CC + 3 * kD) * 4));
+    W.S = reinterpret_cast<float*>(tail + align256(nch * (3 * REC_CD + 2 * REC_DD + 2 * REC_CC + 3 * kD) * 4));
     chunk_offsets_kernel<<<1, 1024, 0, st>>>(W);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -984,7 +994,11 @@ cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace,
         cbwd_grad_state<<<chunk_ctas, NT, SMEM_GRAD_A, st>>>(W);
         grad_local<<<chunk_ctas, NT, SMEM_GRAD_B, st>>>(W);
     }
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the flagged units, exactly, by the token-serial backward (its CTAs for the others return)
+    BwdProblem q = p;
+    q.redo = W.redo;
+    return launch_bwd(q, in_dtype, tail, st);
 }
 
 }  // namespace kda

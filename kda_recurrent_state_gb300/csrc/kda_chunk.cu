@@ -20,6 +20,18 @@
 // as X = Diag(e^{ref}) S0 (what the products with Ktil_p / Qtil_p need), and the
 // state accumulator holds D = X + Khat_p^T U, so S_C = Diag(e^{g_63 - ref}) D.
 //
+// Gates beyond that range: a chunk in which some key channel decays by more than
+// 2^kMaxExp2 over either half (a channel that forgets within a few tokens, down to
+// alpha = 0) cannot be factored this way.  The kernel runs in two instantiations.
+// The first (ROB = false, the hot one) processes every (sequence, head) and only
+// marks the units that met such a chunk; the second (ROB = true) recomputes exactly
+// those units: a chunk within range goes through the same products in the same
+// order (bit-identical to the first), a chunk beyond it skips its state products
+// and the state warpgroup applies its tokens one at a time in fp32 to the state held
+// in TMEM instead (the §四 recurrence itself, exact for any alpha in [0, 1]).  The
+// path of a chunk depends on its own gates only, so a run resumed at a chunk
+// boundary still reproduces the unsplit run bit for bit.
+//
 // The triangular inverse (the WY solve of §六) is a blocked substitution: A is
 // split into 16x16 blocks; the diagonal blocks are inverted in fp32 on CUDA cores
 // (Dg_a = (I + A_aa)^-1, one thread per column), and the blocks below the diagonal
@@ -72,7 +84,13 @@ constexpr int QR = 16;  // token rows per input slot
 constexpr int NTHREADS = 512;
 constexpr int kLptMax = 256;  // most packed sequences the kernel orders by length itself
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMaxExp2 = 15.0f;  // |g - ref| bound (log2 units) for fp16 operands
+// |g - ref| bound (log2 units) of the fp16 operand path.  An element scaled down by 2^-|g-ref|
+// can land in the fp16 subnormals, where its absolute rounding error is 2^-25, and the factor
+// on the other side of its product scales that error by up to 2^|g-ref|.  At 10 the worst such
+// term is 2^-15 of an O(1) operand, below the fp16 rounding of the products themselves; chunks
+// beyond it take the exact fp32 path.
+constexpr float kMaxExp2 = 10.0f;
+constexpr int kSerialRows = 8;  // tokens staged at a time by the exact per-token path
 constexpr int kRowH = 48;          // row stride (bytes) of a 16x16 fp16 block (ldmatrix: no bank conflicts)
 constexpr int kBlkH = 16 * kRowH;  // bytes per fp16 block
 
@@ -112,7 +130,9 @@ struct Cfg {
     static constexpr uint32_t OFF_VEC = OFF_RING + NSLOT * SLOT_BYTES;  // a[3][128], b[3][128]
     static constexpr uint32_t OFF_BETA = OFF_VEC + 6 * 128 * 4;         // [4][64]
     static constexpr uint32_t OFF_GATE = OFF_BETA + 4 * 64 * 4;         // [4][64] scalar gates
-    static constexpr uint32_t OFF_BAR = OFF_GATE + 4 * 64 * 4;
+    static constexpr uint32_t OFF_ONES = OFF_GATE + 4 * 64 * 4;         // [128] 1.0f
+    static constexpr uint32_t OFF_CBAD = OFF_ONES + 128 * 4;            // [3][4] chunk beyond the fp16 range
+    static constexpr uint32_t OFF_BAR = OFF_CBAD + 3 * 4 * 4;
     static constexpr uint32_t NBAR = 40;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 #ifdef KDA_TRACE
@@ -125,6 +145,8 @@ static_assert(Cfg<__nv_bfloat16>::SMEM_BYTES <= 232448, "smem budget (bf16)");
 static_assert(Cfg<float>::SMEM_BYTES <= 232448, "smem budget (fp32)");
 static_assert(Cfg<__nv_bfloat16>::OFF_RING % 128 == 0 && Cfg<float>::OFF_RING % 128 == 0, "TMA destinations");
 static_assert(Cfg<__nv_bfloat16>::OFF_STG % 128 == 0, "TMA store source");
+static_assert(Cfg<__nv_bfloat16>::OFF_BAR % 8 == 0 && Cfg<float>::OFF_BAR % 8 == 0, "mbarrier alignment");
+static_assert(kSerialRows * 4 * 128 * 4 <= 32768, "exact path staging fits the output staging / KT-QT pair");
 
 // barrier indices
 enum {
@@ -149,7 +171,8 @@ enum {
     B_BFREE = 29,    // [4] beta ring slot consumed
     B_VFREE = 33,    // [3] decay vectors of a chunk consumed (ring of 3, by chunk index mod 3)
     B_STGR = 36,     // own staging buffer read by the previous bulk store (STG_OWN)
-    B_COUNT = 37
+    B_PDONE = 37,    // prep has seen every chunk (the unit's range flag is final); ROB = false
+    B_COUNT = 38
 };
 static_assert(B_COUNT <= (int)Cfg<float>::NBAR, "barrier space");
 
@@ -304,26 +327,132 @@ __device__ __noinline__ void store_state_bf16(__nv_bfloat16* dst, uint32_t taddr
     }
 }
 
+// The exact path for one chunk whose gates leave the fp16 operand range: its tokens applied one at
+// a time, in fp32, to this thread's value column j of the state, which stays in TMEM (taddr: the
+// D_S row of lane j, columns = key channels).  Per token ("Kimi K3" article §四 with the §二.1 read):
+// p = (Diag(alpha) S)^T k, u = beta (v - p), S <- Diag(alpha) S + k u^T, o = S^T q.  Called by the
+// 128 threads of the state warpgroup; `stage` is 16 KB of shared memory the warpgroup owns for the
+// call; named barrier 1 orders its use.  row0: the chunk's first packed token.  The output rows go
+// straight to global memory.  Out of line: it runs only for such chunks.
+template <typename Tin, typename Tout, bool SG>
+__device__ __noinline__ void serial_chunk(uint32_t taddr, int j, int64_t row0, int valid, int h, int H,
+                                          const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                          const Tin* __restrict__ v, const float* __restrict__ log_alpha,
+                                          const float* __restrict__ beta, Tout* __restrict__ out, float* stage) {
+    // stage[r][0][c] = alpha_c k_c, [1] = alpha_c, [2] = k_c, [3] = q_c for kSerialRows tokens
+#pragma unroll 1
+    for (int r0 = 0; r0 < valid; r0 += kSerialRows) {
+        const int nt = valid - r0 < kSerialRows ? valid - r0 : kSerialRows;
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the previous group's rows are consumed
+        float vv[kSerialRows], bb[kSerialRows];
+#pragma unroll
+        for (int r = 0; r < kSerialRows; ++r) {
+            vv[r] = 0.f;
+            bb[r] = 0.f;
+            if (r < nt) {
+                const size_t tok = (size_t)(row0 + r0 + r) * H + h, off = tok * kD + j;
+                const float kk = ld_in(k, off);
+                float la = 0.f;
+                if constexpr (SG)
+                    la = log_alpha ? log_alpha[tok] : 0.f;
+                else
+                    la = log_alpha[off];
+                const float a = expf(la);
+                float* st = stage + r * 4 * kD;
+                st[j] = a * kk;
+                st[kD + j] = a;
+                st[2 * kD + j] = kk;
+                st[3 * kD + j] = ld_in(q, off);
+                vv[r] = ld_in(v, off);
+                bb[r] = beta[tok];
+            }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll 1
+        for (int r = 0; r < nt; ++r) {
+            const float* st = stage + r * 4 * kD;
+            uint32_t sp[32];
+            float p = 0.f;  // (Diag(alpha) S)^T k for column j
+#pragma unroll 1
+            for (int piece = 0; piece < 4; ++piece) {
+                tmem_ld32(taddr + piece * 32, sp);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 w = *reinterpret_cast<const float4*>(st + piece * 32 + 4 * e4);
+                    p = fmaf(w.x, __uint_as_float(sp[4 * e4]), p);
+                    p = fmaf(w.y, __uint_as_float(sp[4 * e4 + 1]), p);
+                    p = fmaf(w.z, __uint_as_float(sp[4 * e4 + 2]), p);
+                    p = fmaf(w.w, __uint_as_float(sp[4 * e4 + 3]), p);
+                }
+            }
+            float vr = vv[0], br = bb[0];
+#pragma unroll
+            for (int i = 1; i < kSerialRows; ++i)
+                if (i == r) {
+                    vr = vv[i];
+                    br = bb[i];
+                }
+            const float u = br * (vr - p);
+            float o = 0.f;
+#pragma unroll 1
+            for (int piece = 0; piece < 4; ++piece) {
+                tmem_ld32(taddr + piece * 32, sp);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const int c = piece * 32 + 4 * e4;
+                    const float4 a = *reinterpret_cast<const float4*>(st + kD + c);
+                    const float4 kk = *reinterpret_cast<const float4*>(st + 2 * kD + c);
+                    const float4 qq = *reinterpret_cast<const float4*>(st + 3 * kD + c);
+                    const float av[4] = {a.x, a.y, a.z, a.w}, kv[4] = {kk.x, kk.y, kk.z, kk.w},
+                                qv[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float sn = fmaf(kv[e], u, av[e] * __uint_as_float(sp[4 * e4 + e]));
+                        o = fmaf(qv[e], sn, o);
+                        sp[4 * e4 + e] = __float_as_uint(sn);
+                    }
+                }
+                tmem_st32(taddr + piece * 32, sp);
+            }
+            tmem_st_wait();  // the next token reads these columns back
+            const size_t off = ((size_t)(row0 + r0 + r) * H + h) * kD + j;
+            if constexpr (sizeof(Tout) == 2)
+                out[off] = __float2bfloat16_rn(o);
+            else
+                out[off] = o;
+        }
+    }
+}
+
+// ROB: the instantiation that recomputes the units the first pass marked in `redo`
+// (every other unit returns at once), taking each chunk beyond the fp16 range through
+// the exact per-token path; without it, the kernel marks such units in `redo`.
 // SG: one log-decay per (token, head) (the scalar gate of Gated DeltaNet), or none at
 // all (DeltaNet, alpha = 1) when P.log_alpha is null.  The gates then come in with beta
 // through the beta loader, and the TMA ring carries q, k and v only.
 // PB: the state pool holds bf16 states (a separate instantiation, so that the common
 // kernels' code is not touched by it).
-template <typename Tin, typename Tout, bool SG, bool PB>
+template <typename Tin, typename Tout, bool SG, bool PB, bool ROB>
 __global__ void __launch_bounds__(NTHREADS, 1)
     chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
-                 const __grid_constant__ CUtensorMap tm_out, const SeqProblem P, const PoolSlots pool) {
+                 const __grid_constant__ CUtensorMap tm_out, const SeqProblem P, const PoolSlots pool,
+                 int* __restrict__ redo) {
     using L = Cfg<Tin>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::OFF_MISC);
+    volatile int* range_bad = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 8);  // ROB = false
     Abort* ab = reinterpret_cast<Abort*>(sm + L::OFF_MISC + 16);
     float* vec_a = reinterpret_cast<float*>(sm + L::OFF_VEC);         // [3][128] e^{ref}
     float* vec_b = reinterpret_cast<float*>(sm + L::OFF_VEC + 1536);  // [3][128] e^{g_63 - ref}
     float* sbeta = reinterpret_cast<float*>(sm + L::OFF_BETA);        // [4][64]
     float* sgate = reinterpret_cast<float*>(sm + L::OFF_GATE);        // [4][64] (SG)
+    float* ones = reinterpret_cast<float*>(sm + L::OFF_ONES);         // [128] 1.0f
+    int* cbad = reinterpret_cast<int*>(sm + L::OFF_CBAD);             // [3][4]: per prep warp, by chunk % 3
 #ifdef KDA_TRACE
     unsigned int* trace_sm = reinterpret_cast<unsigned int*>(sm + L::OFF_MISC + 64);
 #endif
@@ -354,6 +483,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         s = *pick;
         __syncthreads();
     }
+    if constexpr (ROB)
+        if (!redo[(size_t)s * P.H + h]) return;  // every chunk of this unit was within range
     int64_t t0, len;
     seq_bounds(P, s, t0, len);
     const int nch = (int)((len + C - 1) / C);
@@ -378,6 +509,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
 
     if (nch == 0) {  // empty sequence: the final state is the initial state
+        if constexpr (!ROB)
+            if (tid == 0) redo[(size_t)s * P.H + h] = 0;
         if (P.final_state) {
             const float* S0 = init_state();
             for (int i = tid; i < kD * kD; i += NTHREADS) P.final_state[sbase + i] = S0 ? init_at(S0, i) : 0.f;
@@ -401,10 +534,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int i = 0; i < 3; ++i) mbar_init(&bar[B_VFREE + i], 128);
         mbar_init(&bar[B_STGR], 1);
+        mbar_init(&bar[B_PDONE], 128);
         ab->flag = 0;
+        *range_bad = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) tmem_alloc(tmem_holder, 512);
+    if constexpr (ROB)
+        if (tid < 128) ones[tid] = 1.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -491,7 +628,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ------------------------------------------------------------ prep warpgroup
         const int c = tid - 128;  // key channel (and TMEM lane) of this thread
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        float max_x = 0.f;  // largest |g - ref| seen (log2 units), for the range check
+        float max_x = 0.f;  // largest |g - ref| of the chunk (log2 units), for the range check
 
         // prep1(n): decay cumsum, operand tiles KT/QT/KH, V16, decay vectors.
         // Rows past the end of a sequence get log alpha = 0 and k = 0 (their beta
@@ -530,6 +667,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             };
             const bool full = valid == C;
             float x = 0.f;
+            if constexpr (ROB) max_x = 0.f;  // per chunk; otherwise over the whole unit
             // g decreases monotonically (log alpha <= 0), so |x| is largest at a quarter's
             // first or last row: the range check looks at those.
             auto quarter = [&](int i, auto full_chunk, auto reverse) {
@@ -610,6 +748,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if constexpr (SG) mbar_arrive(&bar[B_BFREE + (n & 3)]);  // done with this chunk's gates
             vec_a[v3 * 128 + c] = fast_exp2(ref);
             vec_b[v3 * 128 + c] = fast_exp2(x);  // e^{g_63 - ref}
+            if constexpr (ROB) {  // does any key channel of this warp leave the fp16 range in this chunk?
+                const unsigned bad = __ballot_sync(0xffffffffu, !(max_x <= kMaxExp2));  // (NaN: yes)
+                if ((c & 31) == 0) cbad[v3 * 4 + (warp & 3)] = bad != 0u;
+            }
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -630,7 +772,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         };
         for (int n = 0; n < nch; ++n)
             if (!prep1(n)) break;
-        if (max_x > kMaxExp2) atomicCAS(status, 0, (int)KDA_STATUS_GATE_RANGE);
+        if constexpr (!ROB) {  // mark the unit for the exact pass (NaN: yes), before the state reads it
+            if (!(max_x <= kMaxExp2)) *range_bad = 1;
+            mbar_arrive(&bar[B_PDONE]);
+        }
     } else if (warp < 12) {
         // ------------------------------------------------------------ state warpgroup
         const int j = tid - 256;  // value column (and TMEM lane) of this thread
@@ -639,6 +784,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool ok = true;
         uint32_t ph_stg = 0;    // phase of the staging barrier (every thread waits on it)
         bool u_issued = false;  // (i) of the coming chunk already issued (thread 0)
+        // chunk m goes the exact per-token way (read once prep(m) has arrived on B_PREPD)
+        auto bad_chunk = [&](int m) -> bool {
+            if constexpr (!ROB) return false;
+            const volatile int* cb = cbad + (m % 3) * 4;
+            return (cb[0] | cb[1] | cb[2] | cb[3]) != 0;
+        };
         // (i): U += X16 x WT for chunk m, once X_m and WT(m) are ready (thread 0)
         auto issue_u = [&](int m) -> bool {
             if (!mbar_wait(&bar[B_XRDY], m & 1, ab, status)) return false;
@@ -646,8 +797,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
             KDA_TR(m, 24);
             const uint64_t db = mn_desc(sm_base + L::OFF_WT, 8192);
+            if (!bad_chunk(m)) {
 #pragma unroll
-            for (int st = 0; st < 8; ++st) mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, db + 128u * st, ID_MN, 1);
+                for (int st = 0; st < 8; ++st) mma_ts(tmem + TM_U, tmem + TM_X16 + st * 8, db + 128u * st, ID_MN, 1);
+            }
             mma_commit(&bar[B_UIDONE]);
             KDA_TR(m, 10);
             return true;
@@ -657,14 +810,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (m > 0 && !mbar_wait(&bar[B_OFREE], (m - 1) & 1, ab, status)) return false;
             tc_fence_after();
             const uint64_t db = mn_desc(sm_base + L::OFF_KQ + (m & 1) * 32768 + 16384, 8192);
+            if (!bad_chunk(m)) {
 #pragma unroll
-            for (int st = 0; st < 8; ++st) mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, db + 128u * st, ID_MN, st > 0);
+                for (int st = 0; st < 8; ++st)
+                    mma_ts(tmem + TM_O, tmem + TM_X16 + st * 8, db + 128u * st, ID_MN, st > 0);
+            }
             KDA_TR(m, 11);
             return true;
         };
         {  // X_0 = Diag(a_0) S_0 into D_S and X16
             const float* S0 = init_state();
             if (!(ok = mbar_wait(&bar[B_PREPD], 0, ab, status))) goto state_done;
+            const float* a0 = ROB && bad_chunk(0) ? ones : vec_a;  // the exact path works on S itself
 #pragma unroll 1
             for (int piece = 0; piece < 4; ++piece) {
                 uint32_t xs[32], x16[16];
@@ -672,7 +829,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int e = 0; e < 32; ++e) {
                     const int cc = piece * 32 + e;
                     const float s0 = S0 ? init_at(S0, (size_t)cc * kD + j) : 0.f;
-                    xs[e] = __float_as_uint(s0 * vec_a[cc]);
+                    xs[e] = __float_as_uint(s0 * a0[cc]);
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -724,10 +881,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tc_fence_after();
                     const uint64_t dkh = k_desc(sm_base + L::OFF_KH + b * 16384);
                     const uint64_t dpp = k_desc(sm_base + L::OFF_PP + (n % L::NPP) * 8192);
+                    if (!bad_chunk(n)) {
 #pragma unroll
-                    for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, dkh + 2u * st, ID_S, 1);
+                        for (int st = 0; st < 4; ++st)
+                            mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, dkh + 2u * st, ID_S, 1);
 #pragma unroll
-                    for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, dpp + 2u * st, ID_KK, 1);
+                        for (int st = 0; st < 4; ++st)
+                            mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, dpp + 2u * st, ID_KK, 1);
+                    }
                     mma_commit(&bar[B_SDONE]);
                     mma_commit(&bar[B_KQFREE + b]);
                     KDA_TR(n, 13);
@@ -738,6 +899,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!(ok = mbar_wait(&bar[B_SDONE], n & 1, ab, status))) break;
             tc_fence_after();
             if (j == 0) KDA_TR(n, 14);
+            const bool bad = ROB && bad_chunk(n);
+            if (bad) {  // the exact per-token path on D_S = S (no product of this chunk touched it)
+                uint8_t* stage = sm + (L::STG_OWN ? L::OFF_STG : L::OFF_KQ + b * 32768);
+                if constexpr (L::STG_OWN)  // the previous chunk's bulk store has read the buffer
+                    if (n > 0 && !(ok = mbar_wait(&bar[B_STGR], (n - 1) & 1, ab, status))) break;
+                serial_chunk<Tin, Tout, SG>(tmem + lane_base + TM_S, j, t0 + (int64_t)C * n, valid, h, P.H,
+                                            static_cast<const Tin*>(P.q), static_cast<const Tin*>(P.k),
+                                            static_cast<const Tin*>(P.v), P.log_alpha, P.beta,
+                                            static_cast<Tout*>(P.out), reinterpret_cast<float*>(stage));
+            }
             {
                 const int64_t end_pos = (int64_t)C * n + valid;  // tokens of the sequence consumed so far
                 float* snap = nullptr;
@@ -753,7 +924,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
                 float* fin = (last && P.final_state) ? P.final_state + sbase : nullptr;
-                const float* bv = vec_b + (n % 3) * 128;
+                if constexpr (!ROB) {
+                    // A unit marked for the exact pass is recomputed from its initial state, which
+                    // the final state may alias: it must not be overwritten here.
+                    if (last && !(ok = mbar_wait(&bar[B_PDONE], 0, ab, status))) break;
+                    if (*range_bad) fin = nullptr;
+                }
+                const float* bv = ROB && bad ? ones : vec_b + (n % 3) * 128;
                 if constexpr (PB)
                     if (snap16) store_state_bf16(snap16, tmem + lane_base + TM_S, bv, j);
                 if (snap || fin) {  // true state S = Diag(b_n) D, at snapshot positions and the end
@@ -774,7 +951,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!last) {  // X_{n+1} = Diag(a_{n+1}) (Diag(b_n) D) into D_S (fp32) and X16 (fp16)
                     // (the same two roundings as a run resumed from the returned state)
                     if (!(ok = mbar_wait(&bar[B_PREPD + ((n + 1) & 1)], ((n + 1) >> 1) & 1, ab, status))) break;
-                    const float* an = vec_a + ((n + 1) % 3) * 128;
+                    const float* an = ROB && bad_chunk(n + 1) ? ones : vec_a + ((n + 1) % 3) * 128;
                     uint32_t da[32], db[32];
 #pragma unroll 1
                     for (int pp = 0; pp < 4; pp += 2) {
@@ -818,7 +995,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     u_issued = true;
                 }
             }
-            {  // O(n): read out, hand D_O back to (iii-a) of the next chunk, store
+            if (bad) {  // its output rows are stored already
+                tc_fence_before();
+                mbar_arrive(&bar[B_OFREE]);
+            } else {  // O(n): read out, hand D_O back to (iii-a) of the next chunk, store
                 uint32_t o0[32], o1[32];
                 tmem_ld32(tmem + lane_base + TM_O, o0);
                 tmem_ld32(tmem + lane_base + TM_O + 32, o1);
@@ -1044,6 +1224,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     if (warp == 1) tmem_dealloc(tmem, 512);
+    if constexpr (!ROB)
+        if (tid == 0) redo[(size_t)s * P.H + h] = *range_bad;
 #ifdef KDA_TRACE
     if (blockIdx.x == 0)
         for (int i = tid; i < kTrN * kTrEv; i += NTHREADS) g_trace[i] = trace_sm[i];
@@ -1079,7 +1261,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, 
 }
 
 template <typename Tin, typename Tout, bool SG, bool PB>
-cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, cudaStream_t st) {
+cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, int* redo, cudaStream_t st) {
     CUtensorMap mq, mk, mv, ml, mo;
     const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int64_t Tt = p.T_total > 0 ? p.T_total : 1;
@@ -1091,12 +1273,18 @@ cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, cudaStream_t st
                   sizeof(Tout), Tt, p.H))
         return cudaErrorInvalidValue;
     if (SG) ml = mq;  // not read
-    auto kern = chunk_kernel<Tin, Tout, SG, PB>;
+    // the pass over every unit, then the exact pass over the units it marked (its CTAs for the
+    // others return at once)
+    auto kern = chunk_kernel<Tin, Tout, SG, PB, false>;
+    auto rob = chunk_kernel<Tin, Tout, SG, PB, true>;
     const int smem = (int)Cfg<Tin>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(rob, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((int64_t)p.N * p.H);
-    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pool);
+    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pool, redo);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    rob<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pool, redo);
     return cudaGetLastError();
 }
 
@@ -1109,31 +1297,33 @@ extern "C" int kda_trace_read(unsigned int* host, int n) {
 }
 #endif
 
+// One int per (sequence, head): set by the first pass when the unit met a chunk beyond the
+// fp16 operand range, read by the exact pass.
 size_t chunk_prefill_workspace(int N, int H) {
-    (void)N;
-    (void)H;
-    return 0;
+    const size_t b = (size_t)N * H * sizeof(int);
+    return (b + 255) & ~(size_t)255;
 }
 
 template <typename Tin, typename Tout>
-cudaError_t launch_gate(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, cudaStream_t st) {
+cudaError_t launch_gate(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int* redo,
+                        cudaStream_t st) {
     if (pool_bf16)
-        return gate != kGateChannel ? launch_t<Tin, Tout, true, true>(p, pool, st)
-                                    : launch_t<Tin, Tout, false, true>(p, pool, st);
-    return gate != kGateChannel ? launch_t<Tin, Tout, true, false>(p, pool, st)
-                                : launch_t<Tin, Tout, false, false>(p, pool, st);
+        return gate != kGateChannel ? launch_t<Tin, Tout, true, true>(p, pool, redo, st)
+                                    : launch_t<Tin, Tout, false, true>(p, pool, redo, st);
+    return gate != kGateChannel ? launch_t<Tin, Tout, true, false>(p, pool, redo, st)
+                                : launch_t<Tin, Tout, false, false>(p, pool, redo, st);
 }
 
 cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int in_dtype,
                                  int out_dtype, void* workspace, size_t ws_bytes, cudaStream_t st) {
-    (void)workspace;
-    (void)ws_bytes;
     if ((int64_t)p.N * p.H == 0) return cudaSuccess;
+    if (!workspace || ws_bytes < chunk_prefill_workspace(p.N, p.H)) return cudaErrorInvalidValue;
+    int* redo = static_cast<int*>(workspace);
     if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16)
-        return launch_gate<__nv_bfloat16, __nv_bfloat16>(p, pool, pool_bf16, gate, st);
-    if (in_dtype == KDA_BF16) return launch_gate<__nv_bfloat16, float>(p, pool, pool_bf16, gate, st);
-    if (out_dtype == KDA_BF16) return launch_gate<float, __nv_bfloat16>(p, pool, pool_bf16, gate, st);
-    return launch_gate<float, float>(p, pool, pool_bf16, gate, st);
+        return launch_gate<__nv_bfloat16, __nv_bfloat16>(p, pool, pool_bf16, gate, redo, st);
+    if (in_dtype == KDA_BF16) return launch_gate<__nv_bfloat16, float>(p, pool, pool_bf16, gate, redo, st);
+    if (out_dtype == KDA_BF16) return launch_gate<float, __nv_bfloat16>(p, pool, pool_bf16, gate, redo, st);
+    return launch_gate<float, float>(p, pool, pool_bf16, gate, redo, st);
 }
 
 }  // namespace kda

@@ -44,7 +44,7 @@ extern "C" size_t kda_host_fwd_workspace_size(int B, int H, int dk, int dv, int6
     if (B <= 0 || H <= 0 || dk != kda::kD || dv != kda::kD || segment_tokens < 0) return 0;
     const int64_t L = segment_tokens ? segment_tokens : kDefaultSegment;
     const SegLayout s = seg_layout(B, H, L, in_dtype == KDA_BF16 ? 2 : 4, out_dtype == KDA_BF16 ? 2 : 4);
-    return 2 * s.bytes + 2 * align16((size_t)B * H * kda::kD * kda::kD * 4);
+    return 2 * s.bytes + 2 * align16((size_t)B * H * kda::kD * kda::kD * 4) + kda::chunk_prefill_workspace(B, H);
 }
 
 extern "C" int kda_chunk_fwd_host(const void* q, const void* k, const void* v, const float* log_alpha,
@@ -71,6 +71,9 @@ extern "C" int kda_chunk_fwd_host(const void* q, const void* k, const void* v, c
     const size_t state_bytes = (size_t)B * H * kda::kD * kda::kD * 4;
     float* states[2] = {reinterpret_cast<float*>(ws + 2 * lay.bytes),
                         reinterpret_cast<float*>(ws + 2 * lay.bytes + align16(state_bytes))};
+    // the prefill's own workspace (a flag per (sequence, head)), reused by every segment in order
+    uint8_t* kws = ws + 2 * lay.bytes + 2 * align16(state_bytes);
+    const size_t kws_bytes = kda::chunk_prefill_workspace(B, H);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
     cudaStream_t hs = nullptr, ds = nullptr;  // host-to-device and device-to-host copy streams
@@ -117,7 +120,7 @@ extern "C" int kda_chunk_fwd_host(const void* q, const void* k, const void* v, c
         const float* s_in = s == 0 ? init_state : states[(s - 1) & 1];
         const int r = kda_chunk_fwd(buf + lay.q, buf + lay.k, buf + lay.v, reinterpret_cast<const float*>(buf + lay.la),
                                     reinterpret_cast<const float*>(buf + lay.beta), s_in, buf + lay.out, states[s & 1],
-                                    B, Ls, H, dk, dv, 64, in_dtype, out_dtype, nullptr, 0, stream);
+                                    B, Ls, H, dk, dv, 64, in_dtype, out_dtype, kws, kws_bytes, stream);
         if (r != KDA_OK) {
             rc = r;
             break;

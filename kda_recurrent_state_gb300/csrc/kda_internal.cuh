@@ -114,6 +114,7 @@ struct BwdProblem {
     float* ckpt;          // set by launch_bwd from the workspace
     float* scratch;
     int64_t ckpt_slots;
+    const int* redo;      // token-serial backward: nullptr, or [N*H] with only units u, redo[u] != 0, computed
 };
 size_t bwd_workspace(int N, int64_t T_total, int H);
 cudaError_t launch_bwd(BwdProblem p, int in_dtype, void* workspace, cudaStream_t st);

@@ -1,29 +1,20 @@
 // kda_noalloc.cu -- kda_bwd with the library's own static scratch instead of a caller
-// workspace.  The array lives in this translation unit alone, so it is reserved only when
-// this entry point is first used on a device (lazy module loading), not by every user of
-// the library.
-#include <mutex>
-
+// workspace.  The array lives in this translation unit alone.  Under lazy module loading
+// (CUDA_MODULE_LOADING=LAZY, the CUDA 12+ default) it is reserved on a device only when this
+// entry point is first used there; with CUDA_MODULE_LOADING=EAGER every context that loads
+// libkda reserves it when the context is created.
 #include "kda_internal.cuh"
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-std::mutex g_scratch_mu;
-
-// Device address of the static scratch on the current device, looked up once per device.
+// Device address of the static scratch on the current device.  Looked up on every call, not
+// cached: after a cudaDeviceReset the module is loaded again and a cached address would point
+// into memory the library no longer owns.  The first lookup on a device loads the module
+// (lazy loading), so the first call should come before any stream capture.
 void* scratch_ptr() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = p;
-    }
-    return g_scratch_addr[dev];
+    void* p = nullptr;
+    return cudaGetSymbolAddress(&p, g_bwd_scratch) == cudaSuccess ? p : nullptr;
 }
 }  // namespace
 

@@ -15,6 +15,12 @@ Distributions (per tensor, i.i.d. unless stated):
               -Uniform(1e-5, 1e-3)                       ("slow" gates: the
               initial state and the chunk carry stay visible for thousands
               of tokens, so they are actually tested)
+              -Uniform(0.15, 0.2)                        ("steep": a chunk's
+              decay close to what the fp16 operand path factors)
+              "mixed": key channels 0..63 fast, -Uniform(1, 10) (they forget
+              within a few tokens; channels 0..3 exactly -30), channels
+              64..127 slow as above: the per-channel forgetting the method
+              exists for, beyond any per-chunk factoring of the decay
   state     ~ N(0, 0.02)                                (fp32)
 """
 from __future__ import annotations
@@ -37,8 +43,13 @@ def _unit_rows(x: torch.Tensor) -> torch.Tensor:
 
 
 def _gates(shape, g, device, gate: str) -> torch.Tensor:
-    lo, hi = {"config": (0.001, 0.1), "slow": (1e-5, 1e-3)}[gate]
     u = torch.rand(shape, generator=g, device=device, dtype=torch.float32)
+    if gate == "mixed":  # per key channel (the last dimension)
+        c = torch.arange(shape[-1], device=device)
+        fast, slow = -(1.0 + 9.0 * u), -(1e-5 + (1e-3 - 1e-5) * u)
+        la = torch.where(c < shape[-1] // 2, fast, slow)
+        return torch.where(c < 4, torch.full_like(la, -30.0), la)
+    lo, hi = {"config": (0.001, 0.1), "slow": (1e-5, 1e-3), "steep": (0.15, 0.2)}[gate]
     return -(lo + (hi - lo) * u)
 
 

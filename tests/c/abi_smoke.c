@@ -73,9 +73,15 @@ int main(void) {
     CHECK(cudaMemcpy(dv, v, tok * D * 4, cudaMemcpyHostToDevice) == cudaSuccess);
     CHECK(cudaMemcpy(dla, la, tok * D * 4, cudaMemcpyHostToDevice) == cudaSuccess);
     CHECK(cudaMemcpy(dbeta, beta, tok * 4, cudaMemcpyHostToDevice) == cudaSuccess);
-    CHECK(kda_workspace_size(KDA_OP_CHUNK, B, T, H, D, D, 64) == 0);
+    /* one int per (sequence, head), rounded up to 256 bytes */
+    const size_t cws_bytes = kda_workspace_size(KDA_OP_CHUNK, B, T, H, D, D, 64);
+    CHECK(cws_bytes == (((size_t)B * H * 4 + 255) / 256) * 256);
+    void* cws;
+    CHECK(cudaMalloc(&cws, cws_bytes) == cudaSuccess);
     CHECK(kda_chunk_fwd(dq, dk, dv, dla, dbeta, NULL, dout, dfin, B, T, H, D, D, 64, KDA_F32, KDA_F32, NULL, 0,
-                        NULL) == KDA_OK);
+                        NULL) == KDA_ERR_WORKSPACE);
+    CHECK(kda_chunk_fwd(dq, dk, dv, dla, dbeta, NULL, dout, dfin, B, T, H, D, D, 64, KDA_F32, KDA_F32, cws,
+                        cws_bytes, NULL) == KDA_OK);
     CHECK(cudaMemcpy(out_a, dout, tok * D * 4, cudaMemcpyDeviceToHost) == cudaSuccess);
     CHECK(cudaMemcpy(fin_a, dfin, (size_t)B * H * D * D * 4, cudaMemcpyDeviceToHost) == cudaSuccess);
     CHECK(kda_get_device_status(NULL) == KDA_OK);
@@ -91,10 +97,10 @@ int main(void) {
     CHECK(memcmp(fin_a, fin_b, (size_t)B * H * D * D * 4) == 0);
 
     /* argument errors are status codes */
-    CHECK(kda_chunk_fwd(dq, dk, dv, dla, dbeta, NULL, dout, dfin, B, T, H, 64, D, 64, KDA_F32, KDA_F32, NULL, 0,
-                        NULL) == KDA_ERR_UNSUPPORTED);
-    CHECK(kda_chunk_fwd(NULL, dk, dv, dla, dbeta, NULL, dout, dfin, B, T, H, D, D, 64, KDA_F32, KDA_F32, NULL, 0,
-                        NULL) == KDA_ERR_INVALID_ARG);
+    CHECK(kda_chunk_fwd(dq, dk, dv, dla, dbeta, NULL, dout, dfin, B, T, H, 64, D, 64, KDA_F32, KDA_F32, cws,
+                        cws_bytes, NULL) == KDA_ERR_UNSUPPORTED);
+    CHECK(kda_chunk_fwd(NULL, dk, dv, dla, dbeta, NULL, dout, dfin, B, T, H, D, D, 64, KDA_F32, KDA_F32, cws,
+                        cws_bytes, NULL) == KDA_ERR_INVALID_ARG);
     CHECK(strncmp(kda_status_string(KDA_ERR_MISALIGNED), "KDA_", 4) == 0);
     printf("abi_smoke ok\n");
     return 0;

@@ -86,8 +86,9 @@ def test_argument_validation(L):
     assert _chunk(L, B=0) == b.KDA_OK  # nothing to do
     assert _chunk(L, H=0) == b.KDA_OK
     need = L.kda_workspace_size(0, 1, 8, 1, 128, 128, 64)
-    if need:
-        assert _chunk(L, ws=0x2000, ws_bytes=need - 1) == b.KDA_ERR_WORKSPACE
+    assert need == 256  # one int per (sequence, head), rounded up to 256 bytes
+    assert _chunk(L, ws=0x2000, ws_bytes=need - 1) == b.KDA_ERR_WORKSPACE
+    assert _chunk(L, ws=0, ws_bytes=0) == b.KDA_ERR_WORKSPACE
     P = ctypes.c_void_p
     # varlen: interval must be a multiple of the chunk; final_states is required
     assert L.kda_varlen_fwd(P(16), P(16), P(16), P(16), P(16), P(16), 2, 100, 1, 128, 128, 64, None, P(16), 100,
@@ -211,8 +212,16 @@ def test_chunk_bwd_validation(L):
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     nch = (Tt // C + N) * H
     per = 3 * C * D + 2 * D * D + 2 * C * C + 3 * D
-    want = al((N + 1) * 8) + al(nch * per * 4) + al((Tt // C + N) * H * D * D * 4 + N * H * D * D * 4)
+    # plus one int per (sequence, head) flagging the units the token-serial backward recomputes, which
+    # reuses everything from the records on (so that part is at least kda_bwd's workspace)
+    serial = b.kda_workspace_size(b.KDA_OP_BWD, N, Tt, H)
+    tail = max(al(nch * per * 4) + al((Tt // C + N) * H * D * D * 4 + N * H * D * D * 4), al(serial))
+    want = al((N + 1) * 8) + al(N * H * 4) + tail
     assert b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, N, Tt, H, chunk=64) == want
+    # one-token sequences: the token-serial workspace (a checkpoint and 16 scratch states per unit) is
+    # the larger part
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, 8, 8, 2, chunk=64) == \
+        al(9 * 8) + al(8 * 2 * 4) + al(b.kda_workspace_size(b.KDA_OP_BWD, 8, 8, 2))
     assert b.kda_workspace_size(b.KDA_OP_CHUNK_BWD, N, Tt, H, chunk=16) == 0
 
 
@@ -234,8 +243,9 @@ def test_host_fwd_validation(L):
 
     P = ctypes.c_void_p
     need = L.kda_host_fwd_workspace_size(1, 2, 128, 128, 256, 0, 1)
-    # two segments of staging (bf16 q, k, v; fp32 gates, beta, out) and two fp32 states
-    assert need == 2 * (256 * 2 * (3 * 256 + 512 + 4 + 512)) + 2 * 2 * 65536
+    # two segments of staging (bf16 q, k, v; fp32 gates, beta, out), two fp32 states and the
+    # prefill's own workspace (one int per (sequence, head), rounded up to 256 bytes)
+    assert need == 2 * (256 * 2 * (3 * 256 + 512 + 4 + 512)) + 2 * 2 * 65536 + 256
     ptr = P(16)
 
     def call(seg=256, ws=0x10000, ws_bytes=need, T=100):
@@ -252,5 +262,9 @@ def test_workspace_size(L):
     from kda_recurrent_state_gb300 import binding as b
 
     assert b.kda_workspace_size(b.KDA_OP_DECODE, 256, 1, 96) == 0
-    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96) >= 0
+    # chunk 64: one int per (sequence, head), rounded up to 256 bytes, marking the units the exact
+    # pass recomputes; chunk 1 needs none
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96) == 512
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 4, 8192, 32) == 512
+    assert b.kda_workspace_size(b.KDA_OP_VARLEN, 16, 262144, 64) == 4096
     assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96, chunk=1) == 0

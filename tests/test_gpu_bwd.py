@@ -149,9 +149,10 @@ def test_bwd_deterministic(chunk):
         assert torch.equal(g1[name], g2[name]), name
 
 
-def test_chunk_bwd_gate_range_is_reported():
+def test_chunk_bwd_beyond_the_fp32_bound():
     """A half-chunk whose summed log-decay is below -80 cannot be factored in fp32: the chunked
-    backward records KDA_STATUS_GATE_RANGE (nothing faults), and chunk = 1 still matches the oracle."""
+    backward flags the unit and recomputes it with the token-serial backward inside the same call
+    (no status), and the result matches the oracle and the chunk = 1 call."""
     import kda_recurrent_state_gb300 as kda
     from kda_recurrent_state_gb300 import synth
 
@@ -159,16 +160,16 @@ def test_chunk_bwd_gate_range_is_reported():
     la = x["log_alpha"].clone()
     la[0, 40:44] = -30.0  # rows 32..63 of the chunk sum to about -120
     do = torch.randn(1, 64, 1, 128, generator=torch.Generator(device="cuda").manual_seed(5702), device="cuda")
-    kda.kda_get_device_status()
-    kda.kda_bwd(x["q"], x["k"], x["v"], la, x["beta"], do, x["init_state"], chunk=64)
-    torch.cuda.synchronize()
-    assert kda.kda_get_device_status() == kda.binding.KDA_STATUS_GATE_RANGE
-    got = kda.kda_bwd(x["q"], x["k"], x["v"], la, x["beta"], do, x["init_state"], chunk=1)
+    assert kda.kda_get_device_status() == 0
+    got = kda.kda_bwd(x["q"], x["k"], x["v"], la, x["beta"], do, x["init_state"], chunk=64)
     torch.cuda.synchronize()
     assert kda.kda_get_device_status() == 0
+    one = kda.kda_bwd(x["q"], x["k"], x["v"], la, x["beta"], do, x["init_state"], chunk=1)
+    torch.cuda.synchronize()
     ref = _oracle_grads(dict(x, log_alpha=la), la, do, None, [(0, 0)])
     for name in ("dq", "dk", "dv", "dbeta"):
         _close(batch_heads(got[name], [(0, 0)]), ref[name], name)
+        assert torch.equal(got[name], one[name]), name  # the same token-serial kernel computed both
 
 
 def test_chunk_bwd_workspace_and_bad_chunk():

@@ -147,24 +147,22 @@ def test_long_prefill_full_size_sampled(chunk):
     assert kda.kda_get_device_status() == 0
 
 
-def test_gate_range_status():
+def test_steep_decay_is_recomputed():
     """A decay too steep for the fp16 operands of the chunk = 64 path (log alpha = -1 per
-    token: -31 over a half chunk, beyond the -15 ln 2 the kernel supports) is reported in
-    the device status word, with no fault; the token-serial path has no such limit."""
+    token: -31 over a half chunk) needs no status and no chunk = 1 from the caller: the
+    units are recomputed by the token-serial pass inside the same call."""
     import kda_recurrent_state_gb300 as kda
-    from kda_recurrent_state_gb300 import binding, synth
+
+    from kda_recurrent_state_gb300 import synth
 
     x = synth.prefill_inputs(1, 128, 2, seed=synth.SEED_BASE + 9, device="cuda")
     steep = torch.full_like(x["log_alpha"], -1.0)
     assert kda.kda_get_device_status() == 0
-    kda.kda_chunk_fwd(x["q"], x["k"], x["v"], steep, x["beta"], None, chunk=64)
-    torch.cuda.synchronize()
-    assert kda.kda_get_device_status() == binding.KDA_STATUS_GATE_RANGE
-    assert kda.kda_get_device_status() == 0  # reading clears it
-    out, fin = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], steep, x["beta"], None, chunk=1)
+    out, fin = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], steep, x["beta"], None, chunk=64)
     torch.cuda.synchronize()
     assert kda.kda_get_device_status() == 0
     pairs = [(0, 0), (0, 1)]
     ro, rs = oracle.recurrent(batch_heads(x["q"], pairs), batch_heads(x["k"], pairs), batch_heads(x["v"], pairs),
                               batch_heads(steep, pairs), batch_heads(x["beta"], pairs), None)
-    assert_close(batch_heads(out, pairs), ro, "steep decay, token-serial out")
+    assert_close(batch_heads(out, pairs), ro, "steep decay, out")
+    assert_close(np.stack([np64(fin[b, h]) for b, h in pairs]), rs, "steep decay, state")
