@@ -277,7 +277,9 @@ def run_ours(args):
                    "frac": flops / kern_s / 1e12 / peaks["bf16_tflops"],
                    "note": "fp16 dense rate = bf16 dense rate; flops = 139,264 per token-head"},
         "clocks": clk.summary(),
-        "gpu_launches": args.steps,
+        # two launches per step: the chunked kernel over every unit, and its exact second pass,
+        # whose CTAs return at once when no unit was marked (none is, at these gates)
+        "gpu_launches": 2 * args.steps,
     }
 
     # ---- the same prefill with one gate per (token, head) (Gated DeltaNet) and with none
@@ -302,7 +304,7 @@ def run_ours(args):
                      "workload": f"B={B} H={H} T={T}, bf16 q/k/v, "
                                  + ("one fp32 log-decay per token-head" if gate_b else "no decay")
                                  + f", {args.out_dtype} out"}
-        line["gpu_launches"] += 5  # timed launches only (warm-ups excluded)
+        line["gpu_launches"] += 2 * 5  # timed launches only (warm-ups excluded)
     assert kda.kda_get_device_status() == 0, "device status raised by the scalar-gate prefill"
     del la_h
 
@@ -363,8 +365,33 @@ def run_ours(args):
                       "workload": f"16 packed sequences ({ttot} tokens, log-uniform 1024..65536), H=64, chunk 64, "
                                   f"8 resumed from a state, {int(vsnaps.shape[0])} snapshots every 16384 tokens, "
                                   f"fp32 out"}
-    line["gpu_launches"] += 5
+    line["gpu_launches"] += 2 * 5
     del xv, vout, vfin, vsnaps
+
+    # ---- the same prefill with channels that forget within a few tokens (half the key channels
+    # log alpha = -U(1, 10), four at -30): every chunk leaves the fp16 operand range, so every
+    # unit is recomputed by the exact second pass (per token, fp32) after the first pass
+    xm = synth.prefill_inputs(1, 16384, H, seed=synth.SEED_BASE + 8, device=dev, gate="mixed")
+    mout = torch.empty(1, 16384, H, D, dtype=torch.float32, device=dev)
+    mfin = torch.empty(1, H, D, D, dtype=torch.float32, device=dev)
+    mixed = lambda: kda.kda_chunk_fwd(xm["q"], xm["k"], xm["v"], xm["log_alpha"], xm["beta"], None, mout, mfin,
+                                      chunk=args.chunk, workspace=ws)
+    mixed()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(2):
+        mixed()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mt = e0.elapsed_time(e1) / 1e3 / 2
+    line["prefill_fast_forgetting"] = {
+        "tokens_per_s": 16384 / mt, "ms_per_call": mt * 1e3, "us_per_chunk": mt * 1e6 / (16384 // CHUNK),
+        "workload": f"B=1 H={H} T=16384, bf16 q/k/v, half the key channels log alpha = -U(1,10) (four at -30), "
+                    "half -U(1e-5,1e-3): every chunk beyond the fp16 operand range, every unit recomputed by the "
+                    "exact per-token pass"}
+    line["gpu_launches"] += 2 * 2
+    assert kda.kda_get_device_status() == 0, "device status raised by the fast-forgetting prefill"
+    del xm, mout, mfin
 
     # ---- backward (training) at B=4, H=32, T=8192: the chunked reverse mode (fp32 GEMMs on CUDA
     # cores), reported against the fp32 CUDA-core peak (ALU-bound, not a tensor-core path)
@@ -390,14 +417,14 @@ def run_ours(args):
                    "workload": "kda_chunk_bwd chunk 64, B=4 H=32 T=8192, bf16 q/k/v, fp32 gates/state/"
                                f"cotangents, S0 ~ N(0,0.02); flops = {BWD_CHUNK_FLOP:.0f} per token-head "
                                "(the chunked form's fp32 GEMMs)"}
-    line["gpu_launches"] += 12  # 6 launches per call
+    line["gpu_launches"] += 14  # 7 launches per call (the last: the token-serial pass over marked units)
     assert kda.kda_get_device_status() == 0, "device status raised by the backward"
     del xb, do, ws_b
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
         line["e2e"] = e2e(args, x, out, fin, ws, dev, out_dtype)
-        line["gpu_launches"] += args.e2e_steps * ((T + 4095) // 4096)  # one launch per 4096-token segment
+        line["gpu_launches"] += args.e2e_steps * 2 * ((T + 4095) // 4096)  # two launches per 4096-token segment
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle on heads of this very workload, and the GPU result for them (one more

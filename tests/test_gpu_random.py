@@ -5,11 +5,13 @@ same sequence run alone; the host-streamed prefill equals the device one).
 
 Numerical bar: the workloads' rel-L2 <= 2e-3 and max-abs <= 1e-2 (for gradients, of their
 largest magnitude).  One reading is added for inputs outside the workloads: on the chunked
-path the operands are fp16, and when an output's reference is nearly cancelled (a single
-token whose q.k is close to 0, so o = beta (q.k) v is small) their rounding gives a large
-relative error at a tiny absolute one.  There the relative bar is replaced by
-max-abs <= 1e-3, ten times tighter than the absolute bar.  A gradient that is identically
-zero in the oracle has no relative error at all; there the absolute bar alone applies."""
+path the operands are fp16, and when an output is nearly cancelled (a single token whose q.k
+is close to 0, so o = beta (q.k) v is small) their rounding gives a large relative error at a
+tiny absolute one.  Only there, for an output whose reference has an L2 norm below
+CANCEL_NORM (a token's 128 outputs with |q.k| below about 0.02, against a typical 0.09), the
+relative bar is replaced by max-abs <= 1e-3, ten times tighter than the absolute bar; every
+other chunked result must meet the relative bar.  A gradient that is identically zero in the
+oracle has no relative error at all; there the absolute bar alone applies."""
 import random
 
 import numpy as np
@@ -21,6 +23,7 @@ from kda_testutil import MAX_ABS, REL_L2, batch_heads, errors, np64, packed_head
 pytestmark = pytest.mark.gpu
 CASES = 40  # per kind
 CANCEL_ABS = 1e-3
+CANCEL_NORM = 0.1  # L2 norm of a nearly cancelled output (see the module docstring)
 
 
 def _close(got, ref, chunk, grad=False):
@@ -28,7 +31,12 @@ def _close(got, ref, chunk, grad=False):
     scale = max(1.0, float(np.abs(ref).max())) if grad else 1.0
     if mx > MAX_ABS * scale:
         return False, rel, mx
-    return rel <= REL_L2 or (chunk == 64 and mx <= CANCEL_ABS * scale), rel, mx
+    if rel <= REL_L2:
+        return True, rel, mx
+    if grad:  # gradients that vanish identically (oracle exact zeros): the absolute bar applies
+        return float(np.abs(ref).max()) == 0.0 or (chunk == 64 and mx <= CANCEL_ABS * scale), rel, mx
+    cancelled = float(np.linalg.norm(np.asarray(ref, dtype=np.float64))) < CANCEL_NORM
+    return chunk == 64 and cancelled and mx <= CANCEL_ABS, rel, mx
 
 
 def _check(name, got, ref, case, chunk, grad=False):
