@@ -16,9 +16,11 @@
 //                             S_{n+1} = Diag(e^{g_C-ref}) (X + K^^T (U' - W~ X)), every S_n and U kept
 //   dstates (the same)        dS_n = Diag(e^ref) (dD - W~^T (K^ dD) + E), dD = Diag(e^{g_C-ref}) dS_{n+1}
 //   grads   (chunk-parallel, two kernels) every input gradient of the chunk from S_n and dS_{n+1}
-// Every product is a small dense GEMM over shared-memory tiles, so the work runs at CUDA-core
-// throughput instead of the token-serial path's per-token reduction latency.  All arithmetic is
-// fp32; sums are in a fixed order, so the result is bit-reproducible.  e^{g-ref} must stay in fp32
+// Every product is a small dense GEMM over shared-memory tiles (fp32), computed on the tensor
+// cores by warp-level bf16 MMAs with each operand split into bf16 hi + lo (three products per
+// tile, fp32 accumulation: about 2^-16 relative error per product, against the 2e-3 gradient
+// bar), instead of the token-serial path's per-token reduction latency.  Every element-wise
+// step is fp32; sums are in a fixed order, so the result is bit-reproducible.  e^{g-ref} must stay in fp32
 // range: a (sequence, head) with a chunk whose half-chunk log-decay sum is below -80 is flagged,
 // and after these passes the token-serial backward (which has no such limit) recomputes exactly
 // those units.
@@ -30,9 +32,11 @@ namespace {
 constexpr int C = 64;          // chunk
 constexpr int NT = 512;        // 16 warps
 // Row strides of the shared tiles: multiples of 4 floats (16-byte rows for 128-bit loads) and
-// 4 more than a multiple of 32, so 8 consecutive rows start in 8 distinct 16-byte bank groups.
-constexpr int LD = kD + 4;     // C x D and D x D tiles
-constexpr int LC = C + 4;      // C x C tiles
+// 8 more than a multiple of 32.  A tensor-core fragment reads a pair along k from each of 8 rows
+// (rows g, lanes 4g..4g+3): at that stride the 4 rows of a half-warp cover the 32 banks once, and
+// a transposed read (one float from each of 8 rows at 4 k) is conflict-free as well.
+constexpr int LD = kD + 8;     // C x D and D x D tiles
+constexpr int LC = C + 8;      // C x C tiles
 constexpr int TILE_CD = C * LD;
 constexpr int TILE_DD = kD * LD;
 constexpr int TILE_CC = C * LC;
@@ -59,14 +63,22 @@ struct CBwd {
     float* S;   // per (sequence, n) for n = 0..chunks: S_n at slot (co[s] + s + n) * H + h
 };
 
-// Register fragment of an M x N product spread over the 16 warps: warp w holds rows
-// w*MR .. w*MR+MR-1, lane l holds columns l + 32 j.
+// Register fragment of an M x N product spread over the 16 warps, in the accumulator layout of
+// the warp-level tensor-core product m16n8k16: warp w owns MT = M/64 tiles of 16 rows starting at
+// row 16 MT (w % 4) and NTL = N/32 tiles of 8 columns starting at column 8 NTL (w / 4); lane
+// (g, t) = (lane / 4, lane % 4) holds rows g and g + 8 and columns 2t and 2t + 1 of each tile.
+// v[i][j] is row(i), col(j): the element-wise code addresses it through these alone.
 template <int M, int N>
 struct Frag {
-    static constexpr int MR = M / 16, NJ = N / 32;
+    static constexpr int MT = M / 64, NTL = N / 32, MR = 2 * MT, NJ = 2 * NTL;
+    static_assert(M % 64 == 0 && N % 32 == 0, "fragment shape");
     float v[MR][NJ];
-    __device__ __forceinline__ static int row(int i) { return (int)(threadIdx.x >> 5) * MR + i; }
-    __device__ __forceinline__ static int col(int j) { return (int)(threadIdx.x & 31) + 32 * j; }
+    __device__ __forceinline__ static int row(int i) {
+        return (int)((threadIdx.x >> 5) & 3) * MT * 16 + 16 * (i >> 1) + 8 * (i & 1) + (int)((threadIdx.x & 31) >> 2);
+    }
+    __device__ __forceinline__ static int col(int j) {
+        return (int)(threadIdx.x >> 7) * NTL * 8 + 8 * (j >> 1) + 2 * (int)(threadIdx.x & 3) + (j & 1);
+    }
     __device__ __forceinline__ void zero() {
 #pragma unroll
         for (int i = 0; i < MR; ++i)
@@ -75,50 +87,84 @@ struct Frag {
     }
 };
 
+// Two fp32 values as bf16 pairs hi + lo (x ~ hi + lo to 16 significant bits): hi rounded to
+// nearest, lo the rounded remainder.  Lower k index in the low half, as the MMA fragments want.
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+// d (16x8 fp32) += a (16x16 bf16, row fragment) x b (16x8 bf16, column fragment)
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // f (+/-)= A B, A(m, k) = A[m * ARS + k * ACS], B(k, n) = B[k * BRS + n * BCS], k in [0, K).
 // One of ARS, ACS is 1 (A is stored k-contiguous or m-contiguous) and one of BRS, BCS is 1.
-// Four k at a time: A is read by all lanes of a warp at once (a broadcast) with 128-bit loads
-// along its contiguous dimension; B's columns go to distinct lanes, with 128-bit loads along k
-// when B is stored k-contiguous and 32-bit loads otherwise.  Rows, strides and k steps are
-// multiples of 4 floats, so every 128-bit access is aligned.
+// On the tensor cores with fp32-level accuracy from bf16 operands: every operand is split into
+// bf16 hi + lo as its fragment is loaded, and each 16 x 8 x 16 tile takes the three products
+// hi.hi + hi.lo + lo.hi (the dropped lo.lo term and the rounding of lo are below 2^-16 of the
+// product), accumulated in fp32.  Pairs along k are loaded 8 bytes at a time where they are
+// contiguous.
 template <bool NEG, int K, int ARS, int ACS, int BRS, int BCS, int M, int N>
 __device__ __forceinline__ void gemm(Frag<M, N>& f, const float* A, const float* B) {
-    constexpr int MR = M / 16, NJ = N / 32;
+    using F = Frag<M, N>;
+    constexpr int MT = F::MT, NTL = F::NTL;
     constexpr bool A_KC = ACS == 1, B_KC = BRS == 1;
-    static_assert((A_KC || ARS == 1) && (B_KC || BCS == 1) && K % 4 == 0 && MR % 4 == 0, "layout");
-    const int m0 = (threadIdx.x >> 5) * MR, l = threadIdx.x & 31;
-#pragma unroll 4
-    for (int k0 = 0; k0 < K; k0 += 4) {
-        float a[MR][4], b[NJ][4];
+    static_assert((A_KC || ARS == 1) && (B_KC || BCS == 1) && K % 16 == 0, "layout");
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int mb = (int)((threadIdx.x >> 5) & 3) * MT * 16, nb = (int)(threadIdx.x >> 7) * NTL * 8;
+    auto ldA = [&](int m, int k) -> float2 {
+        if constexpr (A_KC) return *reinterpret_cast<const float2*>(A + m * ARS + k);
+        else return make_float2(A[m + k * ACS], A[m + (k + 1) * ACS]);
+    };
+    auto ldB = [&](int k, int n) -> float2 {
+        if constexpr (B_KC) return *reinterpret_cast<const float2*>(B + k + n * BCS);
+        else return make_float2(B[k * BRS + n], B[(k + 1) * BRS + n]);
+    };
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
-        for (int i = 0; i < MR; ++i) {
-            if (A_KC) {
-                const float4 t = *reinterpret_cast<const float4*>(A + (m0 + i) * ARS + k0);
-                a[i][0] = t.x; a[i][1] = t.y; a[i][2] = t.z; a[i][3] = t.w;
-            } else if (i % 4 == 0) {
+        for (int mt = 0; mt < MT; ++mt) {
+            const int r0 = mb + 16 * mt + g, ka = k0 + 2 * t;
+            const float2 x0 = ldA(r0, ka), x1 = ldA(r0 + 8, ka), x2 = ldA(r0, ka + 8), x3 = ldA(r0 + 8, ka + 8);
+            split_bf16(x0.x, x0.y, ah[mt][0], al[mt][0]);
+            split_bf16(x1.x, x1.y, ah[mt][1], al[mt][1]);
+            split_bf16(x2.x, x2.y, ah[mt][2], al[mt][2]);
+            split_bf16(x3.x, x3.y, ah[mt][3], al[mt][3]);
+            if (NEG) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const float4 t = *reinterpret_cast<const float4*>(A + (k0 + kk) * ACS + m0 + i);
-                    a[i][kk] = t.x; a[i + 1][kk] = t.y; a[i + 2][kk] = t.z; a[i + 3][kk] = t.w;
+                for (int q = 0; q < 4; ++q) {
+                    ah[mt][q] ^= 0x80008000u;
+                    al[mt][q] ^= 0x80008000u;
                 }
             }
         }
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            if (B_KC) {
-                const float4 t = *reinterpret_cast<const float4*>(B + (l + 32 * j) * BCS + k0);
-                b[j][0] = t.x; b[j][1] = t.y; b[j][2] = t.z; b[j][3] = t.w;
-            } else {
+        for (int nt = 0; nt < NTL; ++nt) {
+            const int cn = nb + 8 * nt + g, kk = k0 + 2 * t;
+            const float2 y0 = ldB(kk, cn), y1 = ldB(kk + 8, cn);
+            uint32_t bh[2], bl[2];
+            split_bf16(y0.x, y0.y, bh[0], bl[0]);
+            split_bf16(y1.x, y1.y, bh[1], bl[1]);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) b[j][kk] = B[(k0 + kk) * BRS + l + 32 * j];
+            for (int mt = 0; mt < MT; ++mt) {
+                float d[4] = {f.v[2 * mt][2 * nt], f.v[2 * mt][2 * nt + 1], f.v[2 * mt + 1][2 * nt],
+                              f.v[2 * mt + 1][2 * nt + 1]};
+                mma_bf16(d, ah[mt], bh);
+                mma_bf16(d, ah[mt], bl);
+                mma_bf16(d, al[mt], bh);
+                f.v[2 * mt][2 * nt] = d[0];
+                f.v[2 * mt][2 * nt + 1] = d[1];
+                f.v[2 * mt + 1][2 * nt] = d[2];
+                f.v[2 * mt + 1][2 * nt + 1] = d[3];
             }
         }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-            for (int i = 0; i < MR; ++i)
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) f.v[i][j] = fmaf(NEG ? -a[i][kk] : a[i][kk], b[j][kk], f.v[i][j]);
     }
 }
 
@@ -848,15 +894,20 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     __syncthreads();
     gemm<false, C, 1, LC, LD, 1>(dKh, sM, sK);  // + (diag(beta) dA)^T K~
 
-    // beta gradient: this warp's rows are complete across its 32 lanes
+    // beta gradient: a row's columns are spread over the 4 lanes of a quad (t) and the 4 warps w / 4;
+    // sum over the quad, then over the warps in a fixed order (s0 rows 0..3 hold the partials)
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < F::MR; ++i) {
         float x = db[i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        const int r = F::row(i);
-        if ((threadIdx.x & 31) == 0 && r < c.L) P.dbeta[(size_t)(c.tok0 + r) * P.H + h] = x;
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        if ((threadIdx.x & 3) == 0) s0[(threadIdx.x >> 7) * LD + F::row(i)] = x;
     }
+    __syncthreads();
+    if (threadIdx.x < c.L)
+        P.dbeta[(size_t)(c.tok0 + threadIdx.x) * P.H + h] =
+            ((s0[threadIdx.x] + s0[LD + threadIdx.x]) + s0[2 * LD + threadIdx.x]) + s0[3 * LD + threadIdx.x];
     // decay gradient and dq, dk
     __syncthreads();
     load_gates(W, c, h, sX, nullptr, sM);  // g again
