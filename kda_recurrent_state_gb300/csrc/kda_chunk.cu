@@ -90,7 +90,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 // term is 2^-15 of an O(1) operand, below the fp16 rounding of the products themselves; chunks
 // beyond it take the exact fp32 path.
 constexpr float kMaxExp2 = 10.0f;
-constexpr int kSerialRows = 8;  // tokens staged at a time by the exact per-token path
 constexpr int kRowH = 48;          // row stride (bytes) of a 16x16 fp16 block (ldmatrix: no bank conflicts)
 constexpr int kBlkH = 16 * kRowH;  // bytes per fp16 block
 
@@ -146,7 +145,6 @@ static_assert(Cfg<float>::SMEM_BYTES <= 232448, "smem budget (fp32)");
 static_assert(Cfg<__nv_bfloat16>::OFF_RING % 128 == 0 && Cfg<float>::OFF_RING % 128 == 0, "TMA destinations");
 static_assert(Cfg<__nv_bfloat16>::OFF_STG % 128 == 0, "TMA store source");
 static_assert(Cfg<__nv_bfloat16>::OFF_BAR % 8 == 0 && Cfg<float>::OFF_BAR % 8 == 0, "mbarrier alignment");
-static_assert(kSerialRows * 4 * 128 * 4 <= 32768, "exact path staging fits the output staging / KT-QT pair");
 
 // barrier indices
 enum {
@@ -172,7 +170,8 @@ enum {
     B_VFREE = 33,    // [3] decay vectors of a chunk consumed (ring of 3, by chunk index mod 3)
     B_STGR = 36,     // own staging buffer read by the previous bulk store (STG_OWN)
     B_PDONE = 37,    // prep has seen every chunk (the unit's range flag is final); ROB = false
-    B_COUNT = 38
+    B_SER = 38,      // the exact path's coefficient buffers written (state warpgroup; ROB = true)
+    B_COUNT = 39
 };
 static_assert(B_COUNT <= (int)Cfg<float>::NBAR, "barrier space");
 
@@ -327,103 +326,194 @@ __device__ __noinline__ void store_state_bf16(__nv_bfloat16* dst, uint32_t taddr
     }
 }
 
-// The exact path for one chunk whose gates leave the fp16 operand range: its tokens applied one at
-// a time, in fp32, to this thread's value column j of the state, which stays in TMEM (taddr: the
+// The exact path for one chunk whose gates leave the fp16 operand range: its tokens applied in
+// fp32, in order, to this thread's value column j of the state, which stays in TMEM (taddr: the
 // D_S row of lane j, columns = key channels).  Per token ("Kimi K3" article §四 with the §二.1 read):
-// p = (Diag(alpha) S)^T k, u = beta (v - p), S <- Diag(alpha) S + k u^T, o = S^T q.  Called by the
-// 128 threads of the state warpgroup; `stage` is 16 KB of shared memory the warpgroup owns for the
-// call; named barrier 1 orders its use.  row0: the chunk's first packed token.  The output rows go
-// straight to global memory.  Out of line: it runs only for such chunks.
+//   u_t = beta_t (v_t - (alpha_t . k_t)^T S_{t-1}),  S_t = alpha_t . S_{t-1} + k_t u_t,  o_t = S_t^T q_t.
+// kG tokens are folded into one read pass and one write pass over the column.  With the group's
+// start state S, A_t = alpha_0 ... alpha_t and B_{s,t} = alpha_{s+1} ... alpha_t (B_{t,t} = 1),
+// products of gates, so every factor is in [0, 1] whatever the gates:
+//   (alpha_t . k_t)^T S_{t-1} = (k_t A_t)^T S + sum_{s<t} [(k_t B_{s,t})^T k_s] u_s
+//   o_t = (q_t A_t)^T S + sum_{s<=t} [(q_t B_{s,t})^T k_s] u_s
+//   S_{kG-1} = A_{kG-1} . S + sum_s (k_s B_{s,kG-1}) u_s.
+// The bracketed scalars are the same for every column; the 128 threads reduce them together.
+// Called by the 128 threads of the state warpgroup; `stage` (two buffers of kSerBuf floats) is
+// shared memory the warpgroup owns for the call; `sbar` (128 arrivals per use, phase count in
+// `sph`) orders its use, with bounded waits.  row0: the chunk's first packed token.  The output
+// rows go straight to global memory.  Out of line: it runs only for such chunks.  Returns false
+// if a wait gave up.
+constexpr int kG = 4;                                     // tokens per pass pair
+constexpr int kSerVec = 3 * kG + 1;                       // coefficient vectors of a group
+constexpr int kSerM = kG * (kG - 1) / 2, kSerN = kG * (kG + 1) / 2;  // scalars (s < t), (s <= t)
+constexpr int kSerBuf = kSerVec * 128 + 4 * (kSerM + kSerN);  // + one partial sum per warp
+static_assert(2 * kSerBuf * 4 <= 32768 && (kSerBuf * 4) % 16 == 0, "exact path buffers fit the output staging / KT-QT pair");
 template <typename Tin, typename Tout, bool SG>
-__device__ __noinline__ void serial_chunk(uint32_t taddr, int j, int64_t row0, int valid, int h, int H,
+__device__ __noinline__ bool serial_chunk(uint32_t taddr, int j, int64_t row0, int valid, int h, int H,
                                           const Tin* __restrict__ q, const Tin* __restrict__ k,
                                           const Tin* __restrict__ v, const float* __restrict__ log_alpha,
-                                          const float* __restrict__ beta, Tout* __restrict__ out, float* stage) {
-    // stage[r][0][c] = alpha_c k_c, [1] = alpha_c, [2] = k_c, [3] = q_c for kSerialRows tokens
-#pragma unroll 1
-    for (int r0 = 0; r0 < valid; r0 += kSerialRows) {
-        const int nt = valid - r0 < kSerialRows ? valid - r0 : kSerialRows;
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the previous group's rows are consumed
-        float vv[kSerialRows], bb[kSerialRows];
+                                          const float* __restrict__ beta, Tout* __restrict__ out, float* stage,
+                                          uint64_t* sbar, uint32_t& sph, Abort* ab, int* status) {
+    // vectors of a buffer: [t] k_t A_t, [kG + t] q_t A_t, [2 kG] A_{kG-1}, [2 kG + 1 + s] k_s B_{s,kG-1}
+    constexpr int KA = 0, QA = kG, AL = 2 * kG, KB = 2 * kG + 1, PART = kSerVec * 128;
+    const int lane = j & 31, wq = j >> 5;
+    // this thread's channel c = j of every token of a group (and its own value column j)
+    float kk[kG], qq[kG], la[kG], vv[kG], bb[kG];
+    auto load = [&](int r0) {
 #pragma unroll
-        for (int r = 0; r < kSerialRows; ++r) {
-            vv[r] = 0.f;
-            bb[r] = 0.f;
-            if (r < nt) {
-                const size_t tok = (size_t)(row0 + r0 + r) * H + h, off = tok * kD + j;
-                const float kk = ld_in(k, off);
-                float la = 0.f;
+        for (int t = 0; t < kG; ++t) {
+            kk[t] = qq[t] = la[t] = vv[t] = bb[t] = 0.f;  // past the chunk: identity steps
+            if (r0 + t < valid) {
+                const size_t tok = (size_t)(row0 + r0 + t) * H + h, off = tok * kD + j;
+                kk[t] = ld_in(k, off);
+                qq[t] = ld_in(q, off);
+                vv[t] = ld_in(v, off);
+                bb[t] = beta[tok];
                 if constexpr (SG)
-                    la = log_alpha ? log_alpha[tok] : 0.f;
+                    la[t] = log_alpha ? log_alpha[tok] : 0.f;
                 else
-                    la = log_alpha[off];
-                const float a = expf(la);
-                float* st = stage + r * 4 * kD;
-                st[j] = a * kk;
-                st[kD + j] = a;
-                st[2 * kD + j] = kk;
-                st[3 * kD + j] = ld_in(q, off);
-                vv[r] = ld_in(v, off);
-                bb[r] = beta[tok];
+                    la[t] = log_alpha[off];
             }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+    };
+    load(0);
 #pragma unroll 1
-        for (int r = 0; r < nt; ++r) {
-            const float* st = stage + r * 4 * kD;
-            uint32_t sp[32];
-            float p = 0.f;  // (Diag(alpha) S)^T k for column j
-#pragma unroll 1
-            for (int piece = 0; piece < 4; ++piece) {
-                tmem_ld32(taddr + piece * 32, sp);
-                tmem_ld_wait();
+    for (int r0 = 0, g = 0; r0 < valid; r0 += kG, ++g) {
+        float* buf = stage + (g & 1) * kSerBuf;
+        float vt[kG], bt[kG];
+        {  // coefficients of this group (channel j)
+            float al[kG];
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 w = *reinterpret_cast<const float4*>(st + piece * 32 + 4 * e4);
-                    p = fmaf(w.x, __uint_as_float(sp[4 * e4]), p);
-                    p = fmaf(w.y, __uint_as_float(sp[4 * e4 + 1]), p);
-                    p = fmaf(w.z, __uint_as_float(sp[4 * e4 + 2]), p);
-                    p = fmaf(w.w, __uint_as_float(sp[4 * e4 + 3]), p);
-                }
+            for (int t = 0; t < kG; ++t) al[t] = expf(la[t]);
+            float A = 1.f;  // A_t
+#pragma unroll
+            for (int t = 0; t < kG; ++t) {
+                A *= al[t];
+                buf[(KA + t) * 128 + j] = kk[t] * A;
+                buf[(QA + t) * 128 + j] = qq[t] * A;
             }
-            float vr = vv[0], br = bb[0];
+            buf[AL * 128 + j] = A;
+            // Per-channel terms of the scalars, each summed over the warp (xor tree); lane 0 keeps
+            // one partial per warp.  b runs through B_{s,t} for t = s, s + 1, ...
 #pragma unroll
-            for (int i = 1; i < kSerialRows; ++i)
-                if (i == r) {
-                    vr = vv[i];
-                    br = bb[i];
-                }
-            const float u = br * (vr - p);
-            float o = 0.f;
-#pragma unroll 1
-            for (int piece = 0; piece < 4; ++piece) {
-                tmem_ld32(taddr + piece * 32, sp);
-                tmem_ld_wait();
+            for (int s = 0; s < kG; ++s) {
+                float b = 1.f;
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const int c = piece * 32 + 4 * e4;
-                    const float4 a = *reinterpret_cast<const float4*>(st + kD + c);
-                    const float4 kk = *reinterpret_cast<const float4*>(st + 2 * kD + c);
-                    const float4 qq = *reinterpret_cast<const float4*>(st + 3 * kD + c);
-                    const float av[4] = {a.x, a.y, a.z, a.w}, kv[4] = {kk.x, kk.y, kk.z, kk.w},
-                                qv[4] = {qq.x, qq.y, qq.z, qq.w};
+                for (int t = s; t < kG; ++t) {
+                    if (t > s) b *= al[t];
+                    const float kb = kk[s] * b;
+                    float nq = qq[t] * kb, mk = kk[t] * kb;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float sn = fmaf(kv[e], u, av[e] * __uint_as_float(sp[4 * e4 + e]));
-                        o = fmaf(qv[e], sn, o);
-                        sp[4 * e4 + e] = __float_as_uint(sn);
+                    for (int m = 16; m >= 1; m >>= 1) {
+                        nq += __shfl_xor_sync(0xffffffffu, nq, m);
+                        if (t > s) mk += __shfl_xor_sync(0xffffffffu, mk, m);
+                    }
+                    if (lane == 0) {
+                        float* pw = buf + PART + wq * (kSerM + kSerN);
+                        pw[kSerM + t * (t + 1) / 2 + s] = nq;
+                        if (t > s) pw[t * (t - 1) / 2 + s] = mk;
                     }
                 }
-                tmem_st32(taddr + piece * 32, sp);
+                buf[(KB + s) * 128 + j] = kk[s] * b;  // k_s B_{s,kG-1}
             }
-            tmem_st_wait();  // the next token reads these columns back
-            const size_t off = ((size_t)(row0 + r0 + r) * H + h) * kD + j;
-            if constexpr (sizeof(Tout) == 2)
-                out[off] = __float2bfloat16_rn(o);
-            else
-                out[off] = o;
+#pragma unroll
+            for (int t = 0; t < kG; ++t) {
+                vt[t] = vv[t];
+                bt[t] = bb[t];
+            }
         }
+        mbar_arrive(sbar);
+        if (!mbar_wait(sbar, (sph++) & 1, ab, status)) return false;
+        // read pass: x_t = (k_t A_t)^T S, y_t = (q_t A_t)^T S
+        float x[kG], y[kG];
+#pragma unroll
+        for (int t = 0; t < kG; ++t) x[t] = y[t] = 0.f;
+        uint32_t s0[32], s1[32];
+#pragma unroll 1
+        for (int pp = 0; pp < 4; pp += 2) {
+            tmem_ld32(taddr + pp * 32, s0);
+            tmem_ld32(taddr + (pp + 1) * 32, s1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t(&d)[32] = hf ? s1 : s0;
+                const int c0 = (pp + hf) * 32;
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const int c = c0 + 4 * e4;
+#pragma unroll
+                    for (int t = 0; t < kG; ++t) {
+                        const float4 a = *reinterpret_cast<const float4*>(buf + (KA + t) * 128 + c);
+                        const float4 b = *reinterpret_cast<const float4*>(buf + (QA + t) * 128 + c);
+                        x[t] = fmaf(a.x, __uint_as_float(d[4 * e4]), x[t]);
+                        y[t] = fmaf(b.x, __uint_as_float(d[4 * e4]), y[t]);
+                        x[t] = fmaf(a.y, __uint_as_float(d[4 * e4 + 1]), x[t]);
+                        y[t] = fmaf(b.y, __uint_as_float(d[4 * e4 + 1]), y[t]);
+                        x[t] = fmaf(a.z, __uint_as_float(d[4 * e4 + 2]), x[t]);
+                        y[t] = fmaf(b.z, __uint_as_float(d[4 * e4 + 2]), y[t]);
+                        x[t] = fmaf(a.w, __uint_as_float(d[4 * e4 + 3]), x[t]);
+                        y[t] = fmaf(b.w, __uint_as_float(d[4 * e4 + 3]), y[t]);
+                    }
+                }
+            }
+        }
+        if (r0 + kG < valid) load(r0 + kG);  // the next group's inputs in flight during the write pass
+        // the tokens in order: u_t, o_t (scalar i: the four warps' partials, summed in a fixed order)
+        auto sc = [&](int i) -> float {
+            const float* pt = buf + PART + i;
+            return (pt[0] + pt[kSerM + kSerN]) + (pt[2 * (kSerM + kSerN)] + pt[3 * (kSerM + kSerN)]);
+        };
+        float u[kG];
+#pragma unroll
+        for (int t = 0; t < kG; ++t) {
+            float z = x[t];
+#pragma unroll
+            for (int s = 0; s < t; ++s) z = fmaf(sc(t * (t - 1) / 2 + s), u[s], z);
+            u[t] = bt[t] * (vt[t] - z);
+            float o = y[t];
+#pragma unroll
+            for (int s = 0; s <= t; ++s) o = fmaf(sc(kSerM + t * (t + 1) / 2 + s), u[s], o);
+            if (r0 + t < valid) {
+                const size_t off = ((size_t)(row0 + r0 + t) * H + h) * kD + j;
+                if constexpr (sizeof(Tout) == 2)
+                    out[off] = __float2bfloat16_rn(o);
+                else
+                    out[off] = o;
+            }
+        }
+        // write pass: S <- A_{kG-1} . S + sum_s (k_s B_{s,kG-1}) u_s
+#pragma unroll 1
+        for (int pp = 0; pp < 4; pp += 2) {
+            tmem_ld32(taddr + pp * 32, s0);
+            tmem_ld32(taddr + (pp + 1) * 32, s1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t(&d)[32] = hf ? s1 : s0;
+                const int c0 = (pp + hf) * 32;
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const int c = c0 + 4 * e4;
+                    const float4 a = *reinterpret_cast<const float4*>(buf + AL * 128 + c);
+                    float sn[4] = {a.x * __uint_as_float(d[4 * e4]), a.y * __uint_as_float(d[4 * e4 + 1]),
+                                   a.z * __uint_as_float(d[4 * e4 + 2]), a.w * __uint_as_float(d[4 * e4 + 3])};
+#pragma unroll
+                    for (int t = 0; t < kG; ++t) {
+                        const float4 kb = *reinterpret_cast<const float4*>(buf + (KB + t) * 128 + c);
+                        sn[0] = fmaf(kb.x, u[t], sn[0]);
+                        sn[1] = fmaf(kb.y, u[t], sn[1]);
+                        sn[2] = fmaf(kb.z, u[t], sn[2]);
+                        sn[3] = fmaf(kb.w, u[t], sn[3]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d[4 * e4 + e] = __float_as_uint(sn[e]);
+                }
+            }
+            tmem_st32(taddr + pp * 32, s0);
+            tmem_st32(taddr + (pp + 1) * 32, s1);
+        }
+        tmem_st_wait();  // the next group reads these columns back
     }
+    return true;
 }
 
 // ROB: the instantiation that recomputes the units the first pass marked in `redo`
@@ -535,6 +625,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < 3; ++i) mbar_init(&bar[B_VFREE + i], 128);
         mbar_init(&bar[B_STGR], 1);
         mbar_init(&bar[B_PDONE], 128);
+        mbar_init(&bar[B_SER], 128);
         ab->flag = 0;
         *range_bad = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -783,6 +874,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Tout* out = static_cast<Tout*>(P.out);
         bool ok = true;
         uint32_t ph_stg = 0;    // phase of the staging barrier (every thread waits on it)
+        uint32_t ph_ser = 0;    // phase of the exact path's barrier
         bool u_issued = false;  // (i) of the coming chunk already issued (thread 0)
         // chunk m goes the exact per-token way (read once prep(m) has arrived on B_PREPD)
         auto bad_chunk = [&](int m) -> bool {
@@ -904,10 +996,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 uint8_t* stage = sm + (L::STG_OWN ? L::OFF_STG : L::OFF_KQ + b * 32768);
                 if constexpr (L::STG_OWN)  // the previous chunk's bulk store has read the buffer
                     if (n > 0 && !(ok = mbar_wait(&bar[B_STGR], (n - 1) & 1, ab, status))) break;
-                serial_chunk<Tin, Tout, SG>(tmem + lane_base + TM_S, j, t0 + (int64_t)C * n, valid, h, P.H,
-                                            static_cast<const Tin*>(P.q), static_cast<const Tin*>(P.k),
-                                            static_cast<const Tin*>(P.v), P.log_alpha, P.beta,
-                                            static_cast<Tout*>(P.out), reinterpret_cast<float*>(stage));
+                if (j == 0) KDA_TR(n, 1);
+                if (!(ok = serial_chunk<Tin, Tout, SG>(tmem + lane_base + TM_S, j, t0 + (int64_t)C * n, valid, h,
+                                                       P.H, static_cast<const Tin*>(P.q),
+                                                       static_cast<const Tin*>(P.k), static_cast<const Tin*>(P.v),
+                                                       P.log_alpha, P.beta, static_cast<Tout*>(P.out),
+                                                       reinterpret_cast<float*>(stage), &bar[B_SER], ph_ser, ab,
+                                                       status)))
+                    break;
+                if (j == 0) KDA_TR(n, 28);
             }
             {
                 const int64_t end_pos = (int64_t)C * n + valid;  // tokens of the sequence consumed so far
