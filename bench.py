@@ -472,16 +472,20 @@ def e2e(args, x, out, fin, ws, dev, out_dtype):
     for _ in range(2):  # warm-up: first touch of the pinned buffers and the copy engines
         step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.e2e_steps):
         step()
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
-    dt = e0.elapsed_time(e1) / 1e3 / args.e2e_steps
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.e2e_steps)]
+    dt = sum(per) / 1e3 / args.e2e_steps
     del hws
+    # The host link of these boxes has intermittent slow periods (the same pinned copies take
+    # 1x to 2.3x their usual time), so the per-step times are reported beside the mean.
     return {"value": B * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": dt * 1e3, "steps": args.e2e_steps,
+            "per_step_ms": [round(p, 2) for p in per], "median_step_ms": sorted(per)[len(per) // 2],
             "path": f"kda_chunk_fwd_host, pinned host buffers, {seg}-token segments"}
 
 
