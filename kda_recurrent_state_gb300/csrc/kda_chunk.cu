@@ -327,23 +327,26 @@ __device__ __noinline__ void store_state_bf16(__nv_bfloat16* dst, uint32_t taddr
 }
 
 // The exact path for one chunk whose gates leave the fp16 operand range: its tokens applied in
-// fp32, in order, to this thread's value column j of the state, which stays in TMEM (taddr: the
-// D_S row of lane j, columns = key channels).  Per token ("Kimi K3" article §四 with the §二.1 read):
+// fp32, in order, to the state held in TMEM (taddr: D_S of this warp's 32 lanes, lanes = value
+// columns, columns = key channels).  Per token ("Kimi K3" article §四 with the §二.1 read):
 //   u_t = beta_t (v_t - (alpha_t . k_t)^T S_{t-1}),  S_t = alpha_t . S_{t-1} + k_t u_t,  o_t = S_t^T q_t.
-// kG tokens are folded into one read pass and one write pass over the column.  With the group's
+// kG tokens are folded into one read pass and one write pass over the state.  With the group's
 // start state S, A_t = alpha_0 ... alpha_t and B_{s,t} = alpha_{s+1} ... alpha_t (B_{t,t} = 1),
 // products of gates, so every factor is in [0, 1] whatever the gates:
 //   (alpha_t . k_t)^T S_{t-1} = (k_t A_t)^T S + sum_{s<t} [(k_t B_{s,t})^T k_s] u_s
 //   o_t = (q_t A_t)^T S + sum_{s<=t} [(q_t B_{s,t})^T k_s] u_s
 //   S_{kG-1} = A_{kG-1} . S + sum_s (k_s B_{s,kG-1}) u_s.
 // The bracketed scalars are the same for every column; the 128 threads reduce them together.
+// The state is accessed with 16x256b TMEM loads, so that a thread holds two key channels of four
+// value columns at a time and each coefficient it reads from shared memory serves four columns;
+// the four threads that share columns (lane % 4) sum their partial dot products with two shuffles.
 // Called by the 128 threads of the state warpgroup; `stage` (two buffers of kSerBuf floats) is
 // shared memory the warpgroup owns for the call; `sbar` (128 arrivals per use, phase count in
 // `sph`) orders its use, with bounded waits.  row0: the chunk's first packed token.  The output
 // rows go straight to global memory.  Out of line: it runs only for such chunks.  Returns false
 // if a wait gave up.
 constexpr int kG = 4;                                     // tokens per pass pair
-constexpr int kSerVec = 3 * kG + 1;                       // coefficient vectors of a group
+constexpr int kSerVec = 4 * kG + 1;                       // coefficient (and v) vectors of a group
 constexpr int kSerM = kG * (kG - 1) / 2, kSerN = kG * (kG + 1) / 2;  // scalars (s < t), (s <= t)
 constexpr int kSerBuf = kSerVec * 128 + 4 * (kSerM + kSerN);  // + one partial sum per warp
 static_assert(2 * kSerBuf * 4 <= 32768 && (kSerBuf * 4) % 16 == 0, "exact path buffers fit the output staging / KT-QT pair");
@@ -353,10 +356,16 @@ __device__ __noinline__ bool serial_chunk(uint32_t taddr, int j, int64_t row0, i
                                           const Tin* __restrict__ v, const float* __restrict__ log_alpha,
                                           const float* __restrict__ beta, Tout* __restrict__ out, float* stage,
                                           uint64_t* sbar, uint32_t& sph, Abort* ab, int* status) {
-    // vectors of a buffer: [t] k_t A_t, [kG + t] q_t A_t, [2 kG] A_{kG-1}, [2 kG + 1 + s] k_s B_{s,kG-1}
-    constexpr int KA = 0, QA = kG, AL = 2 * kG, KB = 2 * kG + 1, PART = kSerVec * 128;
+    // vectors of a buffer: [t] k_t A_t, [kG + t] q_t A_t, [2 kG] A_{kG-1}, [2 kG + 1 + s] k_s B_{s,kG-1},
+    // [3 kG + 1 + t] v_t (by value column)
+    constexpr int KA = 0, QA = kG, AL = 2 * kG, KB = 2 * kG + 1, VV = 3 * kG + 1, PART = kSerVec * 128;
     const int lane = j & 31, wq = j >> 5;
-    // this thread's channel c = j of every token of a group (and its own value column j)
+    // 16x256b layout: this thread's value columns jc(i) = 32 wq + lane / 4 + 8 i (i = 0, 1 from the
+    // warp's first 16 lanes, 2, 3 from the next 16), its key channels 8 b + cq and 8 b + cq + 1 of
+    // every block b of 8
+    const int cq = 2 * (lane & 3), j0 = 32 * wq + (lane >> 2);
+    const uint32_t tA = taddr, tB = taddr + (16u << 16);
+    // this thread's channel c = j of every token of a group (and value column j)
     float kk[kG], qq[kG], la[kG], vv[kG], bb[kG];
     auto load = [&](int r0) {
 #pragma unroll
@@ -379,8 +388,8 @@ __device__ __noinline__ bool serial_chunk(uint32_t taddr, int j, int64_t row0, i
 #pragma unroll 1
     for (int r0 = 0, g = 0; r0 < valid; r0 += kG, ++g) {
         float* buf = stage + (g & 1) * kSerBuf;
-        float vt[kG], bt[kG];
-        {  // coefficients of this group (channel j)
+        float bt[kG];
+        {  // coefficients of this group (channel j), and v (column j)
             float al[kG];
 #pragma unroll
             for (int t = 0; t < kG; ++t) al[t] = expf(la[t]);
@@ -390,6 +399,8 @@ __device__ __noinline__ bool serial_chunk(uint32_t taddr, int j, int64_t row0, i
                 A *= al[t];
                 buf[(KA + t) * 128 + j] = kk[t] * A;
                 buf[(QA + t) * 128 + j] = qq[t] * A;
+                buf[(VV + t) * 128 + j] = vv[t];
+                bt[t] = bb[t];
             }
             buf[AL * 128 + j] = A;
             // Per-channel terms of the scalars, each summed over the warp (xor tree); lane 0 keeps
@@ -415,101 +426,108 @@ __device__ __noinline__ bool serial_chunk(uint32_t taddr, int j, int64_t row0, i
                 }
                 buf[(KB + s) * 128 + j] = kk[s] * b;  // k_s B_{s,kG-1}
             }
-#pragma unroll
-            for (int t = 0; t < kG; ++t) {
-                vt[t] = vv[t];
-                bt[t] = bb[t];
-            }
         }
         mbar_arrive(sbar);
         if (!mbar_wait(sbar, (sph++) & 1, ab, status)) return false;
-        // read pass: x_t = (k_t A_t)^T S, y_t = (q_t A_t)^T S
-        float x[kG], y[kG];
+        // read pass: x_t = (k_t A_t)^T S and y_t = (q_t A_t)^T S for the four columns (partial over
+        // this thread's channels, then summed over the four threads sharing the columns)
+        float acc[2 * kG][4];
 #pragma unroll
-        for (int t = 0; t < kG; ++t) x[t] = y[t] = 0.f;
-        uint32_t s0[32], s1[32];
+        for (int w = 0; w < 2 * kG; ++w)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[w][i] = 0.f;
 #pragma unroll 1
-        for (int pp = 0; pp < 4; pp += 2) {
-            tmem_ld32(taddr + pp * 32, s0);
-            tmem_ld32(taddr + (pp + 1) * 32, s1);
+        for (int p = 0; p < 4; ++p) {
+            uint32_t ra[16], rb[16];
+            tmem_ld16x256_x4(tA + 32 * p, ra);
+            tmem_ld16x256_x4(tB + 32 * p, rb);
             tmem_ld_wait();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const uint32_t(&d)[32] = hf ? s1 : s0;
-                const int c0 = (pp + hf) * 32;
+            for (int b = 0; b < 4; ++b) {
+                const int c = 32 * p + 8 * b + cq;
+                // sv[e][i]: channel c + e of column jc(i)
+                const float sv[2][4] = {{__uint_as_float(ra[4 * b]), __uint_as_float(ra[4 * b + 2]),
+                                         __uint_as_float(rb[4 * b]), __uint_as_float(rb[4 * b + 2])},
+                                        {__uint_as_float(ra[4 * b + 1]), __uint_as_float(ra[4 * b + 3]),
+                                         __uint_as_float(rb[4 * b + 1]), __uint_as_float(rb[4 * b + 3])}};
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const int c = c0 + 4 * e4;
+                for (int w = 0; w < 2 * kG; ++w) {  // vector w: KA then QA rows of the buffer
+                    const float2 cf = *reinterpret_cast<const float2*>(buf + w * 128 + c);
 #pragma unroll
-                    for (int t = 0; t < kG; ++t) {
-                        const float4 a = *reinterpret_cast<const float4*>(buf + (KA + t) * 128 + c);
-                        const float4 b = *reinterpret_cast<const float4*>(buf + (QA + t) * 128 + c);
-                        x[t] = fmaf(a.x, __uint_as_float(d[4 * e4]), x[t]);
-                        y[t] = fmaf(b.x, __uint_as_float(d[4 * e4]), y[t]);
-                        x[t] = fmaf(a.y, __uint_as_float(d[4 * e4 + 1]), x[t]);
-                        y[t] = fmaf(b.y, __uint_as_float(d[4 * e4 + 1]), y[t]);
-                        x[t] = fmaf(a.z, __uint_as_float(d[4 * e4 + 2]), x[t]);
-                        y[t] = fmaf(b.z, __uint_as_float(d[4 * e4 + 2]), y[t]);
-                        x[t] = fmaf(a.w, __uint_as_float(d[4 * e4 + 3]), x[t]);
-                        y[t] = fmaf(b.w, __uint_as_float(d[4 * e4 + 3]), y[t]);
-                    }
+                    for (int i = 0; i < 4; ++i) acc[w][i] = fmaf(cf.y, sv[1][i], fmaf(cf.x, sv[0][i], acc[w][i]));
                 }
             }
         }
+#pragma unroll
+        for (int w = 0; w < 2 * kG; ++w)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[w][i] += __shfl_xor_sync(0xffffffffu, acc[w][i], 1);
+                acc[w][i] += __shfl_xor_sync(0xffffffffu, acc[w][i], 2);
+            }
         if (r0 + kG < valid) load(r0 + kG);  // the next group's inputs in flight during the write pass
-        // the tokens in order: u_t, o_t (scalar i: the four warps' partials, summed in a fixed order)
-        auto sc = [&](int i) -> float {
+        // the tokens in order: u_t, o_t for the four columns (scalar i: the four warps' partials,
+        // summed in a fixed order); the thread with lane % 4 = i stores column jc(i)
+        float sc[kSerM + kSerN];
+#pragma unroll
+        for (int i = 0; i < kSerM + kSerN; ++i) {
             const float* pt = buf + PART + i;
-            return (pt[0] + pt[kSerM + kSerN]) + (pt[2 * (kSerM + kSerN)] + pt[3 * (kSerM + kSerN)]);
-        };
-        float u[kG];
+            sc[i] = (pt[0] + pt[kSerM + kSerN]) + (pt[2 * (kSerM + kSerN)] + pt[3 * (kSerM + kSerN)]);
+        }
+        float u[kG][4];
 #pragma unroll
         for (int t = 0; t < kG; ++t) {
-            float z = x[t];
+            float o[4];
 #pragma unroll
-            for (int s = 0; s < t; ++s) z = fmaf(sc(t * (t - 1) / 2 + s), u[s], z);
-            u[t] = bt[t] * (vt[t] - z);
-            float o = y[t];
+            for (int i = 0; i < 4; ++i) {
+                float z = acc[t][i];
 #pragma unroll
-            for (int s = 0; s <= t; ++s) o = fmaf(sc(kSerM + t * (t + 1) / 2 + s), u[s], o);
+                for (int s = 0; s < t; ++s) z = fmaf(sc[t * (t - 1) / 2 + s], u[s][i], z);
+                u[t][i] = bt[t] * (buf[(VV + t) * 128 + j0 + 8 * i] - z);
+                o[i] = acc[kG + t][i];
+#pragma unroll
+                for (int s = 0; s <= t; ++s) o[i] = fmaf(sc[kSerM + t * (t + 1) / 2 + s], u[s][i], o[i]);
+            }
             if (r0 + t < valid) {
-                const size_t off = ((size_t)(row0 + r0 + t) * H + h) * kD + j;
+                const int sel = lane & 3;
+                const float os = sel == 0 ? o[0] : sel == 1 ? o[1] : sel == 2 ? o[2] : o[3];
+                const size_t off = ((size_t)(row0 + r0 + t) * H + h) * kD + j0 + 8 * sel;
                 if constexpr (sizeof(Tout) == 2)
-                    out[off] = __float2bfloat16_rn(o);
+                    out[off] = __float2bfloat16_rn(os);
                 else
-                    out[off] = o;
+                    out[off] = os;
             }
         }
         // write pass: S <- A_{kG-1} . S + sum_s (k_s B_{s,kG-1}) u_s
 #pragma unroll 1
-        for (int pp = 0; pp < 4; pp += 2) {
-            tmem_ld32(taddr + pp * 32, s0);
-            tmem_ld32(taddr + (pp + 1) * 32, s1);
+        for (int p = 0; p < 4; ++p) {
+            uint32_t ra[16], rb[16];
+            tmem_ld16x256_x4(tA + 32 * p, ra);
+            tmem_ld16x256_x4(tB + 32 * p, rb);
             tmem_ld_wait();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t(&d)[32] = hf ? s1 : s0;
-                const int c0 = (pp + hf) * 32;
+            for (int b = 0; b < 4; ++b) {
+                const int c = 32 * p + 8 * b + cq;
+                const float2 a = *reinterpret_cast<const float2*>(buf + AL * 128 + c);
+                float2 kb[kG];
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const int c = c0 + 4 * e4;
-                    const float4 a = *reinterpret_cast<const float4*>(buf + AL * 128 + c);
-                    float sn[4] = {a.x * __uint_as_float(d[4 * e4]), a.y * __uint_as_float(d[4 * e4 + 1]),
-                                   a.z * __uint_as_float(d[4 * e4 + 2]), a.w * __uint_as_float(d[4 * e4 + 3])};
+                for (int s2 = 0; s2 < kG; ++s2) kb[s2] = *reinterpret_cast<const float2*>(buf + (KB + s2) * 128 + c);
 #pragma unroll
-                    for (int t = 0; t < kG; ++t) {
-                        const float4 kb = *reinterpret_cast<const float4*>(buf + (KB + t) * 128 + c);
-                        sn[0] = fmaf(kb.x, u[t], sn[0]);
-                        sn[1] = fmaf(kb.y, u[t], sn[1]);
-                        sn[2] = fmaf(kb.z, u[t], sn[2]);
-                        sn[3] = fmaf(kb.w, u[t], sn[3]);
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t* r = i < 2 ? ra : rb;
+                    const int o0 = 4 * b + 2 * (i & 1);  // channel c of column jc(i); c + 1 follows
+                    float s0 = a.x * __uint_as_float(r[o0]), s1 = a.y * __uint_as_float(r[o0 + 1]);
+#pragma unroll
+                    for (int s2 = 0; s2 < kG; ++s2) {
+                        s0 = fmaf(kb[s2].x, u[s2][i], s0);
+                        s1 = fmaf(kb[s2].y, u[s2][i], s1);
                     }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) d[4 * e4 + e] = __float_as_uint(sn[e]);
+                    r[o0] = __float_as_uint(s0);
+                    r[o0 + 1] = __float_as_uint(s1);
                 }
             }
-            tmem_st32(taddr + pp * 32, s0);
-            tmem_st32(taddr + (pp + 1) * 32, s1);
+            tmem_st16x256_x4(tA + 32 * p, ra);
+            tmem_st16x256_x4(tB + 32 * p, rb);
         }
         tmem_st_wait();  // the next group reads these columns back
     }
