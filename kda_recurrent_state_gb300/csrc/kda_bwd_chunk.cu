@@ -714,15 +714,25 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     const float* dSC = W.dS + ch * REC_DD;
     if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
     load_tile<C>(s2, W.Up + ch * REC_CD);  // U, stored by the states pass
-    {  // final-decay gradient: sum_j S_C[c][j] dS_C[c][j], one warp per row
+    {  // final-decay gradient: sum_j S_C[c][j] dS_C[c][j], one warp per row, every load of the
+       // warp's 8 rows issued before the first is used
         const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-        for (int r = w; r < kD; r += 16) {
+        float sv[8][4], dv[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sv[i][j] = SC[(w + 16 * i) * kD + l + 32 * j];
+                dv[i][j] = dSC[(w + 16 * i) * kD + l + 32 * j];
+            }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
             float a = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) a = fmaf(SC[r * kD + l + 32 * j], dSC[r * kD + l + 32 * j], a);
+            for (int j = 0; j < 4; ++j) a = fmaf(sv[i][j], dv[i][j], a);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (l == 0) W.sc[ch * 3 * kD + 2 * kD + r] = a;
+            if (l == 0) W.sc[ch * 3 * kD + 2 * kD + w + 16 * i] = a;
         }
     }
     __syncthreads();
