@@ -251,6 +251,146 @@ __device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
 }
 __device__ __forceinline__ float4 scale4(float4 v, float s) { return make_float4(v.x * s, v.y * s, v.z * s, v.w * s); }
 
+// ---- operands stored pre-split: a tile held as two bf16 arrays hi and lo (x ~ hi + lo, split as
+// by split_bf16) with row stride RS elements, so that the fragments of every product are read with
+// ldmatrix and no warp splits an element again.  RS = width + 8: the 8 rows of an ldmatrix read
+// start 16 bytes apart modulo 128, so a read is free of bank conflicts.
+constexpr int RSD = kD + 8;  // rows of D elements
+constexpr int RSC = C + 8;   // rows of C elements
+struct Split {
+    __nv_bfloat16* hi;
+    __nv_bfloat16* lo;
+};
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a) : "memory");
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a) : "memory");
+}
+// Four consecutive elements of a row into the split tile (8-byte stores of hi and of lo).
+__device__ __forceinline__ void split_store4(const Split& t, int off, float4 v) {
+    uint2 h, l;
+    split_bf16(v.x, v.y, h.x, l.x);
+    split_bf16(v.z, v.w, h.y, l.y);
+    *reinterpret_cast<uint2*>(t.hi + off) = h;
+    *reinterpret_cast<uint2*>(t.lo + off) = l;
+}
+// Dense [ROWS][D] record in global memory -> split tile, optionally scaled per row.  Every thread
+// issues all of its 16-byte loads before it stores any.
+template <int ROWS>
+__device__ __forceinline__ void load_tile_split(const Split& dst, const float* src, const float* row_scale = nullptr) {
+    constexpr int PER = ROWS * (kD / 4) / NT;
+    float4 x[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = reinterpret_cast<const float4*>(src)[threadIdx.x + i * NT];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int g = threadIdx.x + i * NT, r = g >> 5, c4 = (g & 31) * 4;
+        split_store4(dst, r * RSD + c4, row_scale ? scale4(x[i], row_scale[r]) : x[i]);
+    }
+}
+__device__ __forceinline__ void load_cc_split(const Split& dst, const float* src) {
+    constexpr int PER = C * C / 4 / NT;
+    float4 x[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = reinterpret_cast<const float4*>(src)[threadIdx.x + i * NT];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int g = threadIdx.x + i * NT;
+        split_store4(dst, (g >> 4) * RSC + (g & 15) * 4, x[i]);
+    }
+}
+// A fragment into a split tile: adjacent column pairs (col(2i), col(2i+1)) as bf16x2 stores.
+template <int M, int N>
+__device__ __forceinline__ void to_smem_split(const Frag<M, N>& f, const Split& t, int rs) {
+#pragma unroll
+    for (int i = 0; i < Frag<M, N>::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < Frag<M, N>::NJ; j += 2) {
+            uint32_t h, l;
+            split_bf16(f.v[i][j], f.v[i][j + 1], h, l);
+            const int off = Frag<M, N>::row(i) * rs + Frag<M, N>::col(j);
+            *reinterpret_cast<uint32_t*>(t.hi + off) = h;
+            *reinterpret_cast<uint32_t*>(t.lo + off) = l;
+        }
+}
+// f (+/-)= A B on pre-split operands, the same three products per tile and in the same order as
+// gemm() (so the same result bit for bit).  A_KC: A stored [m][k] (else [k][m]); B_KC: B stored
+// [n][k] (else [k][n]); ras, rbs: the tiles' row strides in elements.
+template <bool NEG, int K, bool A_KC, bool B_KC, int M, int N>
+__device__ __forceinline__ void gemm_ps(Frag<M, N>& f, const Split& A, int ras, const Split& B, int rbs) {
+    using F = Frag<M, N>;
+    constexpr int MT = F::MT, NTL = F::NTL;
+    static_assert(K % 16 == 0 && NTL % 2 == 0, "layout");
+    const int lane = threadIdx.x & 31;
+    const int mb = (int)((threadIdx.x >> 5) & 3) * MT * 16, nb = (int)(threadIdx.x >> 7) * NTL * 8;
+    const int l7 = lane & 7, l8 = (lane >> 3) & 1, l16 = lane >> 4;
+    // this lane's row address within an ldmatrix x4 read (see the fragment orders of mma m16n8k16)
+    const uint32_t ah = smem_addr(A.hi), al = smem_addr(A.lo), bh = smem_addr(B.hi), bl = smem_addr(B.lo);
+    auto a_off = [&](int m0, int k0) -> uint32_t {  // matrices (m 0-7|8-15) x (k 0-7|8-15), k-minor first
+        return A_KC ? (uint32_t)(((m0 + l7 + 8 * l8) * ras + k0 + 8 * l16) * 2)
+                    : (uint32_t)(((k0 + l7 + 8 * l16) * ras + m0 + 8 * l8) * 2);
+    };
+    auto b_off = [&](int n0, int k0) -> uint32_t {  // matrices (k 0-7, n0), (k 8-15, n0), (k 0-7, n0+8), (k 8-15, n0+8)
+        return B_KC ? (uint32_t)(((n0 + l7 + 8 * l16) * rbs + k0 + 8 * l8) * 2)
+                    : (uint32_t)(((k0 + l7 + 8 * l8) * rbs + n0 + 8 * l16) * 2);
+    };
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        uint32_t fa[MT][4], fl[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t o = a_off(mb + 16 * mt, k0);
+            if (A_KC) {
+                ldsm4(fa[mt], ah + o);
+                ldsm4(fl[mt], al + o);
+            } else {
+                ldsm4t(fa[mt], ah + o);
+                ldsm4t(fl[mt], al + o);
+            }
+            if (NEG) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    fa[mt][q] ^= 0x80008000u;
+                    fl[mt][q] ^= 0x80008000u;
+                }
+            }
+        }
+#pragma unroll
+        for (int np = 0; np < NTL / 2; ++np) {
+            uint32_t gh[4], gl[4];  // n-tiles 2 np and 2 np + 1
+            const uint32_t o = b_off(nb + 16 * np, k0);
+            if (B_KC) {
+                ldsm4(gh, bh + o);
+                ldsm4(gl, bl + o);
+            } else {
+                ldsm4t(gh, bh + o);
+                ldsm4t(gl, bl + o);
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int nt = 2 * np + h2;
+                const uint32_t bhi[2] = {gh[2 * h2], gh[2 * h2 + 1]}, blo[2] = {gl[2 * h2], gl[2 * h2 + 1]};
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    float d[4] = {f.v[2 * mt][2 * nt], f.v[2 * mt][2 * nt + 1], f.v[2 * mt + 1][2 * nt],
+                                  f.v[2 * mt + 1][2 * nt + 1]};
+                    mma_bf16(d, fa[mt], bhi);
+                    mma_bf16(d, fa[mt], blo);
+                    mma_bf16(d, fl[mt], bhi);
+                    f.v[2 * mt][2 * nt] = d[0];
+                    f.v[2 * mt][2 * nt + 1] = d[1];
+                    f.v[2 * mt + 1][2 * nt] = d[2];
+                    f.v[2 * mt + 1][2 * nt + 1] = d[3];
+                }
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void seq_of(const BwdProblem& P, int s, int64_t& start, int64_t& len) {
     if (P.cu_seqlens) {
         start = P.cu_seqlens[s];
@@ -695,13 +835,21 @@ constexpr int SMEM_GRAD_A = (TILE_DD + 4 * TILE_CD + TILE_CC + 2 * kD) * 4;
 
 __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     extern __shared__ __align__(16) float sm[];
-    float* sR = sm;              // dD, then X
-    float* s1 = sR + TILE_DD;    // K^
-    float* s2 = s1 + TILE_CD;    // U
-    float* s3 = s2 + TILE_CD;    // dU
-    float* s4 = s3 + TILE_CD;    // dO
-    float* s5 = s4 + TILE_CD;    // P, then dP
-    float* sE = s5 + TILE_CC;
+    // Every tile of this pass is only ever a product operand, so each is stored pre-split.
+    uint8_t* base = reinterpret_cast<uint8_t*>(sm);
+    auto split_at = [&](size_t off, int rows, int rs) {
+        __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(base + off);
+        return Split{b, b + (size_t)rows * rs};
+    };
+    constexpr size_t BD = 4ull * kD * RSD, BC = 4ull * C * RSD, BCC = 4ull * C * RSC;  // bytes: hi and lo
+    static_assert(BD + 4 * BC + BCC + 8 * kD == SMEM_GRAD_A, "split tiles take the fp32 tiles' room");
+    const Split sR = split_at(0, kD, RSD);               // dD, then X
+    const Split s1 = split_at(BD, C, RSD);               // K^
+    const Split s2 = split_at(BD + BC, C, RSD);          // U
+    const Split s3 = split_at(BD + 2 * BC, C, RSD);      // dU
+    const Split s4 = split_at(BD + 3 * BC, C, RSD);      // dO
+    const Split s5 = split_at(BD + 4 * BC, C, RSC);      // P, then dP
+    float* sE = reinterpret_cast<float*>(base + BD + 4 * BC + BCC);
     const BwdProblem& P = W.p;
     const int h = blockIdx.x % P.H;
     const int64_t cg = blockIdx.x / P.H;
@@ -713,7 +861,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     const float* SC = W.S + s_slot + (size_t)P.H * REC_DD;  // the next state of the same sequence
     const float* dSC = W.dS + ch * REC_DD;
     if (threadIdx.x < 2 * kD) sE[threadIdx.x] = W.sc[ch * 3 * kD + threadIdx.x];
-    load_tile<C>(s2, W.Up + ch * REC_CD);  // U, stored by the states pass
+    load_tile_split<C>(s2, W.Up + ch * REC_CD);  // U, stored by the states pass
     {  // final-decay gradient: sum_j S_C[c][j] dS_C[c][j], one warp per row, every load of the
        // warp's 8 rows issued before the first is used
         const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -736,49 +884,47 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
         }
     }
     __syncthreads();
-    load_tile<kD>(sR, dSC, sE + kD);  // dD
-    load_tile<C>(s1, W.Kh + ch * REC_CD);
+    load_tile_split<kD>(sR, dSC, sE + kD);  // dD
+    load_tile_split<C>(s1, W.Kh + ch * REC_CD);
     {
         float4 o4[4];
         load_rows(o4, P.dout, c, P.H, h);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int gi = threadIdx.x + i * NT;
-            *reinterpret_cast<float4*>(s4 + (gi >> 5) * LD + (gi & 31) * 4) = o4[i];
+            split_store4(s4, (gi >> 5) * RSD + (gi & 31) * 4, o4[i]);
         }
     }
-    load_cc(s5, W.Pq + ch * REC_CC);
+    load_cc_split(s5, W.Pq + ch * REC_CC);
     __syncthreads();
     Frag<C, kD> du, acc;
     du.zero();
-    gemm<false, kD, LD, 1, LD, 1>(du, s1, sR);  // K^ dD
-    gemm<false, C, 1, LC, LD, 1>(du, s5, s4);   // + P^T dO
-    to_smem(du, s3, LD);
+    gemm_ps<false, kD, true, false>(du, s1, RSD, sR, RSD);  // K^ dD
+    gemm_ps<false, C, false, false>(du, s5, RSC, s4, RSD);  // + P^T dO
+    to_smem_split(du, s3, RSD);
     to_global(du, W.Up + ch * REC_CD);
     acc.zero();
-    gemm<false, kD, LD, 1, 1, LD>(acc, s2, sR);  // dK^ = U dD^T
+    gemm_ps<false, kD, true, true>(acc, s2, RSD, sR, RSD);  // dK^ = U dD^T
     to_global(acc, W.Ej + ch * REC_DD + REC_CD);
     Frag<C, C> dp;
     dp.zero();
-    gemm<false, kD, LD, 1, 1, LD>(dp, s4, s2);  // dP = lower(dO U^T)
-    __syncthreads();
-    load_tile<kD>(sR, S0, sE);  // X again
+    gemm_ps<false, kD, true, true>(dp, s4, RSD, s2, RSD);  // dP = lower(dO U^T)
 #pragma unroll
     for (int i = 0; i < Frag<C, C>::MR; ++i)
 #pragma unroll
-        for (int j = 0; j < Frag<C, C>::NJ; ++j) {
-            const int r = Frag<C, C>::row(i), cc = Frag<C, C>::col(j);
-            const float x = cc <= r ? dp.v[i][j] : 0.f;
-            s5[r * LC + cc] = x;
-            W.Pq[ch * REC_CC + r * C + cc] = x;
-        }
+        for (int j = 0; j < Frag<C, C>::NJ; ++j)
+            if (Frag<C, C>::col(j) > Frag<C, C>::row(i)) dp.v[i][j] = 0.f;
+    __syncthreads();
+    load_tile_split<kD>(sR, S0, sE);  // X again
+    to_smem_split(dp, s5, RSC);
+    to_global(dp, W.Pq + ch * REC_CC);
     __syncthreads();
     acc.zero();
-    gemm<false, kD, LD, 1, 1, LD>(acc, s4, sR);  // dQ~ = dO X^T
-    gemm<false, C, LC, 1, LD, 1>(acc, s5, s1);   //      + dP K^
+    gemm_ps<false, kD, true, true>(acc, s4, RSD, sR, RSD);  // dQ~ = dO X^T
+    gemm_ps<false, C, true, false>(acc, s5, RSC, s1, RSD);  //      + dP K^
     to_global(acc, W.Ej + ch * REC_DD);
     acc.zero();
-    gemm<true, kD, LD, 1, 1, LD>(acc, s3, sR);  // dW~ = -dU X^T
+    gemm_ps<true, kD, true, true>(acc, s3, RSD, sR, RSD);  // dW~ = -dU X^T
     to_global(acc, W.Wt + ch * REC_CD);
 }
 
