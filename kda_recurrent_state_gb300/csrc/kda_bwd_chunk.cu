@@ -24,6 +24,8 @@
 // range: a (sequence, head) with a chunk whose half-chunk log-decay sum is below -80 is flagged,
 // and after these passes the token-serial backward (which has no such limit) recomputes exactly
 // those units.
+#include <type_traits>
+
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -317,39 +319,56 @@ __device__ __forceinline__ void to_smem_split(const Frag<M, N>& f, const Split& 
             *reinterpret_cast<uint32_t*>(t.lo + off) = l;
         }
 }
-// f (+/-)= A B on pre-split operands, the same three products per tile and in the same order as
-// gemm() (so the same result bit for bit).  A_KC: A stored [m][k] (else [k][m]); B_KC: B stored
-// [n][k] (else [k][n]); ras, rbs: the tiles' row strides in elements.
-template <bool NEG, int K, bool A_KC, bool B_KC, int M, int N>
-__device__ __forceinline__ void gemm_ps(Frag<M, N>& f, const Split& A, int ras, const Split& B, int rbs) {
+// Product operands: a tile stored pre-split (Split) or in fp32 (split as its fragments are loaded),
+// each with its row stride in elements.
+struct OpS {
+    Split t;
+    int rs;
+};
+struct OpF {
+    const float* p;
+    int rs;
+};
+// f (+/-)= A B with each operand pre-split or fp32, the same three products per tile in the same
+// order as gemm() (so the same result bit for bit).  A_KC: A stored [m][k] (else [k][m]); B_KC:
+// B stored [n][k] (else [k][n]).
+template <bool NEG, int K, bool A_KC, bool B_KC, int M, int N, class AO, class BO>
+__device__ __forceinline__ void gemm_mx(Frag<M, N>& f, const AO& A, const BO& B) {
     using F = Frag<M, N>;
     constexpr int MT = F::MT, NTL = F::NTL;
+    constexpr bool AS = std::is_same<AO, OpS>::value, BS = std::is_same<BO, OpS>::value;
     static_assert(K % 16 == 0 && NTL % 2 == 0, "layout");
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int mb = (int)((threadIdx.x >> 5) & 3) * MT * 16, nb = (int)(threadIdx.x >> 7) * NTL * 8;
     const int l7 = lane & 7, l8 = (lane >> 3) & 1, l16 = lane >> 4;
-    // this lane's row address within an ldmatrix x4 read (see the fragment orders of mma m16n8k16)
-    const uint32_t ah = smem_addr(A.hi), al = smem_addr(A.lo), bh = smem_addr(B.hi), bl = smem_addr(B.lo);
-    auto a_off = [&](int m0, int k0) -> uint32_t {  // matrices (m 0-7|8-15) x (k 0-7|8-15), k-minor first
-        return A_KC ? (uint32_t)(((m0 + l7 + 8 * l8) * ras + k0 + 8 * l16) * 2)
-                    : (uint32_t)(((k0 + l7 + 8 * l16) * ras + m0 + 8 * l8) * 2);
-    };
-    auto b_off = [&](int n0, int k0) -> uint32_t {  // matrices (k 0-7, n0), (k 8-15, n0), (k 0-7, n0+8), (k 8-15, n0+8)
-        return B_KC ? (uint32_t)(((n0 + l7 + 8 * l16) * rbs + k0 + 8 * l8) * 2)
-                    : (uint32_t)(((k0 + l7 + 8 * l8) * rbs + n0 + 8 * l16) * 2);
-    };
 #pragma unroll 2
     for (int k0 = 0; k0 < K; k0 += 16) {
         uint32_t fa[MT][4], fl[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t o = a_off(mb + 16 * mt, k0);
-            if (A_KC) {
-                ldsm4(fa[mt], ah + o);
-                ldsm4(fl[mt], al + o);
+            const int m0 = mb + 16 * mt;
+            if constexpr (AS) {  // matrices (m 0-7|8-15) x (k 0-7|8-15), m-minor first
+                const int ras = A.rs;
+                const uint32_t o = A_KC ? (uint32_t)(((m0 + l7 + 8 * l8) * ras + k0 + 8 * l16) * 2)
+                                        : (uint32_t)(((k0 + l7 + 8 * l16) * ras + m0 + 8 * l8) * 2);
+                if (A_KC) {
+                    ldsm4(fa[mt], smem_addr(A.t.hi) + o);
+                    ldsm4(fl[mt], smem_addr(A.t.lo) + o);
+                } else {
+                    ldsm4t(fa[mt], smem_addr(A.t.hi) + o);
+                    ldsm4t(fl[mt], smem_addr(A.t.lo) + o);
+                }
             } else {
-                ldsm4t(fa[mt], ah + o);
-                ldsm4t(fl[mt], al + o);
+                auto ldA = [&](int m, int k) -> float2 {
+                    if constexpr (A_KC) return *reinterpret_cast<const float2*>(A.p + m * A.rs + k);
+                    else return make_float2(A.p[m + k * A.rs], A.p[m + (k + 1) * A.rs]);
+                };
+                const int r0 = m0 + g, ka = k0 + 2 * t;
+                const float2 x0 = ldA(r0, ka), x1 = ldA(r0 + 8, ka), x2 = ldA(r0, ka + 8), x3 = ldA(r0 + 8, ka + 8);
+                split_bf16(x0.x, x0.y, fa[mt][0], fl[mt][0]);
+                split_bf16(x1.x, x1.y, fa[mt][1], fl[mt][1]);
+                split_bf16(x2.x, x2.y, fa[mt][2], fl[mt][2]);
+                split_bf16(x3.x, x3.y, fa[mt][3], fl[mt][3]);
             }
             if (NEG) {
 #pragma unroll
@@ -361,14 +380,30 @@ __device__ __forceinline__ void gemm_ps(Frag<M, N>& f, const Split& A, int ras, 
         }
 #pragma unroll
         for (int np = 0; np < NTL / 2; ++np) {
-            uint32_t gh[4], gl[4];  // n-tiles 2 np and 2 np + 1
-            const uint32_t o = b_off(nb + 16 * np, k0);
-            if (B_KC) {
-                ldsm4(gh, bh + o);
-                ldsm4(gl, bl + o);
+            uint32_t gh[4], gl[4];  // (b0, b1) of n-tiles 2 np and 2 np + 1
+            if constexpr (BS) {  // matrices (k 0-7, n0), (k 8-15, n0), (k 0-7, n0+8), (k 8-15, n0+8)
+                const int n0 = nb + 16 * np, rbs = B.rs;
+                const uint32_t o = B_KC ? (uint32_t)(((n0 + l7 + 8 * l16) * rbs + k0 + 8 * l8) * 2)
+                                        : (uint32_t)(((k0 + l7 + 8 * l8) * rbs + n0 + 8 * l16) * 2);
+                if (B_KC) {
+                    ldsm4(gh, smem_addr(B.t.hi) + o);
+                    ldsm4(gl, smem_addr(B.t.lo) + o);
+                } else {
+                    ldsm4t(gh, smem_addr(B.t.hi) + o);
+                    ldsm4t(gl, smem_addr(B.t.lo) + o);
+                }
             } else {
-                ldsm4t(gh, bh + o);
-                ldsm4t(gl, bl + o);
+                auto ldB = [&](int k, int n) -> float2 {
+                    if constexpr (B_KC) return *reinterpret_cast<const float2*>(B.p + k + n * B.rs);
+                    else return make_float2(B.p[k * B.rs + n], B.p[(k + 1) * B.rs + n]);
+                };
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int cn = nb + 8 * (2 * np + h2) + g, kk = k0 + 2 * t;
+                    const float2 y0 = ldB(kk, cn), y1 = ldB(kk + 8, cn);
+                    split_bf16(y0.x, y0.y, gh[2 * h2], gl[2 * h2]);
+                    split_bf16(y1.x, y1.y, gh[2 * h2 + 1], gl[2 * h2 + 1]);
+                }
             }
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -389,6 +424,10 @@ __device__ __forceinline__ void gemm_ps(Frag<M, N>& f, const Split& A, int ras, 
             }
         }
     }
+}
+template <bool NEG, int K, bool A_KC, bool B_KC, int M, int N>
+__device__ __forceinline__ void gemm_ps(Frag<M, N>& f, const Split& A, int ras, const Split& B, int rbs) {
+    gemm_mx<NEG, K, A_KC, B_KC>(f, OpS{A, ras}, OpS{B, rbs});
 }
 
 __device__ __forceinline__ void seq_of(const BwdProblem& P, int s, int64_t& start, int64_t& len) {
@@ -938,12 +977,20 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     float* sQ = s0 + TILE_CD;    // Q~
     float* sK = sQ + TILE_CD;    // K~
     float* sH = sK + TILE_CD;    // K^
-    float* sX = sH + TILE_CD;    // dU, then dW~, then g
-    float* sT = sX + TILE_CD;    // T
-    float* sP = sT + TILE_CC;    // dP, then Y = dT T^T
-    float* sM = sP + TILE_CC;    // dT, then dA, then diag(beta) dA
+    float* sX = sH + TILE_CD;    // dU, then dW~ (pre-split), then g
+    float* sT = sX + TILE_CD;    // T (pre-split)
+    float* sP = sT + TILE_CC;    // dP, then Y = dT T^T (pre-split)
+    float* sM = sP + TILE_CC;    // dT, then dA, then diag(beta) dA (pre-split)
     float* sB = sM + TILE_CC;    // beta
     float* sG = sB + C;          // final-decay gradient
+    // tiles that are only product operands are stored pre-split in the fp32 tiles' room
+    auto split_of = [](float* t, int rows, int rs) {
+        __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(t);
+        return Split{b, b + (size_t)rows * rs};
+    };
+    static_assert(TILE_CD == C * RSD && TILE_CC == C * RSC, "a split tile (2 x 2 bytes per element) fills an fp32 tile");
+    const Split xX = split_of(sX, C, RSD), xT = split_of(sT, C, RSC), xP = split_of(sP, C, RSC),
+                xM = split_of(sM, C, RSC);
     const BwdProblem& P = W.p;
     const int h = blockIdx.x % P.H;
     const int64_t cg = blockIdx.x / P.H;
@@ -956,9 +1003,9 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     load_gates(W, c, h, s0, sB, sM);
     scaled_qk<Tin>(W, c, h, s0, sQ, sK, sH, nullptr);
     if (threadIdx.x < kD) sG[threadIdx.x] = W.sc[ch * 3 * kD + 2 * kD + threadIdx.x];
-    load_cc(sT, W.Tm + ch * REC_CC);
-    load_cc(sP, W.Pq + ch * REC_CC);
-    load_tile<C>(sX, W.Up + ch * REC_CD);  // dU
+    load_cc_split(xT, W.Tm + ch * REC_CC);
+    load_cc_split(xP, W.Pq + ch * REC_CC);
+    load_tile_split<C>(xX, W.Up + ch * REC_CD);  // dU
     __syncthreads();
     {
         float4 v4[4];
@@ -976,12 +1023,12 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     for (int i = 0; i < F::MR; ++i) db[i] = 0.f;
     F dKh, dKt, t;
     from_global(dKh, W.Ej + ch * REC_DD + REC_CD);
-    gemm<false, C, 1, LC, LD, 1>(dKh, sP, sQ);  // + dP^T Q~
+    gemm_mx<false, C, false, false>(dKh, OpS{xP, RSC}, OpF{sQ, LD});  // + dP^T Q~
     FC dT;
     dT.zero();
-    gemm<false, kD, LD, 1, 1, LD>(dT, sX, s0);  // dU V^T
+    gemm_mx<false, kD, true, true>(dT, OpS{xX, RSD}, OpF{s0, LD});  // dU V^T
     t.zero();
-    gemm<false, C, 1, LC, LD, 1>(t, sT, sX);  // T^T dU
+    gemm_ps<false, C, false, false>(t, xT, RSC, xX, RSD);  // T^T dU
 #pragma unroll
     for (int i = 0; i < F::MR; ++i) {
         const int r = F::row(i);
@@ -992,18 +1039,16 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
         }
     }
     __syncthreads();
-    load_tile<C>(sX, W.Wt + ch * REC_CD);  // dW~
+    load_tile_split<C>(xX, W.Wt + ch * REC_CD);  // dW~
     __syncthreads();
-    gemm<false, kD, LD, 1, 1, LD>(dT, sX, sK);  // + dW~ K~^T
+    gemm_mx<false, kD, true, true>(dT, OpS{xX, RSD}, OpF{sK, LD});  // + dW~ K~^T
 #pragma unroll
     for (int i = 0; i < FC::MR; ++i)
 #pragma unroll
-        for (int j = 0; j < FC::NJ; ++j) {
-            const int r = FC::row(i), cc = FC::col(j);
-            sM[r * LC + cc] = sB[cc] * dT.v[i][j];
-        }
+        for (int j = 0; j < FC::NJ; ++j) dT.v[i][j] *= sB[FC::col(j)];
+    to_smem_split(dT, xM, RSC);
     t.zero();
-    gemm<false, C, 1, LC, LD, 1>(t, sT, sX);  // T^T dW~
+    gemm_ps<false, C, false, false>(t, xT, RSC, xX, RSD);  // T^T dW~
 #pragma unroll
     for (int i = 0; i < F::MR; ++i) {
         const int r = F::row(i);
@@ -1017,25 +1062,22 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     {
         FC y;
         y.zero();
-        gemm<false, C, LC, 1, 1, LC>(y, sM, sT);  // Y = dT T^T
-        to_smem(y, sP, LC);
+        gemm_ps<false, C, true, true>(y, xM, RSC, xT, RSC);  // Y = dT T^T
+        to_smem_split(y, xP, RSC);
     }
     __syncthreads();
-    {
-        FC a;
-        a.zero();
-        gemm<true, C, 1, LC, LC, 1>(a, sT, sP);  // dA = -T^T Y, strictly lower part
+    FC a;  // dA = -T^T Y, strictly lower part
+    a.zero();
+    gemm_ps<true, C, false, false>(a, xT, RSC, xP, RSC);
 #pragma unroll
-        for (int i = 0; i < FC::MR; ++i)
+    for (int i = 0; i < FC::MR; ++i)
 #pragma unroll
-            for (int j = 0; j < FC::NJ; ++j) {
-                const int r = FC::row(i), cc = FC::col(j);
-                sM[r * LC + cc] = cc < r ? a.v[i][j] : 0.f;
-            }
-    }
+        for (int j = 0; j < FC::NJ; ++j)
+            if (FC::col(j) >= FC::row(i)) a.v[i][j] = 0.f;
+    to_smem_split(a, xM, RSC);
     __syncthreads();
     t.zero();
-    gemm<false, C, LC, 1, LD, 1>(t, sM, sH);  // dA K^
+    gemm_mx<false, C, true, false>(t, OpS{xM, RSC}, OpF{sH, LD});  // dA K^
 #pragma unroll
     for (int i = 0; i < F::MR; ++i) {
         const int r = F::row(i);
@@ -1046,9 +1088,13 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < C * C; idx += NT) sM[(idx >> 6) * LC + (idx & 63)] *= sB[idx >> 6];
+#pragma unroll
+    for (int i = 0; i < FC::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < FC::NJ; ++j) a.v[i][j] *= sB[FC::row(i)];  // diag(beta) dA
+    to_smem_split(a, xM, RSC);
     __syncthreads();
-    gemm<false, C, 1, LC, LD, 1>(dKh, sM, sK);  // + (diag(beta) dA)^T K~
+    gemm_mx<false, C, false, false>(dKh, OpS{xM, RSC}, OpF{sK, LD});  // + (diag(beta) dA)^T K~
 
     // beta gradient: a row's columns are spread over the 4 lanes of a quad (t) and the 4 warps w / 4;
     // sum over the quad, then over the warps in a fixed order (s0 rows 0..3 hold the partials)
