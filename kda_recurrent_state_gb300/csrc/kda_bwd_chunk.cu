@@ -538,8 +538,9 @@ __device__ __forceinline__ void load_gates(const CBwd& W, const ChunkAt& c, int 
     __syncthreads();
 }
 
-// Q~, K~, K^ of the chunk from q, k and the cumulative decay g (rows >= L: zero).
-template <typename Tin>
+// Q~, K~, K^ of the chunk from q, k and the cumulative decay g (rows >= L: zero).  SPLIT: Q~ and
+// K^ are stored pre-split (sQ and sH then hold Split tiles of row stride RSD).
+template <typename Tin, bool SPLIT = false>
 __device__ __forceinline__ void scaled_qk(const CBwd& W, const ChunkAt& c, int h, const float* g, float* sQ,
                                           float* sK, float* sH, float* Kh_out) {
     float4 q4[4], k4[4];
@@ -562,10 +563,17 @@ __device__ __forceinline__ void scaled_qk(const CBwd& W, const ChunkAt& c, int h
             ko[e] = ka[e] * ee;
             ho[e] = ka[e] * ff;
         }
-        *reinterpret_cast<float4*>(sQ + r * LD + c4) = make_float4(qo[0], qo[1], qo[2], qo[3]);
+        const float4 qv = make_float4(qo[0], qo[1], qo[2], qo[3]), hv = make_float4(ho[0], ho[1], ho[2], ho[3]);
         *reinterpret_cast<float4*>(sK + r * LD + c4) = make_float4(ko[0], ko[1], ko[2], ko[3]);
-        const float4 hv = make_float4(ho[0], ho[1], ho[2], ho[3]);
-        *reinterpret_cast<float4*>(sH + r * LD + c4) = hv;
+        if constexpr (SPLIT) {
+            __nv_bfloat16* q16 = reinterpret_cast<__nv_bfloat16*>(sQ);
+            __nv_bfloat16* h16 = reinterpret_cast<__nv_bfloat16*>(sH);
+            split_store4(Split{q16, q16 + C * RSD}, r * RSD + c4, qv);
+            split_store4(Split{h16, h16 + C * RSD}, r * RSD + c4, hv);
+        } else {
+            *reinterpret_cast<float4*>(sQ + r * LD + c4) = qv;
+            *reinterpret_cast<float4*>(sH + r * LD + c4) = hv;
+        }
         if (Kh_out) *reinterpret_cast<float4*>(Kh_out + r * kD + c4) = hv;
     }
     if (bad) W.redo[(size_t)c.s * W.p.H + h] = 1;
@@ -628,15 +636,21 @@ constexpr int SMEM_LOCAL = (5 * TILE_CD + 2 * TILE_CC + 3 * 256 + C) * 4;
 template <typename Tin>
 __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
     extern __shared__ __align__(16) float sm[];
-    float* sA = sm;              // g, then beta V, then W~
-    float* sQ = sA + TILE_CD;    // Q~
-    float* sK = sQ + TILE_CD;    // K~, then beta K~, then P^T dO
-    float* sH = sK + TILE_CD;    // K^
-    float* sO = sH + TILE_CD;    // dO
-    float* sP = sO + TILE_CD;    // P
+    float* sA = sm;              // g, then beta V, then W~ (both pre-split)
+    float* sQ = sA + TILE_CD;    // Q~ (pre-split)
+    float* sK = sQ + TILE_CD;    // K~, then beta K~, then P^T dO (pre-split)
+    float* sH = sK + TILE_CD;    // K^ (pre-split)
+    float* sO = sH + TILE_CD;    // dO (pre-split)
+    float* sP = sO + TILE_CD;    // P (pre-split)
     float* sT = sP + TILE_CC;    // strict_lower(beta K~ K^^T), then T
     float* sY = sT + TILE_CC;    // inverse scratch
     float* sB = sY + 3 * 256;    // beta
+    auto split_of = [](float* t, int rows, int rs) {
+        __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(t);
+        return Split{b, b + (size_t)rows * rs};
+    };
+    const Split xA = split_of(sA, C, RSD), xQ = split_of(sQ, C, RSD), xK = split_of(sK, C, RSD),
+                xH = split_of(sH, C, RSD), xO = split_of(sO, C, RSD), xP = split_of(sP, C, RSC);
     const BwdProblem& P = W.p;
     const int h = blockIdx.x % P.H;
     const int64_t cg = blockIdx.x / P.H;
@@ -645,7 +659,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
     const size_t ch = (size_t)cg * P.H + h;
 
     load_gates(W, c, h, sA, sB, sY);
-    scaled_qk<Tin>(W, c, h, sA, sQ, sK, sH, W.Kh + ch * REC_CD);
+    scaled_qk<Tin, true>(W, c, h, sA, sQ, sK, sH, W.Kh + ch * REC_CD);
     if (threadIdx.x < kD) {
         const float ref = sA[31 * LD + threadIdx.x];
         W.sc[ch * 3 * kD + threadIdx.x] = expf(ref);
@@ -659,26 +673,26 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int gi = threadIdx.x + i * NT, r = gi >> 5, c4 = (gi & 31) * 4;
-            *reinterpret_cast<float4*>(sA + r * LD + c4) = scale4(v4[i], sB[r]);
-            *reinterpret_cast<float4*>(sO + r * LD + c4) = o4[i];
+            split_store4(xA, r * RSD + c4, scale4(v4[i], sB[r]));
+            split_store4(xO, r * RSD + c4, o4[i]);
         }
     }
     {
         Frag<C, C> gk, pq;
         gk.zero();
         pq.zero();
-        gemm<false, kD, LD, 1, 1, LD>(gk, sK, sH);  // K~ K^^T
-        gemm<false, kD, LD, 1, 1, LD>(pq, sQ, sH);  // Q~ K^^T
+        gemm_mx<false, kD, true, true>(gk, OpF{sK, LD}, OpS{xH, RSD});  // K~ K^^T
+        gemm_ps<false, kD, true, true>(pq, xQ, RSD, xH, RSD);          // Q~ K^^T
 #pragma unroll
         for (int i = 0; i < Frag<C, C>::MR; ++i)
 #pragma unroll
             for (int j = 0; j < Frag<C, C>::NJ; ++j) {
                 const int r = Frag<C, C>::row(i), cc = Frag<C, C>::col(j);
                 sT[r * LC + cc] = cc < r ? sB[r] * gk.v[i][j] : 0.f;
-                const float pv = cc <= r ? pq.v[i][j] : 0.f;
-                sP[r * LC + cc] = pv;
-                W.Pq[ch * REC_CC + r * C + cc] = pv;
+                if (cc > r) pq.v[i][j] = 0.f;
             }
+        to_smem_split(pq, xP, RSC);
+        to_global(pq, W.Pq + ch * REC_CC);
     }
     __syncthreads();
     invert_unit_lower(sT, sY);
@@ -686,7 +700,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
     {
         Frag<C, kD> u;
         u.zero();
-        gemm<false, C, LC, 1, LD, 1>(u, sT, sA);  // U' = T (beta V)
+        gemm_mx<false, C, true, false>(u, OpF{sT, LC}, OpS{xA, RSD});  // U' = T (beta V)
         to_global(u, W.Up + ch * REC_CD);
     }
     for (int idx = threadIdx.x; idx < C * kD; idx += NT) sK[(idx >> 7) * LD + (idx & 127)] *= sB[idx >> 7];
@@ -695,22 +709,22 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
         Frag<C, kD> w;
         w.zero();
         gemm<false, C, LC, 1, LD, 1>(w, sT, sK);  // W~ = T (beta K~)
-        to_smem(w, sA, LD);
+        to_smem_split(w, xA, RSD);
         to_global(w, W.Wt + ch * REC_CD);
     }
     __syncthreads();
     {
         Frag<C, kD> pd;
         pd.zero();
-        gemm<false, C, 1, LC, LD, 1>(pd, sP, sO);  // P^T dO
-        to_smem(pd, sK, LD);
+        gemm_ps<false, C, false, false>(pd, xP, RSC, xO, RSD);  // P^T dO
+        to_smem_split(pd, xK, RSD);
     }
     __syncthreads();
     {
         Frag<kD, kD> e;
         e.zero();
-        gemm<false, C, 1, LD, LD, 1>(e, sQ, sO);  // Q~^T dO
-        gemm<true, C, 1, LD, LD, 1>(e, sA, sK);   // - W~^T (P^T dO)
+        gemm_ps<false, C, false, false>(e, xQ, RSD, xO, RSD);  // Q~^T dO
+        gemm_ps<true, C, false, false>(e, xA, RSD, xK, RSD);   // - W~^T (P^T dO)
         to_global(e, W.Ej + ch * REC_DD);
     }
 }
