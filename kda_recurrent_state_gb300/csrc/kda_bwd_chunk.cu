@@ -178,19 +178,27 @@ __device__ __forceinline__ void to_smem(const Frag<M, N>& f, float* dst, int ld)
         for (int j = 0; j < Frag<M, N>::NJ; ++j) dst[Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)] = f.v[i][j];
 }
 // Global copies of a fragment: row r of the block at dst + r * ld (a column slice when ld > N).
+// Columns col(2i) and col(2i + 1) are adjacent (and the first is even), so they move as one 8-byte
+// access (ld and the base offset are even).
 template <int M, int N>
 __device__ __forceinline__ void to_global(const Frag<M, N>& f, float* dst, int ld = N) {
 #pragma unroll
     for (int i = 0; i < Frag<M, N>::MR; ++i)
 #pragma unroll
-        for (int j = 0; j < Frag<M, N>::NJ; ++j) dst[(size_t)Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)] = f.v[i][j];
+        for (int j = 0; j < Frag<M, N>::NJ; j += 2)
+            *reinterpret_cast<float2*>(dst + (size_t)Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)) =
+                make_float2(f.v[i][j], f.v[i][j + 1]);
 }
 template <int M, int N>
 __device__ __forceinline__ void from_global(Frag<M, N>& f, const float* src, int ld = N) {
 #pragma unroll
     for (int i = 0; i < Frag<M, N>::MR; ++i)
 #pragma unroll
-        for (int j = 0; j < Frag<M, N>::NJ; ++j) f.v[i][j] = src[(size_t)Frag<M, N>::row(i) * ld + Frag<M, N>::col(j)];
+        for (int j = 0; j < Frag<M, N>::NJ; j += 2) {
+            const float2 x = *reinterpret_cast<const float2*>(src + (size_t)Frag<M, N>::row(i) * ld + Frag<M, N>::col(j));
+            f.v[i][j] = x.x;
+            f.v[i][j + 1] = x.y;
+        }
 }
 
 // Dense [ROWS][D] record in global memory -> shared tile with row stride LD, optionally scaled per
