@@ -272,12 +272,14 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
  * kda_bwd evaluated in chunks.  Same arguments, loss and results as kda_bwd, plus `chunk`:
  *   chunk = 64  the chunked reverse mode of the §六.2 WY form ("Kimi K3" article,
  *               lshu.cn/news/263999): the chunk-local products and all input gradients
- *               run chunk-parallel as fp32 GEMMs on shared-memory tiles; only the
+ *               run chunk-parallel as GEMMs on shared-memory tiles; only the
  *               chunk-to-chunk state and state-gradient recurrences (two dependent
  *               products per chunk) are serial per (sequence, head), split over value
  *               columns onto 2 or 4 CTAs when the units alone leave SMs idle (the
- *               results are the same bit for bit).  fp32 throughout;
- *               deterministic.  Each chunk factors its decays about its 32nd row, which
+ *               results are the same bit for bit).  Every product runs on the tensor
+ *               cores with each fp32 operand split into bf16 hi + lo (three products,
+ *               fp32 accumulation: about 16 significant bits per operand); every
+ *               element-wise step is fp32; deterministic.  Each chunk factors its decays about its 32nd row, which
  *               stays in fp32 range while every half-chunk's summed log-decay is >= -80;
  *               a (sequence, head) with a chunk beyond that is recomputed in the same
  *               call by the token-serial backward (chunk = 1), so every finite gate is

@@ -1051,13 +1051,26 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     gemm_mx<false, kD, true, true>(dT, OpS{xX, RSD}, OpF{s0, LD});  // dU V^T
     t.zero();
     gemm_ps<false, C, false, false>(t, xT, RSC, xX, RSD);  // T^T dU
+    // dv, dq, dk: adjacent column pairs as 8-byte stores where the arrays allow it
+    const bool pairs = ((reinterpret_cast<uintptr_t>(P.dv) | reinterpret_cast<uintptr_t>(P.dq) |
+                         reinterpret_cast<uintptr_t>(P.dk)) & 7u) == 0;
 #pragma unroll
     for (int i = 0; i < F::MR; ++i) {
         const int r = F::row(i);
 #pragma unroll
-        for (int j = 0; j < F::NJ; ++j) {
+        for (int j = 0; j < F::NJ; j += 2) {
             db[i] = fmaf(t.v[i][j], s0[r * LD + F::col(j)], db[i]);
-            if (r < c.L) P.dv[((size_t)(c.tok0 + r) * P.H + h) * kD + F::col(j)] = sB[r] * t.v[i][j];
+            db[i] = fmaf(t.v[i][j + 1], s0[r * LD + F::col(j + 1)], db[i]);
+            if (r < c.L) {
+                float* dst = P.dv + ((size_t)(c.tok0 + r) * P.H + h) * kD + F::col(j);
+                const float a0 = sB[r] * t.v[i][j], a1 = sB[r] * t.v[i][j + 1];
+                if (pairs) {
+                    *reinterpret_cast<float2*>(dst) = make_float2(a0, a1);
+                } else {
+                    dst[0] = a0;
+                    dst[1] = a1;
+                }
+            }
         }
     }
     __syncthreads();
@@ -1141,19 +1154,32 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_local(CBwd W) {
     for (int i = 0; i < F::MR; ++i) {
         const int r = F::row(i);
 #pragma unroll
-        for (int j = 0; j < F::NJ; ++j) {
-            const int col = F::col(j);
-            const int o = r * LD + col;
-            const float x = sX[o] - sX[31 * LD + col];
-            const float e = expf(x), f = expf(-x);
-            if (r < c.L) {
-                const size_t off = ((size_t)(c.tok0 + r) * P.H + h) * kD + col;
-                P.dq[off] = dQt.v[i][j] * e;
-                P.dk[off] = fmaf(dKt.v[i][j], e, dKh.v[i][j] * f);
+        for (int j = 0; j < F::NJ; j += 2) {
+            float gq[2], gk[2];
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int col = F::col(j + e2);
+                const int o = r * LD + col;
+                const float x = sX[o] - sX[31 * LD + col];
+                const float e = expf(x), f = expf(-x);
+                gq[e2] = dQt.v[i][j + e2] * e;
+                gk[e2] = fmaf(dKt.v[i][j + e2], e, dKh.v[i][j + e2] * f);
+                float dl = fmaf(dQt.v[i][j + e2], sQ[o], fmaf(dKt.v[i][j + e2], sK[o], -dKh.v[i][j + e2] * sH[o]));
+                if (r == C - 1) dl += sG[col];
+                s0[o] = dl;
             }
-            float dl = fmaf(dQt.v[i][j], sQ[o], fmaf(dKt.v[i][j], sK[o], -dKh.v[i][j] * sH[o]));
-            if (r == C - 1) dl += sG[col];
-            s0[o] = dl;
+            if (r < c.L) {
+                const size_t off = ((size_t)(c.tok0 + r) * P.H + h) * kD + F::col(j);
+                if (pairs) {
+                    *reinterpret_cast<float2*>(P.dq + off) = make_float2(gq[0], gq[1]);
+                    *reinterpret_cast<float2*>(P.dk + off) = make_float2(gk[0], gk[1]);
+                } else {
+                    P.dq[off] = gq[0];
+                    P.dq[off + 1] = gq[1];
+                    P.dk[off] = gk[0];
+                    P.dk[off + 1] = gk[1];
+                }
+            }
         }
     }
     __syncthreads();
