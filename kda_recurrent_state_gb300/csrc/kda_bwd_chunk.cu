@@ -220,17 +220,6 @@ __device__ __forceinline__ void load_tile(float* dst, const float* src, const fl
         *reinterpret_cast<float4*>(dst + r * LD + c4) = v;
     }
 }
-__device__ __forceinline__ void load_cc(float* dst, const float* src) {
-    constexpr int PER = C * C / 4 / NT;
-    float4 x[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) x[i] = reinterpret_cast<const float4*>(src)[threadIdx.x + i * NT];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int g = threadIdx.x + i * NT;
-        *reinterpret_cast<float4*>(dst + (g >> 4) * LC + (g & 15) * 4) = x[i];
-    }
-}
 
 // Asynchronous 16-byte global -> shared copies (cp.async), committed and awaited in groups.
 __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
@@ -240,14 +229,7 @@ __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-// A dense [C][D] record into a shared tile with row stride LD, and a vector of 2 D scales.
-__device__ __forceinline__ void tile_async(float* dst, const float* src) {
-#pragma unroll
-    for (int i = 0; i < C * kD / 4 / NT; ++i) {
-        const int g = threadIdx.x + i * NT;
-        cp_async16(dst + (g >> 5) * LD + (g & 31) * 4, src + g * 4);
-    }
-}
+// A vector of 2 D scales.
 __device__ __forceinline__ void scales_async(float* dst, const float* src) {
     if (threadIdx.x < 2 * kD / 4) cp_async16(dst + 4 * threadIdx.x, src + 4 * threadIdx.x);
 }
@@ -279,6 +261,13 @@ __device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t a) {
 __device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t a) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a) : "memory");
+}
+__device__ __forceinline__ void ldsm2(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(a) : "memory");
+}
+__device__ __forceinline__ void ldsm2t(uint32_t (&r)[4], uint32_t a) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(a)
+                 : "memory");
 }
 // Four consecutive elements of a row into the split tile (8-byte stores of hi and of lo).
 __device__ __forceinline__ void split_store4(const Split& t, int off, float4 v) {
@@ -313,6 +302,59 @@ __device__ __forceinline__ void load_cc_split(const Split& dst, const float* src
         split_store4(dst, (g >> 4) * RSC + (g & 15) * 4, x[i]);
     }
 }
+// Split records in the workspace: a [C][D] record held as its bf16 hi array followed by its lo
+// array (the bytes of one fp32 record).  Copied into a split tile of row stride RSD with cp.async.
+__device__ __forceinline__ Split record_split(float* rec) {
+    __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(rec);
+    return Split{b, b + C * kD};
+}
+__device__ __forceinline__ void cp_async16b(void* dst, const void* src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void tile_async_split(const Split& dst, const float* rec) {
+    const __nv_bfloat16* hi = reinterpret_cast<const __nv_bfloat16*>(rec);
+    const __nv_bfloat16* lo = hi + C * kD;
+#pragma unroll
+    for (int i = 0; i < C * kD / 8 / NT; ++i) {  // 16-byte pieces (8 elements) of each array
+        const int g = threadIdx.x + i * NT, r = g >> 4, c8 = (g & 15) * 8;
+        cp_async16b(dst.hi + r * RSD + c8, hi + g * 8);
+        cp_async16b(dst.lo + r * RSD + c8, lo + g * 8);
+    }
+}
+// A split record into a split tile with plain loads (all of a thread's loads issued first).
+__device__ __forceinline__ void load_record_split(const Split& dst, const float* rec) {
+    const uint4* hi = reinterpret_cast<const uint4*>(rec);
+    const uint4* lo = hi + C * kD / 8;
+    constexpr int PER = C * kD / 8 / NT;
+    uint4 xh[PER], xl[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        xh[i] = hi[threadIdx.x + i * NT];
+        xl[i] = lo[threadIdx.x + i * NT];
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int g = threadIdx.x + i * NT, r = g >> 4, c8 = (g & 15) * 8;
+        *reinterpret_cast<uint4*>(dst.hi + r * RSD + c8) = xh[i];
+        *reinterpret_cast<uint4*>(dst.lo + r * RSD + c8) = xl[i];
+    }
+}
+// A [C][D] fragment into a split record in global memory.
+template <int M, int N>
+__device__ __forceinline__ void to_global_split(const Frag<M, N>& f, float* rec) {
+    const Split t = record_split(rec);
+#pragma unroll
+    for (int i = 0; i < Frag<M, N>::MR; ++i)
+#pragma unroll
+        for (int j = 0; j < Frag<M, N>::NJ; j += 2) {
+            uint32_t h, l;
+            split_bf16(f.v[i][j], f.v[i][j + 1], h, l);
+            const int off = Frag<M, N>::row(i) * N + Frag<M, N>::col(j);
+            *reinterpret_cast<uint32_t*>(t.hi + off) = h;
+            *reinterpret_cast<uint32_t*>(t.lo + off) = l;
+        }
+}
 // A fragment into a split tile: adjacent column pairs (col(2i), col(2i+1)) as bf16x2 stores.
 template <int M, int N>
 __device__ __forceinline__ void to_smem_split(const Frag<M, N>& f, const Split& t, int rs) {
@@ -345,7 +387,8 @@ __device__ __forceinline__ void gemm_mx(Frag<M, N>& f, const AO& A, const BO& B)
     using F = Frag<M, N>;
     constexpr int MT = F::MT, NTL = F::NTL;
     constexpr bool AS = std::is_same<AO, OpS>::value, BS = std::is_same<BO, OpS>::value;
-    static_assert(K % 16 == 0 && NTL % 2 == 0, "layout");
+    static_assert(K % 16 == 0 && (NTL == 1 || NTL % 2 == 0), "layout");
+    constexpr int NP = NTL == 1 ? 1 : NTL / 2, NH = NTL == 1 ? 1 : 2;  // n-tile pairs, tiles per pair
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int mb = (int)((threadIdx.x >> 5) & 3) * MT * 16, nb = (int)(threadIdx.x >> 7) * NTL * 8;
     const int l7 = lane & 7, l8 = (lane >> 3) & 1, l16 = lane >> 4;
@@ -387,13 +430,21 @@ __device__ __forceinline__ void gemm_mx(Frag<M, N>& f, const AO& A, const BO& B)
             }
         }
 #pragma unroll
-        for (int np = 0; np < NTL / 2; ++np) {
+        for (int np = 0; np < NP; ++np) {
             uint32_t gh[4], gl[4];  // (b0, b1) of n-tiles 2 np and 2 np + 1
             if constexpr (BS) {  // matrices (k 0-7, n0), (k 8-15, n0), (k 0-7, n0+8), (k 8-15, n0+8)
                 const int n0 = nb + 16 * np, rbs = B.rs;
                 const uint32_t o = B_KC ? (uint32_t)(((n0 + l7 + 8 * l16) * rbs + k0 + 8 * l8) * 2)
                                         : (uint32_t)(((k0 + l7 + 8 * l8) * rbs + n0 + 8 * l16) * 2);
-                if (B_KC) {
+                if constexpr (NTL == 1) {  // one n-tile: the first two matrices (lanes 0-15 address them)
+                    if (B_KC) {
+                        ldsm2(gh, smem_addr(B.t.hi) + o);
+                        ldsm2(gl, smem_addr(B.t.lo) + o);
+                    } else {
+                        ldsm2t(gh, smem_addr(B.t.hi) + o);
+                        ldsm2t(gl, smem_addr(B.t.lo) + o);
+                    }
+                } else if (B_KC) {
                     ldsm4(gh, smem_addr(B.t.hi) + o);
                     ldsm4(gl, smem_addr(B.t.lo) + o);
                 } else {
@@ -406,7 +457,7 @@ __device__ __forceinline__ void gemm_mx(Frag<M, N>& f, const AO& A, const BO& B)
                     else return make_float2(B.p[k * B.rs + n], B.p[(k + 1) * B.rs + n]);
                 };
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
+                for (int h2 = 0; h2 < NH; ++h2) {
                     const int cn = nb + 8 * (2 * np + h2) + g, kk = k0 + 2 * t;
                     const float2 y0 = ldB(kk, cn), y1 = ldB(kk + 8, cn);
                     split_bf16(y0.x, y0.y, gh[2 * h2], gl[2 * h2]);
@@ -414,7 +465,7 @@ __device__ __forceinline__ void gemm_mx(Frag<M, N>& f, const AO& A, const BO& B)
                 }
             }
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+            for (int h2 = 0; h2 < NH; ++h2) {
                 const int nt = 2 * np + h2;
                 const uint32_t bhi[2] = {gh[2 * h2], gh[2 * h2 + 1]}, blo[2] = {gl[2 * h2], gl[2 * h2 + 1]};
 #pragma unroll
@@ -582,7 +633,7 @@ __device__ __forceinline__ void scaled_qk(const CBwd& W, const ChunkAt& c, int h
             *reinterpret_cast<float4*>(sQ + r * LD + c4) = qv;
             *reinterpret_cast<float4*>(sH + r * LD + c4) = hv;
         }
-        if (Kh_out) *reinterpret_cast<float4*>(Kh_out + r * kD + c4) = hv;
+        if (Kh_out) split_store4(record_split(Kh_out), r * kD + c4, hv);  // the K^ record, pre-split
     }
     if (bad) W.redo[(size_t)c.s * W.p.H + h] = 1;
 }
@@ -718,7 +769,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
         w.zero();
         gemm<false, C, LC, 1, LD, 1>(w, sT, sK);  // W~ = T (beta K~)
         to_smem_split(w, xA, RSD);
-        to_global(w, W.Wt + ch * REC_CD);
+        to_global_split(w, W.Wt + ch * REC_CD);  // the W~ record, pre-split
     }
     __syncthreads();
     {
@@ -742,9 +793,12 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
 // kD / NCOL CTAs, each carrying NCOL columns of the state (or its gradient); the launch splits
 // when the units alone would leave SMs idle.  Every output element sums over k in the same order
 // at every NCOL, so the split changes no bit of the result.
+// Every tile of these passes is a product operand only, stored pre-split: the state (or its
+// gradient) slice and U (or K^ dD) with row stride NCOL + 8, W~ and K^ copied from their split
+// records (row stride RSD).
 template <int NCOL>
 constexpr int smem_serial() {
-    return (kD * (NCOL + 4) + C * (NCOL + 4) + 2 * TILE_CD + 4 * kD) * 4;
+    return (kD * (NCOL + 8) + C * (NCOL + 8) + 2 * C * RSD) * 4 + 4 * kD * 4;
 }
 
 // Pass 2: chunk-start states.  W~ and the scales of chunk n+1 are copied in while K^^T U of
@@ -752,13 +806,14 @@ constexpr int smem_serial() {
 // scales are double-buffered).
 template <int NCOL>
 __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
-    constexpr int LS = NCOL + 4;  // row stride of the column-slice tiles
+    constexpr int RS = NCOL + 8;  // row stride of the column-slice tiles (elements)
     extern __shared__ __align__(16) float sm[];
-    float* sX = sm;              // X = Diag(e^ref) S, this CTA's columns
-    float* sU = sX + kD * LS;    // U, this CTA's columns
-    float* sW = sU + C * LS;     // W~
-    float* sH = sW + TILE_CD;    // K^
-    float* sE = sH + TILE_CD;    // [2][e^ref, e^{g_C - ref}]
+    __nv_bfloat16* b16 = reinterpret_cast<__nv_bfloat16*>(sm);
+    const Split xX{b16, b16 + kD * RS};                        // X = Diag(e^ref) S, this CTA's columns
+    const Split xU{xX.lo + kD * RS, xX.lo + kD * RS + C * RS};  // U, this CTA's columns
+    const Split xW{xU.lo + C * RS, xU.lo + C * RS + C * RSD};  // W~
+    const Split xH{xW.lo + C * RSD, xW.lo + 2 * C * RSD};      // K^
+    float* sE = reinterpret_cast<float*>(xH.lo + C * RSD);     // [2][e^ref, e^{g_C - ref}]
     const BwdProblem& P = W.p;
     constexpr int PARTS = kD / NCOL;
     const int unit = blockIdx.x / PARTS, c0 = (blockIdx.x % PARTS) * NCOL;
@@ -772,10 +827,10 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
     else S.zero();
     if (nc > 0) {
         const size_t ch0 = (size_t)base * P.H + h;
-        tile_async(sW, W.Wt + ch0 * REC_CD);
+        tile_async_split(xW, W.Wt + ch0 * REC_CD);
         scales_async(sE, W.sc + ch0 * 3 * kD);
         cp_commit();
-        tile_async(sH, W.Kh + ch0 * REC_CD);
+        tile_async_split(xH, W.Kh + ch0 * REC_CD);
         cp_commit();
     }
     for (int64_t n = 0; n <= nc; ++n) {
@@ -791,14 +846,14 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
             for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= e[F::row(i)];
-        to_smem(S, sX, LS);
+        to_smem_split(S, xX, RS);
         __syncthreads();
-        gemm<true, kD, LD, 1, LS, 1>(u, sW, sX);  // U = U' - W~ X
-        to_smem(u, sU, LS);
+        gemm_ps<true, kD, true, false>(u, xW, RSD, xX, RS);  // U = U' - W~ X
+        to_smem_split(u, xU, RS);
         to_global(u, W.Up + ch * REC_CD + c0, kD);  // U replaces U' (read back by the gradient pass)
         __syncthreads();
         if (n + 1 < nc) {
-            tile_async(sW, W.Wt + (ch + P.H) * REC_CD);
+            tile_async_split(xW, W.Wt + (ch + P.H) * REC_CD);
             scales_async(sE + ((n + 1) & 1) * 2 * kD, W.sc + (ch + P.H) * 3 * kD);
             cp_commit();
             cp_wait<1>();  // K^ of this chunk
@@ -806,14 +861,14 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
             cp_wait<0>();
         }
         __syncthreads();
-        gemm<false, C, 1, LD, LS, 1>(S, sH, sU);  // X + K^^T U
+        gemm_ps<false, C, false, false>(S, xH, RSD, xU, RS);  // X + K^^T U
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
             for (int j = 0; j < F::NJ; ++j) S.v[i][j] *= e[kD + F::row(i)];
         __syncthreads();
         if (n + 1 < nc) {
-            tile_async(sH, W.Kh + (ch + P.H) * REC_CD);
+            tile_async_split(xH, W.Kh + (ch + P.H) * REC_CD);
             cp_commit();
         }
     }
@@ -823,13 +878,14 @@ __global__ void __launch_bounds__(NT, 1) cbwd_states(CBwd W) {
 // copied in while W~^T Z of chunk n runs, and W~ of chunk n-1 while the next chunk's K^ dD runs.
 template <int NCOL>
 __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
-    constexpr int LS = NCOL + 4;
+    constexpr int RS = NCOL + 8;
     extern __shared__ __align__(16) float sm[];
-    float* sD = sm;              // dD = Diag(e^{g_C - ref}) dS, this CTA's columns
-    float* sZ = sD + kD * LS;    // K^ dD, this CTA's columns
-    float* sW = sZ + C * LS;     // W~
-    float* sH = sW + TILE_CD;    // K^
-    float* sE = sH + TILE_CD;    // [2][e^ref, e^{g_C - ref}]
+    __nv_bfloat16* b16 = reinterpret_cast<__nv_bfloat16*>(sm);
+    const Split xD{b16, b16 + kD * RS};                        // dD = Diag(e^{g_C - ref}) dS, this CTA's columns
+    const Split xZ{xD.lo + kD * RS, xD.lo + kD * RS + C * RS};  // K^ dD, this CTA's columns
+    const Split xW{xZ.lo + C * RS, xZ.lo + C * RS + C * RSD};  // W~
+    const Split xH{xW.lo + C * RSD, xW.lo + 2 * C * RSD};      // K^
+    float* sE = reinterpret_cast<float*>(xH.lo + C * RSD);     // [2][e^ref, e^{g_C - ref}]
     const BwdProblem& P = W.p;
     constexpr int PARTS = kD / NCOL;
     const int unit = blockIdx.x / PARTS, c0 = (blockIdx.x % PARTS) * NCOL;
@@ -843,10 +899,10 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
     else dS.zero();
     if (nc > 0) {
         const size_t chl = (size_t)(base + nc - 1) * P.H + h;
-        tile_async(sH, W.Kh + chl * REC_CD);
+        tile_async_split(xH, W.Kh + chl * REC_CD);
         scales_async(sE + ((nc - 1) & 1) * 2 * kD, W.sc + chl * 3 * kD);
         cp_commit();
-        tile_async(sW, W.Wt + chl * REC_CD);
+        tile_async_split(xW, W.Wt + chl * REC_CD);
         cp_commit();
     }
     for (int64_t n = nc - 1; n >= 0; --n) {
@@ -859,15 +915,15 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
         for (int i = 0; i < F::MR; ++i)
 #pragma unroll
             for (int j = 0; j < F::NJ; ++j) dS.v[i][j] *= e[kD + F::row(i)];
-        to_smem(dS, sD, LS);
+        to_smem_split(dS, xD, RS);
         __syncthreads();
         Frag<C, NCOL> z;
         z.zero();
-        gemm<false, kD, LD, 1, LS, 1>(z, sH, sD);  // K^ dD
-        to_smem(z, sZ, LS);
+        gemm_ps<false, kD, true, false>(z, xH, RSD, xD, RS);  // K^ dD
+        to_smem_split(z, xZ, RS);
         __syncthreads();
         if (n > 0) {
-            tile_async(sH, W.Kh + (ch - P.H) * REC_CD);
+            tile_async_split(xH, W.Kh + (ch - P.H) * REC_CD);
             scales_async(sE + ((n - 1) & 1) * 2 * kD, W.sc + (ch - P.H) * 3 * kD);
             cp_commit();
             cp_wait<1>();  // W~ of this chunk
@@ -875,7 +931,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
             cp_wait<0>();
         }
         __syncthreads();
-        gemm<true, C, 1, LD, LS, 1>(dS, sW, sZ);  // dD - W~^T (K^ dD)
+        gemm_ps<true, C, false, false>(dS, xW, RSD, xZ, RS);  // dD - W~^T (K^ dD)
         const float* E = W.Ej + ch * REC_DD + c0;
 #pragma unroll
         for (int i = 0; i < F::MR; ++i)
@@ -884,7 +940,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
                 dS.v[i][j] = (dS.v[i][j] + E[(size_t)F::row(i) * kD + F::col(j)]) * e[F::row(i)];
         __syncthreads();
         if (n > 0) {
-            tile_async(sW, W.Wt + (ch - P.H) * REC_CD);
+            tile_async_split(xW, W.Wt + (ch - P.H) * REC_CD);
             cp_commit();
         }
     }
@@ -946,7 +1002,7 @@ __global__ void __launch_bounds__(NT, 1) cbwd_grad_state(CBwd W) {
     }
     __syncthreads();
     load_tile_split<kD>(sR, dSC, sE + kD);  // dD
-    load_tile_split<C>(s1, W.Kh + ch * REC_CD);
+    load_record_split(s1, W.Kh + ch * REC_CD);
     {
         float4 o4[4];
         load_rows(o4, P.dout, c, P.H, h);
