@@ -1067,33 +1067,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // (the same two roundings as a run resumed from the returned state)
                     if (!(ok = mbar_wait(&bar[B_PREPD + ((n + 1) & 1)], ((n + 1) >> 1) & 1, ab, status))) break;
                     const float* an = ROB && bad_chunk(n + 1) ? ones : vec_a + ((n + 1) % 3) * 128;
-                    uint32_t da[32], db[32];
+                    // 16x256b accesses: per block of 8 key channels a thread holds channels cq, cq + 1
+                    // of four value columns (lanes lane/4 + {0, 8} of the warp's two 16-lane halves), so
+                    // each pair of factors it reads serves eight elements; the fp16 pairs go back with
+                    // the matching 16x128b stores (X16 column = channel / 2)
+                    const int cq = 2 * (lane & 3);
+                    const uint32_t tA = tmem + lane_base, tB = tA + (16u << 16);
 #pragma unroll 1
-                    for (int pp = 0; pp < 4; pp += 2) {
-                        tmem_ld32(tmem + lane_base + TM_S + pp * 32, da);
-                        tmem_ld32(tmem + lane_base + TM_S + (pp + 1) * 32, db);
+                    for (int p = 0; p < 4; ++p) {
+                        uint32_t ra[16], rb[16], xa[8], xb[8];
+                        tmem_ld16x256_x4(tA + TM_S + 32 * p, ra);
+                        tmem_ld16x256_x4(tB + TM_S + 32 * p, rb);
                         tmem_ld_wait();
-                        if (j == 0 && pp == 0) KDA_TR(n, 26);
+                        if (j == 0 && p == 0) KDA_TR(n, 26);
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t(&d)[32] = half ? db : da;
-                            const int piece = pp + half;
-                            uint32_t x16[16];
+                        for (int bk = 0; bk < 4; ++bk) {
+                            const int cc = 32 * p + 8 * bk + cq;
+                            const float2 b2 = *reinterpret_cast<const float2*>(bv + cc);
+                            const float2 a2 = *reinterpret_cast<const float2*>(an + cc);
 #pragma unroll
-                            for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 b4 = *reinterpret_cast<const float4*>(bv + piece * 32 + 4 * e4);
-                                const float4 a4 = *reinterpret_cast<const float4*>(an + piece * 32 + 4 * e4);
-                                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    d[4 * e4 + q] = __float_as_uint(__uint_as_float(d[4 * e4 + q]) * bb[q] * aa[q]);
+                            for (int e = 0; e < 4; ++e) {  // e & 1: channel cc + 1
+                                const float bb = (e & 1) ? b2.y : b2.x, aa = (e & 1) ? a2.y : a2.x;
+                                ra[4 * bk + e] = __float_as_uint(__uint_as_float(ra[4 * bk + e]) * bb * aa);
+                                rb[4 * bk + e] = __float_as_uint(__uint_as_float(rb[4 * bk + e]) * bb * aa);
                             }
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                x16[e] = pack_half2(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
-                            tmem_st32(tmem + lane_base + TM_S + piece * 32, d);
-                            tmem_st16(tmem + lane_base + TM_X16 + piece * 16, x16);
+                            for (int hh = 0; hh < 2; ++hh) {
+                                xa[2 * bk + hh] = pack_half2(__uint_as_float(ra[4 * bk + 2 * hh]),
+                                                             __uint_as_float(ra[4 * bk + 2 * hh + 1]));
+                                xb[2 * bk + hh] = pack_half2(__uint_as_float(rb[4 * bk + 2 * hh]),
+                                                             __uint_as_float(rb[4 * bk + 2 * hh + 1]));
+                            }
                         }
+                        tmem_st16x256_x4(tA + TM_S + 32 * p, ra);
+                        tmem_st16x256_x4(tB + TM_S + 32 * p, rb);
+                        tmem_st16x128_x4(tA + TM_X16 + 16 * p, xa);
+                        tmem_st16x128_x4(tB + TM_X16 + 16 * p, xb);
                     }
                     if (j == 0) KDA_TR(n, 27);
                     tmem_st_wait();
