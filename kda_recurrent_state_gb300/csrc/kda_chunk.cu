@@ -44,13 +44,14 @@
 //
 // Data layout on chip (one CTA = one (sequence, head), all of d_v = 128):
 //   TMEM (fp32 accumulators, lanes = the M rows):
-//     D_S [j][c] state (128 cols)   X16 [j][c] fp16 A operand   D_U [j][r] U'/U
-//     U16 [j][r] fp16 A operand (over D_U)   D_O [j][r] output   D_G [r|64+r][i] Gram
+//     D_S [j][c] state (128 cols)   D_O [j][r] output (right after D_S)   X16 [j][c] fp16 A operand
+//     D_U [j][r] U'/U   U16 [j][r] fp16 A operand (over D_U)   D_G [r|64+r][i] Gram
 //     D_W [c][r] W^T    V16 [2][j][i] fp16 A operand (v^T), by chunk parity
 //   SMEM (fp16 operand tiles, 128-byte swizzled rows of 64 elements):
 //     KT[c][r] = Ktil_p, QT[c][r] = Qtil_p (adjacent: together the M = 128 A
 //     operand of the Gram; once a chunk's products are done the pair stages
-//     its output for the TMA store), KH[c][r] = Khat_p, PP[r][i] = P,
+//     its output for the TMA store), KH[c][r] = Khat_p followed by PP[r][i] = P (one
+//     N = 192 operand),
 //     WT[c][r] = -W^T, NR[r][i] = T diag(beta); the 16x16 blocks of A (diagonal
 //     ones fp32, the rest fp16) and of Dg (fp16);
 //     a ring of 16-token input slots filled by TMA.
@@ -58,8 +59,8 @@
 //     Gram  D_G = [KT;QT] x KH                 M=128 N=64  K=128
 //     WY    D_W = KT x NR,  D_U = V16 x NR     M=128 N=64  K=64
 //     (i)   D_U += X16 x WT                    M=128 N=64  K=128
-//     (iii) D_O = X16 x QT, D_O += U16 x PP    M=128 N=64  K=128, 64
-//     (ii)  D_S += U16 x KH                    M=128 N=128 K=64
+//     (iii-a) D_O = X16 x QT                   M=128 N=64  K=128
+//     (ii) + (iii-b)  [D_S | D_O] += U16 x [KH | PP]   M=128 N=192 K=64 (one product)
 //
 // Warp roles (16 warps): 0 TMA producer, 1 beta loader (+ TMEM allocation),
 // 4-7 "prep" warpgroup (decay cumsum, operand tiles, issues the Gram), 8-11
@@ -93,10 +94,11 @@ constexpr float kMaxExp2 = 10.0f;
 constexpr int kRowH = 48;          // row stride (bytes) of a 16x16 fp16 block (ldmatrix: no bank conflicts)
 constexpr int kBlkH = 16 * kRowH;  // bytes per fp16 block
 
-// TMEM column map (512 columns allocated).  The fp16 U operand is written over
+// TMEM column map (512 columns allocated).  D_O follows D_S, so that the state update and
+// the intra-chunk output term are one N = 192 product.  The fp16 U operand is written over
 // the first 32 columns of the U accumulator once that has been read out; V16
 // (the fp16 v^T operand) is double-buffered by chunk parity.
-constexpr uint32_t TM_S = 0, TM_X16 = 128, TM_U = 192, TM_U16 = 192, TM_O = 256, TM_G = 320, TM_W = 384,
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_X16 = 192, TM_U = 256, TM_U16 = 256, TM_G = 320, TM_W = 384,
                    TM_V16 = 448;
 
 template <typename Tin>
@@ -109,7 +111,6 @@ struct Cfg {
 #define KDA_CFG_STG_OWN 1
 #endif
     static constexpr int NSLOT = ES == 2 ? KDA_CFG_NSLOT : 2;  // input ring slots (tiles are pulled into L2 ahead)
-    static constexpr int NPP = 1;                              // P buffers
     static constexpr bool STG_OWN = ES == 2 && KDA_CFG_STG_OWN;  // own staging buffer for the output (else KT/QT)
     static constexpr uint32_t SLOT_Q = 0;
     static constexpr uint32_t SLOT_K = QR * 128 * ES;
@@ -118,9 +119,9 @@ struct Cfg {
     static constexpr uint32_t SLOT_BYTES = 3 * QR * 128 * ES + QR * 128 * 4;
     // shared memory map (offsets from a 1024-byte aligned base)
     static constexpr uint32_t OFF_KQ = 0;                    // [2] x (KT 16K | QT 16K)
-    static constexpr uint32_t OFF_KH = 65536;                // [2] x 16K
-    static constexpr uint32_t OFF_PP = 98304;                // [NPP] x 8K
-    static constexpr uint32_t OFF_WT = OFF_PP + NPP * 8192;  // 16K
+    static constexpr uint32_t OFF_KH = 65536;                // [2] x (KH 16K | PP 8K)
+    static constexpr uint32_t KHP = 24576;                   // stride of the KH/PP pairs
+    static constexpr uint32_t OFF_WT = OFF_KH + 2 * KHP;     // 16K
     static constexpr uint32_t OFF_NR = OFF_WT + 16384;       // 8K
     static constexpr uint32_t OFF_INV = OFF_NR + 8192;  // A diagonal blocks (fp32), A below them and Dg (fp16)
     static constexpr uint32_t INV_BYTES = 4 * 1024 + 10 * kBlkH;
@@ -666,7 +667,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr uint32_t ID_G = idesc_f16(128, 64, 1, 1);
     constexpr uint32_t ID_MN = idesc_f16(128, 64, 0, 1);
     constexpr uint32_t ID_KK = idesc_f16(128, 64, 0, 0);
-    constexpr uint32_t ID_S = idesc_f16(128, 128, 0, 0);
+    constexpr uint32_t ID_SO = idesc_f16(128, 192, 0, 0);  // [D_S | D_O]: D_O follows D_S in TMEM
     // Every product group is issued by thread 0 of the role that completes its last
     // input, after waiting for that input and for the previous reader of its
     // accumulator; the commits below are what the other roles wait on.
@@ -762,7 +763,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int valid = (int)((len - (int64_t)C * n) < C ? (len - (int64_t)C * n) : C);
             uint8_t* kt = sm + L::OFF_KQ + b * 32768;
             uint8_t* qt = kt + 16384;
-            uint8_t* kh = sm + L::OFF_KH + b * 16384;
+            uint8_t* kh = sm + L::OFF_KH + b * L::KHP;
             // Quarters in the order 1, 0 (rows 31 down to 0), 2, 3 (rows 32 up to 63), one ring
             // slot each.  Relative to ref = g_31: rows r <= 31 use x_r = g_r - ref =
             // -(L_{r+1} + .. + L_31), accumulated downwards from row 31 (which also yields
@@ -871,7 +872,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (n > 0 && !mbar_wait(&bar[B_P2D], (n - 1) & 1, ab, status)) return false;
                 tc_fence_after();
                 const uint64_t da = mn_desc(sm_base + L::OFF_KQ + b * 32768, 16384);
-                const uint64_t db = mn_desc(sm_base + L::OFF_KH + b * 16384, 8192);
+                const uint64_t db = mn_desc(sm_base + L::OFF_KH + b * L::KHP, 8192);
 #pragma unroll
                 for (int st = 0; st < 8; ++st) mma_ss(tmem + TM_G, da + 128u * st, db + 128u * st, ID_G, st > 0);
                 mma_commit(&bar[B_GDONE]);
@@ -989,15 +990,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j == 0) {  // (ii) state update and (iii-b) the intra-chunk part of the output
                     if (!(ok = mbar_wait(&bar[B_URDY], n & 1, ab, status))) break;
                     tc_fence_after();
-                    const uint64_t dkh = k_desc(sm_base + L::OFF_KH + b * 16384);
-                    const uint64_t dpp = k_desc(sm_base + L::OFF_PP + (n % L::NPP) * 8192);
+                    // one product: [D_S | D_O] += U16 x [KH | PP] (N = 192; PP follows KH)
+                    const uint64_t dkp = k_desc(sm_base + L::OFF_KH + b * L::KHP);
                     if (!bad_chunk(n)) {
 #pragma unroll
                         for (int st = 0; st < 4; ++st)
-                            mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, dkh + 2u * st, ID_S, 1);
-#pragma unroll
-                        for (int st = 0; st < 4; ++st)
-                            mma_ts(tmem + TM_O, tmem + TM_U16 + st * 8, dpp + 2u * st, ID_KK, 1);
+                            mma_ts(tmem + TM_S, tmem + TM_U16 + st * 8, dkp + 2u * st, ID_SO, 1);
                     }
                     mma_commit(&bar[B_SDONE]);
                     mma_commit(&bar[B_KQFREE + b]);
@@ -1312,12 +1310,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mma_commit(&bar[B_V16FREE + b]);
                 KDA_TR(n, 8);
             }
-            if (c >= 64) {  // P of this chunk, once the D products of chunk n - NPP are done with PP
-                if (n >= L::NPP) {
-                    const int m = n - L::NPP;
+            if (c >= 64) {  // P of this chunk beside its KH, once the products of chunk n - 2 are done with the pair
+                if (n >= 2) {
+                    const int m = n - 2;
                     if (!mbar_wait(&bar[B_KQFREE + (m & 1)], (m >> 1) & 1, ab, status)) break;
                 }
-                store_row16_packed(sm + L::OFF_PP + (n % L::NPP) * 8192, c - 64, pr);
+                store_row16_packed(sm + L::OFF_KH + b * L::KHP + 16384, c - 64, pr);
             }
             // ---- P4: WT = -W^T (fp16), once the WY products are complete and (i) of
             // chunk n - 1 has consumed the previous WT
