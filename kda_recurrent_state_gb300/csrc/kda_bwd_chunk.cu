@@ -27,6 +27,7 @@
 #include <type_traits>
 
 #include "kda_internal.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
@@ -947,6 +948,280 @@ __global__ void __launch_bounds__(NT, 1) cbwd_dstates(CBwd W) {
     if (P.dinit) to_global(dS, P.dinit + ((size_t)s * P.H + h) * REC_DD + c0, kD);
 }
 
+// ---- passes 2 and 3 on the tcgen05 tensor cores -----------------------------------------------------
+// One CTA of 256 threads per (sequence, head) carries all 128 value columns of the chain.  The chain
+// matrix lives in TMEM in fp32 (lanes = value columns j, columns = key channels c), next to its bf16
+// hi/lo split, which is the A operand of the chunk's first product.  W~ and K^ (split records written
+// by the local pass) are copied with cp.async into 128-byte-swizzled tiles, rows t with the 128 key
+// channels in two 64-channel atoms; the same bytes are the K-major B operand of a product over c and
+// the MN-major B operand of a product over t.  Per chunk (TMEM holds the transposes):
+//   states  (REV = false): D_U = U'^T - X^T W~^T    (A: X split, negated; B: W~, over c); U stored
+//                          D_S = X^T + U^T K^       (A: U split;          B: K^, over t)
+//                          S_{n+1} = D_S e^{g_C - ref} stored; X_{n+1} = S_{n+1} e^{ref'} into D_S, split
+//   dstates (REV = true):  D_U = dD^T K^^T          (A: dD split;         B: K^, over c)
+//                          D_S = dD^T - Z^T W~      (A: Z split, negated; B: W~, over t)
+//                          dS_n = (D_S + E^T) e^{ref} stored; dD' = dS_n e^{g_C' - ref'} into D_S, split
+// Each product is three bf16 MMAs (hi.hi + hi.lo + lo.hi) accumulating in fp32, the operand split of
+// the warp-level passes.  Thread 0 issues the products; all threads do the element-wise work, warps
+// w and w + 4 sharing TMEM lanes 32 (w % 4) .. + 31 and splitting the columns in halves.  U' and E are
+// read straight from global memory, asked of L2 one chunk ahead.  Every wait is bounded.
+namespace tcs {
+constexpr int NTS = 256;
+constexpr uint32_t T_S = 0, T_XH = 128, T_XL = 192, T_U = 256, T_UH = 320, T_UL = 352;  // TMEM columns
+constexpr uint32_t HALF = 16384;               // one bf16 array of a split record as a swizzled tile
+constexpr uint32_t OFF_SC = 8 * HALF;          // [3][2][D] fp32: e^ref, e^{g_C - ref} by chunk % 3
+constexpr uint32_t OFF_BAR = OFF_SC + 3 * 2 * kD * 4;
+constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;  // + alignment slack
+constexpr uint32_t ID_C = sm100::idesc_bf16(128, 64, 0, 0);   // over c: M = 128, N = 64, B K-major
+constexpr uint32_t ID_T = sm100::idesc_bf16(128, 128, 0, 1);  // over t: M = 128, N = 128, B MN-major
+
+// Split record (hi [C][D] bf16, then lo) -> two swizzled tiles (hi, lo): element (t, c) of a tile at
+// atom c / 64, row t, 16-byte chunk ((c % 64) / 8) ^ (t % 8).
+__device__ __forceinline__ void stage_record(uint8_t* tiles, const float* rec) {
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(rec);
+#pragma unroll
+    for (int k = 0; k < 2 * C * 16 / NTS; ++k) {
+        const int i = threadIdx.x + k * NTS, p = i >> 10, t = (i >> 4) & 63, ck = i & 15;
+        cp_async16b(tiles + p * HALF + (ck >> 3) * 8192 + t * 128 + (((ck & 7) ^ (t & 7)) << 4),
+                    src + p * 16384 + t * 256 + ck * 16);
+    }
+}
+// L2 prefetch hint of every 128-byte line of `bytes` bytes
+__device__ __forceinline__ void l2_prefetch(const float* p, int bytes) {
+    for (int i = threadIdx.x * 128; i < bytes; i += NTS * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p) + i));
+}
+}  // namespace tcs
+
+template <bool REV>
+__global__ void __launch_bounds__(tcs::NTS, 1) cbwd_serial_tc(CBwd W) {
+    using namespace tcs;
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // [0] first product, [1] second, [2] CTA
+    sm100::Abort* ab = reinterpret_cast<sm100::Abort*>(sm + OFF_BAR + 24);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
+    float* ssc = reinterpret_cast<float*>(sm + OFF_SC);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int hf = warp >> 2;                    // column half of the element-wise work
+    const int j = 32 * (warp & 3) + (tid & 31);  // value column = TMEM lane
+    const BwdProblem& P = W.p;
+    const int h = blockIdx.x % P.H, s = blockIdx.x / P.H;
+    int64_t start, len;
+    seq_of(P, s, start, len);
+    const int nc = (int)((len + C - 1) / C);
+    const int64_t base = W.co[s];
+    const size_t unit_dd = ((size_t)s * P.H + h) * REC_DD;
+    auto chi = [&](int n) -> size_t { return (size_t)(base + n) * P.H + h; };
+    auto slot = [&](int n) -> float* { return W.S + ((size_t)(base + s + n) * P.H + h) * REC_DD; };
+    if (tid == 0) {
+        sm100::mbar_init(&bar[0], 1);
+        sm100::mbar_init(&bar[1], 1);
+        sm100::mbar_init(&bar[2], NTS);
+        ab->flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) sm100::tmem_alloc(holder, 512);
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::tc_fence_after();
+    const uint32_t tm = *holder, tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t sb = sm100::smem_u32(sm);
+    uint32_t ph_sync = 0;
+    auto cta_sync = [&]() -> bool {
+        sm100::tc_fence_before();
+        sm100::mbar_arrive(&bar[2]);
+        const bool r = sm100::mbar_wait(&bar[2], (ph_sync++) & 1, ab, W.status);
+        sm100::tc_fence_after();
+        return r;
+    };
+    // the records of chunk n into buffer b; the scales of chunk n into slot n % 3
+    auto stage = [&](int n, int b) {
+        const size_t ch = chi(n);
+        stage_record(sm + (4 * b + 0) * HALF, W.Wt + ch * REC_CD);
+        stage_record(sm + (4 * b + 2) * HALF, W.Kh + ch * REC_CD);
+    };
+    auto stage_sc = [&](int n) {
+        if (tid < 2 * kD / 4) cp_async16b(ssc + (n % 3) * 2 * kD + 4 * tid, W.sc + chi(n) * 3 * kD + 4 * tid);
+    };
+    // the cp.async data of every thread, visible to all threads and to the tensor cores
+    auto staged = [&]() -> bool {
+        cp_wait<0>();
+        sm100::fence_proxy_async_smem();
+        return cta_sync();
+    };
+    // this thread's 64 columns of D_S <- v, and its split beside it (negated for the states pass)
+    auto put_chain = [&](uint32_t (&v)[2][32]) {
+#pragma unroll
+        for (int pc = 0; pc < 2; ++pc) {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float x0 = __uint_as_float(v[pc][2 * e]), x1 = __uint_as_float(v[pc][2 * e + 1]);
+                split_bf16(REV ? x0 : -x0, REV ? x1 : -x1, hi[e], lo[e]);
+            }
+            sm100::tmem_st32(tl + T_S + 64 * hf + 32 * pc, v[pc]);
+            sm100::tmem_st16(tl + T_XH + 32 * hf + 16 * pc, hi);
+            sm100::tmem_st16(tl + T_XL + 32 * hf + 16 * pc, lo);
+        }
+        sm100::tmem_st_wait();
+    };
+    auto col = [&](int pc, int e) { return 64 * hf + 32 * pc + e; };  // key channel of v[pc][e]
+    const int n0 = REV ? nc - 1 : 0, dn = REV ? -1 : 1;  // first chunk of the chain, direction
+    uint32_t un[32];  // states: U' of the coming chunk (this thread's 32 tokens)
+    bool ok = true;
+    if (nc > 0) {
+        stage(n0, 0);
+        stage_sc(n0);
+        if (nc > 1) stage_sc(n0 + dn);
+        if (!REV)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) un[e] = __float_as_uint(W.Up[chi(n0) * REC_CD + (size_t)(32 * hf + e) * kD + j]);
+    }
+    cp_commit();
+    {  // the chain's start, S_0 (states) or the cotangent of the end state (dstates): stored, then scaled
+        const float* src = REV ? P.dfinal : P.init;
+        uint32_t v[2][32];
+#pragma unroll
+        for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[pc][e] = __float_as_uint(src ? src[unit_dd + (size_t)col(pc, e) * kD + j] : 0.f);
+        float* dst = !REV ? slot(0) : nc > 0 ? W.dS + chi(nc - 1) * REC_DD : P.dinit ? P.dinit + unit_dd : nullptr;
+        if (dst)
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) dst[(size_t)col(pc, e) * kD + j] = __uint_as_float(v[pc][e]);
+        if (nc > 0) {
+            ok = staged();
+            const float* sc = ssc + (n0 % 3) * 2 * kD + (REV ? kD : 0);  // e^{g_C - ref} or e^{ref} of chunk n0
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[pc][e] = __float_as_uint(__uint_as_float(v[pc][e]) * sc[col(pc, e)]);
+            put_chain(v);
+            if (ok) ok = cta_sync();
+        }
+    }
+    for (int k = 0; ok && k < nc; ++k) {
+        const int n = n0 + dn * k, b = k & 1;
+        const size_t ch = chi(n);
+        const bool more = k + 1 < nc;
+        if (more) {  // the next chunk's records, the scales of the one after it, U' / E of the next chunk to L2
+            stage(n + dn, b ^ 1);
+            if (k + 2 < nc) stage_sc(n + 2 * dn);
+            if (REV)
+                l2_prefetch(W.Ej + chi(n + dn) * REC_DD, REC_DD * 4);
+            else
+                l2_prefetch(W.Up + chi(n + dn) * REC_CD, REC_CD * 4);
+        }
+        cp_commit();
+        if (!REV) {  // D_U <- U'
+            sm100::tmem_st32(tl + T_U + 32 * hf, un);
+            sm100::tmem_st_wait();
+            if (!(ok = cta_sync())) break;
+        }
+        const uint32_t tw = sb + (4 * b + 0) * HALF, th = sb + (4 * b + 2) * HALF;  // W~, K^ (hi; lo at + HALF)
+        if (tid == 0) {  // first product, over the key channels
+            const uint32_t t1 = REV ? th : tw;
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+                const uint64_t bh = sm100::sdesc(t1 + (st >> 2) * 8192, 16, 1024) + 2u * (st & 3);
+                const uint64_t bl = sm100::sdesc(t1 + HALF + (st >> 2) * 8192, 16, 1024) + 2u * (st & 3);
+                sm100::mma_ts(tm + T_U, tm + T_XH + 8 * st, bh, ID_C, REV ? (st > 0) : 1);
+                sm100::mma_ts(tm + T_U, tm + T_XH + 8 * st, bl, ID_C, 1);
+                sm100::mma_ts(tm + T_U, tm + T_XL + 8 * st, bh, ID_C, 1);
+            }
+            sm100::mma_commit(&bar[0]);
+        }
+        if (!(ok = sm100::mbar_wait(&bar[0], k & 1, ab, W.status))) break;
+        sm100::tc_fence_after();
+        {  // U (stored; its split is the next A operand) or Z (its split negated)
+            uint32_t u[32], hi[16], lo[16];
+            sm100::tmem_ld32(tl + T_U + 32 * hf, u);
+            sm100::tmem_ld_wait();
+            if (!REV)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) W.Up[ch * REC_CD + (size_t)(32 * hf + e) * kD + j] = __uint_as_float(u[e]);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float x0 = __uint_as_float(u[2 * e]), x1 = __uint_as_float(u[2 * e + 1]);
+                split_bf16(REV ? -x0 : x0, REV ? -x1 : x1, hi[e], lo[e]);
+            }
+            sm100::tmem_st16(tl + T_UH + 16 * hf, hi);
+            sm100::tmem_st16(tl + T_UL + 16 * hf, lo);
+            sm100::tmem_st_wait();
+        }
+        if (!(ok = cta_sync())) break;
+        if (tid == 0) {  // second product, over the tokens
+            const uint32_t t2 = REV ? tw : th;
+#pragma unroll
+            for (int st = 0; st < 4; ++st) {
+                const uint64_t bh = sm100::sdesc(t2, 8192, 1024) + 128u * st;
+                const uint64_t bl = sm100::sdesc(t2 + HALF, 8192, 1024) + 128u * st;
+                sm100::mma_ts(tm + T_S, tm + T_UH + 8 * st, bh, ID_T, 1);
+                sm100::mma_ts(tm + T_S, tm + T_UH + 8 * st, bl, ID_T, 1);
+                sm100::mma_ts(tm + T_S, tm + T_UL + 8 * st, bh, ID_T, 1);
+            }
+            sm100::mma_commit(&bar[1]);
+        }
+        // loaded while the product runs: E^T of this chunk (dstates), U' of the next (states)
+        float ev[2][32];
+        if (REV) {
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ev[pc][e] = W.Ej[ch * REC_DD + (size_t)col(pc, e) * kD + j];
+        } else if (more) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) un[e] = __float_as_uint(W.Up[chi(n + 1) * REC_CD + (size_t)(32 * hf + e) * kD + j]);
+        }
+        if (!(ok = sm100::mbar_wait(&bar[1], k & 1, ab, W.status))) break;
+        sm100::tc_fence_after();
+        {
+            const float* e_ref = ssc + (n % 3) * 2 * kD;                               // e^{ref} of this chunk
+            const float* e_dec = e_ref + kD;                                           // e^{g_C - ref}
+            const float* nxt = ssc + ((n + dn + 3) % 3) * 2 * kD + (REV ? kD : 0);  // the next chunk's factor
+            uint32_t v[2][32];
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+                sm100::tmem_ld32(tl + T_S + 64 * hf + 32 * pc, v[pc]);
+                sm100::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float x = __uint_as_float(v[pc][e]);
+                    v[pc][e] = __float_as_uint(REV ? (x + ev[pc][e]) * e_ref[col(pc, e)] : x * e_dec[col(pc, e)]);
+                }
+            }
+            // S_{n+1} into its slot; dS_n into the record of chunk n - 1, or d_init after the first chunk
+            float* dst = !REV ? slot(n + 1) : more ? W.dS + chi(n - 1) * REC_DD : P.dinit ? P.dinit + unit_dd : nullptr;
+            if (dst)
+#pragma unroll
+                for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dst[(size_t)col(pc, e) * kD + j] = __uint_as_float(v[pc][e]);
+            if (more) {
+#pragma unroll
+                for (int pc = 0; pc < 2; ++pc)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[pc][e] = __float_as_uint(__uint_as_float(v[pc][e]) * nxt[col(pc, e)]);
+                put_chain(v);
+            }
+        }
+        if (!(ok = staged())) break;
+    }
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::tc_fence_after();
+    if (ab->flag) {  // aborted: let any product still in flight drain before TMEM goes away
+        const long long t0 = clock64();
+        while (clock64() - t0 < 2000000) {
+        }
+    }
+    if (warp == 0) sm100::tmem_dealloc(tm, 512);
+}
+
 // ---- pass 4a: the state-dependent gradient products of each chunk --------------------------------
 constexpr int SMEM_GRAD_A = (TILE_DD + 4 * TILE_CD + TILE_CC + 2 * kD) * 4;
 
@@ -1329,11 +1604,15 @@ cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace,
     const int64_t units = (int64_t)p.N * p.H;
     int parts = 1;
     while (parts < 4 && units * parts * 2 <= sms) parts *= 2;
-    const void* states = parts == 1 ? (const void*)cbwd_states<128> : parts == 2 ? (const void*)cbwd_states<64>
-                                                                                : (const void*)cbwd_states<32>;
-    const void* dstates = parts == 1 ? (const void*)cbwd_dstates<128> : parts == 2 ? (const void*)cbwd_dstates<64>
-                                                                                  : (const void*)cbwd_dstates<32>;
-    const int smem_ser = parts == 1 ? smem_serial<128>() : parts == 2 ? smem_serial<64>() : smem_serial<32>();
+    // One CTA per unit: the tcgen05 form of the serial passes (256 threads); with the columns split,
+    // the warp-level form.
+    const bool tc = parts == 1;
+    const void* states = tc ? (const void*)cbwd_serial_tc<false>
+                            : parts == 2 ? (const void*)cbwd_states<64> : (const void*)cbwd_states<32>;
+    const void* dstates = tc ? (const void*)cbwd_serial_tc<true>
+                             : parts == 2 ? (const void*)cbwd_dstates<64> : (const void*)cbwd_dstates<32>;
+    const int smem_ser = tc ? (int)tcs::SMEM : parts == 2 ? smem_serial<64>() : smem_serial<32>();
+    const int nt_ser = tc ? tcs::NTS : NT;
     const K ks[] = {{(const void*)local, SMEM_LOCAL},
                     {states, smem_ser},
                     {dstates, smem_ser},
@@ -1345,8 +1624,8 @@ cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace,
     const unsigned chunk_ctas = (unsigned)nch, seq_ctas = (unsigned)(units * parts);
     if (chunk_ctas > 0) local<<<chunk_ctas, NT, SMEM_LOCAL, st>>>(W);
     void* args[] = {&W};
-    if ((e = cudaLaunchKernel(states, dim3(seq_ctas), dim3(NT), args, (size_t)smem_ser, st)) != cudaSuccess) return e;
-    if ((e = cudaLaunchKernel(dstates, dim3(seq_ctas), dim3(NT), args, (size_t)smem_ser, st)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernel(states, dim3(seq_ctas), dim3(nt_ser), args, (size_t)smem_ser, st)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernel(dstates, dim3(seq_ctas), dim3(nt_ser), args, (size_t)smem_ser, st)) != cudaSuccess) return e;
     if (chunk_ctas > 0) {
         cbwd_grad_state<<<chunk_ctas, NT, SMEM_GRAD_A, st>>>(W);
         grad_local<<<chunk_ctas, NT, SMEM_GRAD_B, st>>>(W);

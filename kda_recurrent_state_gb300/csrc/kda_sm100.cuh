@@ -222,6 +222,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, i
     return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with bf16 A and B (A and B types 1), fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
+    return idesc_f16(M, N, a_mn_major, b_mn_major) | (1u << 7) | (1u << 10);
+}
 
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
