@@ -545,6 +545,23 @@ def profile_bwd():
     print("profile bwd done")
 
 
+def profile_bwd_serial():
+    """Backward workload for ncu captures of the tcgen05 serial passes: the chunked backward on
+    B=4, H=32, T=2048 (128 (sequence, head) units, one CTA each; 32 chunks), two calls."""
+    import torch
+
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    x = synth.prefill_inputs(4, 2048, 32, seed=synth.SEED_BASE + 6, device="cuda", init="normal")
+    do = torch.randn(4, 2048, 32, D, generator=torch.Generator(device="cuda").manual_seed(8), device="cuda")
+    for _ in range(2):
+        kda.kda_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], do, x["init_state"], chunk=CHUNK)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    print("profile bwd serial done")
+
+
 def profile_decode():
     """Small decode workload for ncu captures: 64 sessions x 96 heads (fp32 state 0.40 GB, bf16
     state 0.20 GB, both larger than L2), three steps of each kernel, the state updated in place."""
@@ -583,6 +600,9 @@ def main():
     ap.add_argument("--profile-bwd", action="store_true",
                     help="run two chunked backward calls on B=1,H=32,T=8192 and exit: the small case of the "
                          "committed backward ncu summary")
+    ap.add_argument("--profile-bwd-serial", action="store_true",
+                    help="run two chunked backward calls on B=4,H=32,T=2048 and exit: the case of the committed "
+                         "ncu summary of the tcgen05 serial passes")
     ap.add_argument("--profile-decode", action="store_true",
                     help="run three steps each of the fp32-state and bf16-state decode on 64 sessions x 96 heads "
                          "and exit: the small case of the committed decode ncu summary")
@@ -594,6 +614,8 @@ def main():
         profile_case()
     elif args.profile_bwd:
         profile_bwd()
+    elif args.profile_bwd_serial:
+        profile_bwd_serial()
     elif args.impl == "reference":
         run_reference(args)
     else:

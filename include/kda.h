@@ -274,12 +274,13 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
  *               lshu.cn/news/263999): the chunk-local products and all input gradients
  *               run chunk-parallel as GEMMs on shared-memory tiles; only the
  *               chunk-to-chunk state and state-gradient recurrences (two dependent
- *               products per chunk) are serial per (sequence, head), split over value
- *               columns onto 2 or 4 CTAs when the units alone leave SMs idle (the
- *               results are the same bit for bit).  Every product runs on the tensor
+ *               products per chunk) are serial per (sequence, head): one CTA per unit
+ *               with the products on tcgen05 and TMEM accumulators, or, when the units
+ *               fill at most a quarter of the SMs, warp-level products with each unit's
+ *               value columns split over 4 CTAs.  Every product runs on the tensor
  *               cores with each fp32 operand split into bf16 hi + lo (three products,
  *               fp32 accumulation: about 16 significant bits per operand); every
- *               element-wise step is fp32; deterministic.  Each chunk factors its decays about its 32nd row, which
+ *               element-wise step is fp32; deterministic for a given device and shape.  Each chunk factors its decays about its 32nd row, which
  *               stays in fp32 range while every half-chunk's summed log-decay is >= -80;
  *               a (sequence, head) with a chunk beyond that is recomputed in the same
  *               call by the token-serial backward (chunk = 1), so every finite gate is

@@ -1,4 +1,4 @@
-// kda_bwd_chunk.cu -- gradients of the KDA recurrence in chunked form (C = 64), fp32 on CUDA cores.
+// kda_bwd_chunk.cu -- gradients of the KDA recurrence in chunked form (C = 64).
 //
 // The forward is the "Kimi K3" article's (lshu.cn/news/263999) §四 update with the §二.1 read,
 // rewritten per chunk in the WY form of §六.2.  With the chunk's start state S_0, the in-chunk
@@ -12,14 +12,16 @@
 // output does not depend on ref, so its adjoint is zero and is not formed.  Four passes:
 //   local   (chunk-parallel)  g, Q~, K~, K^, T, W~, U', P, and the chunk's output-gradient term
 //                             E = Q~^T dO - W~^T (P^T dO) of the state gradient
-//   states  (serial per head, split over value columns when SMs are idle)
+//   states  (serial per head: tcgen05 products, or warp-level ones split over value columns when
+//            the heads leave most SMs idle)
 //                             S_{n+1} = Diag(e^{g_C-ref}) (X + K^^T (U' - W~ X)), every S_n and U kept
 //   dstates (the same)        dS_n = Diag(e^ref) (dD - W~^T (K^ dD) + E), dD = Diag(e^{g_C-ref}) dS_{n+1}
 //   grads   (chunk-parallel, two kernels) every input gradient of the chunk from S_n and dS_{n+1}
-// Every product is a small dense GEMM over shared-memory tiles (fp32), computed on the tensor
-// cores by warp-level bf16 MMAs with each operand split into bf16 hi + lo (three products per
-// tile, fp32 accumulation: about 2^-16 relative error per product, against the 2e-3 gradient
-// bar), instead of the token-serial path's per-token reduction latency.  Every element-wise
+// Every product is a small dense GEMM computed on the tensor cores with each operand split into
+// bf16 hi + lo (three products per tile, fp32 accumulation: about 2^-16 relative error per
+// product, against the 2e-3 gradient bar), instead of the token-serial path's per-token reduction
+// latency: warp-level MMAs over shared-memory tiles in the chunk-parallel passes, tcgen05 MMAs with
+// TMEM accumulators in the serial ones.  Every element-wise
 // step is fp32; sums are in a fixed order, so the result is bit-reproducible.  e^{g-ref} must stay in fp32
 // range: a (sequence, head) with a chunk whose half-chunk log-decay sum is below -80 is flagged,
 // and after these passes the token-serial backward (which has no such limit) recomputes exactly
@@ -789,11 +791,11 @@ __global__ void __launch_bounds__(NT, 1) cbwd_local(CBwd W) {
     }
 }
 
-// ---- passes 2 and 3: the serial recurrences ----------------------------------------------------
-// Value columns are independent in both recurrences, so a (sequence, head) unit may be split over
-// kD / NCOL CTAs, each carrying NCOL columns of the state (or its gradient); the launch splits
-// when the units alone would leave SMs idle.  Every output element sums over k in the same order
-// at every NCOL, so the split changes no bit of the result.
+// ---- passes 2 and 3: the serial recurrences, warp-level form ------------------------------------
+// Used when the (sequence, head) units would leave most SMs idle (otherwise the tcgen05 form below
+// runs).  Value columns are independent in both recurrences, so a unit is split over kD / NCOL
+// CTAs, each carrying NCOL columns of the state (or its gradient).  Every output element sums over
+// k in the same order at every NCOL, so the split changes no bit of the result.
 // Every tile of these passes is a product operand only, stored pre-split: the state (or its
 // gradient) slice and U (or K^ dD) with row stride NCOL + 8, W~ and K^ copied from their split
 // records (row stride RSD).
@@ -1595,23 +1597,19 @@ cudaError_t launch_chunk_bwd(const BwdProblem& p, int in_dtype, void* workspace,
         const void* fn;
         int smem;
     };
-    // Column split of the serial passes: while twice the units still fit on the SMs, halve the
-    // columns per CTA (128, 64 or 32).
+    // The serial passes: one CTA per (sequence, head) on tcgen05 (256 threads) while the units fill
+    // more than a quarter of the SMs; with fewer, the warp-level form with each unit's value columns
+    // split over 4 CTAs of 32 columns (measured faster there: 1.49 against 1.64 ms at B=1, H=8).
     int sms = 0, dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
     const int64_t units = (int64_t)p.N * p.H;
-    int parts = 1;
-    while (parts < 4 && units * parts * 2 <= sms) parts *= 2;
-    // One CTA per unit: the tcgen05 form of the serial passes (256 threads); with the columns split,
-    // the warp-level form.
-    const bool tc = parts == 1;
-    const void* states = tc ? (const void*)cbwd_serial_tc<false>
-                            : parts == 2 ? (const void*)cbwd_states<64> : (const void*)cbwd_states<32>;
-    const void* dstates = tc ? (const void*)cbwd_serial_tc<true>
-                             : parts == 2 ? (const void*)cbwd_dstates<64> : (const void*)cbwd_dstates<32>;
-    const int smem_ser = tc ? (int)tcs::SMEM : parts == 2 ? smem_serial<64>() : smem_serial<32>();
+    const bool tc = units * 4 > sms;
+    const int parts = tc ? 1 : 4;
+    const void* states = tc ? (const void*)cbwd_serial_tc<false> : (const void*)cbwd_states<32>;
+    const void* dstates = tc ? (const void*)cbwd_serial_tc<true> : (const void*)cbwd_dstates<32>;
+    const int smem_ser = tc ? (int)tcs::SMEM : smem_serial<32>();
     const int nt_ser = tc ? tcs::NTS : NT;
     const K ks[] = {{(const void*)local, SMEM_LOCAL},
                     {states, smem_ser},
