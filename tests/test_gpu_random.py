@@ -199,19 +199,25 @@ def test_random_decode():
         _check("state", np64(state[b, h].float())[None], rs, c, 1)
 
 
-def test_random_bwd_packed():
+@pytest.mark.parametrize("units", ["few", "many"])
+def test_random_bwd_packed(units):
     """The chunked backward on random packed batches (empty and one-token sequences, every gate
     layout, both input dtypes, with and without a final-state cotangent): a sampled (sequence,
     head) against the oracle, and empty sequences passing d_final through.  A gradient that is
     identically zero in the oracle (dlog alpha of a one-token sequence from a zero state: the
-    output does not depend on that gate) has no relative error, so there the absolute bar applies."""
+    output does not depend on that gate) has no relative error, so there the absolute bar applies.
+    "few": at most 18 (sequence, head) units, the serial passes' warp-level form with split value
+    columns; "many": 40 to 128 units, their tcgen05 form (one CTA per unit) on a 152-SM GPU."""
     import kda_recurrent_state_gb300 as kda
     from kda_recurrent_state_gb300 import synth
     from oracle import oracle
 
-    rng = random.Random("bwd-packed")
+    rng = random.Random("bwd-packed" if units == "few" else "bwd-packed-many")
     for _ in range(CASES):
-        N, H = rng.randrange(1, 7), rng.choice([1, 2, 3])
+        if units == "few":
+            N, H = rng.randrange(1, 7), rng.choice([1, 2, 3])
+        else:
+            N, H = rng.randrange(5, 9), rng.choice([8, 12, 16])
         lengths = [rng.choice([0, 1, 2, 63, 64, 65, 128, rng.randrange(0, 700)]) for _ in range(N)]
         dt, gl, gate = rng.choice([torch.bfloat16, torch.float32]), rng.choice(["config", "slow"]), rng.choice([0, 0, 1, 2])
         seed = rng.randrange(10**6)
