@@ -1254,10 +1254,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             if (!wg_sync()) break;  // A written
             if (c == 0) KDA_TR(n, 5);
-            if (c < 64) {
-                // ---- diagonal blocks: column jj of Dg_a = (I + A_aa)^-1 (thread c = 16 a + jj)
-                // by right-looking substitution
-                const int a = c >> 4, jj = c & 15;
+            if ((c & 31) < 16) {
+                // ---- diagonal blocks: column jj of Dg_a = (I + A_aa)^-1 (lane jj of warp 12 + a)
+                // by right-looking substitution, one block per warp so that the four run on
+                // four sub-partitions
+                const int a = c >> 5, jj = c & 15;
                 const float* blk = adiag + a * 256;
                 float x[16];
 #pragma unroll
