@@ -48,7 +48,7 @@ BWD_CHUNK_FLOP = (15 * 2 * CHUNK * CHUNK * D + 10 * 2 * CHUNK * D * D + 2 * 2 * 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_chunk_prefill_B1_H16_T32768.json")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_chunk_prefill_B1_H96_T131072.json")
 CHUNK_SRC = os.path.join(ROOT, "kda_recurrent_state_gb300", "csrc", "kda_chunk.cu")
 
 
@@ -528,6 +528,24 @@ def profile_case():
     print("profile case done")
 
 
+def profile_long():
+    """The bench's long-prefill workload (B=1, H=96, T=131072, fp32 out), two calls, for captures of
+    single-pass counters (DRAM bytes, duration) on one full-size launch."""
+    import torch
+
+    import kda_recurrent_state_gb300 as kda
+    from kda_recurrent_state_gb300 import synth
+
+    x = synth.prefill_inputs(B, T, H, seed=synth.SEED_BASE + 2, device="cuda")
+    out = torch.empty(B, T, H, D, dtype=torch.float32, device="cuda")
+    fin = torch.empty(B, H, D, D, dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, out, fin, chunk=CHUNK)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status() == 0
+    print("profile long done")
+
+
 def profile_bwd():
     """Small backward workload for ncu captures: the chunked backward on B=1, H=32, T=8192
     (4,096 chunk-heads, 1.4 GB of workspace), two calls."""
@@ -597,6 +615,9 @@ def main():
     ap.add_argument("--profile-case", action="store_true",
                     help="run two launches of the chunked prefill on B=1,H=16,T=32768 (fp32 out) and exit: the "
                          "small case the committed ncu summaries are captured on")
+    ap.add_argument("--profile-long", action="store_true",
+                    help="run two launches of the long prefill (B=1,H=96,T=131072, fp32 out) and exit: the case of "
+                         "the committed single-pass DRAM capture at full size")
     ap.add_argument("--profile-bwd", action="store_true",
                     help="run two chunked backward calls on B=1,H=32,T=8192 and exit: the small case of the "
                          "committed backward ncu summary")
@@ -612,6 +633,8 @@ def main():
         profile_decode()
     elif args.profile_case:
         profile_case()
+    elif args.profile_long:
+        profile_long()
     elif args.profile_bwd:
         profile_bwd()
     elif args.profile_bwd_serial:
