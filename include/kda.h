@@ -108,7 +108,9 @@ typedef enum { KDA_GATE_CHANNEL = 0, KDA_GATE_HEAD = 1, KDA_GATE_NONE = 2 } kda_
  *   workspace   device scratch of at least kda_workspace_size(KDA_OP_CHUNK, ...)
  *               bytes, 16-byte aligned (chunk = 64: one int per (sequence, head),
  *               rounded up to 256 bytes, marking the units the exact pass
- *               recomputes; chunk = 1: 0 bytes, may be NULL); contents need no
+ *               recomputes, then 256 bytes of counters with which the CTAs of a
+ *               launch with fewer (sequence, head) units than SMs claim their
+ *               units; chunk = 1: 0 bytes, may be NULL); contents need no
  *               initialisation and are not preserved.
  * B, T or H equal to 0 is valid (nothing to compute; with T = 0 the final
  * state is the initial state).  init_state may alias final_state.

@@ -84,6 +84,13 @@ constexpr int C = 64;   // chunk length
 constexpr int QR = 16;  // token rows per input slot
 constexpr int NTHREADS = 512;
 constexpr int kLptMax = 256;  // most packed sequences the kernel orders by length itself
+constexpr long long kClaimDelay = 4000;  // cycles a CTA on a higher-numbered SM waits before it claims a unit
+// Launches of at most this many (sequence, head) units place them on the lowest-numbered SMs.  The
+// scheduler starts a launch on SMs 148..151 and then pairs of SMs across the chip; for the 96 heads
+// of the long prefill that placement (SMs 0..91 and 148..151) ran 15% slower than SMs 0..95 (8.73
+// against 10.24 ms, bit-identical), while at 16 and 64 units the two were within 1% and at 128 units
+// the scheduler's placement was 12% faster, so the rule stops at 96.
+constexpr int kPackUnits = 96;
 constexpr float kLog2e = 1.4426950408889634f;
 // |g - ref| bound (log2 units) of the fp16 operand path.  An element scaled down by 2^-|g-ref|
 // can land in the fp16 subnormals, where its absolute rounding error is 2^-25, and the factor
@@ -567,7 +574,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #endif
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = blockIdx.x;
+    int unit = blockIdx.x;
+    if (pool.claim) {
+        // A launch of at most kPackUnits units, one CTA per SM: each CTA claims the next unit, and in
+        // the first pass CTAs on SMs with an ID of at least the unit count wait a moment first, so
+        // that the units land on the SMs with the lowest IDs.  Every CTA claims once, so every unit
+        // is taken whatever the placement.
+        __shared__ int claimed;
+        if (tid == 0) {
+            unsigned id;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+            if (!ROB && id >= (unsigned)(P.N * P.H)) {
+                const long long tw = clock64();
+                while (clock64() - tw < kClaimDelay) {
+                }
+            }
+            claimed = atomicAdd(pool.claim + (ROB ? 1 : 0), 1);
+        }
+        __syncthreads();
+        unit = claimed;
+        if (unit >= P.N * P.H) return;
+    }
     const int h = unit % P.H;
     // Packed sequences of different lengths: CTAs are handed out longest sequence first
     // (CTA u takes the sequence of length rank u / H), so that the longest chains start
@@ -1384,7 +1411,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, 
 }
 
 template <typename Tin, typename Tout, bool SG, bool PB>
-cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, int* redo, cudaStream_t st) {
+cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, int* redo, int* claim, cudaStream_t st) {
     CUtensorMap mq, mk, mv, ml, mo;
     const CUtensorMapDataType dt = sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const int64_t Tt = p.T_total > 0 ? p.T_total : 1;
@@ -1404,10 +1431,22 @@ cudaError_t launch_t(const SeqProblem& p, const PoolSlots& pool, int* redo, cuda
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(rob, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((int64_t)p.N * p.H);
-    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pool, redo);
+    const int64_t units = (int64_t)p.N * p.H;
+    unsigned grid = (unsigned)units;
+    PoolSlots pl = pool;
+    pl.claim = nullptr;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    if (units <= kPackUnits && units < sms) {  // one CTA per SM; units claimed by the lowest-numbered SMs
+        if ((e = cudaMemsetAsync(claim, 0, 2 * sizeof(int), st)) != cudaSuccess) return e;
+        grid = (unsigned)sms;
+        pl.claim = claim;
+    }
+    kern<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pl, redo);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    rob<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pool, redo);
+    rob<<<grid, NTHREADS, smem, st>>>(mq, mk, mv, ml, mo, p, pl, redo);
     return cudaGetLastError();
 }
 
@@ -1422,19 +1461,21 @@ extern "C" int kda_trace_read(unsigned int* host, int n) {
 
 // One int per (sequence, head): set by the first pass when the unit met a chunk beyond the
 // fp16 operand range, read by the exact pass.
+// [N * H] exact-pass flags, then (in the last 256 bytes) the two unit counters of a launch with
+// fewer units than SMs
 size_t chunk_prefill_workspace(int N, int H) {
     const size_t b = (size_t)N * H * sizeof(int);
-    return (b + 255) & ~(size_t)255;
+    return ((b + 255) & ~(size_t)255) + 256;
 }
 
 template <typename Tin, typename Tout>
-cudaError_t launch_gate(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int* redo,
+cudaError_t launch_gate(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int* redo, int* claim,
                         cudaStream_t st) {
     if (pool_bf16)
-        return gate != kGateChannel ? launch_t<Tin, Tout, true, true>(p, pool, redo, st)
-                                    : launch_t<Tin, Tout, false, true>(p, pool, redo, st);
-    return gate != kGateChannel ? launch_t<Tin, Tout, true, false>(p, pool, redo, st)
-                                : launch_t<Tin, Tout, false, false>(p, pool, redo, st);
+        return gate != kGateChannel ? launch_t<Tin, Tout, true, true>(p, pool, redo, claim, st)
+                                    : launch_t<Tin, Tout, false, true>(p, pool, redo, claim, st);
+    return gate != kGateChannel ? launch_t<Tin, Tout, true, false>(p, pool, redo, claim, st)
+                                : launch_t<Tin, Tout, false, false>(p, pool, redo, claim, st);
 }
 
 cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, bool pool_bf16, int gate, int in_dtype,
@@ -1442,11 +1483,12 @@ cudaError_t launch_chunk_prefill(const SeqProblem& p, const PoolSlots& pool, boo
     if ((int64_t)p.N * p.H == 0) return cudaSuccess;
     if (!workspace || ws_bytes < chunk_prefill_workspace(p.N, p.H)) return cudaErrorInvalidValue;
     int* redo = static_cast<int*>(workspace);
+    int* claim = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + chunk_prefill_workspace(p.N, p.H) - 256);
     if (in_dtype == KDA_BF16 && out_dtype == KDA_BF16)
-        return launch_gate<__nv_bfloat16, __nv_bfloat16>(p, pool, pool_bf16, gate, redo, st);
-    if (in_dtype == KDA_BF16) return launch_gate<__nv_bfloat16, float>(p, pool, pool_bf16, gate, redo, st);
-    if (out_dtype == KDA_BF16) return launch_gate<float, __nv_bfloat16>(p, pool, pool_bf16, gate, redo, st);
-    return launch_gate<float, float>(p, pool, pool_bf16, gate, redo, st);
+        return launch_gate<__nv_bfloat16, __nv_bfloat16>(p, pool, pool_bf16, gate, redo, claim, st);
+    if (in_dtype == KDA_BF16) return launch_gate<__nv_bfloat16, float>(p, pool, pool_bf16, gate, redo, claim, st);
+    if (out_dtype == KDA_BF16) return launch_gate<float, __nv_bfloat16>(p, pool, pool_bf16, gate, redo, claim, st);
+    return launch_gate<float, float>(p, pool, pool_bf16, gate, redo, claim, st);
 }
 
 }  // namespace kda

@@ -52,6 +52,7 @@ struct PoolSlots {
     const int64_t* init_slots;
     const int64_t* snap_slots;
     int64_t n_slots;
+    int* claim;  // chunk kernel only: [2] unit counters (first pass, exact pass), or null (unit = CTA index)
 };
 
 // Pool slot `i` checked against the pool: -1 (none) passes through, anything else outside

@@ -73,9 +73,9 @@ int main(void) {
     CHECK(cudaMemcpy(dv, v, tok * D * 4, cudaMemcpyHostToDevice) == cudaSuccess);
     CHECK(cudaMemcpy(dla, la, tok * D * 4, cudaMemcpyHostToDevice) == cudaSuccess);
     CHECK(cudaMemcpy(dbeta, beta, tok * 4, cudaMemcpyHostToDevice) == cudaSuccess);
-    /* one int per (sequence, head), rounded up to 256 bytes */
+    /* one int per (sequence, head), rounded up to 256 bytes, then 256 bytes of unit counters */
     const size_t cws_bytes = kda_workspace_size(KDA_OP_CHUNK, B, T, H, D, D, 64);
-    CHECK(cws_bytes == (((size_t)B * H * 4 + 255) / 256) * 256);
+    CHECK(cws_bytes == (((size_t)B * H * 4 + 255) / 256) * 256 + 256);
     void* cws;
     CHECK(cudaMalloc(&cws, cws_bytes) == cudaSuccess);
     CHECK(kda_chunk_fwd(dq, dk, dv, dla, dbeta, NULL, dout, dfin, B, T, H, D, D, 64, KDA_F32, KDA_F32, NULL, 0,

@@ -86,7 +86,7 @@ def test_argument_validation(L):
     assert _chunk(L, B=0) == b.KDA_OK  # nothing to do
     assert _chunk(L, H=0) == b.KDA_OK
     need = L.kda_workspace_size(0, 1, 8, 1, 128, 128, 64)
-    assert need == 256  # one int per (sequence, head), rounded up to 256 bytes
+    assert need == 512  # one int per (sequence, head), rounded up to 256 bytes, and 256 bytes of unit counters
     assert _chunk(L, ws=0x2000, ws_bytes=need - 1) == b.KDA_ERR_WORKSPACE
     assert _chunk(L, ws=0, ws_bytes=0) == b.KDA_ERR_WORKSPACE
     P = ctypes.c_void_p
@@ -244,8 +244,9 @@ def test_host_fwd_validation(L):
     P = ctypes.c_void_p
     need = L.kda_host_fwd_workspace_size(1, 2, 128, 128, 256, 0, 1)
     # two segments of staging (bf16 q, k, v; fp32 gates, beta, out), two fp32 states and the
-    # prefill's own workspace (one int per (sequence, head), rounded up to 256 bytes)
-    assert need == 2 * (256 * 2 * (3 * 256 + 512 + 4 + 512)) + 2 * 2 * 65536 + 256
+    # prefill's own workspace (one int per (sequence, head), rounded up to 256 bytes, and 256 bytes
+    # of unit counters)
+    assert need == 2 * (256 * 2 * (3 * 256 + 512 + 4 + 512)) + 2 * 2 * 65536 + 512
     ptr = P(16)
 
     def call(seg=256, ws=0x10000, ws_bytes=need, T=100):
@@ -263,8 +264,8 @@ def test_workspace_size(L):
 
     assert b.kda_workspace_size(b.KDA_OP_DECODE, 256, 1, 96) == 0
     # chunk 64: one int per (sequence, head), rounded up to 256 bytes, marking the units the exact
-    # pass recomputes; chunk 1 needs none
-    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96) == 512
-    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 4, 8192, 32) == 512
-    assert b.kda_workspace_size(b.KDA_OP_VARLEN, 16, 262144, 64) == 4096
+    # pass recomputes, and 256 bytes of unit counters; chunk 1 needs none
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96) == 512 + 256
+    assert b.kda_workspace_size(b.KDA_OP_CHUNK, 4, 8192, 32) == 512 + 256
+    assert b.kda_workspace_size(b.KDA_OP_VARLEN, 16, 262144, 64) == 4096 + 256
     assert b.kda_workspace_size(b.KDA_OP_CHUNK, 1, 131072, 96, chunk=1) == 0
