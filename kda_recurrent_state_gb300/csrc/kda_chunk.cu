@@ -576,15 +576,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int unit = blockIdx.x;
     if (pool.claim) {
-        // A launch of at most kPackUnits units, one CTA per SM: each CTA claims the next unit, and in
-        // the first pass CTAs on SMs with an ID of at least the unit count wait a moment first, so
-        // that the units land on the SMs with the lowest IDs.  Every CTA claims once, so every unit
-        // is taken whatever the placement.
+        // A launch of at most kPackUnits units, one CTA per SM: each CTA claims the next unit, and
+        // CTAs on SMs with an ID of at least the unit count wait a moment first, so that the units
+        // land on the SMs with the lowest IDs.  Every CTA claims once, so every unit is taken
+        // whatever the placement.
         __shared__ int claimed;
         if (tid == 0) {
             unsigned id;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
-            if (!ROB && id >= (unsigned)(P.N * P.H)) {
+            if (id >= (unsigned)(P.N * P.H)) {
                 const long long tw = clock64();
                 while (clock64() - tw < kClaimDelay) {
                 }
