@@ -291,7 +291,7 @@ int kda_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
  *   chunk = 1   the token-serial evaluation of kda_bwd (no gate limit).
  *   workspace   device, kda_workspace_size(KDA_OP_CHUNK_BWD, N, T_total, H, dk, dv, chunk)
  *               bytes, 16-byte aligned.  For chunk = 64 it holds every chunk's local
- *               products, state and state gradient: about 4.1 KB per (token, head)
+ *               products, state and state gradient: about 5.2 KB per (token, head)
  *               (about 5.4 GB at N=4, T=8192, H=32), and at least the token-serial
  *               backward's workspace, which the recomputation reuses.
  * Returns KDA_ERR_UNSUPPORTED for any other chunk.
