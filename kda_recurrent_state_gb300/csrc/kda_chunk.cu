@@ -63,11 +63,13 @@
 //     (ii) + (iii-b)  [D_S | D_O] += U16 x [KH | PP]   M=128 N=192 K=64 (one product)
 //
 // Warp roles (16 warps): 0 TMA producer, 1 beta loader (+ TMEM allocation),
-// 4-7 "prep" warpgroup (decay cumsum, operand tiles, issues the Gram), 8-11
-// "state" warpgroup (U conversion, state rescale, snapshots, outputs; issues
-// (i)-(iii)), 12-15 "tri" warpgroup (Gram readout, the inverse, W readout;
-// issues WY).  Warps 2-3 have no role.  Roles hand work to each other through
-// mbarriers; every wait is bounded.
+// 2 issues the Gram, 3 issues the WY products (in the exact second pass the tri
+// warpgroup issues them itself), 4-7 "prep" warpgroup (decay cumsum, operand
+// tiles), 8-11 "state" warpgroup (U conversion, state rescale, snapshots, outputs;
+// issues (i)-(iii)), 12-15 "tri" warpgroup (Gram readout, the inverse, W readout).
+// A product group is issued by a thread whose warp has nothing else to do, so that
+// no warp of the working roles stalls behind the issue.  Roles hand work to each
+// other through mbarriers; every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -179,7 +181,8 @@ enum {
     B_STGR = 36,     // own staging buffer read by the previous bulk store (STG_OWN)
     B_PDONE = 37,    // prep has seen every chunk (the unit's range flag is final); ROB = false
     B_SER = 38,      // the exact path's coefficient buffers written (state warpgroup; ROB = true)
-    B_COUNT = 39
+    B_NRD = 39,      // NR = T diag(beta) written by the tri warpgroup (ROB = false)
+    B_COUNT = 40
 };
 static_assert(B_COUNT <= (int)Cfg<float>::NBAR, "barrier space");
 
@@ -672,6 +675,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(&bar[B_STGR], 1);
         mbar_init(&bar[B_PDONE], 128);
         mbar_init(&bar[B_SER], 128);
+        mbar_init(&bar[B_NRD], 128);
         ab->flag = 0;
         *range_bad = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -695,9 +699,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr uint32_t ID_MN = idesc_f16(128, 64, 0, 1);
     constexpr uint32_t ID_KK = idesc_f16(128, 64, 0, 0);
     constexpr uint32_t ID_SO = idesc_f16(128, 192, 0, 0);  // [D_S | D_O]: D_O follows D_S in TMEM
-    // Every product group is issued by thread 0 of the role that completes its last
-    // input, after waiting for that input and for the previous reader of its
-    // accumulator; the commits below are what the other roles wait on.
+    // Every product group is issued by one thread after waiting for its inputs and for the
+    // previous reader of its accumulator; the commits below are what the other roles wait on.
+    // WY products of chunk n, once V16/KT of the chunk are ready and the state update of
+    // chunk n - 1 has consumed U16 (NR complete is the caller's wait).
+    auto issue_wy = [&](int n) -> bool {
+        const int b = n & 1;
+        if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) return false;
+        if (n > 0 && !mbar_wait(&bar[B_SDONE], (n - 1) & 1, ab, status)) return false;
+        tc_fence_after();
+        KDA_TR(n, 22);
+        const uint64_t dkt = k_desc(sm_base + L::OFF_KQ + b * 32768), dnr = k_desc(sm_base + L::OFF_NR);
+        const uint32_t v16 = tmem + TM_V16 + b * 32;
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+            mma_ss(tmem + TM_W, dkt + 2u * st, dnr + 2u * st, ID_KK, st > 0);
+            mma_ts(tmem + TM_U, v16 + st * 8, dnr + 2u * st, ID_KK, st > 0);
+        }
+        mma_commit(&bar[B_WYDONE]);
+        mma_commit(&bar[B_V16FREE + b]);
+        KDA_TR(n, 8);
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -759,8 +782,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             mbar_arrive(&bar[B_BFULL + k4]);
         }
-    } else if (warp < 4) {
-        // no role
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ Gram issuer
+        // the Gram of each chunk, once all its operand rows are ready and the tri warpgroup has
+        // read out the previous one (D_G free)
+        if (lane == 0)
+            for (int n = 0; n < nch; ++n) {
+                const int b = n & 1;
+                if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) break;
+                if (n > 0 && !mbar_wait(&bar[B_P2D], (n - 1) & 1, ab, status)) break;
+                tc_fence_after();
+                const uint64_t da = mn_desc(sm_base + L::OFF_KQ + b * 32768, 16384);
+                const uint64_t db = mn_desc(sm_base + L::OFF_KH + b * L::KHP, 8192);
+#pragma unroll
+                for (int st = 0; st < 8; ++st) mma_ss(tmem + TM_G, da + 128u * st, db + 128u * st, ID_G, st > 0);
+                mma_commit(&bar[B_GDONE]);
+                KDA_TR(n, 3);
+            }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ WY issuer (first pass)
+        // the WY products of each chunk, once NR is written, V16/KT of the chunk are ready and
+        // the state update of the previous chunk has consumed U16
+        if constexpr (!ROB)
+            if (lane == 0)
+                for (int n = 0; n < nch; ++n) {
+                    if (!mbar_wait(&bar[B_NRD], n & 1, ab, status)) break;
+                    if (!issue_wy(n)) break;
+                }
     } else if (warp < 8) {
         // ------------------------------------------------------------ prep warpgroup
         const int c = tid - 128;  // key channel (and TMEM lane) of this thread
@@ -894,17 +942,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             mbar_arrive(&bar[B_PREPD + b]);
             if (c == 0) KDA_TR(n, 2);
-            if (c == 0) {  // the Gram of this chunk, once all operand rows and D_G (read by the tri warps) are ready
-                if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) return false;
-                if (n > 0 && !mbar_wait(&bar[B_P2D], (n - 1) & 1, ab, status)) return false;
-                tc_fence_after();
-                const uint64_t da = mn_desc(sm_base + L::OFF_KQ + b * 32768, 16384);
-                const uint64_t db = mn_desc(sm_base + L::OFF_KH + b * L::KHP, 8192);
-#pragma unroll
-                for (int st = 0; st < 8; ++st) mma_ss(tmem + TM_G, da + 128u * st, db + 128u * st, ID_G, st > 0);
-                mma_commit(&bar[B_GDONE]);
-                KDA_TR(n, 3);
-            }
             return true;
         };
         for (int n = 0; n < nch; ++n)
@@ -1319,24 +1356,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (c == 0) KDA_TR(n, 31);
             }
             fence_proxy_async_smem();
-            if (!wg_sync()) break;  // NR = T diag(beta) complete
-            if (c == 0) KDA_TR(n, 7);
-            mbar_arrive(&bar[B_BFREE + (n & 3)]);
-            if (c == 0) {  // WY products, once V16/KT of the chunk are ready and D(n-1) has consumed U16
-                if (!mbar_wait(&bar[B_PREPD + b], (n >> 1) & 1, ab, status)) break;
-                if (n > 0 && !mbar_wait(&bar[B_SDONE], (n - 1) & 1, ab, status)) break;
-                tc_fence_after();
-                KDA_TR(n, 22);
-                const uint64_t dkt = k_desc(sm_base + L::OFF_KQ + b * 32768), dnr = k_desc(sm_base + L::OFF_NR);
-                const uint32_t v16 = tmem + TM_V16 + b * 32;
-#pragma unroll
-                for (int st = 0; st < 4; ++st) {
-                    mma_ss(tmem + TM_W, dkt + 2u * st, dnr + 2u * st, ID_KK, st > 0);
-                    mma_ts(tmem + TM_U, v16 + st * 8, dnr + 2u * st, ID_KK, st > 0);
-                }
-                mma_commit(&bar[B_WYDONE]);
-                mma_commit(&bar[B_V16FREE + b]);
-                KDA_TR(n, 8);
+            if constexpr (!ROB) {  // NR = T diag(beta) complete: warp 3 issues the WY products
+                tc_fence_before();
+                mbar_arrive(&bar[B_NRD]);
+                if (c == 0) KDA_TR(n, 7);
+                mbar_arrive(&bar[B_BFREE + (n & 3)]);
+            } else {  // the exact pass issues them here (2% faster there, where every chunk takes it)
+                if (!wg_sync()) break;
+                if (c == 0) KDA_TR(n, 7);
+                mbar_arrive(&bar[B_BFREE + (n & 3)]);
+                if (c == 0 && !issue_wy(n)) break;
             }
             if (c >= 64) {  // P of this chunk beside its KH, once the products of chunk n - 2 are done with the pair
                 if (n >= 2) {
